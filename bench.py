@@ -1,0 +1,497 @@
+"""Benchmark of the Mamba-3 scan on B300: prefill tokens/s (headline), decode
+tokens/s, roofline fractions, end-to-end and CPU-oracle baselines.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one m3_scan_fwd call on the 1.5B-layer SISO prefill workload
+(batch 8, L 2048, H 32, P 64, N 128, R 1, chunk 64, bf16 activations, fp32
+state). Inputs are resident in HBM; L2 is flushed (a 256 MiB write) before
+every timed launch, and only the launch is timed, with CUDA events on the
+launching stream. Under torchrun each rank runs its own copy of the workload
+on its own GPU (independent sequences: no data-path collective), and the
+aggregate is all ranks' tokens over the slowest rank's time.
+
+Printed on rank 0: one JSON line. Besides the contract keys it carries
+  roofline         HBM roof of the prefill kernel (algorithmic bytes / time)
+  roofline_tensor  tensor-pipe roof of the same kernel (algorithmic FLOPs / time)
+  decode           1024-step CUDA-graph decode, batch 128 x 32 heads, R = 1 and 4
+  prefill_mimo     the R = 4 prefill workload (chunk 16)
+  e2e              through the C ABI from pinned host buffers, copies included
+  cpu_baseline     the fp64 CPU oracle on a bounded sample of the workload
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import m3synth  # noqa: E402
+
+METRIC = "Mamba-3 scan prefill tok/s & decode tok/s per B300; % of roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p["bf16_tflops_sustained"]), src="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, src="fallback")
+
+
+def prefill_bytes(s: m3synth.ScanShape) -> int:
+    """Algorithmic HBM bytes of one prefill call: every input read once, every
+    output written once (activations in bf16, dt/lambda/theta/state fp32)."""
+    act = 2 if s.bf16 else 4
+    b, L, H, G, P, N, R = s.batch, s.seqlen, s.heads, s.groups, s.headdim, s.dstate, s.R
+    return (2 * b * L * H * P * R * act          # x in, y out
+            + 2 * b * L * H * 4                  # dt, lambda
+            + 2 * b * L * G * N * R * act        # B, C
+            + b * L * G * (N // 2) * 4           # theta
+            + b * H * N * P * 4                  # final state
+            + H * 4 + 2 * H * N * R * 4)         # A, biases
+
+
+def prefill_flops(s: m3synth.ScanShape) -> int:
+    """Dense chunked-SSD FLOPs: per token and head 2 Q R^2 (N + P) for the
+    intra-chunk block (scores and their product with X over the full Q R x Q R
+    tile) plus 4 R N P for the state read-out and the chunk-state update."""
+    Q, R, N, P = s.chunk, s.R, s.dstate, s.headdim
+    return s.batch * s.seqlen * s.heads * (2 * Q * R * R * (N + P) + 4 * R * N * P)
+
+
+def decode_bytes(s: m3synth.ScanShape) -> int:
+    """Per decode step: state read + write, plus the token's activations."""
+    b, H, G, P, N, R = s.batch, s.heads, s.groups, s.headdim, s.dstate, s.R
+    act = 2
+    return (2 * b * H * N * P * 4 + 3 * b * H * P * R * act + 3 * b * G * N * R * act
+            + b * G * (N // 2) * 4 + 2 * b * H * 4)
+
+
+class Clocks:
+    """nvidia-smi sampling during a timed region (median SM clock, throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _traffic_from_profiles(kernel_tag: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches the
+    current kernel source (otherwise None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    src = os.path.join(ROOT, "selective_state_space_129_b300", "csrc", kernel_tag)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+    for line in open(path):
+        if line.startswith("traffic:"):
+            f = dict(kv.split("=", 1) for kv in line[len("traffic:"):].split())
+            if f.get("source") == kernel_tag and f.get("sha") == sha:
+                return int(f["bytes_per_launch"])
+    return None
+
+
+# ---------------------------------------------------------------- oracle arm
+def _stack_heads(shape, inp, bs, hs):
+    """k single-head sequences of the workload stacked along the batch axis."""
+    g = hs // (shape.heads // shape.groups)
+    k = len(bs)
+    sl = lambda a, ix: np.stack([a[bs[i], :, ix[i]] for i in range(k)])[:, :, None]
+    h0 = int(hs[0])
+    return dict(x=sl(inp["x"], hs), dt=sl(inp["dt"], hs), A=inp["A"][h0:h0 + 1],
+                lam=sl(inp["lam"], hs), B=sl(inp["B"], g), C=sl(inp["C"], g),
+                theta=sl(inp["theta"], g), B_bias=inp["B_bias"][h0:h0 + 1],
+                C_bias=inp["C_bias"][h0:h0 + 1])
+
+
+def oracle_rate(shape, inp, budget_s=12.0):
+    """Oracle tok/s on whole single-head sequences of the workload (OpenMP over
+    the stacked sequences, all host cores), sized to about ``budget_s``."""
+    from oracle import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    rng = np.random.default_rng(7)
+
+    def timed(k):
+        sub = _stack_heads(shape, inp, rng.integers(0, shape.batch, k),
+                           rng.integers(0, shape.heads, k))
+        t0 = time.perf_counter()
+        oracle.scan_seq(nthreads=threads, **sub)
+        return k * shape.seqlen, time.perf_counter() - t0
+
+    k0 = min(threads, 16)
+    tok, el = timed(k0)
+    k = int(max(k0, min(256, k0 * budget_s / max(el, 1e-6))))
+    k = max(threads, (k // threads) * threads) if k >= threads else k
+    tok, el = timed(k)
+    sample = ("%d whole single-head sequences of %d tokens drawn from the workload "
+              "(timing sample; A and biases of one head)" % (k, shape.seqlen))
+    return tok / el, min(threads, k), sample
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle timed as it stands on the host cores."""
+    if rank != 0:
+        return
+    idx, shape = m3synth.WORKLOADS["prefill_siso"]
+    inp = m3synth.scan_inputs(shape, seed=idx)
+    from oracle import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    rng = np.random.default_rng(17)
+    k = min(shape.batch * shape.heads, max(threads, 8))
+
+    def step():
+        sub = _stack_heads(shape, inp, rng.integers(0, shape.batch, k),
+                           rng.integers(0, shape.heads, k))
+        oracle.scan_seq(nthreads=threads, **sub)
+        return k * shape.seqlen
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    tok = sum(step() for _ in range(args.steps))
+    el = time.perf_counter() - t0
+    value = tok / el
+    sample = "%d whole sequences of %d tokens per step (one head each)" % (k, shape.seqlen)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill_siso b8 L2048 H32 P64 N128 R1 chunk64",
+                   "note": "fp64 CPU oracle (sequential explicit-rotation recurrence)"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def to_device(inp, bf16, dev):
+    """Seeded numpy inputs -> torch tensors (activations bf16 when asked)."""
+    import torch
+    out = {}
+    for k, v in inp.items():
+        if k == "bits":
+            continue
+        t = torch.from_numpy(np.ascontiguousarray(v))
+        if bf16 and k in ("x", "B", "C"):
+            t = t.to(torch.bfloat16)
+        out[k] = t.to(dev)
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import selective_state_space_129_b300 as m3
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    m3.load()
+    peaks = _peaks()
+    stream = torch.cuda.current_stream()
+
+    idx, shape = m3synth.WORKLOADS["prefill_siso"]
+    inp = m3synth.scan_inputs(shape, seed=idx + 1000 * rank)
+    d = to_device(inp, True, dev)
+    out = torch.empty_like(d["x"])
+    fs = torch.empty((shape.batch, shape.heads, shape.dstate, shape.headdim),
+                     dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def launch():
+        m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"], R=shape.R,
+                       chunk=shape.chunk, out=out, final_state=fs, B_bias=d["B_bias"],
+                       C_bias=d["C_bias"], stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local_rank) as clk:
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    status = m3.m3_device_status()
+    times = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms = sum(times) / len(times)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = shape.tokens * world
+    value = tokens / (ms * 1e-3)
+    if rank != 0:
+        return
+
+    nbytes = prefill_bytes(shape)
+    nflops = prefill_flops(shape)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    tfs = nflops / (ms * 1e-3) / 1e12
+    tc_kernel = "scan_tc.cu"
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "prefill_siso b8 L2048 H32 P64 N128 G1 R1 chunk64",
+                   "global_batch": shape.batch * world, "seq_len": shape.seqlen,
+                   "parallelism": "independent replicas" if world > 1 else "single GPU",
+                   "l2": "flushed before every timed launch (256 MiB write)",
+                   "state": "fp32", "activations": "bf16"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm"], "traffic": _traffic_from_profiles(tc_kernel),
+                     "algorithmic_bytes": nbytes, "peak_source": peaks["src"] + " (burst)"},
+        "roofline_tensor": {"bound": "tensor", "achieved": tfs, "peak": peaks["bf16"],
+                            "unit": "TFLOP/s", "frac": tfs / peaks["bf16"],
+                            "algorithmic_flops": nflops,
+                            "peak_source": peaks["src"] + " bf16 dense (burst)"},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps,
+        "device_status": m3.m3_status_string(status),
+    }
+    del flush
+    torch.cuda.empty_cache()
+    line["prefill_mimo"] = bench_prefill_other(torch, m3, dev, "prefill_mimo", args, peaks)
+    line["decode"] = {"siso": bench_decode(torch, m3, dev, "decode_siso", peaks),
+                      "mimo_r4": bench_decode(torch, m3, dev, "decode_mimo", peaks)}
+    sis, mim = line["decode"]["siso"], line["decode"]["mimo_r4"]
+    if sis.get("ms_per_step") and mim.get("ms_per_step"):
+        line["decode"]["r4_over_r1_latency"] = mim["ms_per_step"] / sis["ms_per_step"]
+    line["e2e"] = bench_e2e(torch, m3, dev, shape, inp, args)
+    if not args.no_cpu_baseline:
+        rate, cores, sample = oracle_rate(shape, inp)
+        line["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def bench_prefill_other(torch, m3, dev, name, args, peaks):
+    idx, shape = m3synth.WORKLOADS[name]
+    inp = m3synth.scan_inputs(shape, seed=idx)
+    d = to_device(inp, True, dev)
+    out = torch.empty_like(d["x"])
+    fs = torch.empty((shape.batch, shape.heads, shape.dstate, shape.headdim),
+                     dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def launch():
+        m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"], R=shape.R,
+                       chunk=shape.chunk, out=out, final_state=fs, B_bias=d["B_bias"],
+                       C_bias=d["C_bias"], stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = sum(times) / len(times)
+    nbytes, nflops = prefill_bytes(shape), prefill_flops(shape)
+    return {"workload": "%s b%d L%d H%d P%d N%d R%d chunk%d" % (
+                name, shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate,
+                shape.R, shape.chunk),
+            "tok_s": shape.tokens / (ms * 1e-3), "ms": ms,
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
+            "tensor_frac": nflops / (ms * 1e-3) / 1e12 / peaks["bf16"]}
+
+
+def bench_decode(torch, m3, dev, name, peaks, n_sets=16, steps=m3synth.DECODE_STEPS):
+    """1024 decode steps captured in one CUDA graph; per-step inputs cycle over
+    ``n_sets`` seeded token sets (B_prev/x_prev are the previous set's)."""
+    idx, shape = m3synth.WORKLOADS[name]
+    sets = [to_device(m3synth.decode_inputs(shape, seed=idx, step=i), True, dev)
+            for i in range(n_sets)]
+    st = torch.zeros((shape.batch, shape.heads, shape.dstate, shape.headdim),
+                     dtype=torch.float32, device=dev)
+    out = torch.empty_like(sets[0]["x"])
+    s = torch.cuda.Stream(device=dev)
+
+    def step(i, stream):
+        cur, prev = sets[i % n_sets], sets[(i - 1) % n_sets]
+        m3.m3_decode_step(st, cur["x"], cur["dt"], cur["A"], cur["lam"], cur["B"], cur["C"],
+                          cur["theta"], R=shape.R, B_prev=prev["B"], x_prev=prev["x"], out=out,
+                          B_bias=cur["B_bias"], C_bias=cur["C_bias"], stream=stream)
+
+    with torch.cuda.stream(s):
+        for i in range(8):
+            step(i, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(steps):
+            step(i, s)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    reps = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for _ in range(reps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    ms_step = e0.elapsed_time(e1) / (reps * steps)
+    nbytes = decode_bytes(shape)
+    gbs = nbytes / (ms_step * 1e-3) / 1e9
+    return {"workload": "%s b%d H%d P%d N%d R%d, %d steps in one CUDA graph" % (
+                name, shape.batch, shape.heads, shape.headdim, shape.dstate, shape.R, steps),
+            "tok_s": shape.batch / (ms_step * 1e-3), "ms_per_step": ms_step,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "algorithmic_bytes": nbytes},
+            "gpu_launches": steps * reps,
+            "l2": "state 134 MB exceeds the 126 MB L2; no flush between steps"}
+
+
+def bench_e2e(torch, m3, dev, shape, inp, args):
+    """Same workload through the public call from pinned host buffers: every
+    step copies the inputs host->device, runs the scan and reads the outputs
+    back (y and final state) into pinned host memory."""
+    host = {k: v.pin_memory() for k, v in to_device(inp, True, "cpu").items()}
+    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_h = torch.empty_like(host["x"]).pin_memory()
+    fs_h = torch.empty((shape.batch, shape.heads, shape.dstate, shape.headdim),
+                       dtype=torch.float32).pin_memory()
+    out = torch.empty_like(devb["x"])
+    fs = torch.empty(fs_h.shape, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size() + fs_h.numel() * 4
+
+    def step():
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        m3.m3_scan_fwd(devb["x"], devb["dt"], devb["A"], devb["lam"], devb["B"], devb["C"],
+                       devb["theta"], R=shape.R, chunk=shape.chunk, out=out, final_state=fs,
+                       B_bias=devb["B_bias"], C_bias=devb["C_bias"], stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        fs_h.copy_(fs, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    return {"value": shape.tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

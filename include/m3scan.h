@@ -1,0 +1,138 @@
+/*
+ * m3scan.h -- C ABI of the B300 (sm_103a) Mamba-3 scan library, libm3scan.so.
+ *
+ * The scan (Mamba-3, "Improved Sequence Modeling using State Space
+ * Principles"): per batch row b and head h,
+ *
+ *   h_t = alpha_t R_t h_{t-1} + beta_t R_t B_{t-1} x_{t-1}^T + gamma_t B_t x_t^T
+ *   y_t = C_t^T h_t
+ *
+ *   alpha_t = exp(Delta_t A),  beta_t = (1 - lambda_t) Delta_t alpha_t,  gamma_t = lambda_t Delta_t
+ *       -- exponential-trapezoidal discretisation, aipaper.cc summary, sec. 4.1, Prop. 1
+ *   R_t = block-diagonal 2x2 rotations [[cos,-sin],[sin,cos]] by Delta_t theta[t,k] on state
+ *         rows (2k, 2k+1)  -- complex-valued state, aipaper.cc sec. 4.2 (Prop. 2/3);
+ *         rotation matrix from the metaphor-xennon blog, sec. 2.2
+ *   B_t = B[b,t,g] + B_bias[h] (N x R), C_t = C[b,t,g] + C_bias[h], x_t (P x R)
+ *       -- MIMO rank R, papernotes.org sec. 3; head-specific B/C bias, papernotes.org sec. 4
+ *   g = h / (H / G): heads are split into G equal groups that share B, C and theta.
+ *   h_{-1} = 0 and B_{-1} x_{-1} = 0 for prefill.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers to row-major, contiguous arrays
+ *     (any CUDA allocation, including managed memory). The caller owns every
+ *     buffer; the library keeps no allocation between calls.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *     the legacy default stream). A call returns once the work is enqueued.
+ *   - Arguments are validated on the host before anything is enqueued. An
+ *     invalid or unsupported call returns a non-zero status and touches no
+ *     output. A failed launch returns M3_ERR_CUDA.
+ *   - Kernels never trap or assert. A bounded device-side wait that expires
+ *     records a flag that m3_device_status() reports as M3_ERR_TIMEOUT.
+ *   - Outputs must not alias inputs (decode's `state` is updated in place).
+ *   - The library runs on compute capability 10.3 (B300) only; elsewhere the
+ *     compute entry points return M3_ERR_UNSUPPORTED.
+ */
+#ifndef M3SCAN_H_
+#define M3SCAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  M3_OK = 0,
+  M3_ERR_INVALID_ARG = 1, /* null pointer, negative size, odd N, G not dividing H, ... */
+  M3_ERR_UNSUPPORTED = 2, /* valid but not implemented: dtype, shape, device arch      */
+  M3_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed                      */
+  M3_ERR_TIMEOUT = 4      /* a bounded device-side wait expired (see m3_device_status) */
+} m3_status;
+
+typedef enum {
+  M3_F32 = 0, /* x, B, C, B_prev, x_prev, out are float32 (the fp32 precision mode) */
+  M3_BF16 = 1 /* ... are bfloat16; dt, lambda, theta, A, biases and state stay fp32 */
+} m3_dtype;
+
+typedef struct {
+  int64_t batch;   /* b  >= 0                                             */
+  int64_t seqlen;  /* L  >= 0 (prefill); ignored by decode                 */
+  int64_t heads;   /* H  >= 1                                             */
+  int64_t groups;  /* G  >= 1, divides H                                  */
+  int64_t headdim; /* P  >= 1                                             */
+  int64_t dstate;  /* N  >= 2, even (N/2 rotating pairs)                  */
+  int32_t act_dtype;  /* an m3_dtype                                      */
+  int32_t reserved;   /* must be 0                                        */
+  const float* B_bias; /* [H, N, R] fp32 device pointer, or NULL (zero bias) */
+  const float* C_bias; /* [H, N, R] fp32 device pointer, or NULL            */
+  void* workspace;        /* device scratch for long sequences, or NULL     */
+  size_t workspace_bytes; /* its size; see m3_scan_workspace_bytes()        */
+} m3_dims;
+
+/*
+ * Prefill: the whole scan over L tokens (chunked SSD algorithm).
+ *
+ * Layouts (R = MIMO rank, N = dstate, P = headdim):
+ *   x, out       [b, L, H, P, R]   act_dtype
+ *   dt, lambda   [b, L, H]         fp32, dt > 0, lambda in [0, 1]
+ *   A            [H]               fp32 (A < 0 decays; A = 0 allowed)
+ *   B, C         [b, L, G, N, R]   act_dtype
+ *   theta        [b, L, G, N/2]    fp32 (rotation rate per state pair; angle = dt * theta)
+ *   final_state  [b, H, N, P]      fp32, or NULL. h_{L-1} in the explicit
+ *                (unrotated) frame. It does not include the next token's
+ *                beta term; m3_decode_step adds that from B_prev/x_prev.
+ * `chunk` is the chunk length Q in tokens (>= 1); the chunked algorithm is
+ * exact up to rounding for any Q. The tensor-core bf16 path needs Q * R = 64
+ * with P = 64 and N in {64, 128}; other bf16 shapes and every fp32 shape run
+ * on the CUDA-core path (still on the GPU). Out-of-range chunk sizes return
+ * M3_ERR_UNSUPPORTED.
+ * Scratch: none is needed for the shapes of this release; `workspace` is
+ * accepted and ignored when m3_scan_workspace_bytes() returns 0.
+ * L = 0 writes zeros to final_state (if given) and nothing else.
+ */
+m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const float* lambda,
+                      const void* B, const void* C, const float* theta, const m3_dims* dims,
+                      int R, int chunk, void* out, float* final_state, void* stream);
+
+/*
+ * Decode: one token of the recurrence for every (b, h), state updated in place.
+ *
+ *   state   [b, H, N, P]  fp32, h_{t-1} on entry, h_t on return (explicit frame)
+ *   x, out  [b, H, P, R]  act_dtype
+ *   dt, lambda [b, H] fp32;  A [H] fp32
+ *   B, C    [b, G, N, R]  act_dtype (raw: the kernel adds the bias)
+ *   theta   [b, G, N/2]   fp32
+ *   B_prev  [b, G, N, R]  raw B of the previous token, and
+ *   x_prev  [b, H, P, R]  x of the previous token; both NULL for the first
+ *           token of a sequence (then B_{t-1} x_{t-1}^T = 0). One NULL and
+ *           one non-NULL is M3_ERR_INVALID_ARG.
+ * dims->seqlen, workspace and workspace_bytes are ignored. The product
+ * B_prev x_prev^T is formed on the fly (passing N x P products per head would
+ * double the step's memory traffic).
+ */
+m3_status m3_decode_step(float* state, const void* x, const float* dt, const float* A,
+                         const float* lambda, const void* B_prev, const void* x_prev,
+                         const void* B, const void* C, const float* theta, const m3_dims* dims,
+                         int R, void* out, void* stream);
+
+/* Bytes of device scratch m3_scan_fwd wants for these arguments (0 if none);
+ * (size_t)-1 if the arguments are invalid. Pure host function. */
+size_t m3_scan_workspace_bytes(const m3_dims* dims, int R, int chunk);
+
+/* Static, human-readable name of a status. Pure host function. */
+const char* m3_status_string(m3_status status);
+
+/* Synchronises `stream`, then reads and clears this device's flag of expired
+ * device-side waits: M3_OK if none expired since the last call,
+ * M3_ERR_TIMEOUT otherwise, M3_ERR_CUDA if the synchronisation failed. */
+m3_status m3_device_status(void* stream);
+
+/* Library version as major*10000 + minor*100 + patch. Pure host function. */
+int m3_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M3SCAN_H_ */

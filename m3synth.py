@@ -77,10 +77,13 @@ WORKLOADS = {
 
 def to_bf16(a: np.ndarray) -> np.ndarray:
     """Round float32 to the nearest bf16 (ties to even); returns float32."""
-    a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    rounded = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
-    return rounded.astype(np.uint32).view(np.float32)
+    a = np.array(a, dtype=np.float32, copy=True, order="C")
+    u = a.view(np.uint32)  # finite inputs: the sum below cannot overflow 32 bits
+    bias = (u >> 16) & 1
+    bias += 0x7FFF
+    u += bias
+    u &= np.uint32(0xFFFF0000)
+    return a
 
 
 def _softplus(v):

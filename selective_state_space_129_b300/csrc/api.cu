@@ -1,0 +1,192 @@
+// C ABI of libm3scan.so: argument validation and kernel dispatch.
+// The declarations, layouts and error behaviour are documented in m3scan.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "launch.h"
+#include "m3scan.h"
+
+namespace {
+
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > kMaxElems / a) return false;
+  *out = a * b;
+  return true;
+}
+
+bool count(std::initializer_list<int64_t> dims, int64_t* out) {
+  int64_t c = 1;
+  for (int64_t d : dims)
+    if (!mul_ok(c, d, &c)) return false;
+  *out = c;
+  return true;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A pointer may be NULL only when the tensor it points to is empty.
+bool ptr_ok(const void* p, int64_t elems, size_t align) {
+  if (elems == 0) return true;
+  return p != nullptr && aligned(p, align);
+}
+
+m3_status check_dims(const m3_dims* d, int R) {
+  if (d == nullptr) return M3_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->heads < 1 || d->groups < 1 || d->headdim < 1 || d->dstate < 2)
+    return M3_ERR_INVALID_ARG;
+  if (d->dstate % 2 != 0 || d->heads % d->groups != 0) return M3_ERR_INVALID_ARG;
+  if (d->reserved != 0 || R < 1) return M3_ERR_INVALID_ARG;
+  if (d->act_dtype != M3_F32 && d->act_dtype != M3_BF16) return M3_ERR_UNSUPPORTED;
+  if (d->heads > (1 << 20) || d->headdim > (1 << 20) || d->dstate > (1 << 20) || R > 1024)
+    return M3_ERR_UNSUPPORTED;
+  return M3_OK;
+}
+
+m3_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return M3_ERR_CUDA;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return M3_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return M3_ERR_UNSUPPORTED;
+  return M3_OK;
+}
+
+m3_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return M3_OK;
+  cudaGetLastError();
+  return M3_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int m3_version(void) { return 100; }
+
+const char* m3_status_string(m3_status s) {
+  switch (s) {
+    case M3_OK: return "M3_OK";
+    case M3_ERR_INVALID_ARG: return "M3_ERR_INVALID_ARG";
+    case M3_ERR_UNSUPPORTED: return "M3_ERR_UNSUPPORTED";
+    case M3_ERR_CUDA: return "M3_ERR_CUDA";
+    case M3_ERR_TIMEOUT: return "M3_ERR_TIMEOUT";
+  }
+  return "M3_ERR_UNKNOWN";
+}
+
+size_t m3_scan_workspace_bytes(const m3_dims* dims, int R, int chunk) {
+  if (check_dims(dims, R) == M3_ERR_INVALID_ARG || chunk < 1 || dims->seqlen < 0)
+    return (size_t)-1;
+  return 0;
+}
+
+m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const float* lambda,
+                      const void* B, const void* C, const float* theta, const m3_dims* dims,
+                      int R, int chunk, void* out, float* final_state, void* stream) {
+  m3_status st = check_dims(dims, R);
+  if (st != M3_OK) return st;
+  if (chunk < 1 || dims->seqlen < 0) return M3_ERR_INVALID_ARG;
+  const int64_t b = dims->batch, L = dims->seqlen, H = dims->heads, G = dims->groups,
+                P = dims->headdim, N = dims->dstate;
+  const size_t act = dims->act_dtype == M3_BF16 ? 2 : 4;
+  int64_t n_x, n_t, n_bc, n_th, n_st, n_bias;
+  if (!count({b, L, H, P, R}, &n_x) || !count({b, L, H}, &n_t) ||
+      !count({b, L, G, N, R}, &n_bc) || !count({b, L, G, N / 2}, &n_th) ||
+      !count({b, H, N, P}, &n_st) || !count({H, N, R}, &n_bias))
+    return M3_ERR_INVALID_ARG;
+  if (!ptr_ok(x, n_x, act) || !ptr_ok(out, n_x, act) || !ptr_ok(dt, n_t, 4) ||
+      !ptr_ok(lambda, n_t, 4) || !ptr_ok(A, H, 4) || !ptr_ok(B, n_bc, act) ||
+      !ptr_ok(C, n_bc, act) || !ptr_ok(theta, n_th, 4))
+    return M3_ERR_INVALID_ARG;
+  if (final_state && !aligned(final_state, 4)) return M3_ERR_INVALID_ARG;
+  if ((dims->B_bias && !aligned(dims->B_bias, 4)) || (dims->C_bias && !aligned(dims->C_bias, 4)))
+    return M3_ERR_INVALID_ARG;
+  if ((int64_t)chunk * R > 4096 || chunk > 4096) return M3_ERR_UNSUPPORTED;
+
+  const bool bf16 = dims->act_dtype == M3_BF16;
+  const bool use_tc = bf16 && m3::scan_tc_supported(N, P, R, chunk);
+  if (!use_tc) {
+    const size_t smem = m3::scan_simt_smem_bytes(N, P, R, chunk);
+    if (smem > 227 * 1024) return M3_ERR_UNSUPPORTED;
+  }
+  if (b * H > 0x7fffffff) return M3_ERR_UNSUPPORTED;
+
+  st = check_device();
+  if (st != M3_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n_st == 0) return M3_OK;
+  if (L == 0) {
+    if (final_state)
+      return from_cuda(cudaMemsetAsync(final_state, 0, sizeof(float) * (size_t)n_st, s));
+    return M3_OK;
+  }
+  m3::ScanArgs a;
+  a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B = B; a.C = C; a.theta = theta;
+  a.B_bias = dims->B_bias; a.C_bias = dims->C_bias; a.out = out; a.final_state = final_state;
+  a.batch = b; a.L = L; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R; a.Q = chunk;
+  if (use_tc) {
+    unsigned int* status = nullptr;
+    st = from_cuda(m3::status_word(&status));
+    if (st != M3_OK) return st;
+    return from_cuda(m3::launch_scan_tc(a, status, s));
+  }
+  return from_cuda(m3::launch_scan_simt(a, bf16, s));
+}
+
+m3_status m3_decode_step(float* state, const void* x, const float* dt, const float* A,
+                         const float* lambda, const void* B_prev, const void* x_prev,
+                         const void* B, const void* C, const float* theta, const m3_dims* dims,
+                         int R, void* out, void* stream) {
+  m3_status st = check_dims(dims, R);
+  if (st != M3_OK) return st;
+  if ((B_prev == nullptr) != (x_prev == nullptr)) return M3_ERR_INVALID_ARG;
+  const int64_t b = dims->batch, H = dims->heads, G = dims->groups, P = dims->headdim,
+                N = dims->dstate;
+  const size_t act = dims->act_dtype == M3_BF16 ? 2 : 4;
+  int64_t n_x, n_t, n_bc, n_th, n_st;
+  if (!count({b, H, P, R}, &n_x) || !count({b, H}, &n_t) || !count({b, G, N, R}, &n_bc) ||
+      !count({b, G, N / 2}, &n_th) || !count({b, H, N, P}, &n_st))
+    return M3_ERR_INVALID_ARG;
+  if (!ptr_ok(state, n_st, 16) || !ptr_ok(x, n_x, act) || !ptr_ok(out, n_x, act) ||
+      !ptr_ok(dt, n_t, 4) || !ptr_ok(lambda, n_t, 4) || !ptr_ok(A, H, 4) ||
+      !ptr_ok(B, n_bc, act) || !ptr_ok(C, n_bc, act) || !ptr_ok(theta, n_th, 4))
+    return M3_ERR_INVALID_ARG;
+  if (B_prev && (!ptr_ok(B_prev, n_bc, act) || !ptr_ok(x_prev, n_x, act)))
+    return M3_ERR_INVALID_ARG;
+  if ((dims->B_bias && !aligned(dims->B_bias, 4)) || (dims->C_bias && !aligned(dims->C_bias, 4)))
+    return M3_ERR_INVALID_ARG;
+  if (!m3::decode_supported(N, P, R)) return M3_ERR_UNSUPPORTED;
+  if (b * H > 0x7fffffff) return M3_ERR_UNSUPPORTED;
+
+  st = check_device();
+  if (st != M3_OK) return st;
+  if (n_st == 0) return M3_OK;
+  m3::DecodeArgs a;
+  a.state = state; a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B_prev = B_prev;
+  a.x_prev = x_prev; a.B = B; a.C = C; a.theta = theta; a.B_bias = dims->B_bias;
+  a.C_bias = dims->C_bias; a.out = out; a.batch = b; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R;
+  return from_cuda(m3::launch_decode(a, dims->act_dtype == M3_BF16,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+m3_status m3_device_status(void* stream) {
+  unsigned int v = 0;
+  if (m3::read_clear_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return M3_ERR_CUDA;
+  }
+  return v ? M3_ERR_TIMEOUT : M3_OK;
+}
+
+}  // extern "C"

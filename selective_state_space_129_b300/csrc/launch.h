@@ -1,0 +1,60 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace m3 {
+
+struct ScanArgs {
+  const void* x;
+  const float* dt;
+  const float* A;
+  const float* lam;
+  const void* B;
+  const void* C;
+  const float* theta;
+  const float* B_bias;
+  const float* C_bias;
+  void* out;
+  float* final_state;
+  int64_t batch, L, H, G, P, N;
+  int R, Q;
+};
+
+struct DecodeArgs {
+  float* state;
+  const void* x;
+  const float* dt;
+  const float* A;
+  const float* lam;
+  const void* B_prev;
+  const void* x_prev;
+  const void* B;
+  const void* C;
+  const float* theta;
+  const float* B_bias;
+  const float* C_bias;
+  void* out;
+  int64_t batch, H, G, P, N;
+  int R;
+};
+
+// CUDA-core chunked prefill (any shape whose tiles fit shared memory).
+size_t scan_simt_smem_bytes(int64_t N, int64_t P, int R, int Q);
+cudaError_t launch_scan_simt(const ScanArgs& a, bool bf16, cudaStream_t s);
+
+// Tensor-core (tcgen05) chunked prefill, bf16 activations.
+bool scan_tc_supported(int64_t N, int64_t P, int R, int Q);
+cudaError_t launch_scan_tc(const ScanArgs& a, unsigned int* status, cudaStream_t s);
+
+// Decode step.
+bool decode_supported(int64_t N, int64_t P, int R);
+cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s);
+
+// Device address of this device's status word of expired waits.
+cudaError_t status_word(unsigned int** ptr);
+cudaError_t read_clear_status(unsigned int* value, cudaStream_t s);
+
+}  // namespace m3

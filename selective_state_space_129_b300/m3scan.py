@@ -1,0 +1,172 @@
+"""Python binding of libm3scan.so (argument marshalling only).
+
+The names mirror the C ABI in include/m3scan.h. Tensors are PyTorch CUDA
+tensors (PyTorch supplies device memory and streams); every step of the scan
+runs in the library's CUDA kernels. There is no CPU fallback: if the library
+cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libm3scan.so")
+
+M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA, M3_ERR_TIMEOUT = range(5)
+M3_F32, M3_BF16 = 0, 1
+
+# Exported entry points (kept in step with include/m3scan.h).
+EXPORTS = ("m3_scan_fwd", "m3_decode_step", "m3_scan_workspace_bytes", "m3_status_string",
+           "m3_device_status", "m3_version")
+
+
+class M3Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s" % (where, m3_status_string(status)))
+
+
+class m3_dims(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int64),
+        ("seqlen", ctypes.c_int64),
+        ("heads", ctypes.c_int64),
+        ("groups", ctypes.c_int64),
+        ("headdim", ctypes.c_int64),
+        ("dstate", ctypes.c_int64),
+        ("act_dtype", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("B_bias", ctypes.c_void_p),
+        ("C_bias", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once). Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libm3scan.so is not built (%s); run "
+                           "`python -m selective_state_space_129_b300.build`" % path)
+    lib = ctypes.CDLL(path)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    dims_p = ctypes.POINTER(m3_dims)
+    lib.m3_scan_fwd.argtypes = [vp] * 7 + [dims_p, i32, i32, vp, vp, vp]
+    lib.m3_scan_fwd.restype = i32
+    lib.m3_decode_step.argtypes = [vp] * 10 + [dims_p, i32, vp, vp]
+    lib.m3_decode_step.restype = i32
+    lib.m3_scan_workspace_bytes.argtypes = [dims_p, i32, i32]
+    lib.m3_scan_workspace_bytes.restype = ctypes.c_size_t
+    lib.m3_status_string.argtypes = [i32]
+    lib.m3_status_string.restype = ctypes.c_char_p
+    lib.m3_device_status.argtypes = [vp]
+    lib.m3_device_status.restype = i32
+    lib.m3_version.argtypes = []
+    lib.m3_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def m3_status_string(status: int) -> str:
+    return load().m3_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _act_dtype(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return M3_BF16
+    if t.dtype == torch.float32:
+        return M3_F32
+    raise TypeError("activations must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def make_dims(batch, seqlen, heads, groups, headdim, dstate, act_dtype, B_bias=None,
+              C_bias=None, workspace=None):
+    d = m3_dims()
+    d.batch, d.seqlen, d.heads, d.groups, d.headdim, d.dstate = (
+        int(batch), int(seqlen), int(heads), int(groups), int(headdim), int(dstate))
+    d.act_dtype = int(act_dtype)
+    d.reserved = 0
+    d.B_bias = None if B_bias is None else B_bias.data_ptr()
+    d.C_bias = None if C_bias is None else C_bias.data_ptr()
+    d.workspace = None if workspace is None else workspace.data_ptr()
+    d.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return d
+
+
+def _check(status, where):
+    if status != M3_OK:
+        raise M3Error(status, where)
+
+
+def m3_scan_workspace_bytes(dims: m3_dims, R: int, chunk: int) -> int:
+    return int(load().m3_scan_workspace_bytes(ctypes.byref(dims), int(R), int(chunk)))
+
+
+def m3_scan_fwd(x, dt, A, lam, B, C, theta, R, chunk, out=None, final_state=None,
+                B_bias=None, C_bias=None, workspace=None, stream=None, want_state=True):
+    """Prefill. Shapes: x [b,L,H,P,R], dt/lam [b,L,H], A [H], B/C [b,L,G,N,R],
+    theta [b,L,G,N/2]. Returns (out, final_state)."""
+    import torch
+    lib = load()
+    b, L, H, P, R_ = x.shape
+    if R_ != R:
+        raise ValueError("x.shape[-1] must equal R")
+    G, N = B.shape[2], B.shape[3]
+    if out is None:
+        out = torch.empty_like(x)
+    if final_state is None and want_state:
+        final_state = torch.empty((b, H, N, P), dtype=torch.float32, device=x.device)
+    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias, workspace)
+    st = lib.m3_scan_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B), _ptr(C), _ptr(theta),
+                         ctypes.byref(dims), int(R), int(chunk), _ptr(out), _ptr(final_state),
+                         _stream_handle(stream))
+    _check(st, "m3_scan_fwd")
+    return out, final_state
+
+
+def m3_decode_step(state, x, dt, A, lam, B, C, theta, R, B_prev=None, x_prev=None, out=None,
+                   B_bias=None, C_bias=None, stream=None):
+    """One decode token; ``state`` [b,H,N,P] fp32 is updated in place. Returns out [b,H,P,R]."""
+    import torch
+    lib = load()
+    b, H, P, R_ = x.shape
+    if R_ != R:
+        raise ValueError("x.shape[-1] must equal R")
+    G, N = B.shape[1], B.shape[2]
+    if out is None:
+        out = torch.empty_like(x)
+    dims = make_dims(b, 1, H, G, P, N, _act_dtype(x), B_bias, C_bias)
+    st = lib.m3_decode_step(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B_prev),
+                            _ptr(x_prev), _ptr(B), _ptr(C), _ptr(theta), ctypes.byref(dims),
+                            int(R), _ptr(out), _stream_handle(stream))
+    _check(st, "m3_decode_step")
+    return out
+
+
+def m3_device_status(stream=None) -> int:
+    return int(load().m3_device_status(_stream_handle(stream)))
+
+
+def m3_version() -> int:
+    return int(load().m3_version())

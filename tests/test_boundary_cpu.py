@@ -1,0 +1,145 @@
+"""Host-side checks of the C ABI (no GPU work is ever launched here).
+
+The library must load, export every function include/m3scan.h declares, and
+reject invalid or unsupported arguments on the host with the documented
+status before touching a device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_129_b300 import m3scan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # aligned, never dereferenced: validation fails before any device call
+
+
+def _declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(m3_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return m3scan.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 6
+    raw = ctypes.CDLL(m3scan.LIB_PATH)
+    for name in declared:
+        assert hasattr(raw, name), name
+    assert set(declared) == set(m3scan.EXPORTS)
+
+
+def test_status_strings(lib):
+    assert m3scan.m3_status_string(0) == "M3_OK"
+    assert m3scan.m3_status_string(4) == "M3_ERR_TIMEOUT"
+    assert m3scan.m3_status_string(99) == "M3_ERR_UNKNOWN"
+    assert m3scan.m3_version() >= 100
+
+
+def _dims(**kw):
+    base = dict(batch=2, seqlen=16, heads=4, groups=2, headdim=8, dstate=8,
+                act_dtype=m3scan.M3_F32)
+    base.update(kw)
+    return m3scan.make_dims(**base)
+
+
+def _scan(lib, dims, R=1, chunk=4, **ptrs):
+    p = dict(x=FAKE, dt=FAKE, A=FAKE, lam=FAKE, B=FAKE, C=FAKE, theta=FAKE, out=FAKE, fs=FAKE)
+    p.update(ptrs)
+    v = lambda k: ctypes.c_void_p(p[k]) if p[k] else None
+    return lib.m3_scan_fwd(v("x"), v("dt"), v("A"), v("lam"), v("B"), v("C"), v("theta"),
+                           ctypes.byref(dims), R, chunk, v("out"), v("fs"), None)
+
+
+def _decode(lib, dims, R=1, **ptrs):
+    p = dict(state=FAKE, x=FAKE, dt=FAKE, A=FAKE, lam=FAKE, Bp=0, xp=0, B=FAKE, C=FAKE,
+             theta=FAKE, out=FAKE)
+    p.update(ptrs)
+    v = lambda k: ctypes.c_void_p(p[k]) if p[k] else None
+    return lib.m3_decode_step(v("state"), v("x"), v("dt"), v("A"), v("lam"), v("Bp"), v("xp"),
+                              v("B"), v("C"), v("theta"), ctypes.byref(dims), R, v("out"), None)
+
+
+@pytest.mark.parametrize("missing", ["x", "dt", "A", "lam", "B", "C", "theta", "out"])
+def test_scan_null_pointer(lib, missing):
+    assert _scan(lib, _dims(), **{missing: 0}) == m3scan.M3_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,R,chunk,expect", [
+    (dict(dstate=7), 1, 4, m3scan.M3_ERR_INVALID_ARG),        # odd N
+    (dict(groups=3), 1, 4, m3scan.M3_ERR_INVALID_ARG),        # G does not divide H
+    (dict(batch=-1), 1, 4, m3scan.M3_ERR_INVALID_ARG),
+    (dict(seqlen=-5), 1, 4, m3scan.M3_ERR_INVALID_ARG),
+    (dict(heads=0), 1, 4, m3scan.M3_ERR_INVALID_ARG),
+    (dict(), 0, 4, m3scan.M3_ERR_INVALID_ARG),                # R < 1
+    (dict(), 1, 0, m3scan.M3_ERR_INVALID_ARG),                # chunk < 1
+    (dict(act_dtype=7), 1, 4, m3scan.M3_ERR_UNSUPPORTED),     # unknown dtype
+    (dict(), 1, 5000, m3scan.M3_ERR_UNSUPPORTED),             # chunk too long
+    (dict(dstate=4096, headdim=512), 1, 64, m3scan.M3_ERR_UNSUPPORTED),  # tiles exceed smem
+])
+def test_scan_rejects(lib, kw, R, chunk, expect):
+    assert _scan(lib, _dims(**kw), R=R, chunk=chunk) == expect
+
+
+def test_scan_misaligned_pointer(lib):
+    assert _scan(lib, _dims(), x=FAKE + 2) == m3scan.M3_ERR_INVALID_ARG
+    d = _dims(act_dtype=m3scan.M3_BF16)
+    assert _scan(lib, d, x=FAKE + 1) == m3scan.M3_ERR_INVALID_ARG
+
+
+def test_scan_reserved_field_must_be_zero(lib):
+    d = _dims()
+    d.reserved = 1
+    assert _scan(lib, d) == m3scan.M3_ERR_INVALID_ARG
+
+
+def test_scan_null_dims(lib):
+    v = ctypes.c_void_p(FAKE)
+    assert lib.m3_scan_fwd(v, v, v, v, v, v, v, None, 1, 4, v, v, None) == \
+        m3scan.M3_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,R,expect", [
+    (dict(headdim=6), 1, m3scan.M3_ERR_UNSUPPORTED),   # P not a multiple of 4
+    (dict(), 3, m3scan.M3_ERR_UNSUPPORTED),            # R outside {1, 2, 4}
+    (dict(dstate=5), 1, m3scan.M3_ERR_INVALID_ARG),
+])
+def test_decode_rejects(lib, kw, R, expect):
+    assert _decode(lib, _dims(**kw), R=R) == expect
+
+
+def test_decode_prev_pointers_come_in_pairs(lib):
+    assert _decode(lib, _dims(), Bp=FAKE) == m3scan.M3_ERR_INVALID_ARG
+    assert _decode(lib, _dims(), xp=FAKE) == m3scan.M3_ERR_INVALID_ARG
+
+
+def test_decode_state_alignment(lib):
+    assert _decode(lib, _dims(), state=FAKE + 4) == m3scan.M3_ERR_INVALID_ARG
+
+
+def test_workspace_query(lib):
+    d = _dims()
+    assert m3scan.m3_scan_workspace_bytes(d, 1, 4) == 0
+    bad = _dims(dstate=7)
+    assert m3scan.m3_scan_workspace_bytes(bad, 1, 4) == ctypes.c_size_t(-1).value
+
+
+def test_valid_call_without_a_device_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present; the no-device path is not reachable")
+    assert _scan(lib, _dims()) == m3scan.M3_ERR_CUDA
+    assert _decode(lib, _dims()) == m3scan.M3_ERR_CUDA
+    assert lib.m3_device_status(None) == m3scan.M3_ERR_CUDA

@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Small shapes are compared element by element over several chunks and a
+ragged tail; the full-size workloads are run whole on the GPU and compared on
+seeded samples of (batch, head) sequences, each checked in full, since heads
+are independent. Tolerances are in tests/gpu_util.py.
+"""
+import numpy as np
+import pytest
+
+import m3synth
+from gpu_util import assert_bf16, assert_f32, head_slice, max_over_rms, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import selective_state_space_129_b300 as m3  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m3.load()
+    yield
+    assert m3.m3_device_status() == 0
+
+
+def _gpu_scan(inp, shape, chunk=None, bf16=None):
+    bf16 = shape.bf16 if bf16 is None else bf16
+    d = to_device(inp, bf16)
+    out, fs = m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"],
+                             R=shape.R, chunk=chunk or shape.chunk, B_bias=d["B_bias"],
+                             C_bias=d["C_bias"])
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), fs.cpu().numpy()
+
+
+def _oracle(orc, inp):
+    return orc.scan_seq(inp["x"], inp["dt"], inp["A"], inp["lam"], inp["B"], inp["C"],
+                        inp["theta"], inp["B_bias"], inp["C_bias"], nthreads=0)
+
+
+# ---------------------------------------------------------------- fp32 mode
+def test_tiny_workload_fp32(orc):
+    shape = m3synth.TINY
+    inp = m3synth.scan_inputs(shape, seed=0)
+    y, fs = _gpu_scan(inp, shape)
+    y_ref, fs_ref = _oracle(orc, inp)
+    assert_f32(y, y_ref, "y")
+    assert_f32(fs, fs_ref, "final_state")
+
+
+SMALL_CASES = [
+    # L, chunk, R, G, H, N, P
+    (37, 8, 1, 1, 2, 16, 16),     # ragged tail
+    (1, 16, 1, 1, 2, 16, 16),     # single token
+    (50, 4, 4, 2, 4, 16, 8),      # MIMO, two groups
+    (128, 64, 1, 1, 2, 128, 64),  # two full chunks at the 1.5B-layer head shape
+    (130, 16, 4, 1, 2, 128, 64),  # MIMO head shape, ragged
+    (100, 32, 2, 2, 4, 32, 8),
+    (65, 1, 1, 1, 1, 8, 4),       # chunk of one token
+]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: "L%d_Q%d_R%d_G%d_H%d_N%d_P%d" % c)
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_small_shapes(orc, case, bf16):
+    L, Q, R, G, H, N, P = case
+    shape = m3synth.ScanShape(2, L, H, G, P, N, R=R, chunk=Q, bf16=bf16, rms_bc=True)
+    inp = m3synth.scan_inputs(shape, seed=100 + L)
+    y, fs = _gpu_scan(inp, shape)
+    y_ref, fs_ref = _oracle(orc, inp)
+    if bf16:
+        assert_bf16(y, y_ref, "y")
+        assert_bf16(fs, fs_ref, "final_state")
+    else:
+        assert_f32(y, y_ref, "y")
+        assert_f32(fs, fs_ref, "final_state")
+
+
+def test_no_bias_and_zero_length(orc):
+    shape = m3synth.ScanShape(1, 20, 2, 1, 8, 8, R=1, chunk=8, bf16=False, rms_bc=False)
+    inp = m3synth.scan_inputs(shape, seed=3)
+    inp["B_bias"][:] = 0
+    inp["C_bias"][:] = 0
+    d = to_device(inp, False)
+    out, fs = m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"],
+                             R=1, chunk=8)
+    y_ref, fs_ref = _oracle(orc, inp)
+    assert_f32(out.cpu().numpy(), y_ref, "y")
+    # L = 0: final state is zero, nothing else is written
+    z = {k: v[:, :0] if k in ("x", "dt", "lam", "B", "C", "theta") else v for k, v in d.items()}
+    fs0 = torch.full((1, 2, 8, 8), 7.0, device="cuda")
+    m3.m3_scan_fwd(z["x"], z["dt"], z["A"], z["lam"], z["B"], z["C"], z["theta"], R=1, chunk=8,
+                   final_state=fs0)
+    torch.cuda.synchronize()
+    assert float(fs0.abs().max()) == 0.0
+
+
+def _sampled(orc, inp, y, fs, pairs, check):
+    for (b, h) in pairs:
+        sub = head_slice(inp, b, h)
+        y_ref, fs_ref = _oracle(orc, sub)
+        check(y[b:b + 1, :, h:h + 1], y_ref, "y[b=%d,h=%d]" % (b, h))
+        check(fs[b:b + 1, h:h + 1], fs_ref, "state[b=%d,h=%d]" % (b, h))
+
+
+def _pairs(shape, n, seed):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(shape.batch)), int(rng.integers(shape.heads))) for _ in range(n)]
+
+
+def test_prefill_siso_1p5b_fp32_sampled(orc):
+    shape = m3synth.ScanShape(8, 2048, 32, 1, 64, 128, R=1, chunk=64, bf16=False)
+    inp = m3synth.scan_inputs(shape, seed=1)
+    y, fs = _gpu_scan(inp, shape)
+    _sampled(orc, inp, y, fs, _pairs(shape, 4, 11), assert_f32)
+
+
+# ---------------------------------------------------------------- bf16 mode
+@pytest.mark.parametrize("name", ["prefill_siso", "prefill_mimo"])
+def test_prefill_1p5b_bf16_sampled(orc, name):
+    idx, shape = m3synth.WORKLOADS[name]
+    inp = m3synth.scan_inputs(shape, seed=idx)
+    y, fs = _gpu_scan(inp, shape)
+    _sampled(orc, inp, y, fs, _pairs(shape, 4, 12), assert_bf16)
+
+
+@pytest.mark.parametrize("name", ["long_siso_n64", "long_siso_n128", "long_mimo_n128"])
+def test_long_context_bf16_sampled(orc, name):
+    idx, shape = m3synth.WORKLOADS[name]
+    inp = m3synth.scan_inputs(shape, seed=idx)
+    y, fs = _gpu_scan(inp, shape)
+    _sampled(orc, inp, y, fs, _pairs(shape, 2, 13), assert_bf16)
+
+
+def test_long_context_parity_signs(orc):
+    """A = 0 and theta = pi*bit/dt: the output's sign carries the running parity."""
+    idx, shape = m3synth.WORKLOADS["long_siso_n128"]
+    inp = m3synth.scan_inputs(shape, seed=idx, parity=True)
+    y, fs = _gpu_scan(inp, shape)
+    for (b, h) in _pairs(shape, 2, 14):
+        sub = head_slice(inp, b, h)
+        y_ref, _ = _oracle(orc, sub)
+        got = y[b:b + 1, :, h:h + 1]
+        assert max_over_rms(got, y_ref) <= 2e-2
+        rms = np.sqrt(np.mean(y_ref ** 2))
+        big = np.abs(y_ref) > 1e-2 * rms
+        assert big.mean() > 0.5
+        assert np.array_equal(np.sign(got[big]), np.sign(y_ref[big]))
+
+
+# ---------------------------------------------------------------- decode
+@pytest.mark.parametrize("R", [1, 2, 4])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_decode_steps(orc, R, bf16):
+    shape = m3synth.ScanShape(4, 1, 8, 2, 64, 128, R=R, chunk=1, bf16=bf16)
+    steps = [m3synth.decode_inputs(shape, seed=30 + R, step=i) for i in range(5)]
+    b, H, N, P = shape.batch, shape.heads, shape.dstate, shape.headdim
+    st_ref = np.random.default_rng(5).standard_normal((b, H, N, P))
+    st = torch.from_numpy(st_ref.astype(np.float32)).cuda()
+    st_ref = st.cpu().numpy().astype(np.float64)
+    prev = None
+    for i, s in enumerate(steps):
+        d = to_device(s, bf16)
+        kw = {}
+        if prev is not None:
+            kw = dict(B_prev=prev["B"], x_prev=prev["x"])
+        out = m3.m3_decode_step(st, d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"],
+                                R=R, B_bias=d["B_bias"], C_bias=d["C_bias"], **kw)
+        okw = {}
+        if prev is not None:
+            okw = dict(B_prev=steps[i - 1]["B"], x_prev=steps[i - 1]["x"])
+        y_ref, st_ref = orc.decode_step(st_ref, s["x"], s["dt"], s["A"], s["lam"], s["B"], s["C"],
+                                        s["theta"], B_bias=s["B_bias"], C_bias=s["C_bias"], **okw)
+        torch.cuda.synchronize()
+        chk = assert_bf16 if bf16 else assert_f32
+        chk(out.float().cpu().numpy(), y_ref, "y step %d" % i)
+        prev = d
+    chk(st.cpu().numpy(), st_ref, "state")
+
+
+def test_decode_full_batch_shape(orc):
+    """The 128 x 32 decode batch, SISO, bf16: two steps from a nonzero state."""
+    shape = m3synth.DECODE_SISO
+    b, H, N, P = shape.batch, shape.heads, shape.dstate, shape.headdim
+    st0 = (0.1 * np.random.default_rng(8).standard_normal((b, H, N, P))).astype(np.float32)
+    st = torch.from_numpy(st0).cuda()
+    s0 = m3synth.decode_inputs(shape, seed=3, step=0)
+    s1 = m3synth.decode_inputs(shape, seed=3, step=1)
+    d0, d1 = to_device(s0, True), to_device(s1, True)
+    m3.m3_decode_step(st, d0["x"], d0["dt"], d0["A"], d0["lam"], d0["B"], d0["C"], d0["theta"],
+                      R=1, B_bias=d0["B_bias"], C_bias=d0["C_bias"])
+    out = m3.m3_decode_step(st, d1["x"], d1["dt"], d1["A"], d1["lam"], d1["B"], d1["C"],
+                            d1["theta"], R=1, B_prev=d0["B"], x_prev=d0["x"],
+                            B_bias=d1["B_bias"], C_bias=d1["C_bias"])
+    _, r0 = orc.decode_step(st0, s0["x"], s0["dt"], s0["A"], s0["lam"], s0["B"], s0["C"],
+                            s0["theta"], B_bias=s0["B_bias"], C_bias=s0["C_bias"])
+    y1, r1 = orc.decode_step(r0, s1["x"], s1["dt"], s1["A"], s1["lam"], s1["B"], s1["C"],
+                             s1["theta"], B_prev=s0["B"], x_prev=s0["x"], B_bias=s1["B_bias"],
+                             C_bias=s1["C_bias"])
+    torch.cuda.synchronize()
+    assert_bf16(out.float().cpu().numpy(), y1, "y")
+    assert_bf16(st.cpu().numpy(), r1, "state")
+
+
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_prefill_then_decode_matches_longer_prefill(orc, bf16):
+    shape = m3synth.ScanShape(2, 33, 4, 1, 64, 128, R=1, chunk=16, bf16=bf16)
+    inp = m3synth.scan_inputs(shape, seed=21)
+    d = to_device(inp, bf16)
+    L = 32
+    cut = {k: (v[:, :L].contiguous() if k in ("x", "dt", "lam", "B", "C", "theta") else v)
+           for k, v in d.items()}
+    _, fs = m3.m3_scan_fwd(cut["x"], cut["dt"], cut["A"], cut["lam"], cut["B"], cut["C"],
+                           cut["theta"], R=1, chunk=16, B_bias=d["B_bias"], C_bias=d["C_bias"])
+    y1 = m3.m3_decode_step(fs, d["x"][:, L].contiguous(), d["dt"][:, L].contiguous(), d["A"],
+                           d["lam"][:, L].contiguous(), d["B"][:, L].contiguous(),
+                           d["C"][:, L].contiguous(), d["theta"][:, L].contiguous(), R=1,
+                           B_prev=d["B"][:, L - 1].contiguous(),
+                           x_prev=d["x"][:, L - 1].contiguous(),
+                           B_bias=d["B_bias"], C_bias=d["C_bias"])
+    y_ref, fs_ref = _oracle(orc, inp)
+    torch.cuda.synchronize()
+    chk = assert_bf16 if bf16 else assert_f32
+    chk(y1.float().cpu().numpy(), y_ref[:, L], "decoded token")
+    chk(fs.cpu().numpy(), fs_ref, "state after decode")

@@ -6,6 +6,12 @@ Tolerances (stated once, used by every parity test):
   bf16 mode   max |error|        <= 2e-2 * RMS(oracle output)
 Both follow from the scan's precision contract: fp32 inputs with fp32
 arithmetic, or bf16 inputs with fp32 state and accumulation.
+
+An output stored in bf16 also carries its own storage rounding, up to half a
+bf16 ulp (2^-8 |y|) per element, which no kernel can avoid; for bf16-stored
+outputs the tolerance above is applied to what is left after that bound:
+  max_i ( |got_i - ref_i| - 2^-8 |ref_i| ) <= 2e-2 * RMS(ref).
+fp32 outputs (the final state) get the plain bound.
 """
 import numpy as np
 
@@ -58,6 +64,25 @@ def assert_f32(got, ref, what=""):
     assert e <= F32_REL_L2, "%s: relative L2 error %.3e > %.1e" % (what, e, F32_REL_L2)
 
 
+BF16_HALF_ULP = 2.0 ** -8
+
+
+def max_over_rms_bf16_stored(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    excess = np.abs(got - ref) - BF16_HALF_ULP * np.abs(ref)
+    return float(np.max(excess) / max(rms, 1e-300))
+
+
 def assert_bf16(got, ref, what=""):
+    """fp32-stored result of a bf16-input computation."""
     e = max_over_rms(got, ref)
     assert e <= BF16_MAX_OVER_RMS, "%s: max|err|/RMS %.3e > %.1e" % (what, e, BF16_MAX_OVER_RMS)
+
+
+def assert_bf16_out(got, ref, what=""):
+    """bf16-stored output: the tolerance applies beyond the storage rounding."""
+    e = max_over_rms_bf16_stored(got, ref)
+    assert e <= BF16_MAX_OVER_RMS, "%s: max(|err| - 2^-8|y|)/RMS %.3e > %.1e" % (
+        what, e, BF16_MAX_OVER_RMS)

@@ -9,7 +9,8 @@ import numpy as np
 import pytest
 
 import m3synth
-from gpu_util import assert_bf16, assert_f32, head_slice, max_over_rms, to_device
+from gpu_util import (assert_bf16, assert_bf16_out, assert_f32, head_slice,
+                      max_over_rms_bf16_stored, to_device)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -72,7 +73,7 @@ def test_small_shapes(orc, case, bf16):
     y, fs = _gpu_scan(inp, shape)
     y_ref, fs_ref = _oracle(orc, inp)
     if bf16:
-        assert_bf16(y, y_ref, "y")
+        assert_bf16_out(y, y_ref, "y")
         assert_bf16(fs, fs_ref, "final_state")
     else:
         assert_f32(y, y_ref, "y")
@@ -98,12 +99,12 @@ def test_no_bias_and_zero_length(orc):
     assert float(fs0.abs().max()) == 0.0
 
 
-def _sampled(orc, inp, y, fs, pairs, check):
+def _sampled(orc, inp, y, fs, pairs, check_y, check_state):
     for (b, h) in pairs:
         sub = head_slice(inp, b, h)
         y_ref, fs_ref = _oracle(orc, sub)
-        check(y[b:b + 1, :, h:h + 1], y_ref, "y[b=%d,h=%d]" % (b, h))
-        check(fs[b:b + 1, h:h + 1], fs_ref, "state[b=%d,h=%d]" % (b, h))
+        check_y(y[b:b + 1, :, h:h + 1], y_ref, "y[b=%d,h=%d]" % (b, h))
+        check_state(fs[b:b + 1, h:h + 1], fs_ref, "state[b=%d,h=%d]" % (b, h))
 
 
 def _pairs(shape, n, seed):
@@ -115,7 +116,7 @@ def test_prefill_siso_1p5b_fp32_sampled(orc):
     shape = m3synth.ScanShape(8, 2048, 32, 1, 64, 128, R=1, chunk=64, bf16=False)
     inp = m3synth.scan_inputs(shape, seed=1)
     y, fs = _gpu_scan(inp, shape)
-    _sampled(orc, inp, y, fs, _pairs(shape, 4, 11), assert_f32)
+    _sampled(orc, inp, y, fs, _pairs(shape, 4, 11), assert_f32, assert_f32)
 
 
 # ---------------------------------------------------------------- bf16 mode
@@ -124,7 +125,7 @@ def test_prefill_1p5b_bf16_sampled(orc, name):
     idx, shape = m3synth.WORKLOADS[name]
     inp = m3synth.scan_inputs(shape, seed=idx)
     y, fs = _gpu_scan(inp, shape)
-    _sampled(orc, inp, y, fs, _pairs(shape, 4, 12), assert_bf16)
+    _sampled(orc, inp, y, fs, _pairs(shape, 4, 12), assert_bf16_out, assert_bf16)
 
 
 @pytest.mark.parametrize("name", ["long_siso_n64", "long_siso_n128", "long_mimo_n128"])
@@ -132,7 +133,7 @@ def test_long_context_bf16_sampled(orc, name):
     idx, shape = m3synth.WORKLOADS[name]
     inp = m3synth.scan_inputs(shape, seed=idx)
     y, fs = _gpu_scan(inp, shape)
-    _sampled(orc, inp, y, fs, _pairs(shape, 2, 13), assert_bf16)
+    _sampled(orc, inp, y, fs, _pairs(shape, 2, 13), assert_bf16_out, assert_bf16)
 
 
 def test_long_context_parity_signs(orc):
@@ -144,7 +145,7 @@ def test_long_context_parity_signs(orc):
         sub = head_slice(inp, b, h)
         y_ref, _ = _oracle(orc, sub)
         got = y[b:b + 1, :, h:h + 1]
-        assert max_over_rms(got, y_ref) <= 2e-2
+        assert max_over_rms_bf16_stored(got, y_ref) <= 2e-2
         rms = np.sqrt(np.mean(y_ref ** 2))
         big = np.abs(y_ref) > 1e-2 * rms
         assert big.mean() > 0.5
@@ -175,10 +176,10 @@ def test_decode_steps(orc, R, bf16):
         y_ref, st_ref = orc.decode_step(st_ref, s["x"], s["dt"], s["A"], s["lam"], s["B"], s["C"],
                                         s["theta"], B_bias=s["B_bias"], C_bias=s["C_bias"], **okw)
         torch.cuda.synchronize()
-        chk = assert_bf16 if bf16 else assert_f32
-        chk(out.float().cpu().numpy(), y_ref, "y step %d" % i)
+        chk_y = assert_bf16_out if bf16 else assert_f32
+        chk_y(out.float().cpu().numpy(), y_ref, "y step %d" % i)
         prev = d
-    chk(st.cpu().numpy(), st_ref, "state")
+    (assert_bf16 if bf16 else assert_f32)(st.cpu().numpy(), st_ref, "state")
 
 
 def test_decode_full_batch_shape(orc):
@@ -201,7 +202,7 @@ def test_decode_full_batch_shape(orc):
                              s1["theta"], B_prev=s0["B"], x_prev=s0["x"], B_bias=s1["B_bias"],
                              C_bias=s1["C_bias"])
     torch.cuda.synchronize()
-    assert_bf16(out.float().cpu().numpy(), y1, "y")
+    assert_bf16_out(out.float().cpu().numpy(), y1, "y")
     assert_bf16(st.cpu().numpy(), r1, "state")
 
 
@@ -223,6 +224,6 @@ def test_prefill_then_decode_matches_longer_prefill(orc, bf16):
                            B_bias=d["B_bias"], C_bias=d["C_bias"])
     y_ref, fs_ref = _oracle(orc, inp)
     torch.cuda.synchronize()
-    chk = assert_bf16 if bf16 else assert_f32
-    chk(y1.float().cpu().numpy(), y_ref[:, L], "decoded token")
-    chk(fs.cpu().numpy(), fs_ref, "state after decode")
+    (assert_bf16_out if bf16 else assert_f32)(y1.float().cpu().numpy(), y_ref[:, L],
+                                              "decoded token")
+    (assert_bf16 if bf16 else assert_f32)(fs.cpu().numpy(), fs_ref, "state after decode")

@@ -115,7 +115,11 @@ m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const floa
   if ((int64_t)chunk * R > 4096 || chunk > 4096) return M3_ERR_UNSUPPORTED;
 
   const bool bf16 = dims->act_dtype == M3_BF16;
-  const bool use_tc = bf16 && m3::scan_tc_supported(N, P, R, chunk);
+  // The tensor-core path moves tiles with TMA and 128-bit accesses: it takes
+  // 16-byte-aligned activations and final state; other calls use the CUDA cores.
+  const bool use_tc = bf16 && m3::scan_tc_supported(N, P, R, chunk) && aligned(x, 16) &&
+                      aligned(out, 16) && aligned(B, 16) && aligned(C, 16) &&
+                      (final_state == nullptr || aligned(final_state, 16));
   if (!use_tc) {
     const size_t smem = m3::scan_simt_smem_bytes(N, P, R, chunk);
     if (smem > 227 * 1024) return M3_ERR_UNSUPPORTED;

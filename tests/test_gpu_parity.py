@@ -64,6 +64,33 @@ SMALL_CASES = [
 ]
 
 
+# Shapes of the tensor-core path (bf16, P = 64, chunk * R = 64): every MIMO
+# rank, both state sizes, grouped B/C, ragged tails, a single partial chunk.
+TC_CASES = [
+    # L, chunk, R, G, H, N, P
+    (200, 64, 1, 1, 2, 128, 64),
+    (77, 64, 1, 2, 4, 64, 64),
+    (150, 32, 2, 1, 2, 128, 64),
+    (97, 32, 2, 2, 4, 64, 64),
+    (83, 16, 4, 2, 4, 128, 64),
+    (64, 16, 4, 1, 2, 64, 64),
+    (40, 64, 1, 1, 2, 128, 64),    # shorter than one chunk
+    (1, 16, 4, 1, 2, 128, 64),     # one token
+    (1000, 64, 1, 1, 2, 128, 64),  # many chunks: state carried 16 times
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: "L%d_Q%d_R%d_G%d_H%d_N%d_P%d" % c)
+def test_tensor_core_shapes_bf16(orc, case):
+    L, Q, R, G, H, N, P = case
+    shape = m3synth.ScanShape(2, L, H, G, P, N, R=R, chunk=Q, bf16=True, rms_bc=True)
+    inp = m3synth.scan_inputs(shape, seed=300 + L + R)
+    y, fs = _gpu_scan(inp, shape)
+    y_ref, fs_ref = _oracle(orc, inp)
+    assert_bf16_out(y, y_ref, "y")
+    assert_bf16(fs, fs_ref, "final_state")
+
+
 @pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: "L%d_Q%d_R%d_G%d_H%d_N%d_P%d" % c)
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 def test_small_shapes(orc, case, bf16):

@@ -257,7 +257,13 @@ def run_ours(args, rank, world, local_rank):
     peaks = _peaks()
     stream = torch.cuda.current_stream()
 
-    idx, shape = m3synth.WORKLOADS["prefill_siso"]
+    if args.only in ("decode_siso", "decode_mimo"):
+        if rank == 0:
+            print(json.dumps(bench_decode(torch, m3, dev, args.only, peaks,
+                                          steps=args.decode_steps)), flush=True)
+        return
+    name = args.only if args.only in ("prefill_siso", "prefill_mimo") else "prefill_siso"
+    idx, shape = m3synth.WORKLOADS[name]
     inp = m3synth.scan_inputs(shape, seed=idx + 1000 * rank)
     d = to_device(inp, True, dev)
     out = torch.empty_like(d["x"])
@@ -311,7 +317,9 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "prefill_siso b8 L2048 H32 P64 N128 G1 R1 chunk64",
+        "config": {"workload": "%s b%d L%d H%d P%d N%d G%d R%d chunk%d" % (
+                       name, shape.batch, shape.seqlen, shape.heads, shape.headdim,
+                       shape.dstate, shape.groups, shape.R, shape.chunk),
                    "global_batch": shape.batch * world, "seq_len": shape.seqlen,
                    "parallelism": "independent replicas" if world > 1 else "single GPU",
                    "l2": "flushed before every timed launch (256 MiB write)",
@@ -329,6 +337,10 @@ def run_ours(args, rank, world, local_rank):
     }
     del flush
     torch.cuda.empty_cache()
+    if args.only != "all":
+        # a single workload (used for profiling): no side benchmarks
+        print(json.dumps(line), flush=True)
+        return
     line["prefill_mimo"] = bench_prefill_other(torch, m3, dev, "prefill_mimo", args, peaks)
     line["decode"] = {"siso": bench_decode(torch, m3, dev, "decode_siso", peaks),
                       "mimo_r4": bench_decode(torch, m3, dev, "decode_mimo", peaks)}
@@ -473,6 +485,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="all",
+                    choices=["all", "prefill_siso", "prefill_mimo", "decode_siso", "decode_mimo"],
+                    help="run one workload alone (profiling); the default runs them all")
+    ap.add_argument("--decode-steps", type=int, default=m3synth.DECODE_STEPS,
+                    help="decode steps per CUDA graph with --only decode_*")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     rank = int(os.environ.get("RANK", "0"))

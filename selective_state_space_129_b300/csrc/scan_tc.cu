@@ -28,27 +28,35 @@
 // the score matrix sums products much larger than y itself (|B|^2 = N for
 // RMS-normalised B). Their operand tiles (Bt, Ct, w X and the state copy) are
 // therefore fp16 (11-bit significand, kind::f16 MMA with fp32 accumulation),
-// each scaled by a power of two chosen per chunk from a block-wide bound of
-// its magnitude, so fp16's range never limits the inputs. The scales are undone
+// each scaled by a power of two chosen per chunk from a bound of its
+// magnitude, so fp16's range never limits the inputs. The scales are undone
 // exactly where a per-element factor is applied anyway (mask, state update,
 // output). P is split into bf16 high and low parts so that P X (X is an exact
-// bf16 input) keeps ~16 significant bits.
+// bf16 input) keeps ~16 significant bits. The cumulative angle is carried
+// from chunk to chunk as a float-float pair fed by Kahan-compensated sums, so
+// it does not drift over long sequences.
 //
-// One CTA (256 threads, two CTAs per SM) walks one (b, h) sequence chunk by
-// chunk. Per chunk:
-//   phase 0  warp 0: decay scan, trapezoid weights (warp shuffles)
-//   phase 1  all: cumulative angles (per-thread prefix + cross-thread carry),
-//            sincos, rotate B/C (+bias) into fp16 UMMA tiles; build w X
-//   phase 2  one thread: S, D = Bt^T (w X), Yoff = Ct H_in    (tcgen05.mma)
-//   phase 3  all: mask S -> P (bf16 hi + lo); H = exp(Lam_end) H + D
-//   phase 4  one thread: Y = P X                               (tcgen05.mma)
-//   phase 5  all: y = Y + exp(Lam_t) Yoff -> bf16 -> TMA store; fp16 state copy
-// Operand tiles are 128-byte-swizzled rows of 64 16-bit elements; a
-// [rows][64k] tile is at once the K-major operand along its columns and the
-// MN-major operand along its rows, so Bt serves both S (K = N) and the state
-// GEMM (K = tokens).
+// Organisation: a persistent, warp-specialised CTA (384 threads, one per SM)
+// walks whole (b, h) sequences, chunk by chunk, as a software pipeline:
+//   warps 0-7    prologue: decay scan, angles, RoPE fold of B/C into fp16
+//                UMMA tiles, w X, into one of two operand slots per chunk;
+//                its thread 0 also issues the TMA of the next chunk's raw B,
+//                C, theta, x tiles (one raw slot), one warp prefetches the
+//                next chunk's dt, lambda
+//   warps 8-11   core: mask S -> P, state H = exp(Lam_end) H + D and its fp16
+//                copy, y = Y + exp(Lam_t) Yoff -> TMA store, final state; its
+//                thread 0 issues the MMAs: Y = P X for chunk c, then
+//                S, D = Bt^T (w X), Yoff = Ct H for chunk c+1 into the other
+//                of two TMEM accumulator sets, overlapping chunk c's epilogue
+// so the prologue of chunk c+1 runs while the core finishes chunk c. Roles
+// hand off through mbarriers; a role synchronises internally with its own
+// named barrier. Operand tiles are 128-byte-swizzled rows of 64 16-bit
+// elements; a [rows][64k] tile is at once the K-major operand along its
+// columns and the MN-major operand along its rows, so Bt serves both S (K = N)
+// and the state GEMM (K = tokens).
 // Every mbarrier wait is bounded; on expiry the CTA records the status word,
-// stops issuing work and still frees its tensor memory.
+// every role leaves its loop at the next chunk boundary, and the CTA still
+// frees its tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -61,11 +69,16 @@
 namespace m3 {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kProWarps = 8, kCoreWarps = 4;
+constexpr int kProThreads = kProWarps * 32;    // 256
+constexpr int kCoreThreads = kCoreWarps * 32;  // 128
+constexpr int kThreads = kProThreads + kCoreThreads;  // 384 (168 registers per thread)
+constexpr int kWarpTmem = kProWarps;                  // allocates / frees TMEM
+constexpr uint32_t kBarPro = 1, kBarCore = 2;          // named barrier ids
 constexpr int kQR = 64;  // rows of the flattened (token, rank) tile
 constexpr int kP = 64;   // head dim of the tensor-core path
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemSlot = 256;          // columns per accumulator set
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 constexpr uint32_t kTileBytes = 64 * 128;    // 64 rows x 128 B
 constexpr float kLog2e = 1.4426950408889634f;
@@ -75,44 +88,71 @@ constexpr float kInvTwoPi = 0.15915494309189535f;
 constexpr float kPi2a = 6.28125f;
 constexpr float kPi2b = 1.9353071795864769e-3f;
 constexpr float kPi2c = 1.0253131677e-11f;
+// sin.approx / cos.approx keep their accuracy for arguments up to 100 pi;
+// angles beyond this bound are reduced first.
+constexpr float kAngleDirect = 300.f;
 
-// TMEM column offsets of the four fp32 accumulators.
+// TMEM column offsets of the four fp32 accumulators within a set.
 constexpr uint32_t kColS = 0, kColD = 64, kColY = 128, kColYo = 192;
+
+constexpr uint32_t align1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 
 template <int R, int NS>
 struct Cfg {
-  static constexpr int Q = kQR / R;         // tokens per chunk
-  static constexpr int KP = NS / 2;         // rotating state pairs
-  static constexpr int TG = kThreads / KP;  // token groups in the angle phase
-  static constexpr int TPG = Q / TG;        // tokens per thread in the angle phase
-  static_assert(Q % TG == 0, "token groups must divide the chunk");
-  static constexpr int HR = NS * kP / kThreads;  // fp32 state values per thread
-  // byte offsets in dynamic shared memory (1024-aligned base)
-  static constexpr uint32_t kBt = 0;                          // [64][NS] fp16
-  static constexpr uint32_t kCt = kBt + 64 * NS * 2;          // [64][NS] fp16
-  static constexpr uint32_t kXs = kCt + 64 * NS * 2;          // 2 TMA stages of x
-  static constexpr uint32_t kXb = kXs + 2 * kTileBytes;       // X re-laid (R > 1), bf16
-  static constexpr uint32_t kXw = kXb + kTileBytes;           // w-scaled X, fp16
-  static constexpr uint32_t kPh = kXw + kTileBytes;           // masked scores, bf16 high
-  static constexpr uint32_t kPl = kPh + kTileBytes;           // masked scores, bf16 low
-  static constexpr uint32_t kH = kPl + kTileBytes;            // [NS][64] fp16 state copy
-  static constexpr uint32_t kYs = kH + NS * 128;              // output staging
+  static constexpr int Q = kQR / R;          // tokens per chunk
+  static constexpr int KP = NS / 2;          // rotating state pairs
+  static constexpr int KP2 = KP / 2;         // pair-pairs: a prologue thread owns two pairs
+  static constexpr int TG = kProThreads / KP2;  // token groups in the prologue
+  static constexpr int TPG = Q / TG;         // tokens per prologue thread
+  static_assert(TPG >= 1 && Q % TG == 0, "token groups must divide the chunk");
+  static constexpr int HR = NS * kP / kCoreThreads;  // fp32 state values per core thread
+  static constexpr int BW = 2 * R;           // raw 32-bit words of B (or C) per token and thread
+  // raw slot (TMA destination): B, C [Q][NS*R] bf16, theta [Q][KP] fp32, x [Q][P*R] bf16
+  static constexpr uint32_t kRawB = 0;
+  static constexpr uint32_t kRawC = kRawB + Q * NS * R * 2;
+  static constexpr uint32_t kRawTh = kRawC + Q * NS * R * 2;
+  static constexpr uint32_t kRawX = align1k(kRawTh + Q * KP * 4);  // 128B-swizzled for R = 1
+  static constexpr uint32_t kRawBytes = kRawX + (uint32_t)(Q * kP * R * 2);
+  // two operand slots: Bt, Ct [64][NS] fp16, w X [64][64] fp16, X [64][64] bf16
+  static constexpr uint32_t kOpBt = 0;
+  static constexpr uint32_t kOpCt = 64 * NS * 2;
+  static constexpr uint32_t kOpXw = 2 * 64 * NS * 2;
+  static constexpr uint32_t kOpXo = kOpXw + kTileBytes;
+  static constexpr uint32_t kOpBytes = kOpXo + kTileBytes;
+  static constexpr uint32_t kOp0 = align1k(kRawBytes);
+  // core tiles: P high / low (bf16), fp16 state copy [NS][64], output staging
+  static constexpr uint32_t kPh = kOp0 + 2 * kOpBytes;
+  static constexpr uint32_t kPl = kPh + kTileBytes;
+  static constexpr uint32_t kH = kPl + kTileBytes;
+  static constexpr uint32_t kYs = kH + NS * 128;
   static constexpr uint32_t kBytes = kYs + kTileBytes;
-  static constexpr uint32_t kSmem = kBytes + 1024;            // + alignment slack
+  static constexpr uint32_t kSmem = kBytes + 1024;  // + alignment slack
+  // bytes landing on the raw barrier per chunk
+  static constexpr uint32_t kTxBytes =
+      2u * Q * NS * R * 2 + (uint32_t)(Q * KP * 4) + (uint32_t)(Q * kP * R * 2);
+};
+
+// Per-chunk scalars handed from the prologue to the core (one set per slot).
+template <int KP>
+struct SlotScalars {
+  float lam2[64];  // Lam_t in log2 units
+  float gam[64];   // gamma_t
+  float wp[64];    // gamma_t + bhat_{t+1}
+  float eL[64];    // exp(Lam_t)
+  float wend[64];  // exp(Lam_end - Lam_t) (gamma_t + bhat_{t+1})
+  float fang[KP];  // cumulative angle after the chunk (last chunk of a sequence)
+  float eLend, wmax, invB, invC, invX, pad[3];
 };
 
 struct TcParams {
   const float* dt;
   const float* A;
   const float* lam;
-  const __nv_bfloat16* B;
-  const __nv_bfloat16* C;
-  const float* theta;
   const float* B_bias;
   const float* C_bias;
   float* final_state;
   unsigned int* status;
-  int64_t L, H, G;
+  int64_t L, H, G, batch;
   int nchunks;
 };
 
@@ -134,7 +174,12 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-// Largest magnitude of the two bf16 values of a word, as a float.
+// element e of a run of bf16 values packed two per word (little-endian)
+template <int N>
+__device__ __forceinline__ float bf_at(const uint32_t (&w)[N], int e) {
+  return (e & 1) ? bf_hi(w[e >> 1]) : bf_lo(w[e >> 1]);
+}
+// largest magnitude held in an accumulator of bf16x2 abs-maxima, as a float
 __device__ __forceinline__ float bf_absmax(uint32_t w) {
   const uint32_t a = w & 0x7fff7fffu;
   return fmaxf(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
@@ -146,6 +191,44 @@ __device__ __forceinline__ void pow2_scale(float M, float* sigma, float* inv) {
   e = e < -100 ? -100 : (e > 127 ? 127 : e);
   *sigma = __uint_as_float((uint32_t)(127 + 14 - e) << 23);
   *inv = __uint_as_float((uint32_t)(127 - 14 + e) << 23);
+}
+
+// Packed fp32 pair arithmetic (sm_100 family), elementwise on (x, y).
+__device__ __forceinline__ uint64_t f2_pack(float2 a) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t r) {
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(r));
+  return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
+  return f2_unpack(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(d);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Float-float addition (Knuth's TwoSum, then a renormalising Fast2Sum):
@@ -167,6 +250,12 @@ __device__ __forceinline__ void ff_wrap(float& ah, float& al) {
   ah = h + l;
   al = l - (ah - h);
 }
+// Reduce an fp32 angle to about [-pi, pi].
+__device__ __forceinline__ float wrap_rad(float a) {
+  const float k = rintf(a * kInvTwoPi);
+  a = fmaf(-k, kPi2a, a);
+  return fmaf(-k, kPi2b, a);
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -178,9 +267,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
-}
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
   asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
@@ -196,6 +282,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
 
 // Shared-memory operand descriptors of the 128-byte-swizzled tiles.
 // K-major: 16-element K step kk of a [rows][K] tile.
@@ -209,8 +300,8 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk, uint32_t lbo)
   return ptx::smem_desc_sw128(base + (uint32_t)kk * 2048u, lbo, 1024u);
 }
 
-// Wait on an mbarrier phase; on expiry record the status word and the CTA's
-// abort flag. Returns false once the CTA is aborting.
+// Bounded wait on an mbarrier phase; on expiry record the status word and the
+// CTA's abort flag. Returns false if the CTA is (now) aborting.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag,
                                               unsigned int* status) {
   if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
@@ -220,581 +311,772 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
   return false;
 }
 
+// Position of a CTA in its schedule: sequences blockIdx.x, +gridDim.x, ...,
+// each walked chunk by chunk; g counts the CTA's chunks (slots and mbarrier
+// phases follow it).
+struct Sched {
+  int64_t seq;
+  int c;
+  __device__ __forceinline__ bool next(int64_t nseq, int nC) {
+    if (++c < nC) return true;
+    c = 0;
+    seq += gridDim.x;
+    return seq < nseq;
+  }
+};
+
+// Raw decay inputs of a chunk's tokens: dt, lambda of the token and of its
+// successor (zero past the end of the sequence); lane handles tokens lane and
+// lane + 32. Only loads: the arithmetic waits until the values are needed, so
+// that the load latency overlaps other work.
+struct DecayRaw {
+  float dt[2], lam[2], dtn[2], lamn[2];
+};
+__device__ __forceinline__ void load_decay_raw(const TcParams& p, int64_t b, int64_t h, int64_t t0,
+                                               int Q, int lane, DecayRaw& d) {
+  const int64_t L = p.L, H = p.H;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int i = lane + 32 * j;
+    const int64_t t = t0 + i;
+    const bool in = i < Q && t < L, inn = i < Q && t + 1 < L;
+    d.dt[j] = in ? p.dt[(b * L + t) * H + h] : 0.f;
+    d.lam[j] = in ? p.lam[(b * L + t) * H + h] : 0.f;
+    d.dtn[j] = inn ? p.dt[(b * L + t + 1) * H + h] : 0.f;
+    d.lamn[j] = inn ? p.lam[(b * L + t + 1) * H + h] : 1.f;
+  }
+}
+// dt, lambda and bhat of the successor into the chunk's decay-input buffer
+__device__ __forceinline__ void store_decay(const DecayRaw& d, int lane, float* sdt, float* slam,
+                                            float* sbn) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    sdt[lane + 32 * j] = d.dt[j];
+    slam[lane + 32 * j] = d.lam[j];
+    sbn[lane + 32 * j] = (1.f - d.lamn[j]) * d.dtn[j];
+  }
+}
+
 template <int R, int NS>
-__global__ void __launch_bounds__(kThreads, 2)
-    scan_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+__global__ void __launch_bounds__(kThreads, 1)
+    scan_tc_kernel(const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
+                   const __grid_constant__ CUtensorMap tm_th, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_y, TcParams p) {
   using K = Cfg<R, NS>;
-  constexpr int Q = K::Q, KP = K::KP, TG = K::TG, TPG = K::TPG, HR = K::HR;
+  constexpr int Q = K::Q, KP = K::KP, KP2 = K::KP2, TG = K::TG, TPG = K::TPG, HR = K::HR;
+  constexpr uint32_t kIdS = ptx::idesc_f16_f32(64, 64, false, false);
+  constexpr uint32_t kIdD = ptx::idesc_f16_f32(NS, 64, true, true);
+  constexpr uint32_t kIdYo = ptx::idesc_f16_f32(64, 64, false, true);
+  constexpr uint32_t kIdY = ptx::idesc_bf16_f32(64, 64, false, true);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
 
-  __shared__ uint64_t bar_x[2], bar_m1, bar_m3;
+  __shared__ uint64_t bar_raw_full;
+  __shared__ uint64_t bar_op_full[2], bar_slot_free[2], bar_acc_full[2], bar_y_full[2];
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
-  __shared__ float s_lam2[64], s_gam[64], s_wp[64], s_wend[64], s_eL[64], s_dt[64];
-  __shared__ float s_tot[2][TG][KP];    // per token group: angle total (hi, lo)
-  __shared__ float s_carry[2][2][KP];   // [parity][hi, lo][pair]: angle before the chunk
-  __shared__ float s_eLend, s_wmax;
-  __shared__ float s_red[3][kWarps];   // per-warp maxima: |B|, |C|, |x|
-  __shared__ float s_hred[kWarps];     // per-warp maxima of |H|
-  __shared__ float s_bias_red[2][kWarps];
+  __shared__ int s_go[2];  // per-role broadcast of "continue" decisions
+  __shared__ SlotScalars<KP> ss[2];
+  __shared__ float s_dtraw[2][64], s_lamraw[2][64], s_bnx[2][64];
+  __shared__ float s_tot[2][TG][KP];   // per token group: angle total (hi, lo)
+  __shared__ float s_carry[2][2][KP];  // [chunk parity][hi, lo][pair]
+  __shared__ float s_red[3][kProWarps];
+  __shared__ float s_hred[kCoreWarps];
+  __shared__ float s_bias_red[2][kProWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t H = p.H, L = p.L, G = p.G;
-  const int64_t bh = blockIdx.x, b = bh / H, h = bh % H, g = h / (H / G);
-  const float A_h = p.A[h];
+  const int64_t H = p.H, G = p.G;
+  const int64_t nseq = p.batch * H;
   const int nC = p.nchunks;
 
   // ---------------------------------------------------------------- setup
-  if (warp == 0) {
+  if (warp == kWarpTmem) {
     ptx::tmem_alloc(&tmem_holder, kTmemCols);
     ptx::tmem_relinquish();
   }
   if (tid == 0) {
     abort_flag = 0;
-    ptx::mbar_init(&bar_x[0], 1);
-    ptx::mbar_init(&bar_x[1], 1);
-    ptx::mbar_init(&bar_m1, 1);
-    ptx::mbar_init(&bar_m3, 1);
+    ptx::mbar_init(&bar_raw_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&bar_op_full[s], 1);
+      ptx::mbar_init(&bar_slot_free[s], kCoreWarps);
+      ptx::mbar_init(&bar_acc_full[s], 1);
+      ptx::mbar_init(&bar_y_full[s], 1);
+    }
     ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tm_B);
+    ptx::prefetch_tensormap(&tm_C);
+    ptx::prefetch_tensormap(&tm_th);
     ptx::prefetch_tensormap(&tm_x);
     ptx::prefetch_tensormap(&tm_y);
   }
-  for (int i = tid; i < 4 * KP; i += kThreads) (&s_carry[0][0][0])[i] = 0.f;
-  // zero fp16 state copy: the entering state of chunk 0
-  for (uint32_t i = tid * 16; i < (uint32_t)NS * 128u; i += kThreads * 16)
-    sts128(sbase + K::kH + i, make_uint4(0, 0, 0, 0));
-
-  // per-thread constants of the angle phase: pair k, token group tq
-  const int kq = tid % KP, tq = tid / KP;
-  float bbias[2][R], cbias[2][R];
-  float bmax_bias = 0.f, cmax_bias = 0.f;
-#pragma unroll
-  for (int e = 0; e < 2; ++e)
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int64_t ix = (h * NS + 2 * kq + e) * R + r;
-      bbias[e][r] = p.B_bias ? p.B_bias[ix] : 0.f;
-      cbias[e][r] = p.C_bias ? p.C_bias[ix] : 0.f;
-      bmax_bias = fmaxf(bmax_bias, fabsf(bbias[e][r]));
-      cmax_bias = fmaxf(cmax_bias, fabsf(cbias[e][r]));
-    }
-  bmax_bias = warp_max(bmax_bias);
-  cmax_bias = warp_max(cmax_bias);
-  if (lane == 0) {
-    s_bias_red[0][warp] = bmax_bias;
-    s_bias_red[1][warp] = cmax_bias;
-  }
+  // masked-score tiles: blocks above the diagonal are zero and never written again
+  for (uint32_t i = tid * 16; i < 2u * kTileBytes; i += kThreads * 16)
+    sts128(sbase + K::kPh + i, make_uint4(0, 0, 0, 0));
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before_sync();
   __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem = tmem_holder;
-  bmax_bias = 0.f;
-  cmax_bias = 0.f;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    bmax_bias = fmaxf(bmax_bias, s_bias_red[0][w]);
-    cmax_bias = fmaxf(cmax_bias, s_bias_red[1][w]);
-  }
-  constexpr uint32_t kXBytes = (uint32_t)(Q * kP * R * 2);
-  if (tid == 0) {
-    for (int c = 0; c < 2 && c < nC; ++c) {
-      ptx::mbar_arrive_expect_tx(&bar_x[c], kXBytes);
-      ptx::tma_load_4d(smem + K::kXs + c * kTileBytes, &tm_x, &bar_x[c], 0, (int)h, c * Q, (int)b);
+
+  // TMA of one chunk's raw tiles into the raw slot (prologue thread 0)
+  auto issue_raw = [&](int64_t seq, int c) {
+    const int64_t b = seq / H, h = seq % H, gi = h / (H / G);
+    const int t0 = c * Q;
+    ptx::mbar_arrive_expect_tx(&bar_raw_full, K::kTxBytes);
+    ptx::tma_load_5d(smem + K::kRawB, &tm_B, &bar_raw_full, 0, 0, (int)gi, t0, (int)b);
+    ptx::tma_load_5d(smem + K::kRawC, &tm_C, &bar_raw_full, 0, 0, (int)gi, t0, (int)b);
+    ptx::tma_load_4d(smem + K::kRawTh, &tm_th, &bar_raw_full, 0, (int)gi, t0, (int)b);
+    ptx::tma_load_4d(smem + K::kRawX, &tm_x, &bar_raw_full, 0, (int)h, t0, (int)b);
+  };
+
+  if (warp < kProWarps) {
+    // ============================================================ prologue
+    const int kk2 = tid % KP2, tg = tid / KP2;
+    const int k0 = 2 * kk2;  // this thread's pairs: k0, k0 + 1 (rows 4kk2 .. 4kk2 + 3)
+    int64_t cur_h = -1;
+    float bb[4][R], cb[4][R];
+    float bmax_bias = 0.f, cmax_bias = 0.f;
+    int inflight = -1;  // phase parity of a raw load issued and not yet consumed
+    // the first chunk's inputs
+    Sched sch{(int64_t)blockIdx.x, 0};
+    if (tid == 0) {
+      issue_raw(sch.seq, 0);
+      inflight = 0;
     }
-  }
-
-  // state ownership (D accumulator layout): quadrant of the warp and column half
-  const int quad = warp & 3, chalf = warp >> 2;
-  float hreg[HR];
+    if (warp == 1) {
+      DecayRaw d;
+      load_decay_raw(p, sch.seq / H, sch.seq % H, 0, Q, lane, d);
+      store_decay(d, lane, s_dtraw[0], s_lamraw[0], s_bnx[0]);
+    }
+    float A_h = 0.f;
+    for (int g = 0;; ++g) {
+      const int64_t seq = sch.seq, h = seq % H;
+      const int c = sch.c, s = g & 1, db = g & 1;
+      Sched nxt = sch;
+      const bool has_next = nxt.next(nseq, nC);
+      SlotScalars<KP>& sc = ss[s];
+      if (h != cur_h) {
+        // per-head A, bias (fp32) and a block-wide bound of the bias magnitude
+        cur_h = h;
+        A_h = p.A[h];
+        float mb = 0.f, mc = 0.f;
 #pragma unroll
-  for (int i = 0; i < HR; ++i) hreg[i] = 0.f;
-  float h_inv_prev = 1.f;  // 1/sigma of the fp16 state copy the next Yoff reads
-
-  const __nv_bfloat16* Bg = p.B;
-  const __nv_bfloat16* Cg = p.C;
-
-  for (int c = 0; c < nC; ++c) {
-    const int64_t t0 = (int64_t)c * Q;
-    const int stage = c & 1;
-    // ---------------------------------------------------- phase 0: decay scan
-    if (warp == 0) {
-      float dtv[2], lmv[2], bnx[2];
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int i = lane + 32 * j;
-        const int64_t t = t0 + i;
-        dtv[j] = 0.f; lmv[j] = 0.f; bnx[j] = 0.f;
-        if (i < Q && t < L) {
-          dtv[j] = p.dt[(b * L + t) * H + h];
-          lmv[j] = p.lam[(b * L + t) * H + h];
-          if (t + 1 < L)
-            bnx[j] = (1.f - p.lam[(b * L + t + 1) * H + h]) * p.dt[(b * L + t + 1) * H + h];
+          for (int r = 0; r < R; ++r) {
+            const int64_t ix = (h * NS + 4 * kk2 + e) * R + r;
+            bb[e][r] = p.B_bias ? p.B_bias[ix] : 0.f;
+            cb[e][r] = p.C_bias ? p.C_bias[ix] : 0.f;
+            mb = fmaxf(mb, fabsf(bb[e][r]));
+            mc = fmaxf(mc, fabsf(cb[e][r]));
+          }
+        mb = warp_max(mb);
+        mc = warp_max(mc);
+        if (lane == 0) {
+          s_bias_red[0][warp] = mb;
+          s_bias_red[1][warp] = mc;
+        }
+        ptx::named_bar_sync(kBarPro, kProThreads);
+        bmax_bias = 0.f;
+        cmax_bias = 0.f;
+#pragma unroll
+        for (int w = 0; w < kProWarps; ++w) {
+          bmax_bias = fmaxf(bmax_bias, s_bias_red[0][w]);
+          cmax_bias = fmaxf(cmax_bias, s_bias_red[1][w]);
         }
       }
-      // inclusive prefix of Delta*A (in log2 units) over the chunk
-      float a0 = dtv[0] * A_h * kLog2e, a1 = dtv[1] * A_h * kLog2e;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float v0 = __shfl_up_sync(0xffffffffu, a0, o);
-        const float v1 = __shfl_up_sync(0xffffffffu, a1, o);
-        if (lane >= o) { a0 += v0; a1 += v1; }
+      // 1. this chunk's raw tiles have landed and operand slot s is free
+      if (tid == 0) {
+        bool ok = wait_or_abort(&bar_raw_full, (uint32_t)(g & 1), &abort_flag, p.status);
+        if (ok) inflight = -1;
+        if (ok && g >= 2)
+          ok = wait_or_abort(&bar_slot_free[s], (uint32_t)(((g >> 1) & 1) ^ 1), &abort_flag,
+                             p.status);
+        s_go[0] = ok ? 1 : 0;
       }
-      a1 += __shfl_sync(0xffffffffu, a0, 31);
-      const float lam_end = (Q <= 32) ? __shfl_sync(0xffffffffu, a0, Q - 1)
-                                      : __shfl_sync(0xffffffffu, a1, (Q - 1) & 31);
-      float lv[2] = {a0, a1};
-      float wm = 0.f;
+      ptx::named_bar_sync(kBarPro, kProThreads);
+      if (!s_go[0]) break;
+      // 2a. decay scan (warp 0); the next chunk's dt, lambda (warp 1, into registers)
+      DecayRaw nd;
+      if (warp == 0) {
+        float dtv[2], lmv[2], bnx[2];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int i = lane + 32 * j;
-        if (i < Q) {
-          const float gam = lmv[j] * dtv[j];
-          const float wpv = gam + bnx[j];
-          const float we = exp2f(lam_end - lv[j]) * wpv;
-          s_lam2[i] = lv[j];
-          s_gam[i] = gam;
-          s_wp[i] = wpv;
-          s_wend[i] = we;
-          s_eL[i] = exp2f(lv[j]);
-          s_dt[i] = dtv[j];
-          wm = fmaxf(wm, fabsf(we));
+        for (int j = 0; j < 2; ++j) {
+          const int i = lane + 32 * j;
+          dtv[j] = s_dtraw[db][i];
+          lmv[j] = s_lamraw[db][i];
+          bnx[j] = s_bnx[db][i];
         }
-      }
-      wm = warp_max(wm);
-      if (lane == 0) {
-        s_eLend = exp2f(lam_end);
-        s_wmax = wm;
-      }
-    }
-    // raw loads of this thread's tokens (B, C pairs for all ranks; theta)
-    float th[TPG];
-    uint32_t braw[TPG][R], craw[TPG][R];
-    float bmax = 0.f, cmax = 0.f;
+        float a0 = dtv[0] * A_h * kLog2e, a1 = dtv[1] * A_h * kLog2e;
 #pragma unroll
-    for (int i = 0; i < TPG; ++i) {
-      const int64_t t = t0 + tq * TPG + i;
-      th[i] = 0.f;
+        for (int o = 1; o < 32; o <<= 1) {
+          const float v0 = __shfl_up_sync(0xffffffffu, a0, o);
+          const float v1 = __shfl_up_sync(0xffffffffu, a1, o);
+          if (lane >= o) { a0 += v0; a1 += v1; }
+        }
+        a1 += __shfl_sync(0xffffffffu, a0, 31);
+        const float lam_end = (Q <= 32) ? __shfl_sync(0xffffffffu, a0, Q - 1)
+                                        : __shfl_sync(0xffffffffu, a1, (Q - 1) & 31);
+        const float lv[2] = {a0, a1};
+        float wm = 0.f;
 #pragma unroll
-      for (int r = 0; r < R; ++r) { braw[i][r] = 0u; craw[i][r] = 0u; }
-      if (t < L) {
-        th[i] = p.theta[((b * L + t) * G + g) * KP + kq];
-        const int64_t base = ((b * L + t) * G + g) * (int64_t)NS * R + (int64_t)(2 * kq) * R;
+        for (int j = 0; j < 2; ++j) {
+          const int i = lane + 32 * j;
+          if (i < Q) {
+            const float gam = lmv[j] * dtv[j];
+            const float wpv = gam + bnx[j];
+            const float we = ex2(lam_end - lv[j]) * wpv;
+            sc.lam2[i] = lv[j];
+            sc.gam[i] = gam;
+            sc.wp[i] = wpv;
+            sc.wend[i] = we;
+            sc.eL[i] = ex2(lv[j]);
+            wm = fmaxf(wm, fabsf(we));
+          }
+        }
+        wm = warp_max(wm);
+        if (lane == 0) {
+          sc.eLend = ex2(lam_end);
+          sc.wmax = wm;
+        }
+      } else if (warp == 1 && has_next) {
+        load_decay_raw(p, nxt.seq / H, nxt.seq % H, (int64_t)nxt.c * Q, Q, lane, nd);
+      }
+      // 2b. raw tiles -> registers; magnitude bounds; Kahan-compensated angle sums
+      float2 th2[TPG];
+      uint32_t bw[TPG][K::BW], cw[TPG][K::BW];
+      uint32_t bacc = 0u, cacc = 0u;
+#pragma unroll
+      for (int i = 0; i < TPG; ++i) {
+        const int t = tg * TPG + i;
+        const uint2 tv = lds64(sbase + K::kRawTh + (uint32_t)(t * KP + k0) * 4u);
+        th2[i] = make_float2(__uint_as_float(tv.x), __uint_as_float(tv.y));
+        const uint32_t ob = (uint32_t)(t * NS * R + 4 * kk2 * R) * 2u;
         if constexpr (R == 1) {
-          braw[i][0] = *reinterpret_cast<const uint32_t*>(Bg + base);
-          craw[i][0] = *reinterpret_cast<const uint32_t*>(Cg + base);
-        } else if constexpr (R == 2) {
-          const uint2 vb = *reinterpret_cast<const uint2*>(Bg + base);
-          const uint2 vc = *reinterpret_cast<const uint2*>(Cg + base);
-          braw[i][0] = vb.x; braw[i][1] = vb.y;
-          craw[i][0] = vc.x; craw[i][1] = vc.y;
+          const uint2 vb = lds64(sbase + K::kRawB + ob), vc = lds64(sbase + K::kRawC + ob);
+          bw[i][0] = vb.x; bw[i][1] = vb.y;
+          cw[i][0] = vc.x; cw[i][1] = vc.y;
         } else {
-          const uint4 vb = *reinterpret_cast<const uint4*>(Bg + base);
-          const uint4 vc = *reinterpret_cast<const uint4*>(Cg + base);
-          braw[i][0] = vb.x; braw[i][1] = vb.y; braw[i][2] = vb.z; braw[i][3] = vb.w;
-          craw[i][0] = vc.x; craw[i][1] = vc.y; craw[i][2] = vc.z; craw[i][3] = vc.w;
+#pragma unroll
+          for (int q = 0; q < K::BW / 4; ++q) {
+            const uint4 vb = lds128(sbase + K::kRawB + ob + 16u * q);
+            const uint4 vc = lds128(sbase + K::kRawC + ob + 16u * q);
+            bw[i][4 * q] = vb.x; bw[i][4 * q + 1] = vb.y; bw[i][4 * q + 2] = vb.z; bw[i][4 * q + 3] = vb.w;
+            cw[i][4 * q] = vc.x; cw[i][4 * q + 1] = vc.y; cw[i][4 * q + 2] = vc.z; cw[i][4 * q + 3] = vc.w;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < K::BW; ++q) {
+          bacc = ptx::bf16x2_absmax(bacc, bw[i][q]);
+          cacc = ptx::bf16x2_absmax(cacc, cw[i][q]);
         }
       }
+      float2 ph[TPG];
+      {
+        float2 run = make_float2(0.f, 0.f), comp = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        bmax = fmaxf(bmax, bf_absmax(braw[i][r]));
-        cmax = fmaxf(cmax, bf_absmax(craw[i][r]));
+        for (int i = 0; i < TPG; ++i) {
+          const float d = s_dtraw[db][tg * TPG + i];
+          const float2 yk = sub2(mul2(make_float2(d, d), th2[i]), comp);
+          const float2 tk = add2(run, yk);
+          comp = sub2(sub2(tk, run), yk);
+          run = tk;
+          ph[i] = run;
+        }
+        s_tot[0][tg][k0] = run.x;
+        s_tot[0][tg][k0 + 1] = run.y;
+        s_tot[1][tg][k0] = -comp.x;
+        s_tot[1][tg][k0 + 1] = -comp.y;
       }
-    }
-    __syncthreads();  // decay scan visible
-    // ---------------------------------------------------- phase 1: angles, RoPE fold
-    // cumulative angle over this thread's tokens (radians), with Kahan's
-    // compensation so that the chunk-to-chunk carry does not drift over long
-    // sequences; ph[i] is the plain running sum, total = run - comp
-    float ph[TPG];
-    float run = 0.f, comp = 0.f;
-#pragma unroll
-    for (int i = 0; i < TPG; ++i) {
-      const float yk = __fmul_rn(s_dt[tq * TPG + i], th[i]) - comp;
-      const float tk = run + yk;
-      comp = (tk - run) - yk;
-      run = tk;
-      ph[i] = run;
-    }
-    s_tot[0][tq][kq] = run;
-    s_tot[1][tq][kq] = -comp;
-    // this chunk's x tile: wait for its TMA, read this thread's part, bound |x|
-    const bool x_ok = wait_or_abort(&bar_x[stage], (uint32_t)((c >> 1) & 1), &abort_flag, p.status);
-    const uint32_t xs = sbase + K::kXs + stage * kTileBytes;
-    constexpr int kXItems = (R == 1) ? 2 : (Q * (kP / 4)) / kThreads;  // per thread
-    uint4 xv[kXItems][(R == 1) ? 1 : R / 2];
-    float xmax = 0.f;
-    if (x_ok) {
+      // x of this chunk -> registers (w X and the operand copy of X)
+      constexpr int kXItems = (R == 1) ? 2 : (Q * (kP / 4)) / kProThreads;
+      constexpr int kXVec = (R == 1) ? 1 : R / 2;
+      uint4 xv[kXItems][kXVec];
+      uint32_t xacc = 0u;
+      const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
 #pragma unroll
       for (int j = 0; j < kXItems; ++j) {
-        const int it = tid + kThreads * j;
+        const int it = tid + kProThreads * j;
         if constexpr (R == 1) {
-          xv[j][0] = lds128(xs + (uint32_t)it * 16u);  // 16-byte chunk `it`, row it / 8
+          xv[j][0] = lds128(sbase + K::kRawX + (uint32_t)it * 16u);  // 16-byte chunk, row it / 8
         } else {
-          // raw x tile [token][p][r]; item = (token s, block of 4 p): 8R bytes
-          const int s = it / (kP / 4), pb = it % (kP / 4);
-          const uint32_t src = xs + (uint32_t)(s * kP * R + 4 * pb * R) * 2u;
+          const int sx = it / (kP / 4), pb = it % (kP / 4);
+          const uint32_t src = sbase + K::kRawX + (uint32_t)(sx * kP * R + 4 * pb * R) * 2u;
 #pragma unroll
-          for (int q2 = 0; q2 < R / 2; ++q2) xv[j][q2] = lds128(src + 16u * q2);
+          for (int q = 0; q < kXVec; ++q) xv[j][q] = lds128(src + 16u * q);
         }
 #pragma unroll
-        for (int q2 = 0; q2 < ((R == 1) ? 1 : R / 2); ++q2) {
-          xmax = fmaxf(xmax, fmaxf(fmaxf(bf_absmax(xv[j][q2].x), bf_absmax(xv[j][q2].y)),
-                                   fmaxf(bf_absmax(xv[j][q2].z), bf_absmax(xv[j][q2].w))));
+        for (int q = 0; q < kXVec; ++q) {
+          xacc = ptx::bf16x2_absmax(xacc, xv[j][q].x);
+          xacc = ptx::bf16x2_absmax(xacc, xv[j][q].y);
+          xacc = ptx::bf16x2_absmax(xacc, xv[j][q].z);
+          xacc = ptx::bf16x2_absmax(xacc, xv[j][q].w);
         }
       }
-    }
-    bmax = warp_max(bmax);
-    cmax = warp_max(cmax);
-    xmax = warp_max(xmax);
-    if (lane == 0) {
-      s_red[0][warp] = bmax;
-      s_red[1][warp] = cmax;
-      s_red[2][warp] = xmax;
-    }
-    __syncthreads();
-    if (abort_flag) break;
-    // per-chunk fp16 scales of the rotated B / C tiles and of w X
-    float sigB, invB, sigC, invC, sigX, invX;
-    {
-      float mb = 0.f, mc = 0.f, mx = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        mb = fmaxf(mb, s_red[0][w]);
-        mc = fmaxf(mc, s_red[1][w]);
-        mx = fmaxf(mx, s_red[2][w]);
-      }
-      // a rotated pair keeps its norm: |Rot(v)_i| <= sqrt(2) max|v| < 2 max|v|
-      pow2_scale(2.f * (mb + bmax_bias), &sigB, &invB);
-      pow2_scale(2.f * (mc + cmax_bias), &sigC, &invC);
-      pow2_scale(mx * s_wmax, &sigX, &invX);
-    }
-    // angle before this thread's first token: carry + earlier groups (float-float)
-    float oh = s_carry[stage][0][kq], ol = s_carry[stage][1][kq];
-    for (int q2 = 0; q2 < tq; ++q2) ff_add(oh, ol, s_tot[0][q2][kq], s_tot[1][q2][kq]);
-    ff_wrap(oh, ol);
-    if (tq == TG - 1) {
-      float eh = oh, el = ol;
-      ff_add(eh, el, run, -comp);
-      ff_wrap(eh, el);
-      s_carry[stage ^ 1][0][kq] = eh;
-      s_carry[stage ^ 1][1][kq] = el;
-    }
-#pragma unroll
-    for (int i = 0; i < TPG; ++i) {
-      float ang = oh + (ol + ph[i]);
-      const float kw = rintf(ang * kInvTwoPi);
-      ang = fmaf(-kw, kPi2a, ang);
-      ang = fmaf(-kw, kPi2b, ang);
-      float sn, cs;
-      __sincosf(ang, &sn, &cs);
-      const float csB = cs * sigB, snB = sn * sigB, csC = cs * sigC, snC = sn * sigC;
-      const int t = tq * TPG + i;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        // word layout of the 2R raw values: n = 2k at r, then n = 2k + 1 at r
-        float b0, b1, c0, c1;
-        if constexpr (R == 1) {
-          b0 = bf_lo(braw[i][0]); b1 = bf_hi(braw[i][0]);
-          c0 = bf_lo(craw[i][0]); c1 = bf_hi(craw[i][0]);
-        } else {
-          const int w0 = r >> 1, w1 = (R >> 1) + (r >> 1);
-          b0 = (r & 1) ? bf_hi(braw[i][w0]) : bf_lo(braw[i][w0]);
-          b1 = (r & 1) ? bf_hi(braw[i][w1]) : bf_lo(braw[i][w1]);
-          c0 = (r & 1) ? bf_hi(craw[i][w0]) : bf_lo(craw[i][w0]);
-          c1 = (r & 1) ? bf_hi(craw[i][w1]) : bf_lo(craw[i][w1]);
+      {
+        const float bm = warp_max(bf_absmax(bacc)), cm = warp_max(bf_absmax(cacc));
+        const float xm = warp_max(bf_absmax(xacc));
+        if (lane == 0) {
+          s_red[0][warp] = bm;
+          s_red[1][warp] = cm;
+          s_red[2][warp] = xm;
         }
-        b0 += bbias[0][r]; b1 += bbias[1][r];
-        c0 += cbias[0][r]; c1 += cbias[1][r];
-        // sigma Rot(-Phi) = sigma [[cos, sin], [-sin, cos]]
-        const float bt0 = fmaf(csB, b0, snB * b1), bt1 = fmaf(csB, b1, -snB * b0);
-        const float ct0 = fmaf(csC, c0, snC * c1), ct1 = fmaf(csC, c1, -snC * c0);
-        const uint32_t row = (uint32_t)(t * R + r);
-        const uint32_t o = tile_off(row, 2u * kq, 64u);
-        sts32(sbase + K::kBt + o, pack_f16(bt0, bt1));
-        sts32(sbase + K::kCt + o, pack_f16(ct0, ct1));
       }
-    }
-    // w X (fp16, scaled) and, for R > 1, X re-laid as [(token, rank)][p] (bf16)
-#pragma unroll
-    for (int j = 0; j < kXItems; ++j) {
-      const int it = tid + kThreads * j;
-      if constexpr (R == 1) {
-        const uint32_t row = (uint32_t)it >> 3;
-        const float w = s_wend[row] * sigX;
-        const uint4 v = xv[j][0];
-        sts128(sbase + K::kXw + (uint32_t)it * 16u,
-               make_uint4(pack_f16(w * bf_lo(v.x), w * bf_hi(v.x)),
-                          pack_f16(w * bf_lo(v.y), w * bf_hi(v.y)),
-                          pack_f16(w * bf_lo(v.z), w * bf_hi(v.z)),
-                          pack_f16(w * bf_lo(v.w), w * bf_hi(v.w))));
-      } else {
-        const int s = it / (kP / 4), pb = it % (kP / 4);
-        uint32_t wv[2 * R];
-#pragma unroll
-        for (int q2 = 0; q2 < R / 2; ++q2) {
-          wv[4 * q2] = xv[j][q2].x; wv[4 * q2 + 1] = xv[j][q2].y;
-          wv[4 * q2 + 2] = xv[j][q2].z; wv[4 * q2 + 3] = xv[j][q2].w;
+      ptx::named_bar_sync(kBarPro, kProThreads);
+      // every read of the raw slot is done: refill it with the next chunk
+      if (has_next) {
+        if (tid == 0) {
+          issue_raw(nxt.seq, nxt.c);
+          inflight = (g + 1) & 1;
         }
-        const float w = s_wend[s] * sigX;
+        if (warp == 1) store_decay(nd, lane, s_dtraw[db ^ 1], s_lamraw[db ^ 1], s_bnx[db ^ 1]);
+      }
+      // 3. per-chunk fp16 scales of Bt, Ct and w X
+      float sigB, invB, sigC, invC, sigX, invX;
+      {
+        float mb = 0.f, mc = 0.f, mx = 0.f;
+#pragma unroll
+        for (int w = 0; w < kProWarps; ++w) {
+          mb = fmaxf(mb, s_red[0][w]);
+          mc = fmaxf(mc, s_red[1][w]);
+          mx = fmaxf(mx, s_red[2][w]);
+        }
+        // a rotated pair keeps its norm: |Rot(v)_i| <= sqrt(2) max|v| < 2 max|v|
+        pow2_scale(2.f * (mb + bmax_bias), &sigB, &invB);
+        pow2_scale(2.f * (mc + cmax_bias), &sigC, &invC);
+        pow2_scale(mx * sc.wmax, &sigX, &invX);
+        if (tid == 0) {
+          sc.invB = invB;
+          sc.invC = invC;
+          sc.invX = invX;
+        }
+      }
+      // 4. angle before this thread's first token: carry + earlier groups.
+      // Within the chunk an fp32 offset suffices; the carry to the next
+      // chunk is float-float so that it does not drift.
+      const int cpar = g & 1;
+      float2 off;
+      {
+        float o0 = 0.f, o1 = 0.f;
+        for (int q = 0; q < tg; ++q) {
+          o0 += s_tot[0][q][k0] + s_tot[1][q][k0];
+          o1 += s_tot[0][q][k0 + 1] + s_tot[1][q][k0 + 1];
+        }
+        float ch0 = 0.f, cl0 = 0.f, ch1 = 0.f, cl1 = 0.f;
+        if (c > 0) {
+          ch0 = s_carry[cpar][0][k0];
+          cl0 = s_carry[cpar][1][k0];
+          ch1 = s_carry[cpar][0][k0 + 1];
+          cl1 = s_carry[cpar][1][k0 + 1];
+        }
+        off.x = wrap_rad(ch0 + (cl0 + o0));
+        off.y = wrap_rad(ch1 + (cl1 + o1));
+        // the carry of pair k0 is updated by group TG-1, that of k0+1 by TG-2
+        if (tg >= TG - 2) {
+          const int k = (tg == TG - 1) ? k0 : k0 + 1;
+          float eh = (tg == TG - 1) ? ch0 : ch1, el = (tg == TG - 1) ? cl0 : cl1;
+          for (int q = 0; q < TG; ++q) ff_add(eh, el, s_tot[0][q][k], s_tot[1][q][k]);
+          ff_wrap(eh, el);
+          s_carry[cpar ^ 1][0][k] = eh;
+          s_carry[cpar ^ 1][1][k] = el;
+          if (c == nC - 1) sc.fang[k] = eh + el;
+        }
+      }
+      // 5. RoPE fold: sigma Rot(-Phi) (B + bias), likewise C, into fp16 tiles
+      {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < TPG; ++i) {
+          ph[i] = add2(off, ph[i]);
+          amax = fmaxf(amax, fmaxf(fabsf(ph[i].x), fabsf(ph[i].y)));
+        }
+        if (__any_sync(0xffffffffu, amax > kAngleDirect)) {
+#pragma unroll
+          for (int i = 0; i < TPG; ++i) ph[i] = make_float2(wrap_rad(ph[i].x), wrap_rad(ph[i].y));
+        }
+      }
+      const float2 sB2 = make_float2(sigB, sigB), sC2 = make_float2(sigC, sigC);
+#pragma unroll
+      for (int i = 0; i < TPG; ++i) {
+        float2 sn, cs;
+        __sincosf(ph[i].x, &sn.x, &cs.x);
+        __sincosf(ph[i].y, &sn.y, &cs.y);
+        const float2 csB = mul2(cs, sB2), snB = mul2(sn, sB2);
+        const float2 csC = mul2(cs, sC2), snC = mul2(sn, sC2);
+        const float2 nsnB = make_float2(-snB.x, -snB.y), nsnC = make_float2(-snC.x, -snC.y);
+        const int t = tg * TPG + i;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          float v4[4];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int e = q4 * R + r;  // element index within the 4R values
-            v4[q4] = (e & 1) ? bf_hi(wv[e >> 1]) : bf_lo(wv[e >> 1]);
-          }
-          const uint32_t row = (uint32_t)(s * R + r);
-          const uint32_t o = sw128(row, 4u * pb);
-          sts64(sbase + K::kXb + o, pack_bf16(v4[0], v4[1]), pack_bf16(v4[2], v4[3]));
-          sts64(sbase + K::kXw + o, pack_f16(w * v4[0], w * v4[1]), pack_f16(w * v4[2], w * v4[3]));
+          // elements (n, r) for n = 4kk2 + e; .x holds pair k0 (e = 0, 1), .y pair k0+1 (e = 2, 3)
+          float2 b0 = make_float2(bf_at(bw[i], 0 * R + r), bf_at(bw[i], 2 * R + r));
+          float2 b1 = make_float2(bf_at(bw[i], 1 * R + r), bf_at(bw[i], 3 * R + r));
+          float2 c0 = make_float2(bf_at(cw[i], 0 * R + r), bf_at(cw[i], 2 * R + r));
+          float2 c1 = make_float2(bf_at(cw[i], 1 * R + r), bf_at(cw[i], 3 * R + r));
+          b0 = add2(b0, make_float2(bb[0][r], bb[2][r]));
+          b1 = add2(b1, make_float2(bb[1][r], bb[3][r]));
+          c0 = add2(c0, make_float2(cb[0][r], cb[2][r]));
+          c1 = add2(c1, make_float2(cb[1][r], cb[3][r]));
+          // Rot(-Phi) = [[cos, sin], [-sin, cos]]
+          const float2 bt0 = fma2(csB, b0, mul2(snB, b1)), bt1 = fma2(csB, b1, mul2(nsnB, b0));
+          const float2 ct0 = fma2(csC, c0, mul2(snC, c1)), ct1 = fma2(csC, c1, mul2(nsnC, c0));
+          const uint32_t o = tile_off((uint32_t)(t * R + r), 4u * kk2, 64u);
+          sts64(opb + K::kOpBt + o, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
+          sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
         }
       }
+      // 6. w X (fp16, scaled) and X as the [(token, rank)][p] bf16 operand
+#pragma unroll
+      for (int j = 0; j < kXItems; ++j) {
+        const int it = tid + kProThreads * j;
+        if constexpr (R == 1) {
+          // the raw tile is already 128-byte swizzled [token][p]: same offsets
+          const uint32_t row = (uint32_t)it >> 3;
+          const float w = sc.wend[row] * sigX;
+          const uint4 v = xv[j][0];
+          sts128(opb + K::kOpXo + (uint32_t)it * 16u, v);
+          sts128(opb + K::kOpXw + (uint32_t)it * 16u,
+                 make_uint4(pack_f16(w * bf_lo(v.x), w * bf_hi(v.x)),
+                            pack_f16(w * bf_lo(v.y), w * bf_hi(v.y)),
+                            pack_f16(w * bf_lo(v.z), w * bf_hi(v.z)),
+                            pack_f16(w * bf_lo(v.w), w * bf_hi(v.w))));
+        } else {
+          const int sx = it / (kP / 4), pb = it % (kP / 4);
+          uint32_t wv[2 * R];
+#pragma unroll
+          for (int q = 0; q < kXVec; ++q) {
+            wv[4 * q] = xv[j][q].x; wv[4 * q + 1] = xv[j][q].y;
+            wv[4 * q + 2] = xv[j][q].z; wv[4 * q + 3] = xv[j][q].w;
+          }
+          const float w = sc.wend[sx] * sigX;
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            float v4[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) v4[q4] = bf_at(wv, q4 * R + r);
+            const uint32_t o = sw128((uint32_t)(sx * R + r), 4u * pb);
+            sts64(opb + K::kOpXo + o, pack_bf16(v4[0], v4[1]), pack_bf16(v4[2], v4[3]));
+            sts64(opb + K::kOpXw + o, pack_f16(w * v4[0], w * v4[1]), pack_f16(w * v4[2], w * v4[3]));
+          }
+        }
+      }
+      // 7. S = Ct Bt^T and D = Bt^T (w X) of this chunk into TMEM set s (free
+      // since the core released slot s), then publish the slot to the core
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(kBarPro, kProThreads);
+      if (tid == 0) {
+        const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
+        ptx::tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < NS / 16; ++kk)
+          ptx::mma_bf16_ss(tset + kColS, desc_k(opb + K::kOpCt, kk, 64),
+                           desc_k(opb + K::kOpBt, kk, 64), kIdS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kQR / 16; ++kk)
+          ptx::mma_bf16_ss(tset + kColD, desc_mn(opb + K::kOpBt, kk, 64u * 128u),
+                           desc_mn(opb + K::kOpXw, kk, 64u * 128u), kIdD, kk > 0);
+        ptx::mma_commit(&bar_acc_full[s]);
+        ptx::mbar_arrive(&bar_op_full[s]);
+      }
+      if (!has_next) break;
+      sch = nxt;
     }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before_sync();
-    __syncthreads();
-    ptx::tc_fence_after_sync();
-    // ---------------------------------------------------- phase 2: S, D, Yoff
-    const uint32_t xop = (R == 1) ? xs : (sbase + K::kXb);
-    if (tid == 0) {
-      constexpr uint32_t idS = ptx::idesc_f16_f32(64, 64, false, false);
-      constexpr uint32_t idD = ptx::idesc_f16_f32(NS, 64, true, true);
-      constexpr uint32_t idYo = ptx::idesc_f16_f32(64, 64, false, true);
+    // on an early exit, let an issued load land before the CTA ends
+    if (tid == 0 && inflight >= 0) ptx::mbar_wait(&bar_raw_full, (uint32_t)inflight, kWaitNs);
+  } else {
+    // ============================================================ core (+ MMA issue)
+    const int ct = tid - kProThreads;  // 0..127
+    const int quad = warp & 3;         // TMEM lane quadrant of this warp
+    float hreg[HR];
+    float h_inv_prev = 1.f;
+    // Yoff = Ct H of chunk g into set g & 1 (this thread's next commit, after
+    // the chunk's Y, covers it)
+    auto issue_yoff = [&](int g) {
+      const int s = g & 1;
+      const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
+      const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
+      ptx::tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < NS / 16; ++kk)
-        ptx::mma_bf16_ss(tmem + kColS, desc_k(sbase + K::kCt, kk, 64), desc_k(sbase + K::kBt, kk, 64),
-                         idS, kk > 0);
+        ptx::mma_bf16_ss(tset + kColYo, desc_k(opb + K::kOpCt, kk, 64),
+                         desc_mn(sbase + K::kH, kk, (uint32_t)NS * 128u), kIdYo, kk > 0);
+    };
+    Sched sch{(int64_t)blockIdx.x, 0};
+    for (int g = 0;; ++g) {
+      const int64_t seq = sch.seq, b = seq / H, h = seq % H;
+      const int c = sch.c, s = g & 1;
+      Sched nxt = sch;
+      const bool has_next = nxt.next(nseq, nC);
+      const SlotScalars<KP>& sc = ss[s];
+      const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
+      if (c == 0) {
 #pragma unroll
-      for (int kk = 0; kk < kQR / 16; ++kk)
-        ptx::mma_bf16_ss(tmem + kColD, desc_mn(sbase + K::kBt, kk, 64u * 128u),
-                         desc_mn(sbase + K::kXw, kk, 64u * 128u), idD, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < NS / 16; ++kk)
-        ptx::mma_bf16_ss(tmem + kColYo, desc_k(sbase + K::kCt, kk, 64),
-                         desc_mn(sbase + K::kH, kk, (uint32_t)NS * 128u), idYo, kk > 0);
-      ptx::mma_commit(&bar_m1);
-    }
-    __syncwarp();
-    // ---------------------------------------------------- phase 3: mask, state
-    const bool m1_ok = wait_or_abort(&bar_m1, (uint32_t)(c & 1), &abort_flag, p.status);
-    ptx::tc_fence_after_sync();
-    float hmax = 0.f;
-    if (m1_ok) {
-      // masked scores: thread -> row a, 16 consecutive columns (M=64 layout)
+        for (int i = 0; i < HR; ++i) hreg[i] = 0.f;
+      }
+      if (ct == 0)
+        s_go[1] = wait_or_abort(&bar_acc_full[s], (uint32_t)((g >> 1) & 1), &abort_flag, p.status)
+                      ? 1 : 0;
+      ptx::named_bar_sync(kBarCore, kCoreThreads);
+      if (!s_go[1]) break;
+      ptx::tc_fence_after_sync();
+      const float invB = sc.invB, invC = sc.invC, invX = sc.invX;
+      // ---- masked scores: thread -> row a, 16 consecutive columns per block
       {
-        uint32_t sv[16];
-        ptx::tmem_ld16_16x32bx2<16>(tmem + kColS + ((uint32_t)(32 * quad) << 16) + 32u * chalf, sv);
-        ptx::tmem_ld_wait(sv);
         const int a = 16 * quad + (lane & 15);
-        const int c0 = 32 * chalf + 16 * (lane >> 4);
         const int t = a / R;
-        const float invBC = invB * invC;
-        const float lt = s_lam2[t];
-        uint32_t ph_[8], pl_[8];
+        const float einv = (float)((int)((__float_as_uint(invB * invC) >> 23) & 0xffu) - 127);
+        const float lt = sc.lam2[t] + einv;
+        const float gdiag = sc.gam[t] * (invB * invC);
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          float hi2[2], lo2[2];
+        for (int blk = 0; blk < 2; ++blk) {
+          // skip a warp whose 16 rows x 32 columns lie wholly above the diagonal
+          if ((32 * blk) / R > (16 * quad + 15) / R) continue;
+          uint32_t sv[16];
+          ptx::tmem_ld16_16x32bx2<16>(tset + kColS + ((uint32_t)(32 * quad) << 16) + 32u * blk, sv);
+          ptx::tmem_ld_wait(sv);
+          const int c0 = 32 * blk + 16 * (lane >> 4);
+          if (c0 / R > t) continue;
+          constexpr int NT = 16 / R;  // distinct tokens among the 16 columns
+          const int s0 = c0 / R;
+          float lsv[NT], wpv[NT];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int s = (c0 + j + e) / R;
-            float m = 0.f;
-            if (s < t) m = exp2f(lt - s_lam2[s]) * s_wp[s];
-            else if (s == t) m = s_gam[s];
-            const float v = (m * invBC) * __uint_as_float(sv[j + e]);
-            const float vh = __bfloat162float(__float2bfloat16_rn(v));
-            hi2[e] = vh;
-            lo2[e] = v - vh;
+          for (int u = 0; u < NT; ++u) {
+            lsv[u] = sc.lam2[s0 + u];
+            wpv[u] = sc.wp[s0 + u];
           }
-          ph_[j >> 1] = pack_bf16(hi2[0], hi2[1]);
-          pl_[j >> 1] = pack_bf16(lo2[0], lo2[1]);
-        }
-        const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
-        const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
-        sts128(sbase + K::kPh + o0, make_uint4(ph_[0], ph_[1], ph_[2], ph_[3]));
-        sts128(sbase + K::kPh + o1, make_uint4(ph_[4], ph_[5], ph_[6], ph_[7]));
-        sts128(sbase + K::kPl + o0, make_uint4(pl_[0], pl_[1], pl_[2], pl_[3]));
-        sts128(sbase + K::kPl + o1, make_uint4(pl_[4], pl_[5], pl_[6], pl_[7]));
-      }
-      // state: H = exp(Lam_end) H + D / (sigma_B sigma_X)
-      {
-        const float eend = s_eLend;
-        const float invBX = invB * invX;
-        if constexpr (NS == 128) {
-          // M=128 layout: lane = row n; this warp owns p in [32*chalf, +32)
-          uint32_t d0[16], d1[16];
-          const uint32_t ta = tmem + kColD + ((uint32_t)(32 * quad) << 16) + 32u * chalf;
-          ptx::tmem_ld16(ta, d0);
-          ptx::tmem_ld16(ta + 16, d1);
-          ptx::tmem_ld_wait(d0);
-          ptx::tmem_ld_wait(d1);
+          uint32_t ph_[8], pl_[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            hreg[j] = fmaf(invBX, __uint_as_float(d0[j]), eend * hreg[j]);
-            hreg[16 + j] = fmaf(invBX, __uint_as_float(d1[j]), eend * hreg[16 + j]);
+          for (int j = 0; j < 16; j += 2) {
+            float v2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int u = (j + e) / R, s_ = s0 + u;
+              const float moff = ex2(lt - lsv[u]) * wpv[u];
+              const float m = (s_ < t) ? moff : ((s_ == t) ? gdiag : 0.f);
+              v2[e] = m * __uint_as_float(sv[j + e]);
+            }
+            const uint32_t hw = pack_bf16(v2[0], v2[1]);
+            ph_[j >> 1] = hw;
+            pl_[j >> 1] = pack_bf16(v2[0] - bf_lo(hw), v2[1] - bf_hi(hw));
+          }
+          const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
+          const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
+          sts128(sbase + K::kPh + o0, make_uint4(ph_[0], ph_[1], ph_[2], ph_[3]));
+          sts128(sbase + K::kPh + o1, make_uint4(ph_[4], ph_[5], ph_[6], ph_[7]));
+          sts128(sbase + K::kPl + o0, make_uint4(pl_[0], pl_[1], pl_[2], pl_[3]));
+          sts128(sbase + K::kPl + o1, make_uint4(pl_[4], pl_[5], pl_[6], pl_[7]));
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(kBarCore, kCoreThreads);
+      if (ct == 0) {
+        // Y = P X (P = high + low parts) of this chunk
+        const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
+        ptx::tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < kQR / 16; ++kk)
+          ptx::mma_bf16_ss(tset + kColY, desc_k(sbase + K::kPh, kk, 64),
+                           desc_mn(opb + K::kOpXo, kk, 64u * 128u), kIdY, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kQR / 16; ++kk)
+          ptx::mma_bf16_ss(tset + kColY, desc_k(sbase + K::kPl, kk, 64),
+                           desc_mn(opb + K::kOpXo, kk, 64u * 128u), kIdY, 1u);
+        ptx::mma_commit(&bar_y_full[s]);
+      }
+      // ---- state: H = exp(Lam_end) H + D / (sigma_B sigma_X)
+      float hmax = 0.f;
+      {
+        const float2 e2 = make_float2(sc.eLend, sc.eLend);
+        const float iBX = invB * invX;
+        const float2 i2 = make_float2(iBX, iBX);
+#pragma unroll
+        for (int blk = 0; blk < HR / 16; ++blk) {
+          uint32_t d[16];
+          if constexpr (NS == 128) {
+            // M=128 layout: lane = row n; 16 columns per load
+            ptx::tmem_ld16(tset + kColD + ((uint32_t)(32 * quad) << 16) + 16u * blk, d);
+          } else {
+            // M=64 layout: row n = 16*quad + (lane & 15)
+            ptx::tmem_ld16_16x32bx2<16>(tset + kColD + ((uint32_t)(32 * quad) << 16) + 32u * blk, d);
+          }
+          ptx::tmem_ld_wait(d);
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            float2 hv = mul2(e2, make_float2(hreg[16 * blk + j], hreg[16 * blk + j + 1]));
+            hv = fma2(i2, make_float2(__uint_as_float(d[j]), __uint_as_float(d[j + 1])), hv);
+            hreg[16 * blk + j] = hv.x;
+            hreg[16 * blk + j + 1] = hv.y;
+            hmax = fmaxf(hmax, fmaxf(fabsf(hv.x), fabsf(hv.y)));
+          }
+        }
+      }
+      hmax = warp_max(hmax);
+      if (lane == 0) s_hred[quad] = hmax;
+      // Y (and this chunk's Yoff, which read the previous state copy) complete;
+      // the output staging tile is free again
+      if (ct == 0) {
+        s_go[1] = wait_or_abort(&bar_y_full[s], (uint32_t)((g >> 1) & 1), &abort_flag, p.status)
+                      ? 1 : 0;
+        ptx::tma_store_wait_read<0>();
+      }
+      ptx::named_bar_sync(kBarCore, kCoreThreads);
+      if (!s_go[1]) break;
+      ptx::tc_fence_after_sync();
+      float h_sig, h_inv;
+      {
+        float m = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCoreWarps; ++w) m = fmaxf(m, s_hred[w]);
+        pow2_scale(m, &h_sig, &h_inv);
+        const float2 hs2 = make_float2(h_sig, h_sig);
+        // fp16 copy of the new state for the next chunk's Ct H product
+#pragma unroll
+        for (int blk = 0; blk < HR / 16; ++blk) {
+          uint32_t n, cb;
+          if constexpr (NS == 128) {
+            n = (uint32_t)(32 * quad + lane);
+            cb = 16u * blk;
+          } else {
+            n = (uint32_t)(16 * quad + (lane & 15));
+            cb = 32u * blk + 16u * (lane >> 4);
+          }
+          uint32_t wv[8];
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            const float2 v = mul2(hs2, make_float2(hreg[16 * blk + j], hreg[16 * blk + j + 1]));
+            wv[j >> 1] = pack_f16(v.x, v.y);
+          }
+          sts128(sbase + K::kH + sw128(n, cb), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+          sts128(sbase + K::kH + sw128(n, cb + 8u), make_uint4(wv[4], wv[5], wv[6], wv[7]));
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before_sync();
+      ptx::named_bar_sync(kBarCore, kCoreThreads);
+      // the next chunk's Yoff, if its operands are ready already (a chunk that
+      // starts a sequence has none)
+      const bool want_yoff = has_next && nxt.c > 0;
+      bool next_issued = false;
+      if (ct == 0 && want_yoff &&
+          ptx::mbar_try_wait(&bar_op_full[(g + 1) & 1], (uint32_t)(((g + 1) >> 1) & 1))) {
+        issue_yoff(g + 1);
+        next_issued = true;
+      }
+      // ---- outputs: y = Y + exp(Lam_t) Yoff
+      {
+        const int a = 16 * quad + (lane & 15);
+        const float el = sc.eL[a / R] * (invC * h_inv_prev);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          uint32_t yv[16];
+          const uint32_t ta = ((uint32_t)(32 * quad) << 16) + 32u * blk;
+          ptx::tmem_ld16_16x32bx2<16>(tset + kColY + ta, yv);
+          ptx::tmem_ld_wait(yv);
+          const int c0 = 32 * blk + 16 * (lane >> 4);  // first p of this thread
+          float y[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) y[j] = __uint_as_float(yv[j]);
+          if (c > 0) {
+            // the first chunk of a sequence has no entering state (and its
+            // Yoff accumulator was not written)
+            uint32_t yo[16];
+            ptx::tmem_ld16_16x32bx2<16>(tset + kColYo + ta, yo);
+            ptx::tmem_ld_wait(yo);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y[j] = fmaf(el, __uint_as_float(yo[j]), y[j]);
+          }
+          if constexpr (R == 1) {
+            const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
+            const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
+            sts128(sbase + K::kYs + o0, make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
+                                                   pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7])));
+            sts128(sbase + K::kYs + o1,
+                   make_uint4(pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
+                              pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15])));
+          } else {
+            // staging in the global layout of one chunk: [token][p][r]
+            const int t = a / R, r = a % R;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              __nv_bfloat16 v = __float2bfloat16_rn(y[j]);
+              sts16(sbase + K::kYs + (uint32_t)((t * kP + c0 + j) * R + r) * 2u,
+                    *reinterpret_cast<uint16_t*>(&v));
+            }
+          }
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before_sync();
+      ptx::named_bar_sync(kBarCore, kCoreThreads);
+      if (ct == 0) {
+        ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, (int)h, c * Q, (int)b);
+        ptx::tma_store_commit();
+      }
+      // ---- final state of the sequence, explicit frame: h = Rot(Phi_{L-1}) g
+      if (c == nC - 1 && p.final_state) {
+        float* fs = p.final_state + seq * (int64_t)NS * kP;
+        if constexpr (NS == 128) {
+          const int n = 32 * quad + lane;
+          float sn, cs;
+          sincosf(sc.fang[n >> 1], &sn, &cs);
+          const bool odd = n & 1;
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            float o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float hv = hreg[16 * blk + j];
+              const float other = __shfl_xor_sync(0xffffffffu, hv, 1);
+              // even row: c g0 - s g1 ; odd row: s g0 + c g1
+              o[j] = odd ? fmaf(sn, other, cs * hv) : fmaf(-sn, other, cs * hv);
+            }
+            float4* dst = reinterpret_cast<float4*>(fs + (int64_t)n * kP + 16 * blk);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
           }
         } else {
-          // M=64 layout: row n = 16*quad + (lane & 15); 16 columns per thread
-          uint32_t d0[16];
-          ptx::tmem_ld16_16x32bx2<16>(tmem + kColD + ((uint32_t)(32 * quad) << 16) + 32u * chalf, d0);
-          ptx::tmem_ld_wait(d0);
+          const int n = 16 * quad + (lane & 15);
+          float sn, cs;
+          sincosf(sc.fang[n >> 1], &sn, &cs);
+          const bool odd = n & 1;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) hreg[j] = fmaf(invBX, __uint_as_float(d0[j]), eend * hreg[j]);
-        }
+          for (int blk = 0; blk < 2; ++blk) {
+            float o[16];
 #pragma unroll
-        for (int j = 0; j < HR; ++j) hmax = fmaxf(hmax, fabsf(hreg[j]));
-      }
-    }
-    hmax = warp_max(hmax);
-    if (lane == 0) s_hred[warp] = hmax;
-    if (tid == 0) ptx::tma_store_wait_read<0>();  // output staging free again
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before_sync();
-    __syncthreads();
-    if (abort_flag) break;
-    ptx::tc_fence_after_sync();
-    // ---------------------------------------------------- phase 4: Y = P X
-    if (tid == 0) {
-      constexpr uint32_t idY = ptx::idesc_bf16_f32(64, 64, false, true);
+            for (int j = 0; j < 16; ++j) {
+              const float hv = hreg[16 * blk + j];
+              const float other = __shfl_xor_sync(0xffffffffu, hv, 1);
+              o[j] = odd ? fmaf(sn, other, cs * hv) : fmaf(-sn, other, cs * hv);
+            }
+            float4* dst = reinterpret_cast<float4*>(fs + (int64_t)n * kP + 32 * blk +
+                                                    16 * (lane >> 4));
 #pragma unroll
-      for (int kk = 0; kk < kQR / 16; ++kk)
-        ptx::mma_bf16_ss(tmem + kColY, desc_k(sbase + K::kPh, kk, 64), desc_mn(xop, kk, 64u * 128u),
-                         idY, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < kQR / 16; ++kk)
-        ptx::mma_bf16_ss(tmem + kColY, desc_k(sbase + K::kPl, kk, 64), desc_mn(xop, kk, 64u * 128u),
-                         idY, 1u);
-      ptx::mma_commit(&bar_m3);
-    }
-    __syncwarp();
-    // fp16 copy of the new state for the next chunk's Ct H_in product (its
-    // previous copy was last read by this chunk's Yoff MMA, complete above)
-    float h_sig, h_inv;
-    {
-      float m = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) m = fmaxf(m, s_hred[w]);
-      pow2_scale(m, &h_sig, &h_inv);
-      if constexpr (NS == 128) {
-        const uint32_t n = (uint32_t)(32 * quad + lane);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float* hv = hreg + 8 * q4;
-          sts128(sbase + K::kH + sw128(n, 32u * chalf + 8u * q4),
-                 make_uint4(pack_f16(h_sig * hv[0], h_sig * hv[1]), pack_f16(h_sig * hv[2], h_sig * hv[3]),
-                            pack_f16(h_sig * hv[4], h_sig * hv[5]), pack_f16(h_sig * hv[6], h_sig * hv[7])));
-        }
-      } else {
-        const uint32_t n = (uint32_t)(16 * quad + (lane & 15));
-        const uint32_t cb = 32u * chalf + 16u * (lane >> 4);
-#pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
-          const float* hv = hreg + 8 * q4;
-          sts128(sbase + K::kH + sw128(n, cb + 8u * q4),
-                 make_uint4(pack_f16(h_sig * hv[0], h_sig * hv[1]), pack_f16(h_sig * hv[2], h_sig * hv[3]),
-                            pack_f16(h_sig * hv[4], h_sig * hv[5]), pack_f16(h_sig * hv[6], h_sig * hv[7])));
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          }
         }
       }
+      h_inv_prev = h_inv;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bar_slot_free[s]);
+      // the next chunk's S, D, Yoff if they could not go out above
+      if (ct == 0 && want_yoff && !next_issued &&
+          wait_or_abort(&bar_op_full[(g + 1) & 1], (uint32_t)(((g + 1) >> 1) & 1), &abort_flag,
+                        p.status))
+        issue_yoff(g + 1);
+      if (!has_next) break;
+      sch = nxt;
     }
-    const bool m3_ok = wait_or_abort(&bar_m3, (uint32_t)(c & 1), &abort_flag, p.status);
-    ptx::tc_fence_after_sync();
-    // x stage of this chunk is free: prefetch chunk c + 2 into it
-    if (tid == 0 && m3_ok && c + 2 < nC) {
-      ptx::mbar_arrive_expect_tx(&bar_x[stage], kXBytes);
-      ptx::tma_load_4d(smem + K::kXs + stage * kTileBytes, &tm_x, &bar_x[stage], 0, (int)h,
-                       (c + 2) * Q, (int)b);
-    }
-    // ---------------------------------------------------- phase 5: outputs
-    if (m3_ok) {
-      uint32_t yv[16], yo[16];
-      const uint32_t ta = ((uint32_t)(32 * quad) << 16) + 32u * chalf;
-      ptx::tmem_ld16_16x32bx2<16>(tmem + kColY + ta, yv);
-      ptx::tmem_ld16_16x32bx2<16>(tmem + kColYo + ta, yo);
-      ptx::tmem_ld_wait(yv);
-      ptx::tmem_ld_wait(yo);
-      const int a = 16 * quad + (lane & 15);
-      const int c0 = 32 * chalf + 16 * (lane >> 4);  // first p of this thread
-      const float el = s_eL[a / R] * (invC * h_inv_prev);
-      float y[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) y[j] = fmaf(el, __uint_as_float(yo[j]), __uint_as_float(yv[j]));
-      if constexpr (R == 1) {
-        const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
-        const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
-        sts128(sbase + K::kYs + o0, make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
-                                               pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7])));
-        sts128(sbase + K::kYs + o1, make_uint4(pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
-                                               pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15])));
-      } else {
-        // staging in the global layout of one chunk: [token][p][r]
-        const int t = a / R, r = a % R;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          __nv_bfloat16 v = __float2bfloat16_rn(y[j]);
-          sts16(sbase + K::kYs + (uint32_t)((t * kP + c0 + j) * R + r) * 2u,
-                *reinterpret_cast<uint16_t*>(&v));
-        }
-      }
-    }
-    h_inv_prev = h_inv;
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before_sync();
-    __syncthreads();
-    if (abort_flag) break;
-    if (tid == 0) {
-      ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, (int)h, (int)t0, (int)b);
-      ptx::tma_store_commit();
-    }
+    if (ct == 0) ptx::tma_store_wait_all<0>();
   }
 
-  // ---------------------------------------------------------------- final state
-  if (tid == 0) ptx::tma_store_wait_all<0>();
-  if (!abort_flag && p.final_state) {
-    // explicit frame: h = Rot(Phi_{L-1}) g, rows (2k, 2k+1)
-    float* fs = p.final_state + bh * (int64_t)NS * kP;
-    const float* carry_h = s_carry[nC & 1][0];
-    const float* carry_l = s_carry[nC & 1][1];
-    if constexpr (NS == 128) {
-      const int n = 32 * quad + lane;
-      float sn, cs;
-      sincosf(carry_h[n >> 1] + carry_l[n >> 1], &sn, &cs);
-      const bool odd = n & 1;
-      float outv[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float other = __shfl_xor_sync(0xffffffffu, hreg[j], 1);
-        // even row: c*g0 - s*g1 ; odd row: s*g0 + c*g1
-        outv[j] = odd ? fmaf(sn, other, cs * hreg[j]) : fmaf(-sn, other, cs * hreg[j]);
-      }
-      float4* dst = reinterpret_cast<float4*>(fs + (int64_t)n * kP + 32 * chalf);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        dst[j] = make_float4(outv[4 * j], outv[4 * j + 1], outv[4 * j + 2], outv[4 * j + 3]);
-    } else {
-      const int n = 16 * quad + (lane & 15);
-      float sn, cs;
-      sincosf(carry_h[n >> 1] + carry_l[n >> 1], &sn, &cs);
-      const bool odd = n & 1;
-      float outv[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float other = __shfl_xor_sync(0xffffffffu, hreg[j], 1);
-        outv[j] = odd ? fmaf(sn, other, cs * hreg[j]) : fmaf(-sn, other, cs * hreg[j]);
-      }
-      float4* dst = reinterpret_cast<float4*>(fs + (int64_t)n * kP + 32 * chalf + 16 * (lane >> 4));
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        dst[j] = make_float4(outv[4 * j], outv[4 * j + 1], outv[4 * j + 2], outv[4 * j + 3]);
-    }
-  }
+  // ---------------------------------------------------------------- teardown
   ptx::tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kWarpTmem) {
     ptx::tc_fence_after_sync();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
@@ -820,39 +1102,75 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// x / out as a 4-D tensor {P*R, H, L, b}; the box is one head's chunk.
-bool make_act_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(m, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// x / out as a 4-D tensor {P*R, H, L, b}; the box is one head's chunk.
+bool make_act_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
   const uint64_t PR = (uint64_t)a.P * a.R;
   cuuint64_t dims[4] = {PR, (cuuint64_t)a.H, (cuuint64_t)a.L, (cuuint64_t)a.batch};
   cuuint64_t strides[3] = {PR * 2, PR * 2 * a.H, PR * 2 * a.H * a.L};
-  const uint32_t Q = (uint32_t)a.Q;
-  cuuint32_t box[4] = {(cuuint32_t)PR, 1, Q, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUtensorMapSwizzle sw = (a.R == 1) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cuuint32_t box[4] = {(cuuint32_t)PR, 1, (cuuint32_t)a.Q, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box,
+                a.R == 1 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// B / C [b, L, G, N, R] as a 5-D tensor {d0, N*R/d0, G, L, b} with d0 <= 256.
+bool make_bc_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
+  const uint64_t NR = (uint64_t)a.N * a.R;
+  const uint64_t d0 = NR < 256 ? NR : 256, d1 = NR / d0;
+  cuuint64_t dims[5] = {d0, d1, (cuuint64_t)a.G, (cuuint64_t)a.L, (cuuint64_t)a.batch};
+  cuuint64_t strides[4] = {d0 * 2, NR * 2, NR * 2 * a.G, NR * 2 * a.G * a.L};
+  cuuint32_t box[5] = {(cuuint32_t)d0, (cuuint32_t)d1, 1, (cuuint32_t)a.Q, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, ptr, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// theta [b, L, G, N/2] fp32 as {N/2, G, L, b}.
+bool make_theta_map(CUtensorMap* m, const float* ptr, const ScanArgs& a) {
+  const uint64_t KP = (uint64_t)a.N / 2;
+  cuuint64_t dims[4] = {KP, (cuuint64_t)a.G, (cuuint64_t)a.L, (cuuint64_t)a.batch};
+  cuuint64_t strides[3] = {KP * 4, KP * 4 * a.G, KP * 4 * a.G * a.L};
+  cuuint32_t box[4] = {(cuuint32_t)KP, 1, (cuuint32_t)a.Q, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
 }
 
 template <int R, int NS>
 cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
-  CUtensorMap tx, ty;
-  if (!make_act_map(&tx, a.x, a) || !make_act_map(&ty, a.out, a)) return cudaErrorInvalidValue;
+  CUtensorMap tB, tC, tT, tx, ty;
+  if (!make_bc_map(&tB, a.B, a) || !make_bc_map(&tC, a.C, a) || !make_theta_map(&tT, a.theta, a) ||
+      !make_act_map(&tx, a.x, a) || !make_act_map(&ty, a.out, a))
+    return cudaErrorInvalidValue;
   TcParams p;
   p.dt = a.dt; p.A = a.A; p.lam = a.lam;
-  p.B = static_cast<const __nv_bfloat16*>(a.B);
-  p.C = static_cast<const __nv_bfloat16*>(a.C);
-  p.theta = a.theta; p.B_bias = a.B_bias; p.C_bias = a.C_bias;
+  p.B_bias = a.B_bias; p.C_bias = a.C_bias;
   p.final_state = a.final_state; p.status = status;
-  p.L = a.L; p.H = a.H; p.G = a.G;
+  p.L = a.L; p.H = a.H; p.G = a.G; p.batch = a.batch;
   p.nchunks = (int)((a.L + a.Q - 1) / a.Q);
   constexpr uint32_t smem = Cfg<R, NS>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel<R, NS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  scan_tc_kernel<R, NS><<<(unsigned)(a.batch * a.H), kThreads, smem, s>>>(tx, ty, p);
+  const int sms = num_sms();
+  if (sms <= 0) return cudaErrorInvalidValue;
+  const int64_t nseq = a.batch * a.H;
+  const unsigned grid = (unsigned)(nseq < sms ? nseq : sms);
+  scan_tc_kernel<R, NS><<<grid, kThreads, smem, s>>>(tB, tC, tT, tx, ty, p);
   return cudaGetLastError();
 }
 

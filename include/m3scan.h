@@ -87,8 +87,13 @@ typedef struct {
  * with P = 64 and N in {64, 128}; other bf16 shapes and every fp32 shape run
  * on the CUDA-core path (still on the GPU). Out-of-range chunk sizes return
  * M3_ERR_UNSUPPORTED.
- * Scratch: none is needed for the shapes of this release; `workspace` is
- * accepted and ignored when m3_scan_workspace_bytes() returns 0.
+ * Scratch: on the tensor-core path, when there are fewer (b, h) sequences
+ * than SMs, each sequence is cut into segments that run in parallel (a
+ * state-only pass, an ordered combine of the segment states, and the full
+ * pass); that needs m3_scan_workspace_bytes() bytes of device scratch. Pass it
+ * in dims->workspace (16-byte aligned, at least that size, else
+ * M3_ERR_INVALID_ARG), or NULL and the library allocates and frees it on
+ * `stream` (cudaMallocAsync / cudaFreeAsync). Calls that need none ignore it.
  * L = 0 writes zeros to final_state (if given) and nothing else.
  */
 m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const float* lambda,
@@ -116,8 +121,10 @@ m3_status m3_decode_step(float* state, const void* x, const float* dt, const flo
                          const void* B, const void* C, const float* theta, const m3_dims* dims,
                          int R, void* out, void* stream);
 
-/* Bytes of device scratch m3_scan_fwd wants for these arguments (0 if none);
- * (size_t)-1 if the arguments are invalid. Pure host function. */
+/* Bytes of device scratch m3_scan_fwd wants for these arguments when its
+ * pointers are 16-byte aligned (0 if none); (size_t)-1 if the arguments are
+ * invalid. Host function: reads the current device's SM count when a device
+ * is present (assumes 148, a B300, otherwise); launches nothing. */
 size_t m3_scan_workspace_bytes(const m3_dims* dims, int R, int chunk);
 
 /* Static, human-readable name of a status. Pure host function. */

@@ -88,7 +88,12 @@ const char* m3_status_string(m3_status s) {
 size_t m3_scan_workspace_bytes(const m3_dims* dims, int R, int chunk) {
   if (check_dims(dims, R) == M3_ERR_INVALID_ARG || chunk < 1 || dims->seqlen < 0)
     return (size_t)-1;
-  return 0;
+  if (dims->act_dtype != M3_BF16) return 0;
+  m3::ScanArgs a = {};
+  a.batch = dims->batch; a.L = dims->seqlen; a.H = dims->heads; a.G = dims->groups;
+  a.P = dims->headdim; a.N = dims->dstate; a.R = R; a.Q = chunk;
+  if (a.L == 0 || a.batch == 0) return 0;
+  return m3::scan_tc_workspace_bytes(a);
 }
 
 m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const float* lambda,
@@ -138,8 +143,15 @@ m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const floa
   m3::ScanArgs a;
   a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B = B; a.C = C; a.theta = theta;
   a.B_bias = dims->B_bias; a.C_bias = dims->C_bias; a.out = out; a.final_state = final_state;
+  a.workspace = dims->workspace; a.workspace_bytes = dims->workspace_bytes;
   a.batch = b; a.L = L; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R; a.Q = chunk;
   if (use_tc) {
+    // a caller-provided workspace must be large enough; NULL means the
+    // library allocates (stream-ordered) what it needs
+    if (dims->workspace != nullptr) {
+      if (!aligned(dims->workspace, 16)) return M3_ERR_INVALID_ARG;
+      if (dims->workspace_bytes < m3::scan_tc_workspace_bytes(a)) return M3_ERR_INVALID_ARG;
+    }
     unsigned int* status = nullptr;
     st = from_cuda(m3::status_word(&status));
     if (st != M3_OK) return st;

@@ -19,6 +19,8 @@ struct ScanArgs {
   const float* C_bias;
   void* out;
   float* final_state;
+  void* workspace;          // device scratch, or NULL (allocated stream-ordered when needed)
+  size_t workspace_bytes;
   int64_t batch, L, H, G, P, N;
   int R, Q;
 };
@@ -47,6 +49,8 @@ cudaError_t launch_scan_simt(const ScanArgs& a, bool bf16, cudaStream_t s);
 
 // Tensor-core (tcgen05) chunked prefill, bf16 activations.
 bool scan_tc_supported(int64_t N, int64_t P, int R, int Q);
+// Scratch the tensor-core prefill needs (segmented long sequences), 0 if none.
+size_t scan_tc_workspace_bytes(const ScanArgs& a);
 cudaError_t launch_scan_tc(const ScanArgs& a, unsigned int* status, cudaStream_t s);
 
 // Decode step.

@@ -141,7 +141,9 @@ struct SlotScalars {
   float eL[64];    // exp(Lam_t)
   float wend[64];  // exp(Lam_end - Lam_t) (gamma_t + bhat_{t+1})
   float fang[KP];  // cumulative angle after the chunk (last chunk of a sequence)
-  float eLend, wmax, invB, invC, invX, pad[3];
+  float eLend, wmax, invB, invC, invX;
+  float lamend2;  // Lam_end in log2 units
+  float pad[2];
 };
 
 struct TcParams {
@@ -154,6 +156,15 @@ struct TcParams {
   unsigned int* status;
   int64_t L, H, G, batch;
   int nchunks;
+  // work units are (sequence, segment) pairs of seg_chunks chunks each
+  int seg_chunks, nseg;
+  // segment passes: the state-only pass writes each unit's local end state to
+  // ws_state [unit][N][P] and (log2 decay, angle per pair) to ws_scal
+  // [unit][1 + N/2]; the full pass starts unit u from ws_hin[u] (explicit
+  // frame) when ws_hin is not NULL
+  float* ws_state;
+  float* ws_scal;
+  const float* ws_hin;
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col) {
@@ -311,17 +322,26 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
   return false;
 }
 
-// Position of a CTA in its schedule: sequences blockIdx.x, +gridDim.x, ...,
-// each walked chunk by chunk; g counts the CTA's chunks (slots and mbarrier
-// phases follow it).
+// Position of a CTA in its schedule. Work units are (sequence, segment)
+// pairs, unit u = seq * nseg + segment, covering chunks [c_begin, c_end) of
+// the sequence; a CTA walks units blockIdx.x, +gridDim.x, ... chunk by chunk
+// (g counts its chunks; slots and mbarrier phases follow g).
 struct Sched {
-  int64_t seq;
-  int c;
-  __device__ __forceinline__ bool next(int64_t nseq, int nC) {
-    if (++c < nC) return true;
-    c = 0;
-    seq += gridDim.x;
-    return seq < nseq;
+  int64_t unit, seq;
+  int c, c_begin, c_end;
+  __device__ __forceinline__ void start(int64_t u, const TcParams& p) {
+    unit = u;
+    seq = u / p.nseg;
+    c_begin = (int)(u % p.nseg) * p.seg_chunks;
+    c_end = min(p.nchunks, c_begin + p.seg_chunks);
+    c = c_begin;
+  }
+  __device__ __forceinline__ bool next(const TcParams& p) {
+    if (++c < c_end) return true;
+    const int64_t u = unit + gridDim.x;
+    if (u >= p.batch * p.H * p.nseg) return false;
+    start(u, p);
+    return true;
   }
 };
 
@@ -357,7 +377,8 @@ __device__ __forceinline__ void store_decay(const DecayRaw& d, int lane, float* 
   }
 }
 
-template <int R, int NS>
+// SO: the state-only pass of a segmented scan (no C, no outputs).
+template <int R, int NS, bool SO>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
                    const __grid_constant__ CUtensorMap tm_th, const __grid_constant__ CUtensorMap tm_x,
@@ -388,7 +409,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t H = p.H, G = p.G;
-  const int64_t nseq = p.batch * H;
   const int nC = p.nchunks;
 
   // ---------------------------------------------------------------- setup
@@ -425,9 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto issue_raw = [&](int64_t seq, int c) {
     const int64_t b = seq / H, h = seq % H, gi = h / (H / G);
     const int t0 = c * Q;
-    ptx::mbar_arrive_expect_tx(&bar_raw_full, K::kTxBytes);
+    ptx::mbar_arrive_expect_tx(&bar_raw_full, SO ? K::kTxBytes - K::kRawC : K::kTxBytes);
     ptx::tma_load_5d(smem + K::kRawB, &tm_B, &bar_raw_full, 0, 0, (int)gi, t0, (int)b);
-    ptx::tma_load_5d(smem + K::kRawC, &tm_C, &bar_raw_full, 0, 0, (int)gi, t0, (int)b);
+    if (!SO) ptx::tma_load_5d(smem + K::kRawC, &tm_C, &bar_raw_full, 0, 0, (int)gi, t0, (int)b);
     ptx::tma_load_4d(smem + K::kRawTh, &tm_th, &bar_raw_full, 0, (int)gi, t0, (int)b);
     ptx::tma_load_4d(smem + K::kRawX, &tm_x, &bar_raw_full, 0, (int)h, t0, (int)b);
   };
@@ -441,14 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     float bmax_bias = 0.f, cmax_bias = 0.f;
     int inflight = -1;  // phase parity of a raw load issued and not yet consumed
     // the first chunk's inputs
-    Sched sch{(int64_t)blockIdx.x, 0};
+    Sched sch;
+    sch.start(blockIdx.x, p);
     if (tid == 0) {
-      issue_raw(sch.seq, 0);
+      issue_raw(sch.seq, sch.c);
       inflight = 0;
     }
     if (warp == 1) {
       DecayRaw d;
-      load_decay_raw(p, sch.seq / H, sch.seq % H, 0, Q, lane, d);
+      load_decay_raw(p, sch.seq / H, sch.seq % H, (int64_t)sch.c * Q, Q, lane, d);
       store_decay(d, lane, s_dtraw[0], s_lamraw[0], s_bnx[0]);
     }
     float A_h = 0.f;
@@ -456,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t seq = sch.seq, h = seq % H;
       const int c = sch.c, s = g & 1, db = g & 1;
       Sched nxt = sch;
-      const bool has_next = nxt.next(nseq, nC);
+      const bool has_next = nxt.next(p);
       SlotScalars<KP>& sc = ss[s];
       if (h != cur_h) {
         // per-head A, bias (fp32) and a block-wide bound of the bias magnitude
@@ -540,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wm = warp_max(wm);
         if (lane == 0) {
           sc.eLend = ex2(lam_end);
+          sc.lamend2 = lam_end;
           sc.wmax = wm;
         }
       } else if (warp == 1 && has_next) {
@@ -556,22 +578,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         th2[i] = make_float2(__uint_as_float(tv.x), __uint_as_float(tv.y));
         const uint32_t ob = (uint32_t)(t * NS * R + 4 * kk2 * R) * 2u;
         if constexpr (R == 1) {
-          const uint2 vb = lds64(sbase + K::kRawB + ob), vc = lds64(sbase + K::kRawC + ob);
+          const uint2 vb = lds64(sbase + K::kRawB + ob);
           bw[i][0] = vb.x; bw[i][1] = vb.y;
-          cw[i][0] = vc.x; cw[i][1] = vc.y;
+          if constexpr (!SO) {
+            const uint2 vc = lds64(sbase + K::kRawC + ob);
+            cw[i][0] = vc.x; cw[i][1] = vc.y;
+          }
         } else {
 #pragma unroll
           for (int q = 0; q < K::BW / 4; ++q) {
             const uint4 vb = lds128(sbase + K::kRawB + ob + 16u * q);
-            const uint4 vc = lds128(sbase + K::kRawC + ob + 16u * q);
             bw[i][4 * q] = vb.x; bw[i][4 * q + 1] = vb.y; bw[i][4 * q + 2] = vb.z; bw[i][4 * q + 3] = vb.w;
-            cw[i][4 * q] = vc.x; cw[i][4 * q + 1] = vc.y; cw[i][4 * q + 2] = vc.z; cw[i][4 * q + 3] = vc.w;
+            if constexpr (!SO) {
+              const uint4 vc = lds128(sbase + K::kRawC + ob + 16u * q);
+              cw[i][4 * q] = vc.x; cw[i][4 * q + 1] = vc.y; cw[i][4 * q + 2] = vc.z; cw[i][4 * q + 3] = vc.w;
+            }
           }
         }
 #pragma unroll
         for (int q = 0; q < K::BW; ++q) {
           bacc = ptx::bf16x2_absmax(bacc, bw[i][q]);
-          cacc = ptx::bf16x2_absmax(cacc, cw[i][q]);
+          if constexpr (!SO) cacc = ptx::bf16x2_absmax(cacc, cw[i][q]);
         }
       }
       float2 ph[TPG];
@@ -666,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           o1 += s_tot[0][q][k0 + 1] + s_tot[1][q][k0 + 1];
         }
         float ch0 = 0.f, cl0 = 0.f, ch1 = 0.f, cl1 = 0.f;
-        if (c > 0) {
+        if (c > sch.c_begin) {
           ch0 = s_carry[cpar][0][k0];
           cl0 = s_carry[cpar][1][k0];
           ch1 = s_carry[cpar][0][k0 + 1];
@@ -682,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ff_wrap(eh, el);
           s_carry[cpar ^ 1][0][k] = eh;
           s_carry[cpar ^ 1][1][k] = el;
-          if (c == nC - 1) sc.fang[k] = eh + el;
+          if (c == sch.c_end - 1) sc.fang[k] = eh + el;
         }
       }
       // 5. RoPE fold: sigma Rot(-Phi) (B + bias), likewise C, into fp16 tiles
@@ -713,18 +740,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // elements (n, r) for n = 4kk2 + e; .x holds pair k0 (e = 0, 1), .y pair k0+1 (e = 2, 3)
           float2 b0 = make_float2(bf_at(bw[i], 0 * R + r), bf_at(bw[i], 2 * R + r));
           float2 b1 = make_float2(bf_at(bw[i], 1 * R + r), bf_at(bw[i], 3 * R + r));
-          float2 c0 = make_float2(bf_at(cw[i], 0 * R + r), bf_at(cw[i], 2 * R + r));
-          float2 c1 = make_float2(bf_at(cw[i], 1 * R + r), bf_at(cw[i], 3 * R + r));
           b0 = add2(b0, make_float2(bb[0][r], bb[2][r]));
           b1 = add2(b1, make_float2(bb[1][r], bb[3][r]));
-          c0 = add2(c0, make_float2(cb[0][r], cb[2][r]));
-          c1 = add2(c1, make_float2(cb[1][r], cb[3][r]));
           // Rot(-Phi) = [[cos, sin], [-sin, cos]]
           const float2 bt0 = fma2(csB, b0, mul2(snB, b1)), bt1 = fma2(csB, b1, mul2(nsnB, b0));
-          const float2 ct0 = fma2(csC, c0, mul2(snC, c1)), ct1 = fma2(csC, c1, mul2(nsnC, c0));
           const uint32_t o = tile_off((uint32_t)(t * R + r), 4u * kk2, 64u);
           sts64(opb + K::kOpBt + o, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
-          sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
+          if constexpr (!SO) {
+            float2 c0 = make_float2(bf_at(cw[i], 0 * R + r), bf_at(cw[i], 2 * R + r));
+            float2 c1 = make_float2(bf_at(cw[i], 1 * R + r), bf_at(cw[i], 3 * R + r));
+            c0 = add2(c0, make_float2(cb[0][r], cb[2][r]));
+            c1 = add2(c1, make_float2(cb[1][r], cb[3][r]));
+            const float2 ct0 = fma2(csC, c0, mul2(snC, c1)), ct1 = fma2(csC, c1, mul2(nsnC, c0));
+            sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
+          }
         }
       }
       // 6. w X (fp16, scaled) and X as the [(token, rank)][p] bf16 operand
@@ -736,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t row = (uint32_t)it >> 3;
           const float w = sc.wend[row] * sigX;
           const uint4 v = xv[j][0];
-          sts128(opb + K::kOpXo + (uint32_t)it * 16u, v);
+          if constexpr (!SO) sts128(opb + K::kOpXo + (uint32_t)it * 16u, v);
           sts128(opb + K::kOpXw + (uint32_t)it * 16u,
                  make_uint4(pack_f16(w * bf_lo(v.x), w * bf_hi(v.x)),
                             pack_f16(w * bf_lo(v.y), w * bf_hi(v.y)),
@@ -757,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) v4[q4] = bf_at(wv, q4 * R + r);
             const uint32_t o = sw128((uint32_t)(sx * R + r), 4u * pb);
-            sts64(opb + K::kOpXo + o, pack_bf16(v4[0], v4[1]), pack_bf16(v4[2], v4[3]));
+            if constexpr (!SO) sts64(opb + K::kOpXo + o, pack_bf16(v4[0], v4[1]), pack_bf16(v4[2], v4[3]));
             sts64(opb + K::kOpXw + o, pack_f16(w * v4[0], w * v4[1]), pack_f16(w * v4[2], w * v4[3]));
           }
         }
@@ -769,10 +798,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) {
         const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
         ptx::tc_fence_after_sync();
+        if constexpr (!SO) {
 #pragma unroll
-        for (int kk = 0; kk < NS / 16; ++kk)
-          ptx::mma_bf16_ss(tset + kColS, desc_k(opb + K::kOpCt, kk, 64),
-                           desc_k(opb + K::kOpBt, kk, 64), kIdS, kk > 0);
+          for (int kk = 0; kk < NS / 16; ++kk)
+            ptx::mma_bf16_ss(tset + kColS, desc_k(opb + K::kOpCt, kk, 64),
+                             desc_k(opb + K::kOpBt, kk, 64), kIdS, kk > 0);
+        }
 #pragma unroll
         for (int kk = 0; kk < kQR / 16; ++kk)
           ptx::mma_bf16_ss(tset + kColD, desc_mn(opb + K::kOpBt, kk, 64u * 128u),
@@ -791,6 +822,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;         // TMEM lane quadrant of this warp
     float hreg[HR];
     float h_inv_prev = 1.f;
+    float dsum = 0.f;  // log2 decay accumulated over the unit (state-only pass)
+    // state element (n, cb + j) of this thread's 16-column block `blk` is hreg[16 blk + j]
+    auto hpos = [&](int blk, uint32_t& n, uint32_t& cb) {
+      if constexpr (NS == 128) {
+        n = (uint32_t)(32 * quad + lane);  // M=128 accumulator layout: lane = row
+        cb = 16u * blk;
+      } else {
+        n = (uint32_t)(16 * quad + (lane & 15));  // M=64 layout: 16 rows per quadrant
+        cb = 32u * blk + 16u * (lane >> 4);
+      }
+    };
+    // fp16 copy of sigma * hreg into the state tile (operand of the next Yoff)
+    auto write_hcopy = [&](float h_sig) {
+      const float2 hs2 = make_float2(h_sig, h_sig);
+#pragma unroll
+      for (int blk = 0; blk < HR / 16; ++blk) {
+        uint32_t n, cb;
+        hpos(blk, n, cb);
+        uint32_t wv[8];
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const float2 v = mul2(hs2, make_float2(hreg[16 * blk + j], hreg[16 * blk + j + 1]));
+          wv[j >> 1] = pack_f16(v.x, v.y);
+        }
+        sts128(sbase + K::kH + sw128(n, cb), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+        sts128(sbase + K::kH + sw128(n, cb + 8u), make_uint4(wv[4], wv[5], wv[6], wv[7]));
+      }
+    };
     // Yoff = Ct H of chunk g into set g & 1 (this thread's next commit, after
     // the chunk's Y, covers it)
     auto issue_yoff = [&](int g) {
@@ -803,18 +862,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_bf16_ss(tset + kColYo, desc_k(opb + K::kOpCt, kk, 64),
                          desc_mn(sbase + K::kH, kk, (uint32_t)NS * 128u), kIdYo, kk > 0);
     };
-    Sched sch{(int64_t)blockIdx.x, 0};
-    for (int g = 0;; ++g) {
-      const int64_t seq = sch.seq, b = seq / H, h = seq % H;
-      const int c = sch.c, s = g & 1;
-      Sched nxt = sch;
-      const bool has_next = nxt.next(nseq, nC);
-      const SlotScalars<KP>& sc = ss[s];
-      const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
-      if (c == 0) {
+    // State entering unit u: the given explicit-frame state (the unit's local
+    // angle frame starts at zero, so no rotation) or zero; in the full pass its
+    // fp16 copy feeds the unit's first Yoff.
+    auto enter_unit = [&](int64_t u) {
+      dsum = 0.f;
+      if (p.ws_hin) {
+        const float* src = p.ws_hin + u * (int64_t)NS * kP;
+        float m = 0.f;
+#pragma unroll
+        for (int blk = 0; blk < HR / 16; ++blk) {
+          uint32_t n, cb;
+          hpos(blk, n, cb);
+          const float4* q4 = reinterpret_cast<const float4*>(src + (int64_t)n * kP + cb);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 v = q4[j];
+            hreg[16 * blk + 4 * j] = v.x;
+            hreg[16 * blk + 4 * j + 1] = v.y;
+            hreg[16 * blk + 4 * j + 2] = v.z;
+            hreg[16 * blk + 4 * j + 3] = v.w;
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+          }
+        }
+        if constexpr (!SO) {
+          m = warp_max(m);
+          if (lane == 0) s_hred[quad] = m;
+          ptx::named_bar_sync(kBarCore, kCoreThreads);
+          float mm = 0.f;
+#pragma unroll
+          for (int w = 0; w < kCoreWarps; ++w) mm = fmaxf(mm, s_hred[w]);
+          float h_sig;
+          pow2_scale(mm, &h_sig, &h_inv_prev);
+          write_hcopy(h_sig);
+          ptx::fence_proxy_async_smem();
+          ptx::tc_fence_before_sync();
+          ptx::named_bar_sync(kBarCore, kCoreThreads);
+        }
+      } else {
 #pragma unroll
         for (int i = 0; i < HR; ++i) hreg[i] = 0.f;
       }
+    };
+    Sched sch;
+    sch.start(blockIdx.x, p);
+    enter_unit(sch.unit);
+    if (!SO && p.ws_hin && ct == 0 && wait_or_abort(&bar_op_full[0], 0u, &abort_flag, p.status))
+      issue_yoff(0);
+    for (int g = 0;; ++g) {
+      const int64_t seq = sch.seq, b = seq / H, h = seq % H;
+      const int c = sch.c, s = g & 1;
+      const bool first = c == sch.c_begin, last = c == sch.c_end - 1;
+      Sched nxt = sch;
+      const bool has_next = nxt.next(p);
+      const SlotScalars<KP>& sc = ss[s];
+      const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
       if (ct == 0)
         s_go[1] = wait_or_abort(&bar_acc_full[s], (uint32_t)((g >> 1) & 1), &abort_flag, p.status)
                       ? 1 : 0;
@@ -822,8 +924,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!s_go[1]) break;
       ptx::tc_fence_after_sync();
       const float invB = sc.invB, invC = sc.invC, invX = sc.invX;
-      // ---- masked scores: thread -> row a, 16 consecutive columns per block
-      {
+      if constexpr (!SO) {
+        // ---- masked scores: thread -> row a, 16 consecutive columns per block
         const int a = 16 * quad + (lane & 15);
         const int t = a / R;
         const float einv = (float)((int)((__float_as_uint(invB * invC) >> 23) & 0xffu) - 127);
@@ -868,22 +970,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           sts128(sbase + K::kPl + o0, make_uint4(pl_[0], pl_[1], pl_[2], pl_[3]));
           sts128(sbase + K::kPl + o1, make_uint4(pl_[4], pl_[5], pl_[6], pl_[7]));
         }
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::named_bar_sync(kBarCore, kCoreThreads);
-      if (ct == 0) {
-        // Y = P X (P = high + low parts) of this chunk
-        const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
-        ptx::tc_fence_after_sync();
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(kBarCore, kCoreThreads);
+        if (ct == 0) {
+          // Y = P X (P = high + low parts) of this chunk
+          const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
+          ptx::tc_fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < kQR / 16; ++kk)
-          ptx::mma_bf16_ss(tset + kColY, desc_k(sbase + K::kPh, kk, 64),
-                           desc_mn(opb + K::kOpXo, kk, 64u * 128u), kIdY, kk > 0);
+          for (int kk = 0; kk < kQR / 16; ++kk)
+            ptx::mma_bf16_ss(tset + kColY, desc_k(sbase + K::kPh, kk, 64),
+                             desc_mn(opb + K::kOpXo, kk, 64u * 128u), kIdY, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < kQR / 16; ++kk)
-          ptx::mma_bf16_ss(tset + kColY, desc_k(sbase + K::kPl, kk, 64),
-                           desc_mn(opb + K::kOpXo, kk, 64u * 128u), kIdY, 1u);
-        ptx::mma_commit(&bar_y_full[s]);
+          for (int kk = 0; kk < kQR / 16; ++kk)
+            ptx::mma_bf16_ss(tset + kColY, desc_k(sbase + K::kPl, kk, 64),
+                             desc_mn(opb + K::kOpXo, kk, 64u * 128u), kIdY, 1u);
+          ptx::mma_commit(&bar_y_full[s]);
+        }
       }
       // ---- state: H = exp(Lam_end) H + D / (sigma_B sigma_X)
       float hmax = 0.f;
@@ -895,10 +997,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int blk = 0; blk < HR / 16; ++blk) {
           uint32_t d[16];
           if constexpr (NS == 128) {
-            // M=128 layout: lane = row n; 16 columns per load
             ptx::tmem_ld16(tset + kColD + ((uint32_t)(32 * quad) << 16) + 16u * blk, d);
           } else {
-            // M=64 layout: row n = 16*quad + (lane & 15)
             ptx::tmem_ld16_16x32bx2<16>(tset + kColD + ((uint32_t)(32 * quad) << 16) + 32u * blk, d);
           }
           ptx::tmem_ld_wait(d);
@@ -908,122 +1008,124 @@ __global__ void __launch_bounds__(kThreads, 1)
             hv = fma2(i2, make_float2(__uint_as_float(d[j]), __uint_as_float(d[j + 1])), hv);
             hreg[16 * blk + j] = hv.x;
             hreg[16 * blk + j + 1] = hv.y;
-            hmax = fmaxf(hmax, fmaxf(fabsf(hv.x), fabsf(hv.y)));
+            if constexpr (!SO) hmax = fmaxf(hmax, fmaxf(fabsf(hv.x), fabsf(hv.y)));
           }
         }
       }
-      hmax = warp_max(hmax);
-      if (lane == 0) s_hred[quad] = hmax;
-      // Y (and this chunk's Yoff, which read the previous state copy) complete;
-      // the output staging tile is free again
-      if (ct == 0) {
-        s_go[1] = wait_or_abort(&bar_y_full[s], (uint32_t)((g >> 1) & 1), &abort_flag, p.status)
-                      ? 1 : 0;
-        ptx::tma_store_wait_read<0>();
-      }
-      ptx::named_bar_sync(kBarCore, kCoreThreads);
-      if (!s_go[1]) break;
-      ptx::tc_fence_after_sync();
-      float h_sig, h_inv;
-      {
-        float m = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCoreWarps; ++w) m = fmaxf(m, s_hred[w]);
-        pow2_scale(m, &h_sig, &h_inv);
-        const float2 hs2 = make_float2(h_sig, h_sig);
-        // fp16 copy of the new state for the next chunk's Ct H product
-#pragma unroll
-        for (int blk = 0; blk < HR / 16; ++blk) {
-          uint32_t n, cb;
-          if constexpr (NS == 128) {
-            n = (uint32_t)(32 * quad + lane);
-            cb = 16u * blk;
-          } else {
-            n = (uint32_t)(16 * quad + (lane & 15));
-            cb = 32u * blk + 16u * (lane >> 4);
-          }
-          uint32_t wv[8];
-#pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            const float2 v = mul2(hs2, make_float2(hreg[16 * blk + j], hreg[16 * blk + j + 1]));
-            wv[j >> 1] = pack_f16(v.x, v.y);
-          }
-          sts128(sbase + K::kH + sw128(n, cb), make_uint4(wv[0], wv[1], wv[2], wv[3]));
-          sts128(sbase + K::kH + sw128(n, cb + 8u), make_uint4(wv[4], wv[5], wv[6], wv[7]));
-        }
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before_sync();
-      ptx::named_bar_sync(kBarCore, kCoreThreads);
-      // the next chunk's Yoff, if its operands are ready already (a chunk that
-      // starts a sequence has none)
-      const bool want_yoff = has_next && nxt.c > 0;
+      if constexpr (SO) dsum += sc.lamend2;
       bool next_issued = false;
-      if (ct == 0 && want_yoff &&
-          ptx::mbar_try_wait(&bar_op_full[(g + 1) & 1], (uint32_t)(((g + 1) >> 1) & 1))) {
-        issue_yoff(g + 1);
-        next_issued = true;
-      }
-      // ---- outputs: y = Y + exp(Lam_t) Yoff
-      {
-        const int a = 16 * quad + (lane & 15);
-        const float el = sc.eL[a / R] * (invC * h_inv_prev);
+      if constexpr (!SO) {
+        hmax = warp_max(hmax);
+        if (lane == 0) s_hred[quad] = hmax;
+        // Y (and this chunk's Yoff, which read the previous state copy) complete;
+        // the output staging tile is free again
+        if (ct == 0) {
+          s_go[1] = wait_or_abort(&bar_y_full[s], (uint32_t)((g >> 1) & 1), &abort_flag, p.status)
+                        ? 1 : 0;
+          ptx::tma_store_wait_read<0>();
+        }
+        ptx::named_bar_sync(kBarCore, kCoreThreads);
+        if (!s_go[1]) break;
+        ptx::tc_fence_after_sync();
+        float h_inv = h_inv_prev;
+        if (!last) {
+          // fp16 copy of the new state for the next chunk's Ct H product
+          float m = 0.f;
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          uint32_t yv[16];
-          const uint32_t ta = ((uint32_t)(32 * quad) << 16) + 32u * blk;
-          ptx::tmem_ld16_16x32bx2<16>(tset + kColY + ta, yv);
-          ptx::tmem_ld_wait(yv);
-          const int c0 = 32 * blk + 16 * (lane >> 4);  // first p of this thread
-          float y[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) y[j] = __uint_as_float(yv[j]);
-          if (c > 0) {
-            // the first chunk of a sequence has no entering state (and its
-            // Yoff accumulator was not written)
-            uint32_t yo[16];
-            ptx::tmem_ld16_16x32bx2<16>(tset + kColYo + ta, yo);
-            ptx::tmem_ld_wait(yo);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = fmaf(el, __uint_as_float(yo[j]), y[j]);
+          for (int w = 0; w < kCoreWarps; ++w) m = fmaxf(m, s_hred[w]);
+          float h_sig;
+          pow2_scale(m, &h_sig, &h_inv);
+          write_hcopy(h_sig);
+          ptx::fence_proxy_async_smem();
+          ptx::tc_fence_before_sync();
+          ptx::named_bar_sync(kBarCore, kCoreThreads);
+          // the next chunk's Yoff, if its operands are ready already
+          if (ct == 0 &&
+              ptx::mbar_try_wait(&bar_op_full[(g + 1) & 1], (uint32_t)(((g + 1) >> 1) & 1))) {
+            issue_yoff(g + 1);
+            next_issued = true;
           }
-          if constexpr (R == 1) {
-            const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
-            const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
-            sts128(sbase + K::kYs + o0, make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
-                                                   pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7])));
-            sts128(sbase + K::kYs + o1,
-                   make_uint4(pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
-                              pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15])));
-          } else {
-            // staging in the global layout of one chunk: [token][p][r]
-            const int t = a / R, r = a % R;
+        }
+        // ---- outputs: y = Y + exp(Lam_t) Yoff
+        {
+          const int a = 16 * quad + (lane & 15);
+          const float el = sc.eL[a / R] * (invC * h_inv_prev);
+          const bool has_yoff = !first || p.ws_hin != nullptr;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              __nv_bfloat16 v = __float2bfloat16_rn(y[j]);
-              sts16(sbase + K::kYs + (uint32_t)((t * kP + c0 + j) * R + r) * 2u,
-                    *reinterpret_cast<uint16_t*>(&v));
+          for (int blk = 0; blk < 2; ++blk) {
+            uint32_t yv[16];
+            const uint32_t ta = ((uint32_t)(32 * quad) << 16) + 32u * blk;
+            ptx::tmem_ld16_16x32bx2<16>(tset + kColY + ta, yv);
+            ptx::tmem_ld_wait(yv);
+            const int c0 = 32 * blk + 16 * (lane >> 4);  // first p of this thread
+            float y[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y[j] = __uint_as_float(yv[j]);
+            if (has_yoff) {
+              // a unit that starts from a zero state has no Yoff for its first
+              // chunk (that accumulator was not written)
+              uint32_t yo[16];
+              ptx::tmem_ld16_16x32bx2<16>(tset + kColYo + ta, yo);
+              ptx::tmem_ld_wait(yo);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) y[j] = fmaf(el, __uint_as_float(yo[j]), y[j]);
+            }
+            if constexpr (R == 1) {
+              const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
+              const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
+              sts128(sbase + K::kYs + o0, make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
+                                                     pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7])));
+              sts128(sbase + K::kYs + o1,
+                     make_uint4(pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
+                                pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15])));
+            } else {
+              // staging in the global layout of one chunk: [token][p][r]
+              const int t = a / R, r = a % R;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                __nv_bfloat16 v = __float2bfloat16_rn(y[j]);
+                sts16(sbase + K::kYs + (uint32_t)((t * kP + c0 + j) * R + r) * 2u,
+                      *reinterpret_cast<uint16_t*>(&v));
+              }
             }
           }
         }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before_sync();
+        ptx::named_bar_sync(kBarCore, kCoreThreads);
+        if (ct == 0) {
+          ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, (int)h, c * Q, (int)b);
+          ptx::tma_store_commit();
+        }
+        h_inv_prev = h_inv;
       }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before_sync();
-      ptx::named_bar_sync(kBarCore, kCoreThreads);
-      if (ct == 0) {
-        ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, (int)h, c * Q, (int)b);
-        ptx::tma_store_commit();
-      }
-      // ---- final state of the sequence, explicit frame: h = Rot(Phi_{L-1}) g
-      if (c == nC - 1 && p.final_state) {
-        float* fs = p.final_state + seq * (int64_t)NS * kP;
-        if constexpr (NS == 128) {
-          const int n = 32 * quad + lane;
-          float sn, cs;
-          sincosf(sc.fang[n >> 1], &sn, &cs);
-          const bool odd = n & 1;
+      if (last) {
+        if constexpr (SO) {
+          // the unit's local end state and its (log2 decay, angle) totals
+          float* dst = p.ws_state + sch.unit * (int64_t)NS * kP;
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
+          for (int blk = 0; blk < HR / 16; ++blk) {
+            uint32_t n, cb;
+            hpos(blk, n, cb);
+            float4* q4 = reinterpret_cast<float4*>(dst + (int64_t)n * kP + cb);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              q4[j] = make_float4(hreg[16 * blk + 4 * j], hreg[16 * blk + 4 * j + 1],
+                                  hreg[16 * blk + 4 * j + 2], hreg[16 * blk + 4 * j + 3]);
+          }
+          float* sd = p.ws_scal + sch.unit * (int64_t)(1 + KP);
+          if (ct == 0) sd[0] = dsum;
+          if (ct < KP) sd[1 + ct] = sc.fang[ct];
+        } else if (c == nC - 1 && p.final_state) {
+          // final state of the sequence, explicit frame: h = Rot(Phi_{L-1}) g
+          float* fs = p.final_state + seq * (int64_t)NS * kP;
+#pragma unroll
+          for (int blk = 0; blk < HR / 16; ++blk) {
+            uint32_t n, cb;
+            hpos(blk, n, cb);
+            float sn, cs;
+            sincosf(sc.fang[n >> 1], &sn, &cs);
+            const bool odd = n & 1;
             float o[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -1032,41 +1134,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               // even row: c g0 - s g1 ; odd row: s g0 + c g1
               o[j] = odd ? fmaf(sn, other, cs * hv) : fmaf(-sn, other, cs * hv);
             }
-            float4* dst = reinterpret_cast<float4*>(fs + (int64_t)n * kP + 16 * blk);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-          }
-        } else {
-          const int n = 16 * quad + (lane & 15);
-          float sn, cs;
-          sincosf(sc.fang[n >> 1], &sn, &cs);
-          const bool odd = n & 1;
-#pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {
-            float o[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float hv = hreg[16 * blk + j];
-              const float other = __shfl_xor_sync(0xffffffffu, hv, 1);
-              o[j] = odd ? fmaf(sn, other, cs * hv) : fmaf(-sn, other, cs * hv);
-            }
-            float4* dst = reinterpret_cast<float4*>(fs + (int64_t)n * kP + 32 * blk +
-                                                    16 * (lane >> 4));
+            float4* dst = reinterpret_cast<float4*>(fs + (int64_t)n * kP + cb);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
           }
         }
+        if (has_next) enter_unit(nxt.unit);
       }
-      h_inv_prev = h_inv;
+      ptx::tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bar_slot_free[s]);
-      // the next chunk's S, D, Yoff if they could not go out above
-      if (ct == 0 && want_yoff && !next_issued &&
-          wait_or_abort(&bar_op_full[(g + 1) & 1], (uint32_t)(((g + 1) >> 1) & 1), &abort_flag,
-                        p.status))
-        issue_yoff(g + 1);
+      if constexpr (!SO) {
+        // the next chunk's Yoff if it could not go out above
+        const bool want_yoff = has_next && (!last || p.ws_hin != nullptr);
+        if (ct == 0 && want_yoff && !next_issued &&
+            wait_or_abort(&bar_op_full[(g + 1) & 1], (uint32_t)(((g + 1) >> 1) & 1), &abort_flag,
+                          p.status))
+          issue_yoff(g + 1);
+      }
       if (!has_next) break;
       sch = nxt;
     }
@@ -1150,11 +1236,84 @@ int num_sms() {
   return n;
 }
 
+// Segmented scan, combine step: for every (sequence, state pair, column),
+// walk the segments in order; the state entering segment j+1 is
+//   h_{j+1} = Rot(Phi_j) (2^{d_j} h_j + G_j)
+// with G_j, d_j, Phi_j the state-only pass's local end state, log2 decay and
+// angle of segment j. Entering states overwrite the G's in place.
+__global__ void seg_combine_kernel(float* __restrict__ ws, const float* __restrict__ scal,
+                                   int64_t nseq, int nseg, int N, int P) {
+  const int KP = N / 2;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= nseq * KP * P) return;
+  const int64_t seq = i / ((int64_t)KP * P);
+  const int k = (int)((i / P) % KP), pcol = (int)(i % P);
+  float h0 = 0.f, h1 = 0.f;
+  for (int j = 0; j < nseg; ++j) {
+    const int64_t u = seq * nseg + j;
+    float* st = ws + u * (int64_t)N * P;
+    const float g0 = st[(int64_t)(2 * k) * P + pcol], g1 = st[(int64_t)(2 * k + 1) * P + pcol];
+    st[(int64_t)(2 * k) * P + pcol] = h0;
+    st[(int64_t)(2 * k + 1) * P + pcol] = h1;
+    const float* sc = scal + u * (int64_t)(1 + KP);
+    const float d = exp2f(sc[0]);
+    float sn, cs;
+    sincosf(sc[1 + k], &sn, &cs);
+    const float t0 = fmaf(d, h0, g0), t1 = fmaf(d, h1, g1);
+    h0 = cs * t0 - sn * t1;
+    h1 = sn * t0 + cs * t1;
+  }
+}
+
+struct SegPlan {
+  int nseg, seg_chunks;
+};
+
+// Whole sequences per work unit, unless there are fewer sequences than SMs:
+// then each is cut into segments so that there are about eight units per SM
+// (each of at least four chunks).
+SegPlan plan_segments(const ScanArgs& a, int sms) {
+  const int64_t nseq = a.batch * a.H;
+  const int nC = (int)((a.L + a.Q - 1) / a.Q);
+  if (nseq >= sms || nC < 8) return {1, nC};
+  int64_t target = (8LL * sms + nseq - 1) / nseq;
+  if (target > nC / 4) target = nC / 4;
+  if (target < 2) return {1, nC};
+  const int sc = (int)((nC + target - 1) / target);
+  return {(nC + sc - 1) / sc, sc};
+}
+
+size_t seg_ws_bytes(const ScanArgs& a, const SegPlan& pl) {
+  if (pl.nseg <= 1) return 0;
+  const int64_t units = a.batch * a.H * pl.nseg;
+  return (size_t)units * (size_t)(a.N * a.P + 1 + a.N / 2) * sizeof(float);
+}
+
+int device_sms() {
+  const int n = num_sms();
+  return n > 0 ? n : 148;
+}
+
+template <int R, int NS, bool SO>
+cudaError_t launch_pass(const CUtensorMap* maps, const TcParams& p, int64_t units, cudaStream_t s) {
+  constexpr uint32_t smem = Cfg<R, NS>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel<R, NS, SO>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int sms = num_sms();
+  if (sms <= 0) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)(units < sms ? units : sms);
+  scan_tc_kernel<R, NS, SO><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3],
+                                                          maps[4], p);
+  return cudaGetLastError();
+}
+
 template <int R, int NS>
 cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
-  CUtensorMap tB, tC, tT, tx, ty;
-  if (!make_bc_map(&tB, a.B, a) || !make_bc_map(&tC, a.C, a) || !make_theta_map(&tT, a.theta, a) ||
-      !make_act_map(&tx, a.x, a) || !make_act_map(&ty, a.out, a))
+  CUtensorMap maps[5];
+  if (!make_bc_map(&maps[0], a.B, a) || !make_bc_map(&maps[1], a.C, a) ||
+      !make_theta_map(&maps[2], a.theta, a) || !make_act_map(&maps[3], a.x, a) ||
+      !make_act_map(&maps[4], a.out, a))
     return cudaErrorInvalidValue;
   TcParams p;
   p.dt = a.dt; p.A = a.A; p.lam = a.lam;
@@ -1162,19 +1321,53 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   p.final_state = a.final_state; p.status = status;
   p.L = a.L; p.H = a.H; p.G = a.G; p.batch = a.batch;
   p.nchunks = (int)((a.L + a.Q - 1) / a.Q);
-  constexpr uint32_t smem = Cfg<R, NS>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel<R, NS>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const int sms = num_sms();
-  if (sms <= 0) return cudaErrorInvalidValue;
+  p.ws_state = nullptr; p.ws_scal = nullptr; p.ws_hin = nullptr;
+  const SegPlan pl = plan_segments(a, device_sms());
+  p.nseg = pl.nseg;
+  p.seg_chunks = pl.seg_chunks;
   const int64_t nseq = a.batch * a.H;
-  const unsigned grid = (unsigned)(nseq < sms ? nseq : sms);
-  scan_tc_kernel<R, NS><<<grid, kThreads, smem, s>>>(tB, tC, tT, tx, ty, p);
-  return cudaGetLastError();
+  if (pl.nseg <= 1) return launch_pass<R, NS, false>(maps, p, nseq, s);
+  // segmented: state-only pass, combine, full pass from the entering states
+  const size_t need = seg_ws_bytes(a, pl);
+  float* ws = static_cast<float*>(a.workspace);
+  bool owned = false;
+  if (ws == nullptr) {
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), need, s);
+    if (e != cudaSuccess) return e;
+    owned = true;
+  } else if (a.workspace_bytes < need) {
+    return cudaErrorInvalidValue;
+  }
+  const int64_t units = nseq * pl.nseg;
+  p.ws_state = ws;
+  p.ws_scal = ws + units * a.N * a.P;
+  p.final_state = nullptr;
+  cudaError_t e = launch_pass<R, NS, true>(maps, p, units, s);
+  if (e == cudaSuccess) {
+    const int64_t n = nseq * (a.N / 2) * a.P;
+    seg_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, p.ws_scal, nseq, pl.nseg,
+                                                                   (int)a.N, (int)a.P);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    p.ws_state = nullptr;
+    p.ws_hin = ws;
+    p.final_state = a.final_state;
+    e = launch_pass<R, NS, false>(maps, p, units, s);
+  }
+  if (owned) {
+    const cudaError_t f = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = f;
+  }
+  return e;
 }
 
 }  // namespace
+
+size_t scan_tc_workspace_bytes(const ScanArgs& a) {
+  if (!scan_tc_supported(a.N, a.P, a.R, a.Q)) return 0;
+  return seg_ws_bytes(a, plan_segments(a, device_sms()));
+}
 
 bool scan_tc_supported(int64_t N, int64_t P, int R, int Q) {
   if (P != kP) return false;

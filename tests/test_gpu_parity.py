@@ -254,3 +254,49 @@ def test_prefill_then_decode_matches_longer_prefill(orc, bf16):
     (assert_bf16_out if bf16 else assert_f32)(y1.float().cpu().numpy(), y_ref[:, L],
                                               "decoded token")
     (assert_bf16 if bf16 else assert_f32)(fs.cpu().numpy(), fs_ref, "state after decode")
+
+
+# ---------------------------------------------------------------- segmented prefill
+# Fewer (b, h) sequences than SMs: the tensor-core path cuts each sequence into
+# segments (state-only pass, ordered combine, full pass). These shapes are
+# small enough for the oracle yet give several segments per sequence.
+SEG_CASES = [
+    # L, chunk, R, G, H, N
+    (2048, 64, 1, 1, 2, 128),
+    (2000, 64, 1, 1, 2, 64),     # ragged last chunk and segment
+    (1000, 16, 4, 1, 2, 128),
+    (777, 32, 2, 2, 4, 128),
+]
+
+
+@pytest.mark.parametrize("case", SEG_CASES, ids=lambda c: "L%d_Q%d_R%d_G%d_H%d_N%d" % c)
+def test_segmented_prefill(orc, case):
+    L, Q, R, G, H, N = case
+    shape = m3synth.ScanShape(1, L, H, G, 64, N, R=R, chunk=Q, bf16=True, rms_bc=True)
+    dims = m3.make_dims(1, L, H, G, 64, N, m3.M3_BF16)
+    assert m3.m3_scan_workspace_bytes(dims, R, Q) > 0, "expected a segmented launch"
+    inp = m3synth.scan_inputs(shape, seed=500 + L)
+    y, fs = _gpu_scan(inp, shape)
+    y_ref, fs_ref = _oracle(orc, inp)
+    assert_bf16_out(y, y_ref, "y")
+    assert_bf16(fs, fs_ref, "final_state")
+
+
+def test_segmented_prefill_caller_workspace():
+    L, Q, R, H, N = 2048, 64, 1, 2, 128
+    shape = m3synth.ScanShape(1, L, H, 1, 64, N, R=R, chunk=Q, bf16=True, rms_bc=True)
+    d = to_device(m3synth.scan_inputs(shape, seed=7), True)
+    dims = m3.make_dims(1, L, H, 1, 64, N, m3.M3_BF16)
+    nbytes = m3.m3_scan_workspace_bytes(dims, R, Q)
+    assert nbytes > 0
+    args = (d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"])
+    kw = dict(R=R, chunk=Q, B_bias=d["B_bias"], C_bias=d["C_bias"])
+    y0, s0 = m3.m3_scan_fwd(*args, **kw)
+    ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device="cuda")
+    y1, s1 = m3.m3_scan_fwd(*args, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(s0, s1)
+    small = torch.empty(nbytes // 8, dtype=torch.float32, device="cuda")
+    with pytest.raises(m3.M3Error) as ei:
+        m3.m3_scan_fwd(*args, workspace=small, **kw)
+    assert ei.value.status == m3.M3_ERR_INVALID_ARG

@@ -121,6 +121,31 @@ m3_status m3_decode_step(float* state, const void* x, const float* dt, const flo
                          const void* B, const void* C, const float* theta, const m3_dims* dims,
                          int R, void* out, void* stream);
 
+/*
+ * Prefill that allocates no device memory: the same computation, arguments
+ * and layouts as m3_scan_fwd, for callers that cannot let a library allocate
+ * GPU memory -- an application or framework whose own allocator owns all of
+ * the device's memory, or a latency-critical caller for which a device
+ * allocation (which may block, or fail under memory pressure) is not
+ * acceptable. (The paper has no counterpart; this is a library interface.)
+ *
+ * The scratch a call needs (m3_scan_workspace_bytes) is taken from a fixed
+ * 32 MiB array of this library in device memory, held on every GPU that loads
+ * the library until the process exits; dims->workspace is ignored. A call
+ * that needs more than 32 MiB returns M3_ERR_UNSUPPORTED without launching
+ * anything (use m3_scan_fwd with a caller workspace for those). The first call
+ * on a device looks up that device's address of the array (a host-side
+ * runtime query, no allocation); make that first call before any stream
+ * capture. All calls share the one array, so calls that can overlap on the
+ * GPU (different streams, or different host threads, on the same device)
+ * race on it; serialise them. The scan writes every scratch byte it reads, so
+ * the previous call's leftovers need no clearing.
+ */
+m3_status m3_scan_fwd_noalloc(const void* x, const float* dt, const float* A, const float* lambda,
+                              const void* B, const void* C, const float* theta,
+                              const m3_dims* dims, int R, int chunk, void* out,
+                              float* final_state, void* stream);
+
 /* Bytes of device scratch m3_scan_fwd wants for these arguments when its
  * pointers are 16-byte aligned (0 if none); (size_t)-1 if the arguments are
  * invalid. Host function: reads the current device's SM count when a device

@@ -17,8 +17,8 @@ M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA, M3_ERR_TIMEOUT = ran
 M3_F32, M3_BF16 = 0, 1
 
 # Exported entry points (kept in step with include/m3scan.h).
-EXPORTS = ("m3_scan_fwd", "m3_decode_step", "m3_scan_workspace_bytes", "m3_status_string",
-           "m3_device_status", "m3_version")
+EXPORTS = ("m3_scan_fwd", "m3_scan_fwd_noalloc", "m3_decode_step", "m3_scan_workspace_bytes",
+           "m3_status_string", "m3_device_status", "m3_version")
 
 
 class M3Error(RuntimeError):
@@ -60,6 +60,8 @@ def load(path: str = LIB_PATH):
     dims_p = ctypes.POINTER(m3_dims)
     lib.m3_scan_fwd.argtypes = [vp] * 7 + [dims_p, i32, i32, vp, vp, vp]
     lib.m3_scan_fwd.restype = i32
+    lib.m3_scan_fwd_noalloc.argtypes = [vp] * 7 + [dims_p, i32, i32, vp, vp, vp]
+    lib.m3_scan_fwd_noalloc.restype = i32
     lib.m3_decode_step.argtypes = [vp] * 10 + [dims_p, i32, vp, vp]
     lib.m3_decode_step.restype = i32
     lib.m3_scan_workspace_bytes.argtypes = [dims_p, i32, i32]
@@ -142,6 +144,24 @@ def m3_scan_fwd(x, dt, A, lam, B, C, theta, R, chunk, out=None, final_state=None
                          ctypes.byref(dims), int(R), int(chunk), _ptr(out), _ptr(final_state),
                          _stream_handle(stream))
     _check(st, "m3_scan_fwd")
+    return out, final_state
+
+
+def m3_scan_fwd_noalloc(x, dt, A, lam, B, C, theta, R, chunk, out, final_state, B_bias=None,
+                        C_bias=None, stream=None):
+    """Prefill like m3_scan_fwd into caller-allocated ``out`` / ``final_state``
+    (``final_state`` may be None); the library allocates no device memory (its
+    scratch is a fixed 32 MiB array; larger needs raise M3Error)."""
+    lib = load()
+    b, L, H, P, R_ = x.shape
+    if R_ != R:
+        raise ValueError("x.shape[-1] must equal R")
+    G, N = B.shape[2], B.shape[3]
+    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias)
+    st = lib.m3_scan_fwd_noalloc(_ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B), _ptr(C),
+                                 _ptr(theta), ctypes.byref(dims), int(R), int(chunk), _ptr(out),
+                                 _ptr(final_state), _stream_handle(stream))
+    _check(st, "m3_scan_fwd_noalloc")
     return out, final_state
 
 

@@ -262,6 +262,10 @@ def run_ours(args, rank, world, local_rank):
             print(json.dumps(bench_decode(torch, m3, dev, args.only, peaks,
                                           steps=args.decode_steps)), flush=True)
         return
+    if args.only == "prefill_long":
+        if rank == 0:
+            print(json.dumps(bench_prefill_long(torch, m3, dev, args, peaks)), flush=True)
+        return
     name = args.only if args.only in ("prefill_siso", "prefill_mimo") else "prefill_siso"
     idx, shape = m3synth.WORKLOADS[name]
     inp = m3synth.scan_inputs(shape, seed=idx + 1000 * rank)
@@ -342,6 +346,7 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
         return
     line["prefill_mimo"] = bench_prefill_other(torch, m3, dev, "prefill_mimo", args, peaks)
+    line["prefill_long"] = bench_prefill_long(torch, m3, dev, args, peaks)
     line["decode"] = {"siso": bench_decode(torch, m3, dev, "decode_siso", peaks),
                       "mimo_r4": bench_decode(torch, m3, dev, "decode_mimo", peaks)}
     sis, mim = line["decode"]["siso"], line["decode"]["mimo_r4"]
@@ -390,6 +395,80 @@ def bench_prefill_other(torch, m3, dev, name, args, peaks):
             "tok_s": shape.tokens / (ms * 1e-3), "ms": ms,
             "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
             "tensor_frac": nflops / (ms * 1e-3) / 1e12 / peaks["bf16"]}
+
+
+def device_inputs(torch, shape, dev, seed):
+    """The synthetic recipe's distributions drawn directly on the device (torch
+    RNG): timing inputs for the long-context workloads, whose host-side
+    generation would dominate the run. Parity tests use m3synth's seeded
+    numpy inputs."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    b, L, H, G, P, N, R = (shape.batch, shape.seqlen, shape.heads, shape.groups, shape.headdim,
+                           shape.dstate, shape.R)
+    f32 = dict(device=dev, dtype=torch.float32)
+
+    def rn(*sz):
+        return torch.randn(*sz, generator=gen, **f32)
+
+    def bc():
+        v = rn(b, L, G, N, R)
+        v = v / torch.sqrt(v.square().mean(dim=-2, keepdim=True) + 1e-6)
+        return v.to(torch.bfloat16)
+
+    A = -torch.exp(torch.rand(H, generator=gen, **f32) * float(np.log(16.0)))
+    dt = torch.nn.functional.softplus(rn(b, L, H) * 0.5 - 1.0)
+    lam = torch.sigmoid(rn(b, L, H))
+    theta = (torch.rand(b, L, G, N // 2, generator=gen, **f32) * 2.0 - 1.0) * float(np.pi)
+    return dict(A=A, dt=dt, lam=lam, theta=theta, B=bc(), C=bc(), B_bias=0.1 * rn(H, N, R),
+                C_bias=0.1 * rn(H, N, R), x=rn(b, L, H, P, R).to(torch.bfloat16))
+
+
+def bench_prefill_long(torch, m3, dev, args, peaks):
+    """The long-context workloads (b1 L65536 H32 P64): SISO N64 and N128 (chunk
+    64), MIMO R4 N128 (chunk 16). 32 sequences for 148 SMs: the scan runs
+    segmented (state-only pass, combine, full pass)."""
+    res = {}
+    stream = torch.cuda.current_stream()
+    for name in ("long_siso_n64", "long_siso_n128", "long_mimo_n128"):
+        idx, shape = m3synth.WORKLOADS[name]
+        d = device_inputs(torch, shape, dev, seed=idx)
+        out = torch.empty_like(d["x"])
+        fs = torch.empty((shape.batch, shape.heads, shape.dstate, shape.headdim),
+                         dtype=torch.float32, device=dev)
+        dims = m3.make_dims(shape.batch, shape.seqlen, shape.heads, shape.groups, shape.headdim,
+                            shape.dstate, m3.M3_BF16)
+        ws_bytes = m3.m3_scan_workspace_bytes(dims, shape.R, shape.chunk)
+        ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device=dev)
+
+        def launch():
+            m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"],
+                           R=shape.R, chunk=shape.chunk, out=out, final_state=fs,
+                           B_bias=d["B_bias"], C_bias=d["C_bias"], workspace=ws, stream=stream)
+
+        for _ in range(3):
+            launch()
+        times = []
+        for _ in range(max(3, min(args.steps, 5))):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = sum(times) / len(times)
+        nbytes, nflops = prefill_bytes(shape), prefill_flops(shape)
+        res[name] = {"workload": "%s b%d L%d H%d P%d N%d R%d chunk%d" % (
+                         name, shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate,
+                         shape.R, shape.chunk),
+                     "tok_s": shape.tokens / (ms * 1e-3), "ms": ms,
+                     "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
+                     "tensor_frac": nflops / (ms * 1e-3) / 1e12 / peaks["bf16"],
+                     "workspace_bytes": ws_bytes,
+                     "inputs": "recipe distributions drawn on the device (torch RNG)"}
+        del d, out, fs, ws
+        torch.cuda.empty_cache()
+    return res
 
 
 def bench_decode(torch, m3, dev, name, peaks, n_sets=16, steps=m3synth.DECODE_STEPS):
@@ -486,7 +565,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="all",
-                    choices=["all", "prefill_siso", "prefill_mimo", "decode_siso", "decode_mimo"],
+                    choices=["all", "prefill_siso", "prefill_mimo", "decode_siso", "decode_mimo",
+                             "prefill_long"],
                     help="run one workload alone (profiling); the default runs them all")
     ap.add_argument("--decode-steps", type=int, default=m3synth.DECODE_STEPS,
                     help="decode steps per CUDA graph with --only decode_*")

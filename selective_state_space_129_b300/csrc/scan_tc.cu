@@ -69,10 +69,10 @@
 namespace m3 {
 namespace {
 
-constexpr int kProWarps = 8, kCoreWarps = 4;
+constexpr int kProWarps = 8, kCoreWarps = 8;
 constexpr int kProThreads = kProWarps * 32;    // 256
-constexpr int kCoreThreads = kCoreWarps * 32;  // 128
-constexpr int kThreads = kProThreads + kCoreThreads;  // 384 (168 registers per thread)
+constexpr int kCoreThreads = kCoreWarps * 32;  // 256: two warps per TMEM lane quadrant
+constexpr int kThreads = kProThreads + kCoreThreads;  // 512 (128 registers per thread)
 constexpr int kWarpTmem = kProWarps;                  // allocates / frees TMEM
 constexpr uint32_t kBarPro = 1, kBarCore = 2;          // named barrier ids
 constexpr int kQR = 64;  // rows of the flattened (token, rank) tile
@@ -299,17 +299,24 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
-// Shared-memory operand descriptors of the 128-byte-swizzled tiles.
-// K-major: 16-element K step kk of a [rows][K] tile.
-__device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk, uint32_t rows) {
-  return ptx::smem_desc_sw128(base + (uint32_t)(kk >> 2) * rows * 128u + (uint32_t)(kk & 3) * 32u,
-                              16u, 1024u);
+// A descriptor split into its words; the MMAs of one operand tile differ only
+// in the start-address field (low word), so each is the base plus a constant.
+struct Desc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ Desc make_desc(uint32_t addr, uint32_t lbo) {
+  const uint64_t d = ptx::smem_desc_sw128(addr, lbo, 1024u);
+  return Desc{(uint32_t)d, (uint32_t)(d >> 32)};
 }
-// MN-major: 16-row K step kk of a [K][MN] tile whose 64-wide MN blocks are
-// `lbo` bytes apart.
-__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk, uint32_t lbo) {
-  return ptx::smem_desc_sw128(base + (uint32_t)kk * 2048u, lbo, 1024u);
+// start address advanced by `byte_off` (a multiple of 16, staying in the window)
+__device__ __forceinline__ uint64_t desc_at(const Desc& d, uint32_t byte_off) {
+  return ((uint64_t)d.hi << 32) | (uint64_t)(d.lo + (byte_off >> 4));
 }
+// byte offsets of the 16-element K step kk: K-major [rows][K] tiles, MN-major tiles
+__host__ __device__ constexpr uint32_t koff_k(int kk, uint32_t rows) {
+  return (uint32_t)(kk >> 2) * rows * 128u + (uint32_t)(kk & 3) * 32u;
+}
+__host__ __device__ constexpr uint32_t koff_mn(int kk) { return (uint32_t)kk * 2048u; }
 
 // Bounded wait on an mbarrier phase; on expiry record the status word and the
 // CTA's abort flag. Returns false if the CTA is (now) aborting.
@@ -403,9 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_dtraw[2][64], s_lamraw[2][64], s_bnx[2][64];
   __shared__ float s_tot[2][TG][KP];   // per token group: angle total (hi, lo)
   __shared__ float s_carry[2][2][KP];  // [chunk parity][hi, lo][pair]
-  __shared__ float s_red[3][kProWarps];
+  __shared__ unsigned int s_max[2][3];  // per chunk parity: bounds of |B|, |C|, |x| (float bits)
   __shared__ float s_hred[kCoreWarps];
   __shared__ float s_bias_red[2][kProWarps];
+  // R > 1: the head's B / C bias transposed to [rank][row] (registers for R = 1)
+  __shared__ __align__(16) float s_biasT[2][(R > 1) ? R : 1][(R > 1) ? NS : 4];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t H = p.H, G = p.G;
@@ -418,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     abort_flag = 0;
+    for (int i = 0; i < 6; ++i) (&s_max[0][0])[i] = 0u;
     ptx::mbar_init(&bar_raw_full, 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bar_op_full[s], 1);
@@ -457,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kk2 = tid % KP2, tg = tid / KP2;
     const int k0 = 2 * kk2;  // this thread's pairs: k0, k0 + 1 (rows 4kk2 .. 4kk2 + 3)
     int64_t cur_h = -1;
-    float bb[4][R], cb[4][R];
+    float bb[4][1], cb[4][1];  // R = 1: the four bias values of this thread's rows
     float bmax_bias = 0.f, cmax_bias = 0.f;
     int inflight = -1;  // phase parity of a raw load issued and not yet consumed
     // the first chunk's inputs
@@ -484,16 +494,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur_h = h;
         A_h = p.A[h];
         float mb = 0.f, mc = 0.f;
+        if constexpr (R == 1) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const int64_t ix = (h * NS + 4 * kk2 + e) * R + r;
-            bb[e][r] = p.B_bias ? p.B_bias[ix] : 0.f;
-            cb[e][r] = p.C_bias ? p.C_bias[ix] : 0.f;
-            mb = fmaxf(mb, fabsf(bb[e][r]));
-            mc = fmaxf(mc, fabsf(cb[e][r]));
+          for (int e = 0; e < 4; ++e) {
+            const int64_t ix = h * NS + 4 * kk2 + e;
+            bb[e][0] = p.B_bias ? p.B_bias[ix] : 0.f;
+            cb[e][0] = p.C_bias ? p.C_bias[ix] : 0.f;
+            mb = fmaxf(mb, fabsf(bb[e][0]));
+            mc = fmaxf(mc, fabsf(cb[e][0]));
           }
+        } else {
+          // the previous head's bias was last read before this chunk's first barrier
+          for (int i = tid; i < NS * R; i += kProThreads) {
+            const float vb = p.B_bias ? p.B_bias[h * NS * R + i] : 0.f;
+            const float vc = p.C_bias ? p.C_bias[h * NS * R + i] : 0.f;
+            s_biasT[0][i % R][i / R] = vb;
+            s_biasT[1][i % R][i / R] = vc;
+            mb = fmaxf(mb, fabsf(vb));
+            mc = fmaxf(mc, fabsf(vc));
+          }
+        }
         mb = warp_max(mb);
         mc = warp_max(mc);
         if (lane == 0) {
@@ -644,12 +664,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       {
+        // non-negative floats order like their bit patterns
         const float bm = warp_max(bf_absmax(bacc)), cm = warp_max(bf_absmax(cacc));
         const float xm = warp_max(bf_absmax(xacc));
         if (lane == 0) {
-          s_red[0][warp] = bm;
-          s_red[1][warp] = cm;
-          s_red[2][warp] = xm;
+          atomicMax(&s_max[g & 1][0], __float_as_uint(bm));
+          atomicMax(&s_max[g & 1][1], __float_as_uint(cm));
+          atomicMax(&s_max[g & 1][2], __float_as_uint(xm));
         }
       }
       ptx::named_bar_sync(kBarPro, kProThreads);
@@ -664,12 +685,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 3. per-chunk fp16 scales of Bt, Ct and w X
       float sigB, invB, sigC, invC, sigX, invX;
       {
-        float mb = 0.f, mc = 0.f, mx = 0.f;
-#pragma unroll
-        for (int w = 0; w < kProWarps; ++w) {
-          mb = fmaxf(mb, s_red[0][w]);
-          mc = fmaxf(mc, s_red[1][w]);
-          mx = fmaxf(mx, s_red[2][w]);
+        const float mb = __uint_as_float(s_max[g & 1][0]);
+        const float mc = __uint_as_float(s_max[g & 1][1]);
+        const float mx = __uint_as_float(s_max[g & 1][2]);
+        // the other parity's words are free (read last chunk): clear them for the next
+        if (tid == 0) {
+          s_max[(g + 1) & 1][0] = 0u;
+          s_max[(g + 1) & 1][1] = 0u;
+          s_max[(g + 1) & 1][2] = 0u;
         }
         // a rotated pair keeps its norm: |Rot(v)_i| <= sqrt(2) max|v| < 2 max|v|
         pow2_scale(2.f * (mb + bmax_bias), &sigB, &invB);
@@ -704,8 +727,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the carry of pair k0 is updated by group TG-1, that of k0+1 by TG-2
         if (tg >= TG - 2) {
           const int k = (tg == TG - 1) ? k0 : k0 + 1;
+          // float-float sum of the group totals as a tree, then the carry
+          float th[TG], tl[TG];
+#pragma unroll
+          for (int q = 0; q < TG; ++q) {
+            th[q] = s_tot[0][q][k];
+            tl[q] = s_tot[1][q][k];
+          }
+#pragma unroll
+          for (int w = 1; w < TG; w <<= 1)
+#pragma unroll
+            for (int q = 0; q + w < TG; q += 2 * w) ff_add(th[q], tl[q], th[q + w], tl[q + w]);
           float eh = (tg == TG - 1) ? ch0 : ch1, el = (tg == TG - 1) ? cl0 : cl1;
-          for (int q = 0; q < TG; ++q) ff_add(eh, el, s_tot[0][q][k], s_tot[1][q][k]);
+          ff_add(eh, el, th[0], tl[0]);
           ff_wrap(eh, el);
           s_carry[cpar ^ 1][0][k] = eh;
           s_carry[cpar ^ 1][1][k] = el;
@@ -738,10 +772,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           // elements (n, r) for n = 4kk2 + e; .x holds pair k0 (e = 0, 1), .y pair k0+1 (e = 2, 3)
+          float4 bq, cq;  // bias of rows 4kk2 .. 4kk2 + 3 at rank r
+          if constexpr (R == 1) {
+            bq = make_float4(bb[0][0], bb[1][0], bb[2][0], bb[3][0]);
+            cq = make_float4(cb[0][0], cb[1][0], cb[2][0], cb[3][0]);
+          } else {
+            bq = *reinterpret_cast<const float4*>(&s_biasT[0][r][4 * kk2]);
+            if constexpr (!SO) cq = *reinterpret_cast<const float4*>(&s_biasT[1][r][4 * kk2]);
+          }
           float2 b0 = make_float2(bf_at(bw[i], 0 * R + r), bf_at(bw[i], 2 * R + r));
           float2 b1 = make_float2(bf_at(bw[i], 1 * R + r), bf_at(bw[i], 3 * R + r));
-          b0 = add2(b0, make_float2(bb[0][r], bb[2][r]));
-          b1 = add2(b1, make_float2(bb[1][r], bb[3][r]));
+          b0 = add2(b0, make_float2(bq.x, bq.z));
+          b1 = add2(b1, make_float2(bq.y, bq.w));
           // Rot(-Phi) = [[cos, sin], [-sin, cos]]
           const float2 bt0 = fma2(csB, b0, mul2(snB, b1)), bt1 = fma2(csB, b1, mul2(nsnB, b0));
           const uint32_t o = tile_off((uint32_t)(t * R + r), 4u * kk2, 64u);
@@ -749,8 +791,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (!SO) {
             float2 c0 = make_float2(bf_at(cw[i], 0 * R + r), bf_at(cw[i], 2 * R + r));
             float2 c1 = make_float2(bf_at(cw[i], 1 * R + r), bf_at(cw[i], 3 * R + r));
-            c0 = add2(c0, make_float2(cb[0][r], cb[2][r]));
-            c1 = add2(c1, make_float2(cb[1][r], cb[3][r]));
+            c0 = add2(c0, make_float2(cq.x, cq.z));
+            c1 = add2(c1, make_float2(cq.y, cq.w));
             const float2 ct0 = fma2(csC, c0, mul2(snC, c1)), ct1 = fma2(csC, c1, mul2(nsnC, c0));
             sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
           }
@@ -798,16 +840,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) {
         const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
         ptx::tc_fence_after_sync();
+        const Desc dBk = make_desc(opb + K::kOpBt, 16u), dBm = make_desc(opb + K::kOpBt, 64u * 128u);
+        const Desc dXw = make_desc(opb + K::kOpXw, 64u * 128u);
         if constexpr (!SO) {
+          const Desc dCk = make_desc(opb + K::kOpCt, 16u);
 #pragma unroll
           for (int kk = 0; kk < NS / 16; ++kk)
-            ptx::mma_bf16_ss(tset + kColS, desc_k(opb + K::kOpCt, kk, 64),
-                             desc_k(opb + K::kOpBt, kk, 64), kIdS, kk > 0);
+            ptx::mma_bf16_ss(tset + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
+                             kIdS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < kQR / 16; ++kk)
-          ptx::mma_bf16_ss(tset + kColD, desc_mn(opb + K::kOpBt, kk, 64u * 128u),
-                           desc_mn(opb + K::kOpXw, kk, 64u * 128u), kIdD, kk > 0);
+          ptx::mma_bf16_ss(tset + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD,
+                           kk > 0);
         ptx::mma_commit(&bar_acc_full[s]);
         ptx::mbar_arrive(&bar_op_full[s]);
       }
@@ -820,6 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================================================ core (+ MMA issue)
     const int ct = tid - kProThreads;  // 0..127
     const int quad = warp & 3;         // TMEM lane quadrant of this warp
+    const int half = (warp - kProWarps) >> 2;  // which 32-column half of the tiles it takes
+    const int cwarp = warp - kProWarps;        // 0 .. kCoreWarps - 1
     float hreg[HR];
     float h_inv_prev = 1.f;
     float dsum = 0.f;  // log2 decay accumulated over the unit (state-only pass)
@@ -827,10 +874,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto hpos = [&](int blk, uint32_t& n, uint32_t& cb) {
       if constexpr (NS == 128) {
         n = (uint32_t)(32 * quad + lane);  // M=128 accumulator layout: lane = row
-        cb = 16u * blk;
+        cb = 32u * half + 16u * blk;
       } else {
         n = (uint32_t)(16 * quad + (lane & 15));  // M=64 layout: 16 rows per quadrant
-        cb = 32u * blk + 16u * (lane >> 4);
+        cb = 32u * half + 16u * (lane >> 4);
       }
     };
     // fp16 copy of sigma * hreg into the state tile (operand of the next Yoff)
@@ -856,11 +903,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = g & 1;
       const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
       const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
+      const Desc dCk = make_desc(opb + K::kOpCt, 16u), dH = make_desc(sbase + K::kH, (uint32_t)NS * 128u);
       ptx::tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < NS / 16; ++kk)
-        ptx::mma_bf16_ss(tset + kColYo, desc_k(opb + K::kOpCt, kk, 64),
-                         desc_mn(sbase + K::kH, kk, (uint32_t)NS * 128u), kIdYo, kk > 0);
+        ptx::mma_bf16_ss(tset + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)), kIdYo,
+                         kk > 0);
     };
     // State entering unit u: the given explicit-frame state (the unit's local
     // angle frame starts at zero, so no rotation) or zero; in the full pass its
@@ -887,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (!SO) {
           m = warp_max(m);
-          if (lane == 0) s_hred[quad] = m;
+          if (lane == 0) s_hred[cwarp] = m;
           ptx::named_bar_sync(kBarCore, kCoreThreads);
           float mm = 0.f;
 #pragma unroll
@@ -931,9 +979,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float einv = (float)((int)((__float_as_uint(invB * invC) >> 23) & 0xffu) - 127);
         const float lt = sc.lam2[t] + einv;
         const float gdiag = sc.gam[t] * (invB * invC);
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          // skip a warp whose 16 rows x 32 columns lie wholly above the diagonal
+        // this warp's 32-column block; skip it when its 16 rows x 32 columns lie
+        // wholly above the diagonal
+        for (int blk = half; blk == half; ++blk) {
           if ((32 * blk) / R > (16 * quad + 15) / R) continue;
           uint32_t sv[16];
           ptx::tmem_ld16_16x32bx2<16>(tset + kColS + ((uint32_t)(32 * quad) << 16) + 32u * blk, sv);
@@ -975,15 +1023,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ct == 0) {
           // Y = P X (P = high + low parts) of this chunk
           const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
+          const Desc dPh = make_desc(sbase + K::kPh, 16u), dPl = make_desc(sbase + K::kPl, 16u);
+          const Desc dX = make_desc(opb + K::kOpXo, 64u * 128u);
           ptx::tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < kQR / 16; ++kk)
-            ptx::mma_bf16_ss(tset + kColY, desc_k(sbase + K::kPh, kk, 64),
-                             desc_mn(opb + K::kOpXo, kk, 64u * 128u), kIdY, kk > 0);
+            ptx::mma_bf16_ss(tset + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
+                             kIdY, kk > 0);
 #pragma unroll
           for (int kk = 0; kk < kQR / 16; ++kk)
-            ptx::mma_bf16_ss(tset + kColY, desc_k(sbase + K::kPl, kk, 64),
-                             desc_mn(opb + K::kOpXo, kk, 64u * 128u), kIdY, 1u);
+            ptx::mma_bf16_ss(tset + kColY, desc_at(dPl, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
+                             kIdY, 1u);
           ptx::mma_commit(&bar_y_full[s]);
         }
       }
@@ -997,9 +1047,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int blk = 0; blk < HR / 16; ++blk) {
           uint32_t d[16];
           if constexpr (NS == 128) {
-            ptx::tmem_ld16(tset + kColD + ((uint32_t)(32 * quad) << 16) + 16u * blk, d);
+            ptx::tmem_ld16(tset + kColD + ((uint32_t)(32 * quad) << 16) + 32u * half + 16u * blk, d);
           } else {
-            ptx::tmem_ld16_16x32bx2<16>(tset + kColD + ((uint32_t)(32 * quad) << 16) + 32u * blk, d);
+            ptx::tmem_ld16_16x32bx2<16>(tset + kColD + ((uint32_t)(32 * quad) << 16) + 32u * half, d);
           }
           ptx::tmem_ld_wait(d);
 #pragma unroll
@@ -1016,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool next_issued = false;
       if constexpr (!SO) {
         hmax = warp_max(hmax);
-        if (lane == 0) s_hred[quad] = hmax;
+        if (lane == 0) s_hred[cwarp] = hmax;
         // Y (and this chunk's Yoff, which read the previous state copy) complete;
         // the output staging tile is free again
         if (ct == 0) {
@@ -1051,8 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int a = 16 * quad + (lane & 15);
           const float el = sc.eL[a / R] * (invC * h_inv_prev);
           const bool has_yoff = !first || p.ws_hin != nullptr;
-#pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {
+          for (int blk = half; blk == half; ++blk) {
             uint32_t yv[16];
             const uint32_t ta = ((uint32_t)(32 * quad) << 16) + 32u * blk;
             ptx::tmem_ld16_16x32bx2<16>(tset + kColY + ta, yv);

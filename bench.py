@@ -280,16 +280,18 @@ def run_ours(args, rank, world, local_rank):
                        chunk=shape.chunk, out=out, final_state=fs, B_bias=d["B_bias"],
                        C_bias=d["C_bias"], stream=stream)
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        launch()
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
+    # the clock sampler starts before the warm-up, so that its start-up pause
+    # does not leave an idle (down-clocked) GPU right before the timed steps
     with Clocks(local_rank) as clk:
+        for _ in range(args.warmup):
+            flush.zero_()
+            launch()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         for e0, e1 in ev:
             flush.zero_()
             e0.record(stream)

@@ -192,6 +192,9 @@ m3_status m3_decode_step(float* state, const void* x, const float* dt, const flo
   a.state = state; a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B_prev = B_prev;
   a.x_prev = x_prev; a.B = B; a.C = C; a.theta = theta; a.B_bias = dims->B_bias;
   a.C_bias = dims->C_bias; a.out = out; a.batch = b; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R;
+  a.status = nullptr;
+  st = from_cuda(m3::status_word(&a.status));
+  if (st != M3_OK) return st;
   return from_cuda(m3::launch_decode(a, dims->act_dtype == M3_BF16,
                                      static_cast<cudaStream_t>(stream)));
 }

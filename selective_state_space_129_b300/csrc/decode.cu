@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace m3 {
 namespace {
@@ -225,6 +226,288 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
   }
 }
 
+
+// ---------------------------------------------------------------- streaming
+// Persistent form of the same step. A CTA walks the (batch, head) units
+// u = blockIdx.x, + gridDim.x, ...; its thread 0 stages each unit's state and
+// activations into shared memory with bulk asynchronous copies, kStages units
+// ahead, so that the state stream from HBM does not wait for the arithmetic or
+// for the per-unit barriers. The new state goes straight from registers to
+// global memory. Used when every per-unit block is 16-byte aligned and a
+// multiple of 16 bytes long (the copy engine's rule); other shapes take the
+// kernel above.
+constexpr int kSThreads = 256;
+constexpr int kSWarps = kSThreads / 32;
+constexpr int kStages = 2;
+constexpr uint64_t kStreamWaitNs = 2000000000ull;  // 2 s per wait
+
+__host__ __device__ inline uint32_t up16(uint64_t v) { return (uint32_t)((v + 15) & ~uint64_t(15)); }
+
+// Byte offsets of one unit's blocks inside a stage.
+struct StreamLayout {
+  uint32_t st, x, xp, B, Bp, C, th, bb, cb, dt, lm, bytes, tx;
+};
+
+inline StreamLayout stream_layout(const DecodeArgs& a, int act) {
+  const uint64_t N = a.N, P = a.P, R = a.R;
+  const bool prev = a.B_prev != nullptr;
+  StreamLayout L{};
+  uint32_t o = 0;
+  L.st = o; o += up16(N * P * 4);
+  L.x = o; o += up16(P * R * act);
+  L.xp = o; o += prev ? up16(P * R * act) : 0u;
+  L.B = o; o += up16(N * R * act);
+  L.Bp = o; o += prev ? up16(N * R * act) : 0u;
+  L.C = o; o += up16(N * R * act);
+  L.th = o; o += up16(N / 2 * 4);
+  L.bb = o; o += a.B_bias ? up16(N * R * 4) : 0u;
+  L.cb = o; o += a.C_bias ? up16(N * R * 4) : 0u;
+  L.dt = o; o += 16;
+  L.lm = o; o += 16;
+  L.bytes = o;
+  L.tx = o;  // every block is copied whole (sizes are multiples of 16)
+  return L;
+}
+
+inline size_t stream_smem_bytes(const DecodeArgs& a, const StreamLayout& L) {
+  const size_t N = a.N, P = a.P, R = a.R;
+  return (size_t)kStages * L.bytes +
+         sizeof(float) * (3 * N * R + N + (size_t)kSWarps * P * R + (size_t)a.H);
+}
+
+template <typename T, int R>
+__global__ void __launch_bounds__(kSThreads, 2)
+    decode_stream_kernel(DecodeArgs a, StreamLayout L, int units) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ uint64_t full[kStages];
+  __shared__ int abort_flag;
+  const int N = (int)a.N, P = (int)a.P, K2 = N / 2, PQ = P / 4, H = (int)a.H;
+  const int hpg = (int)(a.H / a.G);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* bg = reinterpret_cast<float*>(dsm + (size_t)kStages * L.bytes);  // gamma (B + bias) [N][R]
+  float* bp = bg + N * R;        // beta_hat (B_prev + bias)  [N][R]
+  float* cc = bp + N * R;        // C + bias                  [N][R]
+  float* rc = cc + N * R;        // alpha cos                 [K2]
+  float* rs = rc + K2;           // alpha sin                 [K2]
+  float* yred = rs + K2;         // partial y per warp        [kSWarps][P][R]
+  float* sA = yred + kSWarps * P * R;  // A                   [H]
+  const bool has_prev = a.B_prev != nullptr;
+  const int q = tid % PQ;  // this thread's column quad (PQ divides 32)
+  const int items = K2 * PQ;
+
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) ptx::mbar_init(&full[s], 1);
+    ptx::fence_mbar_init();
+  }
+  for (int i = tid; i < H; i += kSThreads) sA[i] = a.A[i];
+  __syncthreads();
+
+  // thread 0: stage unit u into stage s
+  auto issue = [&](int u, int s) {
+    const int b = u / H, h = u - b * H, g = h / hpg;
+    uint8_t* st = dsm + (size_t)s * L.bytes;
+    uint64_t* bar = &full[s];
+    const int64_t nr = (int64_t)N * R, pr = (int64_t)P * R;
+    const int64_t bc = ((int64_t)b * a.G + g) * nr;
+    ptx::fence_proxy_async_smem();  // earlier reads of the stage come first
+    ptx::mbar_arrive_expect_tx(bar, L.tx);
+    ptx::bulk_load(st + L.st, a.state + (int64_t)u * N * P, (uint32_t)N * P * 4, bar);
+    ptx::bulk_load(st + L.x, static_cast<const T*>(a.x) + (int64_t)u * pr,
+                   (uint32_t)(pr * sizeof(T)), bar);
+    if (has_prev)
+      ptx::bulk_load(st + L.xp, static_cast<const T*>(a.x_prev) + (int64_t)u * pr,
+                     (uint32_t)(pr * sizeof(T)), bar);
+    ptx::bulk_load(st + L.B, static_cast<const T*>(a.B) + bc, (uint32_t)(nr * sizeof(T)), bar);
+    if (has_prev)
+      ptx::bulk_load(st + L.Bp, static_cast<const T*>(a.B_prev) + bc, (uint32_t)(nr * sizeof(T)),
+                     bar);
+    ptx::bulk_load(st + L.C, static_cast<const T*>(a.C) + bc, (uint32_t)(nr * sizeof(T)), bar);
+    ptx::bulk_load(st + L.th, a.theta + ((int64_t)b * a.G + g) * K2, (uint32_t)K2 * 4, bar);
+    if (a.B_bias) ptx::bulk_load(st + L.bb, a.B_bias + (int64_t)h * nr, (uint32_t)nr * 4, bar);
+    if (a.C_bias) ptx::bulk_load(st + L.cb, a.C_bias + (int64_t)h * nr, (uint32_t)nr * 4, bar);
+    // dt, lambda of unit u: the aligned 16-byte window that holds them
+    ptx::bulk_load(st + L.dt, a.dt + (u & ~3), 16u, bar);
+    ptx::bulk_load(st + L.lm, a.lam + (u & ~3), 16u, bar);
+  };
+  if (tid == 0)
+    for (int j = 0; j < kStages; ++j) {
+      const int u = blockIdx.x + j * gridDim.x;
+      if (u < units) issue(u, j);
+    }
+
+  int k = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
+    const int s = k % kStages;
+    const uint8_t* stg = dsm + (size_t)s * L.bytes;
+    if (!ptx::mbar_wait(&full[s], (uint32_t)((k / kStages) & 1), kStreamWaitNs)) {
+      atomicOr(a.status, 2u);
+      abort_flag = 1;
+    }
+    const int h = u % H;
+    const float d = reinterpret_cast<const float*>(stg + L.dt)[u & 3];
+    const float lm = reinterpret_cast<const float*>(stg + L.lm)[u & 3];
+    const float alpha = expf(d * sA[h]);
+    const float gamma = lm * d, bhat = (1.f - lm) * d;
+    const T* sB = reinterpret_cast<const T*>(stg + L.B);
+    const T* sBp = reinterpret_cast<const T*>(stg + L.Bp);
+    const T* sC = reinterpret_cast<const T*>(stg + L.C);
+    const float* sbb = reinterpret_cast<const float*>(stg + L.bb);
+    const float* scb = reinterpret_cast<const float*>(stg + L.cb);
+    for (int i = tid; i < N * R; i += kSThreads) {
+      const float bb = a.B_bias ? sbb[i] : 0.f;
+      const float cb = a.C_bias ? scb[i] : 0.f;
+      bg[i] = gamma * (ld_act(sB + i) + bb);
+      bp[i] = has_prev ? bhat * (ld_act(sBp + i) + bb) : 0.f;
+      cc[i] = ld_act(sC + i) + cb;
+    }
+    const float* sth = reinterpret_cast<const float*>(stg + L.th);
+    for (int kk = tid; kk < K2; kk += kSThreads) {
+      float sn, cs;
+      sincosf(d * sth[kk], &sn, &cs);
+      rc[kk] = alpha * cs;
+      rs[kk] = alpha * sn;
+    }
+    const T* sx = reinterpret_cast<const T*>(stg + L.x);
+    const T* sxp = reinterpret_cast<const T*>(stg + L.xp);
+    float xr[4][R], xpr[4][R], yp[4][R];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        xr[c][r] = ld_act(sx + (4 * q + c) * R + r);
+        xpr[c][r] = has_prev ? ld_act(sxp + (4 * q + c) * R + r) : 0.f;
+        yp[c][r] = 0.f;
+      }
+    __syncthreads();
+    if (abort_flag) break;  // uniform: read after the barrier
+
+    const float* sst = reinterpret_cast<const float*>(stg + L.st);
+    float* gst = a.state + (int64_t)u * N * P;
+    for (int it = tid; it < items; it += kSThreads) {
+      const int kq = it / PQ;
+      float4 h0 = *reinterpret_cast<const float4*>(sst + (2 * kq) * P + 4 * q);
+      float4 h1 = *reinterpret_cast<const float4*>(sst + (2 * kq + 1) * P + 4 * q);
+      float bp0[R], bp1[R], bg0[R], bg1[R], c0[R], c1[R];
+      ld_row<R>(bp + (2 * kq) * R, bp0);
+      ld_row<R>(bp + (2 * kq + 1) * R, bp1);
+      ld_row<R>(bg + (2 * kq) * R, bg0);
+      ld_row<R>(bg + (2 * kq + 1) * R, bg1);
+      ld_row<R>(cc + (2 * kq) * R, c0);
+      ld_row<R>(cc + (2 * kq + 1) * R, c1);
+      const float ac = rc[kq], as = rs[kq];
+      float* v0 = reinterpret_cast<float*>(&h0);
+      float* v1 = reinterpret_cast<float*>(&h1);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float g0 = v0[c], g1 = v1[c], u0 = 0.f, u1 = 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          g0 = fmaf(bp0[r], xpr[c][r], g0);
+          g1 = fmaf(bp1[r], xpr[c][r], g1);
+          u0 = fmaf(bg0[r], xr[c][r], u0);
+          u1 = fmaf(bg1[r], xr[c][r], u1);
+        }
+        const float n0 = fmaf(ac, g0, fmaf(-as, g1, u0));
+        const float n1 = fmaf(as, g0, fmaf(ac, g1, u1));
+        v0[c] = n0;
+        v1[c] = n1;
+#pragma unroll
+        for (int r = 0; r < R; ++r) yp[c][r] = fmaf(c0[r], n0, fmaf(c1[r], n1, yp[c][r]));
+      }
+      *reinterpret_cast<float4*>(gst + (2 * kq) * P + 4 * q) = h0;
+      *reinterpret_cast<float4*>(gst + (2 * kq + 1) * P + 4 * q) = h1;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        for (int o = PQ; o < 32; o <<= 1) yp[c][r] += __shfl_xor_sync(0xffffffffu, yp[c][r], o);
+    if (lane < PQ) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int r = 0; r < R; ++r) yred[(warp * P + 4 * q + c) * R + r] = yp[c][r];
+    }
+    __syncthreads();
+    // stage s is read: refill it with the unit kStages ahead
+    if (tid == 0) {
+      const int un = u + kStages * (int)gridDim.x;
+      if (un < units) issue(un, s);
+    }
+    T* out = static_cast<T*>(a.out) + (int64_t)u * P * R;
+    for (int i = tid; i < P * R; i += kSThreads) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSWarps; ++w) acc += yred[w * P * R + i];
+      st_act(out + i, acc);
+    }
+  }
+  // after an abort, let the copies in flight land before the CTA ends
+  if (tid == 0) {
+    for (int j = 0; j < kStages; ++j, ++k) {
+      const int u = blockIdx.x + k * (int)gridDim.x;
+      if (u >= units) break;
+      ptx::mbar_wait(&full[k % kStages], (uint32_t)((k / kStages) & 1), kStreamWaitNs);
+    }
+  }
+}
+
+// The streaming kernel's conditions: every per-unit block 16-byte aligned and
+// a multiple of 16 bytes, the dt / lambda windows inside their arrays, and
+// two CTAs' shared memory on one SM.
+bool stream_ok(const DecodeArgs& a, int act, size_t* smem) {
+  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const int64_t N = a.N, P = a.P, R = a.R;
+  if (P % 4 != 0 || 32 % (P / 4) != 0) return false;
+  if ((N * P * 4) % 16 || (P * R * act) % 16 || (N * R * act) % 16 || (N / 2 * 4) % 16) return false;
+  if ((a.B_bias || a.C_bias) && (N * R * 4) % 16) return false;
+  if ((a.batch * a.H) % 4 != 0) return false;
+  if (!al(a.state) || !al(a.x) || !al(a.x_prev) || !al(a.B) || !al(a.B_prev) || !al(a.C) ||
+      !al(a.theta) || !al(a.B_bias) || !al(a.C_bias) || !al(a.dt) || !al(a.lam))
+    return false;
+  const StreamLayout L = stream_layout(a, act);
+  *smem = stream_smem_bytes(a, L);
+  return *smem <= 112 * 1024;
+}
+
+int stream_grid(int units) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 148;
+  }
+  const int g = 2 * sms;
+  return units < g ? units : g;
+}
+
+template <typename T>
+cudaError_t launch_stream_t(const DecodeArgs& a, size_t smem, cudaStream_t s) {
+  const StreamLayout L = stream_layout(a, (int)sizeof(T));
+  const int units = (int)(a.batch * a.H);
+  const dim3 grid((unsigned)stream_grid(units));
+  cudaError_t e = cudaSuccess;
+  switch (a.R) {
+    case 1:
+      e = cudaFuncSetAttribute(decode_stream_kernel<T, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) decode_stream_kernel<T, 1><<<grid, kSThreads, smem, s>>>(a, L, units);
+      break;
+    case 2:
+      e = cudaFuncSetAttribute(decode_stream_kernel<T, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) decode_stream_kernel<T, 2><<<grid, kSThreads, smem, s>>>(a, L, units);
+      break;
+    case 4:
+      e = cudaFuncSetAttribute(decode_stream_kernel<T, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) decode_stream_kernel<T, 4><<<grid, kSThreads, smem, s>>>(a, L, units);
+      break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
   const int N = (int)a.N, P = (int)a.P, R = a.R;
@@ -250,6 +533,9 @@ bool decode_supported(int64_t N, int64_t P, int R) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s) {
+  size_t smem = 0;
+  if (a.status != nullptr && stream_ok(a, bf16 ? 2 : 4, &smem))
+    return bf16 ? launch_stream_t<__nv_bfloat16>(a, smem, s) : launch_stream_t<float>(a, smem, s);
   return bf16 ? launch_t<__nv_bfloat16>(a, s) : launch_t<float>(a, s);
 }
 

@@ -39,6 +39,7 @@ struct DecodeArgs {
   const float* B_bias;
   const float* C_bias;
   void* out;
+  unsigned int* status;  // device word for expired waits (streaming kernel)
   int64_t batch, H, G, P, N;
   int R;
 };

@@ -134,7 +134,7 @@ struct Cfg {
 
 // Per-chunk scalars handed from the prologue to the core (one set per slot).
 template <int KP>
-struct SlotScalars {
+struct __align__(16) SlotScalars {
   float lam2[64];  // Lam_t in log2 units
   float gam[64];   // gamma_t
   float wp[64];    // gamma_t + bhat_{t+1}
@@ -156,8 +156,9 @@ struct TcParams {
   unsigned int* status;
   int64_t L, H, G, batch;
   int nchunks;
-  // work units are (sequence, segment) pairs of seg_chunks chunks each
-  int seg_chunks, nseg;
+  // work units are (sequence, segment) pairs of seg_chunks chunks each;
+  // nunits = batch * heads * nseg < 2^31, hpg = heads per group
+  int seg_chunks, nseg, nunits, heads, hpg;
   // segment passes: the state-only pass writes each unit's local end state to
   // ws_state [unit][N][P] and (log2 decay, angle per pair) to ws_scal
   // [unit][1 + N/2]; the full pass starts unit u from ws_hin[u] (explicit
@@ -268,10 +269,11 @@ __device__ __forceinline__ float wrap_rad(float a) {
   return fmaf(-k, kPi2b, a);
 }
 
+// Maximum over the warp of a NON-NEGATIVE float (every use here is a
+// magnitude): such floats order like their bit patterns, so one integer
+// warp reduction does it.
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
@@ -333,20 +335,24 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
 // pairs, unit u = seq * nseg + segment, covering chunks [c_begin, c_end) of
 // the sequence; a CTA walks units blockIdx.x, +gridDim.x, ... chunk by chunk
 // (g counts its chunks; slots and mbarrier phases follow g).
+// (32-bit indices, divided once per unit: 64-bit division is a long
+// software sequence that would sit on the per-chunk critical path).
 struct Sched {
-  int64_t unit, seq;
+  int unit, b, h;
   int c, c_begin, c_end;
-  __device__ __forceinline__ void start(int64_t u, const TcParams& p) {
+  __device__ __forceinline__ void start(int u, const TcParams& p) {
     unit = u;
-    seq = u / p.nseg;
-    c_begin = (int)(u % p.nseg) * p.seg_chunks;
+    const int seq = u / p.nseg;
+    c_begin = (u - seq * p.nseg) * p.seg_chunks;
     c_end = min(p.nchunks, c_begin + p.seg_chunks);
     c = c_begin;
+    b = seq / p.heads;
+    h = seq - b * p.heads;
   }
   __device__ __forceinline__ bool next(const TcParams& p) {
     if (++c < c_end) return true;
-    const int64_t u = unit + gridDim.x;
-    if (u >= p.batch * p.H * p.nseg) return false;
+    const int u = unit + (int)gridDim.x;
+    if (u >= p.nunits) return false;
     start(u, p);
     return true;
   }
@@ -414,10 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_hred[kCoreWarps];
   __shared__ float s_bias_red[2][kProWarps];
   // R > 1: the head's B / C bias transposed to [rank][row] (registers for R = 1)
-  __shared__ __align__(16) float s_biasT[2][(R > 1) ? R : 1][(R > 1) ? NS : 4];
+  __shared__ __align__(16) float s_biasT[2][R][NS];  // B, C bias of the head, [rank][n]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t H = p.H, G = p.G;
   const int nC = p.nchunks;
 
   // ---------------------------------------------------------------- setup
@@ -432,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bar_op_full[s], 1);
       ptx::mbar_init(&bar_slot_free[s], kCoreWarps);
-      ptx::mbar_init(&bar_acc_full[s], 1);
+      ptx::mbar_init(&bar_acc_full[s], SO ? 1 : 2);  // the S and the D issuer commit
       ptx::mbar_init(&bar_y_full[s], 1);
     }
     ptx::fence_mbar_init();
@@ -452,67 +457,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_holder;
 
   // TMA of one chunk's raw tiles into the raw slot (prologue thread 0)
-  auto issue_raw = [&](int64_t seq, int c) {
-    const int64_t b = seq / H, h = seq % H, gi = h / (H / G);
-    const int t0 = c * Q;
+  auto issue_raw = [&](const Sched& u) {
+    const int b = u.b, h = u.h, gi = h / p.hpg;
+    const int t0 = u.c * Q;
     ptx::mbar_arrive_expect_tx(&bar_raw_full, SO ? K::kTxBytes - K::kRawC : K::kTxBytes);
-    ptx::tma_load_5d(smem + K::kRawB, &tm_B, &bar_raw_full, 0, 0, (int)gi, t0, (int)b);
-    if (!SO) ptx::tma_load_5d(smem + K::kRawC, &tm_C, &bar_raw_full, 0, 0, (int)gi, t0, (int)b);
-    ptx::tma_load_4d(smem + K::kRawTh, &tm_th, &bar_raw_full, 0, (int)gi, t0, (int)b);
-    ptx::tma_load_4d(smem + K::kRawX, &tm_x, &bar_raw_full, 0, (int)h, t0, (int)b);
+    ptx::tma_load_5d(smem + K::kRawB, &tm_B, &bar_raw_full, 0, 0, gi, t0, b);
+    if (!SO) ptx::tma_load_5d(smem + K::kRawC, &tm_C, &bar_raw_full, 0, 0, gi, t0, b);
+    ptx::tma_load_4d(smem + K::kRawTh, &tm_th, &bar_raw_full, 0, gi, t0, b);
+    ptx::tma_load_4d(smem + K::kRawX, &tm_x, &bar_raw_full, 0, h, t0, b);
   };
 
   if (warp < kProWarps) {
     // ============================================================ prologue
     const int kk2 = tid % KP2, tg = tid / KP2;
     const int k0 = 2 * kk2;  // this thread's pairs: k0, k0 + 1 (rows 4kk2 .. 4kk2 + 3)
-    int64_t cur_h = -1;
-    float bb[4][1], cb[4][1];  // R = 1: the four bias values of this thread's rows
+    int cur_h = -1;
     float bmax_bias = 0.f, cmax_bias = 0.f;
     int inflight = -1;  // phase parity of a raw load issued and not yet consumed
     // the first chunk's inputs
     Sched sch;
     sch.start(blockIdx.x, p);
     if (tid == 0) {
-      issue_raw(sch.seq, sch.c);
+      issue_raw(sch);
       inflight = 0;
     }
     if (warp == 1) {
       DecayRaw d;
-      load_decay_raw(p, sch.seq / H, sch.seq % H, (int64_t)sch.c * Q, Q, lane, d);
+      load_decay_raw(p, sch.b, sch.h, (int64_t)sch.c * Q, Q, lane, d);
       store_decay(d, lane, s_dtraw[0], s_lamraw[0], s_bnx[0]);
     }
     float A_h = 0.f;
     for (int g = 0;; ++g) {
-      const int64_t seq = sch.seq, h = seq % H;
+      const int h = sch.h;
       const int c = sch.c, s = g & 1, db = g & 1;
-      Sched nxt = sch;
-      const bool has_next = nxt.next(p);
+      const bool has_next = sch.c + 1 < sch.c_end || sch.unit + (int)gridDim.x < p.nunits;
       SlotScalars<KP>& sc = ss[s];
       if (h != cur_h) {
         // per-head A, bias (fp32) and a block-wide bound of the bias magnitude
         cur_h = h;
         A_h = p.A[h];
         float mb = 0.f, mc = 0.f;
-        if constexpr (R == 1) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int64_t ix = h * NS + 4 * kk2 + e;
-            bb[e][0] = p.B_bias ? p.B_bias[ix] : 0.f;
-            cb[e][0] = p.C_bias ? p.C_bias[ix] : 0.f;
-            mb = fmaxf(mb, fabsf(bb[e][0]));
-            mc = fmaxf(mc, fabsf(cb[e][0]));
-          }
-        } else {
-          // the previous head's bias was last read before this chunk's first barrier
-          for (int i = tid; i < NS * R; i += kProThreads) {
-            const float vb = p.B_bias ? p.B_bias[h * NS * R + i] : 0.f;
-            const float vc = p.C_bias ? p.C_bias[h * NS * R + i] : 0.f;
-            s_biasT[0][i % R][i / R] = vb;
-            s_biasT[1][i % R][i / R] = vc;
-            mb = fmaxf(mb, fabsf(vb));
-            mc = fmaxf(mc, fabsf(vc));
-          }
+        // the previous head's bias was last read before this chunk's first barrier
+        for (int i = tid; i < NS * R; i += kProThreads) {
+          const float vb = p.B_bias ? p.B_bias[(int64_t)h * NS * R + i] : 0.f;
+          const float vc = p.C_bias ? p.C_bias[(int64_t)h * NS * R + i] : 0.f;
+          s_biasT[0][i % R][i / R] = vb;
+          s_biasT[1][i % R][i / R] = vc;
+          mb = fmaxf(mb, fabsf(vb));
+          mc = fmaxf(mc, fabsf(vc));
         }
         mb = warp_max(mb);
         mc = warp_max(mc);
@@ -585,7 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           sc.wmax = wm;
         }
       } else if (warp == 1 && has_next) {
-        load_decay_raw(p, nxt.seq / H, nxt.seq % H, (int64_t)nxt.c * Q, Q, lane, nd);
+        Sched nxt = sch;
+        nxt.next(p);
+        load_decay_raw(p, nxt.b, nxt.h, (int64_t)nxt.c * Q, Q, lane, nd);
       }
       // 2b. raw tiles -> registers; magnitude bounds; Kahan-compensated angle sums
       float2 th2[TPG];
@@ -677,7 +671,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every read of the raw slot is done: refill it with the next chunk
       if (has_next) {
         if (tid == 0) {
-          issue_raw(nxt.seq, nxt.c);
+          Sched nxt = sch;
+          nxt.next(p);
+          issue_raw(nxt);
           inflight = (g + 1) & 1;
         }
         if (warp == 1) store_decay(nd, lane, s_dtraw[db ^ 1], s_lamraw[db ^ 1], s_bnx[db ^ 1]);
@@ -760,6 +756,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float2 sB2 = make_float2(sigB, sigB), sC2 = make_float2(sigC, sigC);
+      float4 bq1, cq1;  // R = 1: the bias of this thread's rows, for every token
+      if constexpr (R == 1) {
+        bq1 = *reinterpret_cast<const float4*>(&s_biasT[0][0][4 * kk2]);
+        if constexpr (!SO) cq1 = *reinterpret_cast<const float4*>(&s_biasT[1][0][4 * kk2]);
+      }
 #pragma unroll
       for (int i = 0; i < TPG; ++i) {
         float2 sn, cs;
@@ -774,8 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // elements (n, r) for n = 4kk2 + e; .x holds pair k0 (e = 0, 1), .y pair k0+1 (e = 2, 3)
           float4 bq, cq;  // bias of rows 4kk2 .. 4kk2 + 3 at rank r
           if constexpr (R == 1) {
-            bq = make_float4(bb[0][0], bb[1][0], bb[2][0], bb[3][0]);
-            cq = make_float4(cb[0][0], cb[1][0], cb[2][0], cb[3][0]);
+            bq = bq1;
+            if constexpr (!SO) cq = cq1;
           } else {
             bq = *reinterpret_cast<const float4*>(&s_biasT[0][r][4 * kk2]);
             if constexpr (!SO) cq = *reinterpret_cast<const float4*>(&s_biasT[1][r][4 * kk2]);
@@ -837,27 +838,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       // since the core released slot s), then publish the slot to the core
       ptx::fence_proxy_async_smem();
       ptx::named_bar_sync(kBarPro, kProThreads);
-      if (tid == 0) {
+      // (S from warp 0 and D from warp 1, so that the two issue sequences overlap)
+      if (tid == 0 || (!SO && tid == 32)) {
         const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
         ptx::tc_fence_after_sync();
-        const Desc dBk = make_desc(opb + K::kOpBt, 16u), dBm = make_desc(opb + K::kOpBt, 64u * 128u);
-        const Desc dXw = make_desc(opb + K::kOpXw, 64u * 128u);
-        if constexpr (!SO) {
-          const Desc dCk = make_desc(opb + K::kOpCt, 16u);
+        if (SO || tid == 32) {
+          const Desc dBm = make_desc(opb + K::kOpBt, 64u * 128u);
+          const Desc dXw = make_desc(opb + K::kOpXw, 64u * 128u);
+#pragma unroll
+          for (int kk = 0; kk < kQR / 16; ++kk)
+            ptx::mma_bf16_ss(tset + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD,
+                             kk > 0);
+        } else {
+          const Desc dBk = make_desc(opb + K::kOpBt, 16u), dCk = make_desc(opb + K::kOpCt, 16u);
 #pragma unroll
           for (int kk = 0; kk < NS / 16; ++kk)
             ptx::mma_bf16_ss(tset + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
                              kIdS, kk > 0);
         }
-#pragma unroll
-        for (int kk = 0; kk < kQR / 16; ++kk)
-          ptx::mma_bf16_ss(tset + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD,
-                           kk > 0);
         ptx::mma_commit(&bar_acc_full[s]);
-        ptx::mbar_arrive(&bar_op_full[s]);
+        if (tid == 0) ptx::mbar_arrive(&bar_op_full[s]);
       }
       if (!has_next) break;
-      sch = nxt;
+      sch.next(p);  // = nxt, recomputed rather than kept live across the body
     }
     // on an early exit, let an issued load land before the CTA ends
     if (tid == 0 && inflight >= 0) ptx::mbar_wait(&bar_raw_full, (uint32_t)inflight, kWaitNs);
@@ -958,11 +961,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!SO && p.ws_hin && ct == 0 && wait_or_abort(&bar_op_full[0], 0u, &abort_flag, p.status))
       issue_yoff(0);
     for (int g = 0;; ++g) {
-      const int64_t seq = sch.seq, b = seq / H, h = seq % H;
+      const int b = sch.b, h = sch.h;
       const int c = sch.c, s = g & 1;
       const bool first = c == sch.c_begin, last = c == sch.c_end - 1;
-      Sched nxt = sch;
-      const bool has_next = nxt.next(p);
+      const bool has_next = sch.c + 1 < sch.c_end || sch.unit + (int)gridDim.x < p.nunits;
       const SlotScalars<KP>& sc = ss[s];
       const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
       if (ct == 0)
@@ -990,11 +992,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c0 / R > t) continue;
           constexpr int NT = 16 / R;  // distinct tokens among the 16 columns
           const int s0 = c0 / R;
-          float lsv[NT], wpv[NT];
+          float lsv[NT], wpv[NT];  // s0 is a multiple of NT >= 4: 16-byte aligned
 #pragma unroll
-          for (int u = 0; u < NT; ++u) {
-            lsv[u] = sc.lam2[s0 + u];
-            wpv[u] = sc.wp[s0 + u];
+          for (int u = 0; u < NT; u += 4) {
+            *reinterpret_cast<float4*>(&lsv[u]) = *reinterpret_cast<const float4*>(&sc.lam2[s0 + u]);
+            *reinterpret_cast<float4*>(&wpv[u]) = *reinterpret_cast<const float4*>(&sc.wp[s0 + u]);
           }
           uint32_t ph_[8], pl_[8];
 #pragma unroll
@@ -1143,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before_sync();
         ptx::named_bar_sync(kBarCore, kCoreThreads);
         if (ct == 0) {
-          ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, (int)h, c * Q, (int)b);
+          ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, h, c * Q, b);
           ptx::tma_store_commit();
         }
         h_inv_prev = h_inv;
@@ -1167,7 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ct < KP) sd[1 + ct] = sc.fang[ct];
         } else if (c == nC - 1 && p.final_state) {
           // final state of the sequence, explicit frame: h = Rot(Phi_{L-1}) g
-          float* fs = p.final_state + seq * (int64_t)NS * kP;
+          float* fs = p.final_state + ((int64_t)b * p.heads + h) * NS * kP;
 #pragma unroll
           for (int blk = 0; blk < HR / 16; ++blk) {
             uint32_t n, cb;
@@ -1189,7 +1191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
           }
         }
-        if (has_next) enter_unit(nxt.unit);
+        if (has_next) enter_unit(sch.unit + (int)gridDim.x);
       }
       ptx::tc_fence_before_sync();
       __syncwarp();
@@ -1203,7 +1205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_yoff(g + 1);
       }
       if (!has_next) break;
-      sch = nxt;
+      sch.next(p);
     }
     if (ct == 0) ptx::tma_store_wait_all<0>();
   }
@@ -1375,6 +1377,12 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   p.nseg = pl.nseg;
   p.seg_chunks = pl.seg_chunks;
   const int64_t nseq = a.batch * a.H;
+  // the kernel indexes units with 32-bit integers (unreachable in practice:
+  // 2^31 sequences of x alone would exceed device memory)
+  if (nseq * pl.nseg > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+  p.nunits = (int)(nseq * pl.nseg);
+  p.heads = (int)a.H;
+  p.hpg = (int)(a.H / a.G);
   if (pl.nseg <= 1) return launch_pass<R, NS, false>(maps, p, nseq, s);
   // segmented: state-only pass, combine, full pass from the entering states
   const size_t need = seg_ws_bytes(a, pl);

@@ -233,6 +233,60 @@ def test_decode_full_batch_shape(orc):
     assert_bf16(st.cpu().numpy(), r1, "state")
 
 
+@pytest.mark.parametrize("R", [1, 4])
+def test_decode_shape_outside_the_streaming_kernel(orc, R):
+    """batch * heads = 9 (not a multiple of 4) and N = 20 (a theta row of 40 bytes)
+    take the per-(batch, head) kernel instead of the streaming one."""
+    shape = m3synth.ScanShape(3, 1, 3, 1, 32, 20, R=R, chunk=1, bf16=True)
+    b, H, N, P = shape.batch, shape.heads, shape.dstate, shape.headdim
+    st_ref = np.random.default_rng(6).standard_normal((b, H, N, P))
+    st = torch.from_numpy(st_ref.astype(np.float32)).cuda()
+    st_ref = st.cpu().numpy().astype(np.float64)
+    s0 = m3synth.decode_inputs(shape, seed=40 + R, step=0)
+    s1 = m3synth.decode_inputs(shape, seed=40 + R, step=1)
+    d0, d1 = to_device(s0, True), to_device(s1, True)
+    m3.m3_decode_step(st, d0["x"], d0["dt"], d0["A"], d0["lam"], d0["B"], d0["C"], d0["theta"],
+                      R=R, B_bias=d0["B_bias"], C_bias=d0["C_bias"])
+    out = m3.m3_decode_step(st, d1["x"], d1["dt"], d1["A"], d1["lam"], d1["B"], d1["C"],
+                            d1["theta"], R=R, B_prev=d0["B"], x_prev=d0["x"],
+                            B_bias=d1["B_bias"], C_bias=d1["C_bias"])
+    _, r0 = orc.decode_step(st_ref, s0["x"], s0["dt"], s0["A"], s0["lam"], s0["B"], s0["C"],
+                            s0["theta"], B_bias=s0["B_bias"], C_bias=s0["C_bias"])
+    y1, r1 = orc.decode_step(r0, s1["x"], s1["dt"], s1["A"], s1["lam"], s1["B"], s1["C"],
+                             s1["theta"], B_prev=s0["B"], x_prev=s0["x"], B_bias=s1["B_bias"],
+                             C_bias=s1["C_bias"])
+    torch.cuda.synchronize()
+    assert_bf16_out(out.float().cpu().numpy(), y1, "y")
+    assert_bf16(st.cpu().numpy(), r1, "state")
+    assert m3.m3_device_status() == m3.M3_OK
+
+
+def test_decode_full_batch_mimo(orc):
+    """The 128 x 32 decode batch at rank 4, bf16: two steps (every CTA of the
+    streaming kernel walks several (batch, head) units through both stages)."""
+    shape = m3synth.DECODE_MIMO
+    b, H, N, P = shape.batch, shape.heads, shape.dstate, shape.headdim
+    st0 = (0.1 * np.random.default_rng(9).standard_normal((b, H, N, P))).astype(np.float32)
+    st = torch.from_numpy(st0).cuda()
+    s0 = m3synth.decode_inputs(shape, seed=4, step=0)
+    s1 = m3synth.decode_inputs(shape, seed=4, step=1)
+    d0, d1 = to_device(s0, True), to_device(s1, True)
+    m3.m3_decode_step(st, d0["x"], d0["dt"], d0["A"], d0["lam"], d0["B"], d0["C"], d0["theta"],
+                      R=4, B_bias=d0["B_bias"], C_bias=d0["C_bias"])
+    out = m3.m3_decode_step(st, d1["x"], d1["dt"], d1["A"], d1["lam"], d1["B"], d1["C"],
+                            d1["theta"], R=4, B_prev=d0["B"], x_prev=d0["x"],
+                            B_bias=d1["B_bias"], C_bias=d1["C_bias"])
+    _, r0 = orc.decode_step(st0, s0["x"], s0["dt"], s0["A"], s0["lam"], s0["B"], s0["C"],
+                            s0["theta"], B_bias=s0["B_bias"], C_bias=s0["C_bias"])
+    y1, r1 = orc.decode_step(r0, s1["x"], s1["dt"], s1["A"], s1["lam"], s1["B"], s1["C"],
+                             s1["theta"], B_prev=s0["B"], x_prev=s0["x"], B_bias=s1["B_bias"],
+                             C_bias=s1["C_bias"])
+    torch.cuda.synchronize()
+    assert_bf16_out(out.float().cpu().numpy(), y1, "y")
+    assert_bf16(st.cpu().numpy(), r1, "state")
+    assert m3.m3_device_status() == m3.M3_OK
+
+
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 def test_prefill_then_decode_matches_longer_prefill(orc, bf16):
     shape = m3synth.ScanShape(2, 33, 4, 1, 64, 128, R=1, chunk=16, bf16=bf16)

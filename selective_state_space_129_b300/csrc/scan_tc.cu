@@ -205,37 +205,10 @@ __device__ __forceinline__ void pow2_scale(float M, float* sigma, float* inv) {
   *inv = __uint_as_float((uint32_t)(127 - 14 + e) << 23);
 }
 
-// Packed fp32 pair arithmetic (sm_100 family), elementwise on (x, y).
-__device__ __forceinline__ uint64_t f2_pack(float2 a) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
-  return r;
-}
-__device__ __forceinline__ float2 f2_unpack(uint64_t r) {
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(r));
-  return d;
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
-  return f2_unpack(d);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
-  return f2_unpack(d);
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
-  return f2_unpack(d);
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
-  return f2_unpack(d);
-}
+using ptx::add2;
+using ptx::fma2;
+using ptx::mul2;
+using ptx::sub2;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;

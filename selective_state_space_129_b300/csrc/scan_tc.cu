@@ -729,46 +729,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float2 sB2 = make_float2(sigB, sigB), sC2 = make_float2(sigC, sigC);
-      float4 bq1, cq1;  // R = 1: the bias of this thread's rows, for every token
       if constexpr (R == 1) {
-        bq1 = *reinterpret_cast<const float4*>(&s_biasT[0][0][4 * kk2]);
-        if constexpr (!SO) cq1 = *reinterpret_cast<const float4*>(&s_biasT[1][0][4 * kk2]);
-      }
+        // sigma (B + bias) = fma(sigma, B, sigma bias), exact for a power-of-two
+        // sigma, so the scale rides on the bias add instead of on cos and sin
+        const float4 bq = *reinterpret_cast<const float4*>(&s_biasT[0][0][4 * kk2]);
+        const float2 bs0 = mul2(sB2, make_float2(bq.x, bq.z)), bs1 = mul2(sB2, make_float2(bq.y, bq.w));
+        float2 cs0 = make_float2(0.f, 0.f), cs1 = cs0;
+        if constexpr (!SO) {
+          const float4 cq = *reinterpret_cast<const float4*>(&s_biasT[1][0][4 * kk2]);
+          cs0 = mul2(sC2, make_float2(cq.x, cq.z));
+          cs1 = mul2(sC2, make_float2(cq.y, cq.w));
+        }
 #pragma unroll
-      for (int i = 0; i < TPG; ++i) {
-        float2 sn, cs;
-        __sincosf(ph[i].x, &sn.x, &cs.x);
-        __sincosf(ph[i].y, &sn.y, &cs.y);
-        const float2 csB = mul2(cs, sB2), snB = mul2(sn, sB2);
-        const float2 csC = mul2(cs, sC2), snC = mul2(sn, sC2);
-        const float2 nsnB = make_float2(-snB.x, -snB.y), nsnC = make_float2(-snC.x, -snC.y);
-        const int t = tg * TPG + i;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          // elements (n, r) for n = 4kk2 + e; .x holds pair k0 (e = 0, 1), .y pair k0+1 (e = 2, 3)
-          float4 bq, cq;  // bias of rows 4kk2 .. 4kk2 + 3 at rank r
-          if constexpr (R == 1) {
-            bq = bq1;
-            if constexpr (!SO) cq = cq1;
-          } else {
-            bq = *reinterpret_cast<const float4*>(&s_biasT[0][r][4 * kk2]);
-            if constexpr (!SO) cq = *reinterpret_cast<const float4*>(&s_biasT[1][r][4 * kk2]);
-          }
-          float2 b0 = make_float2(bf_at(bw[i], 0 * R + r), bf_at(bw[i], 2 * R + r));
-          float2 b1 = make_float2(bf_at(bw[i], 1 * R + r), bf_at(bw[i], 3 * R + r));
-          b0 = add2(b0, make_float2(bq.x, bq.z));
-          b1 = add2(b1, make_float2(bq.y, bq.w));
+        for (int i = 0; i < TPG; ++i) {
+          float2 sn, cs;
+          __sincosf(ph[i].x, &sn.x, &cs.x);
+          __sincosf(ph[i].y, &sn.y, &cs.y);
+          const float2 nsn = make_float2(-sn.x, -sn.y);
+          const int t = tg * TPG + i;
+          // .x holds pair k0 (rows 4kk2, 4kk2 + 1), .y pair k0 + 1
+          const float2 b0 = fma2(sB2, make_float2(bf_at(bw[i], 0), bf_at(bw[i], 2)), bs0);
+          const float2 b1 = fma2(sB2, make_float2(bf_at(bw[i], 1), bf_at(bw[i], 3)), bs1);
           // Rot(-Phi) = [[cos, sin], [-sin, cos]]
-          const float2 bt0 = fma2(csB, b0, mul2(snB, b1)), bt1 = fma2(csB, b1, mul2(nsnB, b0));
-          const uint32_t o = tile_off((uint32_t)(t * R + r), 4u * kk2, 64u);
+          const float2 bt0 = fma2(cs, b0, mul2(sn, b1)), bt1 = fma2(cs, b1, mul2(nsn, b0));
+          const uint32_t o = tile_off((uint32_t)t, 4u * kk2, 64u);
           sts64(opb + K::kOpBt + o, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
           if constexpr (!SO) {
-            float2 c0 = make_float2(bf_at(cw[i], 0 * R + r), bf_at(cw[i], 2 * R + r));
-            float2 c1 = make_float2(bf_at(cw[i], 1 * R + r), bf_at(cw[i], 3 * R + r));
-            c0 = add2(c0, make_float2(cq.x, cq.z));
-            c1 = add2(c1, make_float2(cq.y, cq.w));
-            const float2 ct0 = fma2(csC, c0, mul2(snC, c1)), ct1 = fma2(csC, c1, mul2(nsnC, c0));
+            const float2 c0 = fma2(sC2, make_float2(bf_at(cw[i], 0), bf_at(cw[i], 2)), cs0);
+            const float2 c1 = fma2(sC2, make_float2(bf_at(cw[i], 1), bf_at(cw[i], 3)), cs1);
+            const float2 ct0 = fma2(cs, c0, mul2(sn, c1)), ct1 = fma2(cs, c1, mul2(nsn, c0));
             sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < TPG; ++i) {
+          float2 sn, cs;
+          __sincosf(ph[i].x, &sn.x, &cs.x);
+          __sincosf(ph[i].y, &sn.y, &cs.y);
+          const float2 csB = mul2(cs, sB2), snB = mul2(sn, sB2);
+          const float2 csC = mul2(cs, sC2), snC = mul2(sn, sC2);
+          const float2 nsnB = make_float2(-snB.x, -snB.y), nsnC = make_float2(-snC.x, -snC.y);
+          const int t = tg * TPG + i;
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            // elements (n, r) for n = 4kk2 + e; .x holds pair k0 (e = 0, 1), .y pair k0+1 (e = 2, 3)
+            const float4 bq = *reinterpret_cast<const float4*>(&s_biasT[0][r][4 * kk2]);
+            float2 b0 = make_float2(bf_at(bw[i], 0 * R + r), bf_at(bw[i], 2 * R + r));
+            float2 b1 = make_float2(bf_at(bw[i], 1 * R + r), bf_at(bw[i], 3 * R + r));
+            b0 = add2(b0, make_float2(bq.x, bq.z));
+            b1 = add2(b1, make_float2(bq.y, bq.w));
+            // Rot(-Phi) = [[cos, sin], [-sin, cos]]
+            const float2 bt0 = fma2(csB, b0, mul2(snB, b1)), bt1 = fma2(csB, b1, mul2(nsnB, b0));
+            const uint32_t o = tile_off((uint32_t)(t * R + r), 4u * kk2, 64u);
+            sts64(opb + K::kOpBt + o, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
+            if constexpr (!SO) {
+              const float4 cq = *reinterpret_cast<const float4*>(&s_biasT[1][r][4 * kk2]);
+              float2 c0 = make_float2(bf_at(cw[i], 0 * R + r), bf_at(cw[i], 2 * R + r));
+              float2 c1 = make_float2(bf_at(cw[i], 1 * R + r), bf_at(cw[i], 3 * R + r));
+              c0 = add2(c0, make_float2(cq.x, cq.z));
+              c1 = add2(c1, make_float2(cq.y, cq.w));
+              const float2 ct0 = fma2(csC, c0, mul2(snC, c1)), ct1 = fma2(csC, c1, mul2(nsnC, c0));
+              sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
+            }
           }
         }
       }
@@ -1147,8 +1170,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int blk = 0; blk < HR / 16; ++blk) {
             uint32_t n, cb;
             hpos(blk, n, cb);
+            // the carried angle is wrapped to [-pi, pi]: the fast sincos is
+            // accurate there (and keeps the accurate version's large slow path
+            // out of the loop's code)
             float sn, cs;
-            sincosf(sc.fang[n >> 1], &sn, &cs);
+            __sincosf(sc.fang[n >> 1], &sn, &cs);
             const bool odd = n & 1;
             float o[16];
 #pragma unroll

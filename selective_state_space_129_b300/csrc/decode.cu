@@ -269,10 +269,45 @@ inline StreamLayout stream_layout(const DecodeArgs& a, int act) {
   return L;
 }
 
+// Partial y of warp w, column 4q + c, rank r at yred[(w 4R + c R + r)(P/4 + 1) + q]:
+// the lanes of a warp (consecutive q) store to consecutive words, and the
+// padding keeps the reads of the final sum (consecutive (p, r)) off shared banks.
 inline size_t stream_smem_bytes(const DecodeArgs& a, const StreamLayout& L) {
   const size_t N = a.N, P = a.P, R = a.R;
   return (size_t)kStages * L.bytes +
-         sizeof(float) * (3 * N * R + N + (size_t)kSWarps * P * R + (size_t)a.H);
+         sizeof(float) * (3 * N * R + N + (size_t)kSWarps * R * (P + 4) + (size_t)a.H);
+}
+
+// The 4 x R activations of one column quad (4 R consecutive elements of a
+// 16-byte aligned block, at an offset that is a multiple of 8 bytes) with
+// vector loads.
+template <typename T, int R>
+__device__ __forceinline__ void ld_quad(const T* p, float (&v)[4][R]) {
+  constexpr int kBytes = 4 * R * (int)sizeof(T);
+  if constexpr (sizeof(T) == 2) {
+    uint32_t w[kBytes / 4];
+    if constexpr (kBytes == 8) {
+      const uint2 a = *reinterpret_cast<const uint2*>(p);
+      w[0] = a.x; w[1] = a.y;
+    } else {
+#pragma unroll
+      for (int k = 0; k < kBytes / 16; ++k) {
+        const uint4 a = reinterpret_cast<const uint4*>(p)[k];
+        w[4 * k] = a.x; w[4 * k + 1] = a.y; w[4 * k + 2] = a.z; w[4 * k + 3] = a.w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4 * R; ++i)
+      v[i / R][i % R] = __uint_as_float((i & 1) ? (w[i >> 1] & 0xffff0000u) : (w[i >> 1] << 16));
+  } else {
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      const float4 a = reinterpret_cast<const float4*>(p)[k];
+      const float e[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[(4 * k + j) / R][(4 * k + j) % R] = e[j];
+    }
+  }
 }
 
 template <typename T, int R>
@@ -289,8 +324,8 @@ __global__ void __launch_bounds__(kSThreads, 2)
   float* cc = bp + N * R;        // C + bias                  [N][R]
   float* rc = cc + N * R;        // alpha cos                 [K2]
   float* rs = rc + K2;           // alpha sin                 [K2]
-  float* yred = rs + K2;         // partial y per warp        [kSWarps][P][R]
-  float* sA = yred + kSWarps * P * R;  // A                   [H]
+  float* yred = rs + K2;         // partial y per warp (padded layout above)
+  float* sA = yred + kSWarps * R * (P + 4);  // A             [H]
   const bool has_prev = a.B_prev != nullptr;
   const int q = tid % PQ;  // this thread's column quad (PQ divides 32)
   const int items = K2 * PQ;
@@ -371,14 +406,19 @@ __global__ void __launch_bounds__(kSThreads, 2)
     const T* sx = reinterpret_cast<const T*>(stg + L.x);
     const T* sxp = reinterpret_cast<const T*>(stg + L.xp);
     float xr[4][R], xpr[4][R], yp[4][R];
+    ld_quad<T, R>(sx + 4 * q * R, xr);
+    if (has_prev) {
+      ld_quad<T, R>(sxp + 4 * q * R, xpr);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int r = 0; r < R; ++r) xpr[c][r] = 0.f;
+    }
 #pragma unroll
     for (int c = 0; c < 4; ++c)
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        xr[c][r] = ld_act(sx + (4 * q + c) * R + r);
-        xpr[c][r] = has_prev ? ld_act(sxp + (4 * q + c) * R + r) : 0.f;
-        yp[c][r] = 0.f;
-      }
+      for (int r = 0; r < R; ++r) yp[c][r] = 0.f;
     __syncthreads();
     if (abort_flag) break;  // uniform: read after the barrier
 
@@ -427,7 +467,7 @@ __global__ void __launch_bounds__(kSThreads, 2)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int r = 0; r < R; ++r) yred[(warp * P + 4 * q + c) * R + r] = yp[c][r];
+        for (int r = 0; r < R; ++r) yred[((warp * 4 + c) * R + r) * (PQ + 1) + q] = yp[c][r];
     }
     __syncthreads();
     // stage s is read: refill it with the unit kStages ahead
@@ -437,9 +477,11 @@ __global__ void __launch_bounds__(kSThreads, 2)
     }
     T* out = static_cast<T*>(a.out) + (int64_t)u * P * R;
     for (int i = tid; i < P * R; i += kSThreads) {
+      const int pp = i / R, r = i - pp * R;
+      const int at = ((pp & 3) * R + r) * (PQ + 1) + (pp >> 2);
       float acc = 0.f;
 #pragma unroll
-      for (int w = 0; w < kSWarps; ++w) acc += yred[w * P * R + i];
+      for (int w = 0; w < kSWarps; ++w) acc += yred[w * 4 * R * (PQ + 1) + at];
       st_act(out + i, acc);
     }
   }

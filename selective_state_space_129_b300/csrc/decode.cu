@@ -275,7 +275,7 @@ inline StreamLayout stream_layout(const DecodeArgs& a, int act) {
 inline size_t stream_smem_bytes(const DecodeArgs& a, const StreamLayout& L) {
   const size_t N = a.N, P = a.P, R = a.R;
   return (size_t)kStages * L.bytes +
-         sizeof(float) * (3 * N * R + N + (size_t)kSWarps * R * (P + 4) + (size_t)a.H);
+         sizeof(float) * (3 * N * R + N + 2 * (size_t)kSWarps * R * (P + 4) + (size_t)a.H);
 }
 
 // The 4 x R activations of one column quad (4 R consecutive elements of a
@@ -324,8 +324,9 @@ __global__ void __launch_bounds__(kSThreads, 2)
   float* cc = bp + N * R;        // C + bias                  [N][R]
   float* rc = cc + N * R;        // alpha cos                 [K2]
   float* rs = rc + K2;           // alpha sin                 [K2]
-  float* yred = rs + K2;         // partial y per warp (padded layout above)
-  float* sA = yred + kSWarps * R * (P + 4);  // A             [H]
+  float* yred0 = rs + K2;        // partial y per warp, two tables (padded layout above)
+  const int yred_floats = kSWarps * R * (P + 4);
+  float* sA = yred0 + 2 * yred_floats;  // A                  [H]
   const bool has_prev = a.B_prev != nullptr;
   const int q = tid % PQ;  // this thread's column quad (PQ divides 32)
   const int items = K2 * PQ;
@@ -375,10 +376,23 @@ __global__ void __launch_bounds__(kSThreads, 2)
   for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
     const int s = k % kStages;
     const uint8_t* stg = dsm + (size_t)s * L.bytes;
-    if (!ptx::mbar_wait(&full[s], (uint32_t)((k / kStages) & 1), kStreamWaitNs)) {
+    // every lane waits for the stage; a warp whose wait ran out writes nothing
+    const bool ok =
+        __all_sync(0xffffffffu, ptx::mbar_wait(&full[s], (uint32_t)((k / kStages) & 1), kStreamWaitNs));
+    if (!ok && lane == 0) {
       atomicOr(a.status, 2u);
       abort_flag = 1;
     }
+    // At R = 1 each warp prepares the coefficient rows of the row pairs it
+    // updates itself, so no block-wide barrier separates preparation and
+    // items: its items are it = 32 warp + lane + j kSThreads, i.e. the 32 / PQ
+    // row pairs from (32 warp + j kSThreads) / PQ for every j. At R > 1 the
+    // CTA prepares all rows and meets at a barrier, which measured faster
+    // (b128 H32 P64 N128 R4: 58 us per step against 65 us per-warp; R1: 45 us
+    // per-warp against 47 us).
+    constexpr bool kWarpPrep = (R == 1);
+    const int kpw = 32 / PQ;                                  // row pairs per block of 32 items
+    const int nj = (items - 32 * warp + kSThreads - 1) / kSThreads;  // this warp's blocks
     const int h = u % H;
     const float d = reinterpret_cast<const float*>(stg + L.dt)[u & 3];
     const float lm = reinterpret_cast<const float*>(stg + L.lm)[u & 3];
@@ -389,20 +403,48 @@ __global__ void __launch_bounds__(kSThreads, 2)
     const T* sC = reinterpret_cast<const T*>(stg + L.C);
     const float* sbb = reinterpret_cast<const float*>(stg + L.bb);
     const float* scb = reinterpret_cast<const float*>(stg + L.cb);
-    for (int i = tid; i < N * R; i += kSThreads) {
-      const float bb = a.B_bias ? sbb[i] : 0.f;
-      const float cb = a.C_bias ? scb[i] : 0.f;
-      bg[i] = gamma * (ld_act(sB + i) + bb);
-      bp[i] = has_prev ? bhat * (ld_act(sBp + i) + bb) : 0.f;
-      cc[i] = ld_act(sC + i) + cb;
-    }
     const float* sth = reinterpret_cast<const float*>(stg + L.th);
-    for (int kk = tid; kk < K2; kk += kSThreads) {
-      float sn, cs;
-      sincosf(d * sth[kk], &sn, &cs);
-      rc[kk] = alpha * cs;
-      rs[kk] = alpha * sn;
+    if (!kWarpPrep) {
+      // the whole CTA prepares every row, then one barrier
+      for (int i = tid; ok && i < N * R; i += kSThreads) {
+        const float bb = a.B_bias ? sbb[i] : 0.f;
+        const float cb = a.C_bias ? scb[i] : 0.f;
+        bg[i] = gamma * (ld_act(sB + i) + bb);
+        bp[i] = has_prev ? bhat * (ld_act(sBp + i) + bb) : 0.f;
+        cc[i] = ld_act(sC + i) + cb;
+      }
+      for (int kk = tid; ok && kk < K2; kk += kSThreads) {
+        float sn, cs;
+        sincosf(d * sth[kk], &sn, &cs);
+        rc[kk] = alpha * cs;
+        rs[kk] = alpha * sn;
+      }
+      __syncthreads();
+      if (abort_flag) break;  // uniform: read after the barrier
+    } else if (ok && nj > 0) {
+      const int per_block = kpw * 2 * R;  // coefficient entries (row, rank) per block
+      for (int e = lane; e < nj * per_block; e += 32) {
+        const int jj = e / per_block, rem = e - jj * per_block;
+        const int kq = (32 * warp + jj * kSThreads) / PQ + rem / (2 * R);
+        if (kq >= K2) continue;  // past the last row pair (a partial block)
+        const int i = 2 * kq * R + rem % (2 * R);  // index (n, r) of row n = 2 kq + (rem % 2R) / R
+        const float bb = a.B_bias ? sbb[i] : 0.f;
+        const float cb = a.C_bias ? scb[i] : 0.f;
+        bg[i] = gamma * (ld_act(sB + i) + bb);
+        bp[i] = has_prev ? bhat * (ld_act(sBp + i) + bb) : 0.f;
+        cc[i] = ld_act(sC + i) + cb;
+      }
+      for (int e = lane; e < nj * kpw; e += 32) {
+        const int jj = e / kpw;
+        const int kq = (32 * warp + jj * kSThreads) / PQ + (e - jj * kpw);
+        if (kq >= K2) continue;
+        float sn, cs;
+        sincosf(d * sth[kq], &sn, &cs);
+        rc[kq] = alpha * cs;
+        rs[kq] = alpha * sn;
+      }
     }
+    __syncwarp();
     const T* sx = reinterpret_cast<const T*>(stg + L.x);
     const T* sxp = reinterpret_cast<const T*>(stg + L.xp);
     float xr[4][R], xpr[4][R], yp[4][R];
@@ -419,12 +461,11 @@ __global__ void __launch_bounds__(kSThreads, 2)
     for (int c = 0; c < 4; ++c)
 #pragma unroll
       for (int r = 0; r < R; ++r) yp[c][r] = 0.f;
-    __syncthreads();
-    if (abort_flag) break;  // uniform: read after the barrier
 
     const float* sst = reinterpret_cast<const float*>(stg + L.st);
     float* gst = a.state + (int64_t)u * N * P;
-    for (int it = tid; it < items; it += kSThreads) {
+    float* yred = yred0 + (k & 1) * yred_floats;  // alternates: the last unit's sum may still read the other
+    for (int it = tid; ok && it < items; it += kSThreads) {
       const int kq = it / PQ;
       float4 h0 = *reinterpret_cast<const float4*>(sst + (2 * kq) * P + 4 * q);
       float4 h1 = *reinterpret_cast<const float4*>(sst + (2 * kq + 1) * P + 4 * q);
@@ -470,6 +511,7 @@ __global__ void __launch_bounds__(kSThreads, 2)
         for (int r = 0; r < R; ++r) yred[((warp * 4 + c) * R + r) * (PQ + 1) + q] = yp[c][r];
     }
     __syncthreads();
+    if (abort_flag) break;  // uniform: read after the barrier
     // stage s is read: refill it with the unit kStages ahead
     if (tid == 0) {
       const int un = u + kStages * (int)gridDim.x;

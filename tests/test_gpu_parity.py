@@ -261,6 +261,33 @@ def test_decode_shape_outside_the_streaming_kernel(orc, R):
     assert m3.m3_device_status() == m3.M3_OK
 
 
+@pytest.mark.parametrize("R", [1, 2, 4])
+def test_decode_streaming_partial_item_block(orc, R):
+    """N = 24, P = 8: 24 items per (batch, head), fewer than one warp's 32, so the
+    streaming kernel's per-warp coefficient rows end inside a block."""
+    shape = m3synth.ScanShape(2, 1, 2, 1, 8, 24, R=R, chunk=1, bf16=True)
+    b, H, N, P = shape.batch, shape.heads, shape.dstate, shape.headdim
+    st_ref = np.random.default_rng(7).standard_normal((b, H, N, P))
+    st = torch.from_numpy(st_ref.astype(np.float32)).cuda()
+    st_ref = st.cpu().numpy().astype(np.float64)
+    prev, prev_h = None, None
+    for i in range(3):
+        s_ = m3synth.decode_inputs(shape, seed=60 + R, step=i)
+        d = to_device(s_, True)
+        kw = dict(B_prev=prev["B"], x_prev=prev["x"]) if prev is not None else {}
+        out = m3.m3_decode_step(st, d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"],
+                                d["theta"], R=R, B_bias=d["B_bias"], C_bias=d["C_bias"], **kw)
+        okw = dict(B_prev=prev_h["B"], x_prev=prev_h["x"]) if prev_h is not None else {}
+        y_ref, st_ref = orc.decode_step(st_ref, s_["x"], s_["dt"], s_["A"], s_["lam"], s_["B"],
+                                        s_["C"], s_["theta"], B_bias=s_["B_bias"],
+                                        C_bias=s_["C_bias"], **okw)
+        torch.cuda.synchronize()
+        assert_bf16_out(out.float().cpu().numpy(), y_ref, "y step %d" % i)
+        prev, prev_h = d, s_
+    assert_bf16(st.cpu().numpy(), st_ref, "state")
+    assert m3.m3_device_status() == m3.M3_OK
+
+
 def test_decode_full_batch_mimo(orc):
     """The 128 x 32 decode batch at rank 4, bf16: two steps (every CTA of the
     streaming kernel walks several (batch, head) units through both stages)."""

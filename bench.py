@@ -192,6 +192,17 @@ def oracle_rate(shape, inp, budget_s=12.0):
     return tok / el, min(threads, k), sample
 
 
+def headline_config(shape, world, name="prefill_siso"):
+    """A prefill workload's config (the headline's is identical in both arms)."""
+    return {"workload": "%s b%d L%d H%d P%d N%d G%d R%d chunk%d" % (
+                name, shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate,
+                shape.groups, shape.R, shape.chunk),
+            "global_batch": shape.batch * world, "seq_len": shape.seqlen,
+            "parallelism": "independent replicas" if world > 1 else "single GPU",
+            "l2": "flushed before every timed launch (256 MiB write)",
+            "state": "fp32", "activations": "bf16"}
+
+
 def run_reference(args, rank, world):
     """The reference arm: the CPU oracle timed as it stands on the host cores."""
     if rank != 0:
@@ -222,8 +233,8 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "prefill_siso b8 L2048 H32 P64 N128 R1 chunk64",
-                   "note": "fp64 CPU oracle (sequential explicit-rotation recurrence)"},
+        "config": headline_config(shape, world),
+        "note": "fp64 CPU oracle (sequential explicit-rotation recurrence) on the host cores",
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
@@ -323,13 +334,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "%s b%d L%d H%d P%d N%d G%d R%d chunk%d" % (
-                       name, shape.batch, shape.seqlen, shape.heads, shape.headdim,
-                       shape.dstate, shape.groups, shape.R, shape.chunk),
-                   "global_batch": shape.batch * world, "seq_len": shape.seqlen,
-                   "parallelism": "independent replicas" if world > 1 else "single GPU",
-                   "l2": "flushed before every timed launch (256 MiB write)",
-                   "state": "fp32", "activations": "bf16"},
+        "config": headline_config(shape, world, name),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm"], "traffic": _traffic_from_profiles(tc_kernel),
                      "algorithmic_bytes": nbytes, "peak_source": peaks["src"] + " (burst)"},

@@ -479,22 +479,51 @@ __global__ void __launch_bounds__(kSThreads, 2)
       const float ac = rc[kq], as = rs[kq];
       float* v0 = reinterpret_cast<float*>(&h0);
       float* v1 = reinterpret_cast<float*>(&h1);
+      if constexpr (R == 1) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float g0 = v0[c], g1 = v1[c], u0 = 0.f, u1 = 0.f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          g0 = fmaf(bp0[r], xpr[c][r], g0);
-          g1 = fmaf(bp1[r], xpr[c][r], g1);
-          u0 = fmaf(bg0[r], xr[c][r], u0);
-          u1 = fmaf(bg1[r], xr[c][r], u1);
+        for (int c = 0; c < 4; ++c) {
+          const float g0 = fmaf(bp0[0], xpr[c][0], v0[c]), g1 = fmaf(bp1[0], xpr[c][0], v1[c]);
+          const float u0 = bg0[0] * xr[c][0], u1 = bg1[0] * xr[c][0];
+          const float n0 = fmaf(ac, g0, fmaf(-as, g1, u0));
+          const float n1 = fmaf(as, g0, fmaf(ac, g1, u1));
+          v0[c] = n0;
+          v1[c] = n1;
+          yp[c][0] = fmaf(c0[0], n0, fmaf(c1[0], n1, yp[c][0]));
         }
-        const float n0 = fmaf(ac, g0, fmaf(-as, g1, u0));
-        const float n1 = fmaf(as, g0, fmaf(ac, g1, u1));
-        v0[c] = n0;
-        v1[c] = n1;
+      } else {
+        // rank sums on (r, r + 1) pairs: packed two-lane FMAs, operands straight
+        // from the coefficient rows and the activations
 #pragma unroll
-        for (int r = 0; r < R; ++r) yp[c][r] = fmaf(c0[r], n0, fmaf(c1[r], n1, yp[c][r]));
+        for (int c = 0; c < 4; ++c) {
+          float2 ag0 = ptx::mul2(make_float2(bp0[0], bp0[1]), make_float2(xpr[c][0], xpr[c][1]));
+          float2 ag1 = ptx::mul2(make_float2(bp1[0], bp1[1]), make_float2(xpr[c][0], xpr[c][1]));
+          float2 au0 = ptx::mul2(make_float2(bg0[0], bg0[1]), make_float2(xr[c][0], xr[c][1]));
+          float2 au1 = ptx::mul2(make_float2(bg1[0], bg1[1]), make_float2(xr[c][0], xr[c][1]));
+#pragma unroll
+          for (int r = 2; r < R; r += 2) {
+            const float2 xp2 = make_float2(xpr[c][r], xpr[c][r + 1]);
+            const float2 x2 = make_float2(xr[c][r], xr[c][r + 1]);
+            ag0 = ptx::fma2(make_float2(bp0[r], bp0[r + 1]), xp2, ag0);
+            ag1 = ptx::fma2(make_float2(bp1[r], bp1[r + 1]), xp2, ag1);
+            au0 = ptx::fma2(make_float2(bg0[r], bg0[r + 1]), x2, au0);
+            au1 = ptx::fma2(make_float2(bg1[r], bg1[r + 1]), x2, au1);
+          }
+          const float g0 = v0[c] + (ag0.x + ag0.y), g1 = v1[c] + (ag1.x + ag1.y);
+          const float u0 = au0.x + au0.y, u1 = au1.x + au1.y;
+          const float n0 = fmaf(ac, g0, fmaf(-as, g1, u0));
+          const float n1 = fmaf(as, g0, fmaf(ac, g1, u1));
+          v0[c] = n0;
+          v1[c] = n1;
+          const float2 n02 = make_float2(n0, n0), n12 = make_float2(n1, n1);
+#pragma unroll
+          for (int r = 0; r < R; r += 2) {
+            const float2 y2 = ptx::fma2(make_float2(c0[r], c0[r + 1]), n02,
+                                        ptx::fma2(make_float2(c1[r], c1[r + 1]), n12,
+                                                  make_float2(yp[c][r], yp[c][r + 1])));
+            yp[c][r] = y2.x;
+            yp[c][r + 1] = y2.y;
+          }
+        }
       }
       *reinterpret_cast<float4*>(gst + (2 * kq) * P + 4 * q) = h0;
       *reinterpret_cast<float4*>(gst + (2 * kq + 1) * P + 4 * q) = h1;

@@ -192,6 +192,29 @@ def oracle_rate(shape, inp, budget_s=12.0):
     return tok / el, min(threads, k), sample
 
 
+# ---------------------------------------------------------------- ranks
+# One process per GPU, each on its own batch (independent replicas, weak
+# scaling): no data-path collective, only the barrier around the timed region
+# and the max over ranks of the measured time.
+def rank_seed(idx, rank):
+    """Input seed of a rank: the workload's seed for rank 0, distinct per rank."""
+    return idx + 1000 * rank
+
+
+def max_over_ranks(torch, value, world, device):
+    """The largest value over all ranks (every rank gets it); value itself at N = 1."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(tokens_per_rank, world, ms):
+    """Whole-job throughput: the tokens all ranks processed over the slowest rank's time."""
+    return tokens_per_rank * world / (ms * 1e-3)
+
+
 def headline_config(shape, world, name="prefill_siso"):
     """A prefill workload's config (the headline's is identical in both arms)."""
     return {"workload": "%s b%d L%d H%d P%d N%d G%d R%d chunk%d" % (
@@ -279,7 +302,7 @@ def run_ours(args, rank, world, local_rank):
         return
     name = args.only if args.only in ("prefill_siso", "prefill_mimo") else "prefill_siso"
     idx, shape = m3synth.WORKLOADS[name]
-    inp = m3synth.scan_inputs(shape, seed=idx + 1000 * rank)
+    inp = m3synth.scan_inputs(shape, seed=rank_seed(idx, rank))
     d = to_device(inp, True, dev)
     out = torch.empty_like(d["x"])
     fs = torch.empty((shape.batch, shape.heads, shape.dstate, shape.headdim),
@@ -315,12 +338,12 @@ def run_ours(args, rank, world, local_rank):
     status = m3.m3_device_status()
     times = [e0.elapsed_time(e1) for e0, e1 in ev]
     ms = sum(times) / len(times)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = shape.tokens * world
-    value = tokens / (ms * 1e-3)
+    ms = max_over_ranks(torch, ms, world, dev)
+    value = job_rate(shape.tokens, world, ms)
+    del flush
+    torch.cuda.empty_cache()
+    # end to end through the public call, on every rank at once (whole-job rate)
+    e2e = bench_e2e(torch, m3, dev, shape, inp, args, world) if args.only == "all" else None
     if rank != 0:
         return
 
@@ -346,8 +369,6 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps,
         "device_status": m3.m3_status_string(status),
     }
-    del flush
-    torch.cuda.empty_cache()
     if args.only != "all":
         # a single workload (used for profiling): no side benchmarks
         print(json.dumps(line), flush=True)
@@ -359,7 +380,7 @@ def run_ours(args, rank, world, local_rank):
     sis, mim = line["decode"]["siso"], line["decode"]["mimo_r4"]
     if sis.get("ms_per_step") and mim.get("ms_per_step"):
         line["decode"]["r4_over_r1_latency"] = mim["ms_per_step"] / sis["ms_per_step"]
-    line["e2e"] = bench_e2e(torch, m3, dev, shape, inp, args)
+    line["e2e"] = e2e
     if not args.no_cpu_baseline:
         rate, cores, sample = oracle_rate(shape, inp)
         line["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": cores,
@@ -526,10 +547,11 @@ def bench_decode(torch, m3, dev, name, peaks, n_sets=16, steps=m3synth.DECODE_ST
             "l2": "state 134 MB exceeds the 126 MB L2; no flush between steps"}
 
 
-def bench_e2e(torch, m3, dev, shape, inp, args):
+def bench_e2e(torch, m3, dev, shape, inp, args, world=1):
     """Same workload through the public call from pinned host buffers: every
     step copies the inputs host->device, runs the scan and reads the outputs
-    back (y and final state) into pinned host memory."""
+    back (y and final state) into pinned host memory. All ranks run it at
+    once; the rate is all ranks' tokens over the slowest rank's time."""
     host = {k: v.pin_memory() for k, v in to_device(inp, True, "cpu").items()}
     devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
     out_h = torch.empty_like(host["x"]).pin_memory()
@@ -553,15 +575,18 @@ def bench_e2e(torch, m3, dev, shape, inp, args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    return {"value": shape.tokens / (ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+    ms = max_over_ranks(torch, e0.elapsed_time(e1) / args.steps, world, dev)
+    return {"value": job_rate(shape.tokens, world, ms), "unit": "tok/s",
+            "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
+            "ms_per_step": ms}
 
 
 def main():

@@ -27,7 +27,8 @@
  *     invalid or unsupported call returns a non-zero status and touches no
  *     output. A failed launch returns M3_ERR_CUDA.
  *   - Kernels never trap or assert. A bounded device-side wait that expires
- *     records a flag that m3_device_status() reports as M3_ERR_TIMEOUT.
+ *     records a flag that m3_device_status() reports as M3_ERR_TIMEOUT; the
+ *     outputs of that call (and decode's state) are then unspecified.
  *   - Outputs must not alias inputs (decode's `state` is updated in place).
  *   - The library runs on compute capability 10.3 (B300) only; elsewhere the
  *     compute entry points return M3_ERR_UNSUPPORTED.

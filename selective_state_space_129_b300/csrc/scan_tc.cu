@@ -1291,27 +1291,51 @@ int num_sms() {
 //   h_{j+1} = Rot(Phi_j) (2^{d_j} h_j + G_j)
 // with G_j, d_j, Phi_j the state-only pass's local end state, log2 decay and
 // angle of segment j. Entering states overwrite the G's in place.
-__global__ void seg_combine_kernel(float* __restrict__ ws, const float* __restrict__ scal,
-                                   int64_t nseq, int nseg, int N, int P) {
+// The segments' loads are independent of the recurrence, so a thread issues
+// them kSegBatch at a time before walking those steps (the walk itself is a
+// few flops per segment); the segment angles are wrapped to [-pi, pi], where
+// the fast sincos is accurate.
+constexpr int kSegBatch = 8;
+__global__ void __launch_bounds__(256)
+    seg_combine_kernel(float* __restrict__ ws, const float* __restrict__ scal, int64_t nseq,
+                       int nseg, int N, int P) {
   const int KP = N / 2;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= nseq * KP * P) return;
   const int64_t seq = i / ((int64_t)KP * P);
   const int k = (int)((i / P) % KP), pcol = (int)(i % P);
+  const int64_t o0 = (int64_t)(2 * k) * P + pcol, o1 = o0 + P;
   float h0 = 0.f, h1 = 0.f;
-  for (int j = 0; j < nseg; ++j) {
-    const int64_t u = seq * nseg + j;
-    float* st = ws + u * (int64_t)N * P;
-    const float g0 = st[(int64_t)(2 * k) * P + pcol], g1 = st[(int64_t)(2 * k + 1) * P + pcol];
-    st[(int64_t)(2 * k) * P + pcol] = h0;
-    st[(int64_t)(2 * k + 1) * P + pcol] = h1;
-    const float* sc = scal + u * (int64_t)(1 + KP);
-    const float d = exp2f(sc[0]);
-    float sn, cs;
-    sincosf(sc[1 + k], &sn, &cs);
-    const float t0 = fmaf(d, h0, g0), t1 = fmaf(d, h1, g1);
-    h0 = cs * t0 - sn * t1;
-    h1 = sn * t0 + cs * t1;
+  for (int j0 = 0; j0 < nseg; j0 += kSegBatch) {
+    float g0[kSegBatch], g1[kSegBatch], lg[kSegBatch], ang[kSegBatch];
+#pragma unroll
+    for (int jj = 0; jj < kSegBatch; ++jj) {
+      const int j = j0 + jj;
+      if (j < nseg) {
+        const int64_t u = seq * nseg + j;
+        const float* st = ws + u * (int64_t)N * P;
+        const float* sc = scal + u * (int64_t)(1 + KP);
+        g0[jj] = st[o0];
+        g1[jj] = st[o1];
+        lg[jj] = sc[0];
+        ang[jj] = sc[1 + k];
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < kSegBatch; ++jj) {
+      const int j = j0 + jj;
+      if (j < nseg) {
+        float* st = ws + (seq * nseg + j) * (int64_t)N * P;
+        st[o0] = h0;  // the state entering segment j
+        st[o1] = h1;
+        const float d = exp2f(lg[jj]);
+        float sn, cs;
+        __sincosf(ang[jj], &sn, &cs);
+        const float t0 = fmaf(d, h0, g0[jj]), t1 = fmaf(d, h1, g1[jj]);
+        h0 = cs * t0 - sn * t1;
+        h1 = sn * t0 + cs * t1;
+      }
+    }
   }
 }
 

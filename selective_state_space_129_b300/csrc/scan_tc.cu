@@ -761,6 +761,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
           }
         }
+      } else if constexpr (TPG <= 2) {
+        // few tokens per thread (R = 4): every rank's bias row is loaded once
+        // and applied to the thread's tokens, whose cos / sin are kept
+        float2 csB[TPG], snB[TPG], nsnB[TPG], csC[TPG], snC[TPG], nsnC[TPG];
+#pragma unroll
+        for (int i = 0; i < TPG; ++i) {
+          float2 sn, cs;
+          __sincosf(ph[i].x, &sn.x, &cs.x);
+          __sincosf(ph[i].y, &sn.y, &cs.y);
+          csB[i] = mul2(cs, sB2);
+          snB[i] = mul2(sn, sB2);
+          nsnB[i] = make_float2(-snB[i].x, -snB[i].y);
+          csC[i] = mul2(cs, sC2);
+          snC[i] = mul2(sn, sC2);
+          nsnC[i] = make_float2(-snC[i].x, -snC[i].y);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float4 bq = *reinterpret_cast<const float4*>(&s_biasT[0][r][4 * kk2]);
+          float4 cq = bq;
+          if constexpr (!SO) cq = *reinterpret_cast<const float4*>(&s_biasT[1][r][4 * kk2]);
+#pragma unroll
+          for (int i = 0; i < TPG; ++i) {
+            const int t = tg * TPG + i;
+            float2 b0 = make_float2(bf_at(bw[i], 0 * R + r), bf_at(bw[i], 2 * R + r));
+            float2 b1 = make_float2(bf_at(bw[i], 1 * R + r), bf_at(bw[i], 3 * R + r));
+            b0 = add2(b0, make_float2(bq.x, bq.z));
+            b1 = add2(b1, make_float2(bq.y, bq.w));
+            const float2 bt0 = fma2(csB[i], b0, mul2(snB[i], b1));
+            const float2 bt1 = fma2(csB[i], b1, mul2(nsnB[i], b0));
+            const uint32_t o = tile_off((uint32_t)(t * R + r), 4u * kk2, 64u);
+            sts64(opb + K::kOpBt + o, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
+            if constexpr (!SO) {
+              float2 c0 = make_float2(bf_at(cw[i], 0 * R + r), bf_at(cw[i], 2 * R + r));
+              float2 c1 = make_float2(bf_at(cw[i], 1 * R + r), bf_at(cw[i], 3 * R + r));
+              c0 = add2(c0, make_float2(cq.x, cq.z));
+              c1 = add2(c1, make_float2(cq.y, cq.w));
+              const float2 ct0 = fma2(csC[i], c0, mul2(snC[i], c1));
+              const float2 ct1 = fma2(csC[i], c1, mul2(nsnC[i], c0));
+              sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
+            }
+          }
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < TPG; ++i) {

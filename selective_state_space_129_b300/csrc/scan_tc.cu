@@ -450,7 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the first chunk's inputs
     Sched sch;
     sch.start(blockIdx.x, p);
-    if (tid == 0) {
+    // one-off duties sit on warps without other extra work: TMA of the raw
+    // tiles (warp 4), S and D MMA issue (warps 2 and 3); warp 0 runs the decay
+    // scan, warp 1 loads the next chunk's decay inputs, warps 6 and 7 carry
+    // the angle totals
+    constexpr int kTmaTid = 128, kSTid = 64, kDTid = 96;
+    if (tid == kTmaTid) {
       issue_raw(sch);
       inflight = 0;
     }
@@ -459,6 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_decay_raw(p, sch.b, sch.h, (int64_t)sch.c * Q, Q, lane, d);
       store_decay(d, lane, s_dtraw[0], s_lamraw[0], s_bnx[0]);
     }
+    // the first chunk's decay inputs are in place before warp 0 reads them
+    // (later chunks' are stored before the previous chunk's last barrier)
+    ptx::named_bar_sync(kBarPro, kProThreads);
     float A_h = 0.f;
     for (int g = 0;; ++g) {
       const int h = sch.h;
@@ -470,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur_h = h;
         A_h = p.A[h];
         float mb = 0.f, mc = 0.f;
-        // the previous head's bias was last read before this chunk's first barrier
+        // the previous head's bias was last read before the previous chunk's
+        // last barrier
         for (int i = tid; i < NS * R; i += kProThreads) {
           const float vb = p.B_bias ? p.B_bias[(int64_t)h * NS * R + i] : 0.f;
           const float vc = p.C_bias ? p.C_bias[(int64_t)h * NS * R + i] : 0.f;
@@ -494,20 +503,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           cmax_bias = fmaxf(cmax_bias, s_bias_red[1][w]);
         }
       }
-      // 1. this chunk's raw tiles have landed and operand slot s is free
-      if (tid == 0) {
-        bool ok = wait_or_abort(&bar_raw_full, (uint32_t)(g & 1), &abort_flag, p.status);
-        if (ok) inflight = -1;
-        if (ok && g >= 2)
-          ok = wait_or_abort(&bar_slot_free[s], (uint32_t)(((g >> 1) & 1) ^ 1), &abort_flag,
-                             p.status);
-        s_go[0] = ok ? 1 : 0;
-      }
-      ptx::named_bar_sync(kBarPro, kProThreads);
-      if (!s_go[0]) break;
-      // 2a. decay scan (warp 0); the next chunk's dt, lambda (warp 1, into registers)
+      // 1. every thread waits for this chunk's raw tiles itself (no block
+      // barrier here); an expired wait sets the abort flag, which every thread
+      // reads after the next barrier
+      if (wait_or_abort(&bar_raw_full, (uint32_t)(g & 1), &abort_flag, p.status) && tid == kTmaTid)
+        inflight = -1;
+      // 2a. decay scan (warp 0, once operand slot s and its scalars are free:
+      // the rest of the slot is written after the next barrier); the next
+      // chunk's dt, lambda (warp 1, into registers)
       DecayRaw nd;
-      if (warp == 0) {
+      int slot_ok = 1;
+      if (warp == 0 && g >= 2) {
+        if (lane == 0)
+          slot_ok = wait_or_abort(&bar_slot_free[s], (uint32_t)(((g >> 1) & 1) ^ 1), &abort_flag,
+                                  p.status) ? 1 : 0;
+        slot_ok = __shfl_sync(0xffffffffu, slot_ok, 0);
+      }
+      if (warp == 0 && slot_ok) {
         float dtv[2], lmv[2], bnx[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -641,9 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ptx::named_bar_sync(kBarPro, kProThreads);
+      if (*reinterpret_cast<volatile int*>(&abort_flag)) break;  // uniform after the barrier
       // every read of the raw slot is done: refill it with the next chunk
       if (has_next) {
-        if (tid == 0) {
+        if (tid == kTmaTid) {
           Sched nxt = sch;
           nxt.next(p);
           issue_raw(nxt);
@@ -877,11 +890,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // since the core released slot s), then publish the slot to the core
       ptx::fence_proxy_async_smem();
       ptx::named_bar_sync(kBarPro, kProThreads);
-      // (S from warp 0 and D from warp 1, so that the two issue sequences overlap)
-      if (tid == 0 || (!SO && tid == 32)) {
+      // (S and D from two warps, so that the two issue sequences overlap)
+      if ((!SO && tid == kSTid) || tid == kDTid) {
         const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
         ptx::tc_fence_after_sync();
-        if (SO || tid == 32) {
+        if (tid == kDTid) {
           const Desc dBm = make_desc(opb + K::kOpBt, 64u * 128u);
           const Desc dXw = make_desc(opb + K::kOpXw, 64u * 128u);
 #pragma unroll
@@ -896,13 +909,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                              kIdS, kk > 0);
         }
         ptx::mma_commit(&bar_acc_full[s]);
-        if (tid == 0) ptx::mbar_arrive(&bar_op_full[s]);
+        if (tid == kDTid) ptx::mbar_arrive(&bar_op_full[s]);
       }
       if (!has_next) break;
       sch.next(p);  // = nxt, recomputed rather than kept live across the body
     }
     // on an early exit, let an issued load land before the CTA ends
-    if (tid == 0 && inflight >= 0) ptx::mbar_wait(&bar_raw_full, (uint32_t)inflight, kWaitNs);
+    if (tid == kTmaTid && inflight >= 0) ptx::mbar_wait(&bar_raw_full, (uint32_t)inflight, kWaitNs);
   } else {
     // ============================================================ core (+ MMA issue)
     const int ct = tid - kProThreads;  // 0..127

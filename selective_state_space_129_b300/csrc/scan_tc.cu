@@ -508,7 +508,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       // reads after the next barrier
       if (wait_or_abort(&bar_raw_full, (uint32_t)(g & 1), &abort_flag, p.status) && tid == kTmaTid)
         inflight = -1;
-      // 2a. decay scan (warp 0, once operand slot s and its scalars are free:
+      // 2b. raw tiles -> registers (loads issued first)
+      float2 th2[TPG];
+      uint32_t bw[TPG][K::BW], cw[TPG][K::BW];
+      uint32_t bacc = 0u, cacc = 0u;
+#pragma unroll
+      for (int i = 0; i < TPG; ++i) {
+        const int t = tg * TPG + i;
+        const uint2 tv = lds64(sbase + K::kRawTh + (uint32_t)(t * KP + k0) * 4u);
+        th2[i] = make_float2(__uint_as_float(tv.x), __uint_as_float(tv.y));
+        const uint32_t ob = (uint32_t)(t * NS * R + 4 * kk2 * R) * 2u;
+        if constexpr (R == 1) {
+          const uint2 vb = lds64(sbase + K::kRawB + ob);
+          bw[i][0] = vb.x; bw[i][1] = vb.y;
+          if constexpr (!SO) {
+            const uint2 vc = lds64(sbase + K::kRawC + ob);
+            cw[i][0] = vc.x; cw[i][1] = vc.y;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < K::BW / 4; ++q) {
+            const uint4 vb = lds128(sbase + K::kRawB + ob + 16u * q);
+            bw[i][4 * q] = vb.x; bw[i][4 * q + 1] = vb.y; bw[i][4 * q + 2] = vb.z; bw[i][4 * q + 3] = vb.w;
+            if constexpr (!SO) {
+              const uint4 vc = lds128(sbase + K::kRawC + ob + 16u * q);
+              cw[i][4 * q] = vc.x; cw[i][4 * q + 1] = vc.y; cw[i][4 * q + 2] = vc.z; cw[i][4 * q + 3] = vc.w;
+            }
+          }
+        }
+      }
+      // 2a (while the tile loads above are in flight). Decay scan (warp 0, once
+      // operand slot s and its scalars are free:
       // the rest of the slot is written after the next barrier); the next
       // chunk's dt, lambda (warp 1, into registers)
       DecayRaw nd;
@@ -566,34 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         nxt.next(p);
         load_decay_raw(p, nxt.b, nxt.h, (int64_t)nxt.c * Q, Q, lane, nd);
       }
-      // 2b. raw tiles -> registers; magnitude bounds; Kahan-compensated angle sums
-      float2 th2[TPG];
-      uint32_t bw[TPG][K::BW], cw[TPG][K::BW];
-      uint32_t bacc = 0u, cacc = 0u;
+      // 2c. magnitude bounds, Kahan-compensated angle sums
 #pragma unroll
       for (int i = 0; i < TPG; ++i) {
-        const int t = tg * TPG + i;
-        const uint2 tv = lds64(sbase + K::kRawTh + (uint32_t)(t * KP + k0) * 4u);
-        th2[i] = make_float2(__uint_as_float(tv.x), __uint_as_float(tv.y));
-        const uint32_t ob = (uint32_t)(t * NS * R + 4 * kk2 * R) * 2u;
-        if constexpr (R == 1) {
-          const uint2 vb = lds64(sbase + K::kRawB + ob);
-          bw[i][0] = vb.x; bw[i][1] = vb.y;
-          if constexpr (!SO) {
-            const uint2 vc = lds64(sbase + K::kRawC + ob);
-            cw[i][0] = vc.x; cw[i][1] = vc.y;
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < K::BW / 4; ++q) {
-            const uint4 vb = lds128(sbase + K::kRawB + ob + 16u * q);
-            bw[i][4 * q] = vb.x; bw[i][4 * q + 1] = vb.y; bw[i][4 * q + 2] = vb.z; bw[i][4 * q + 3] = vb.w;
-            if constexpr (!SO) {
-              const uint4 vc = lds128(sbase + K::kRawC + ob + 16u * q);
-              cw[i][4 * q] = vc.x; cw[i][4 * q + 1] = vc.y; cw[i][4 * q + 2] = vc.z; cw[i][4 * q + 3] = vc.w;
-            }
-          }
-        }
 #pragma unroll
         for (int q = 0; q < K::BW; ++q) {
           bacc = ptx::bf16x2_absmax(bacc, bw[i][q]);

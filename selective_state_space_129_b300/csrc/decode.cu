@@ -10,18 +10,20 @@
 //
 // The step is bound by HBM traffic: the fp32 state (N x P per head) is read
 // and written once, everything else is a few KB per head. The rank-R
-// products are formed on the CUDA cores in registers while the state streams;
-// at R <= 4 they are a handful of FMAs per state element, far below the FMA
-// roof, so moving them to the tensor pipe would not shorten the step.
+// products are formed on the CUDA cores in registers while the state streams
+// (about 3R + 2 FMAs per state element); the rank-4 step is the one where this
+// arithmetic and the per-(b, h) set-up start to show next to the stream.
 //
-// Layout of work: one CTA per (batch, head), 256 threads. A work item is one
-// rotating row pair (2k, 2k+1) times four consecutive columns, loaded as two
-// 16-byte vectors, so that a warp reads 2 x 256 contiguous bytes per
-// instruction. Each thread keeps a fixed column quad, so its x / x_prev values
-// and its partial y stay in registers. The first items' state loads are issued
-// before the per-head coefficients are prepared, so that they are in flight
-// during that set-up; the partial y are reduced with warp shuffles and one
-// shared-memory pass, without atomics.
+// Two kernels. The streaming kernel (further below) is used whenever its
+// copy-engine alignment rules hold. The one-CTA-per-(batch, head) kernel here
+// takes every other shape: 256 threads; a work item is one rotating row pair
+// (2k, 2k+1) times four consecutive columns, loaded as two 16-byte vectors, so
+// that a warp reads 2 x 256 contiguous bytes per instruction. Each thread
+// keeps a fixed column quad, so its x / x_prev values and its partial y stay
+// in registers. The first items' state loads are issued before the per-head
+// coefficients are prepared, so that they are in flight during that set-up;
+// the partial y are reduced with warp shuffles and one shared-memory pass,
+// without atomics.
 #include <cuda_bf16.h>
 
 #include "common.cuh"

@@ -36,18 +36,20 @@
 // from chunk to chunk as a float-float pair fed by Kahan-compensated sums, so
 // it does not drift over long sequences.
 //
-// Organisation: a persistent, warp-specialised CTA (384 threads, one per SM)
-// walks whole (b, h) sequences, chunk by chunk, as a software pipeline:
-//   warps 0-7    prologue: decay scan, angles, RoPE fold of B/C into fp16
-//                UMMA tiles, w X, into one of two operand slots per chunk;
-//                its thread 0 also issues the TMA of the next chunk's raw B,
-//                C, theta, x tiles (one raw slot), one warp prefetches the
-//                next chunk's dt, lambda
-//   warps 8-11   core: mask S -> P, state H = exp(Lam_end) H + D and its fp16
-//                copy, y = Y + exp(Lam_t) Yoff -> TMA store, final state; its
-//                thread 0 issues the MMAs: Y = P X for chunk c, then
-//                S, D = Bt^T (w X), Yoff = Ct H for chunk c+1 into the other
-//                of two TMEM accumulator sets, overlapping chunk c's epilogue
+// Organisation: a persistent, warp-specialised CTA (512 threads, one per SM)
+// walks work units (whole (b, h) sequences, or segments of them when there
+// are fewer sequences than SMs), chunk by chunk, as a software pipeline:
+//   warps 0-7    prologue: decay scan (warp 0), angles, RoPE fold of B/C into
+//                fp16 UMMA tiles, w X, into one of two operand slots per chunk;
+//                one thread issues the TMA of the next chunk's raw B, C,
+//                theta, x tiles (one raw slot), two others the chunk's S and D
+//                MMAs into one of two TMEM accumulator sets; one warp
+//                prefetches the next chunk's dt, lambda
+//   warps 8-15   core (two warps per TMEM lane quadrant, 32 columns each):
+//                mask S -> P, state H = exp(Lam_end) H + D and its fp16 copy,
+//                y = Y + exp(Lam_t) Yoff -> TMA store, final state; its thread
+//                0 issues Y = P X for chunk c and Yoff = Ct H for chunk c+1,
+//                overlapping chunk c's epilogue
 // so the prologue of chunk c+1 runs while the core finishes chunk c. Roles
 // hand off through mbarriers; a role synchronises internally with its own
 // named barrier. Operand tiles are 128-byte-swizzled rows of 64 16-bit
@@ -429,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after_sync();
   const uint32_t tmem = tmem_holder;
 
-  // TMA of one chunk's raw tiles into the raw slot (prologue thread 0)
+  // TMA of one chunk's raw tiles into the raw slot (one prologue thread)
   auto issue_raw = [&](const Sched& u) {
     const int b = u.b, h = u.h, gi = h / p.hpg;
     const int t0 = u.c * Q;

@@ -549,44 +549,68 @@ def bench_decode(torch, m3, dev, name, peaks, n_sets=16, steps=m3synth.DECODE_ST
 
 def bench_e2e(torch, m3, dev, shape, inp, args, world=1):
     """Same workload through the public call from pinned host buffers: every
-    step copies the inputs host->device, runs the scan and reads the outputs
-    back (y and final state) into pinned host memory. All ranks run it at
-    once; the rate is all ranks' tokens over the slowest rank's time."""
+    step copies its inputs host->device, runs the scan and reads its outputs
+    (y and final state) back into pinned host memory. Steps are pipelined the
+    way a serving loop would run them: two device buffer sets, one stream each
+    for the copy in, the scan and the copy out, so that step k's scan overlaps
+    step k+1's copy in and step k-1's copy out (PCIe carries both directions at
+    once). All ranks run it at once; the rate is all ranks' tokens over the
+    slowest rank's time."""
     host = {k: v.pin_memory() for k, v in to_device(inp, True, "cpu").items()}
-    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    out_h = torch.empty_like(host["x"]).pin_memory()
-    fs_h = torch.empty((shape.batch, shape.heads, shape.dstate, shape.headdim),
-                       dtype=torch.float32).pin_memory()
-    out = torch.empty_like(devb["x"])
-    fs = torch.empty(fs_h.shape, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
+    nbuf = 2
+    devb = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(nbuf)]
+    out = [torch.empty_like(devb[0]["x"]) for _ in range(nbuf)]
+    fs = [torch.empty((shape.batch, shape.heads, shape.dstate, shape.headdim),
+                      dtype=torch.float32, device=dev) for _ in range(nbuf)]
+    out_h = [torch.empty_like(host["x"]).pin_memory() for _ in range(nbuf)]
+    fs_h = [torch.empty(fs[0].shape, dtype=torch.float32).pin_memory() for _ in range(nbuf)]
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
+    in_done = [ev() for _ in range(nbuf)]
+    run_done = [ev() for _ in range(nbuf)]
+    out_done = [ev() for _ in range(nbuf)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_h.numel() * out_h.element_size() + fs_h.numel() * 4
+    d2h = out_h[0].numel() * out_h[0].element_size() + fs_h[0].numel() * 4
 
-    def step():
-        for k in host:
-            devb[k].copy_(host[k], non_blocking=True)
-        m3.m3_scan_fwd(devb["x"], devb["dt"], devb["A"], devb["lam"], devb["B"], devb["C"],
-                       devb["theta"], R=shape.R, chunk=shape.chunk, out=out, final_state=fs,
-                       B_bias=devb["B_bias"], C_bias=devb["C_bias"], stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        fs_h.copy_(fs, non_blocking=True)
+    def step(k):
+        j = k % nbuf
+        s_in.wait_event(run_done[j])    # step k - 2's scan has read buffer set j
+        with torch.cuda.stream(s_in):
+            for name in host:
+                devb[j][name].copy_(host[name], non_blocking=True)
+            in_done[j].record(s_in)
+        s_run.wait_event(in_done[j])
+        s_run.wait_event(out_done[j])   # step k - 2's outputs have left buffer set j
+        m3.m3_scan_fwd(devb[j]["x"], devb[j]["dt"], devb[j]["A"], devb[j]["lam"], devb[j]["B"],
+                       devb[j]["C"], devb[j]["theta"], R=shape.R, chunk=shape.chunk, out=out[j],
+                       final_state=fs[j], B_bias=devb[j]["B_bias"], C_bias=devb[j]["C_bias"],
+                       stream=s_run)
+        run_done[j].record(s_run)
+        s_out.wait_event(run_done[j])
+        with torch.cuda.stream(s_out):
+            out_h[j].copy_(out[j], non_blocking=True)
+            fs_h[j].copy_(fs[j], non_blocking=True)
+            out_done[j].record(s_out)
 
-    for _ in range(args.warmup):
-        step()
+    for k in range(args.warmup):
+        step(k)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
+    e0.record(s_in)
+    s_run.wait_event(e0)
+    s_out.wait_event(e0)
+    for k in range(args.steps):
+        step(k)
+    s_in.wait_event(out_done[(args.steps - 1) % nbuf])
+    e1.record(s_in)
     torch.cuda.synchronize()
     ms = max_over_ranks(torch, e0.elapsed_time(e1) / args.steps, world, dev)
     return {"value": job_rate(shape.tokens, world, ms), "unit": "tok/s",
             "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
-            "ms_per_step": ms}
+            "ms_per_step": ms, "pipelined": "copy in, scan, copy out on three streams, "
+                                            "two buffer sets"}
 
 
 def main():

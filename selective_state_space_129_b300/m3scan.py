@@ -84,6 +84,46 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _expect(t, name, shape, dtype, optional=False):
+    """The C ABI takes plain pointers to row-major contiguous device arrays:
+    check what a pointer cannot carry (device, dtype, shape, contiguity)."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError("%s is required" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _check_prefill(x, dt, A, lam, B, C, theta, R, out, final_state, B_bias, C_bias):
+    import torch
+    if x.dim() != 5 or B.dim() != 5:
+        raise ValueError("x must be [b,L,H,P,R] and B [b,L,G,N,R]")
+    b, L, H, P, R_ = x.shape
+    if R_ != R:
+        raise ValueError("x.shape[-1] must equal R")
+    G, N = B.shape[2], B.shape[3]
+    f32, act = torch.float32, x.dtype
+    _expect(x, "x", (b, L, H, P, R), act)
+    _expect(dt, "dt", (b, L, H), f32)
+    _expect(lam, "lam", (b, L, H), f32)
+    _expect(A, "A", (H,), f32)
+    _expect(B, "B", (b, L, G, N, R), act)
+    _expect(C, "C", (b, L, G, N, R), act)
+    _expect(theta, "theta", (b, L, G, N // 2), f32)
+    _expect(B_bias, "B_bias", (H, N, R), f32, optional=True)
+    _expect(C_bias, "C_bias", (H, N, R), f32, optional=True)
+    _expect(out, "out", (b, L, H, P, R), act, optional=True)
+    _expect(final_state, "final_state", (b, H, N, P), f32, optional=True)
+    return b, L, H, P, G, N
+
+
 def _stream_handle(stream):
     if stream is None:
         import torch
@@ -131,10 +171,10 @@ def m3_scan_fwd(x, dt, A, lam, B, C, theta, R, chunk, out=None, final_state=None
     theta [b,L,G,N/2]. Returns (out, final_state)."""
     import torch
     lib = load()
-    b, L, H, P, R_ = x.shape
-    if R_ != R:
-        raise ValueError("x.shape[-1] must equal R")
-    G, N = B.shape[2], B.shape[3]
+    b, L, H, P, G, N = _check_prefill(x, dt, A, lam, B, C, theta, R, out, final_state, B_bias,
+                                      C_bias)
+    if workspace is not None and not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
     if out is None:
         out = torch.empty_like(x)
     if final_state is None and want_state:
@@ -153,10 +193,10 @@ def m3_scan_fwd_noalloc(x, dt, A, lam, B, C, theta, R, chunk, out, final_state, 
     (``final_state`` may be None); the library allocates no device memory (its
     scratch is a fixed 32 MiB array; larger needs raise M3Error)."""
     lib = load()
-    b, L, H, P, R_ = x.shape
-    if R_ != R:
-        raise ValueError("x.shape[-1] must equal R")
-    G, N = B.shape[2], B.shape[3]
+    if out is None:
+        raise ValueError("out is required")
+    b, L, H, P, G, N = _check_prefill(x, dt, A, lam, B, C, theta, R, out, final_state, B_bias,
+                                      C_bias)
     dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias)
     st = lib.m3_scan_fwd_noalloc(_ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B), _ptr(C),
                                  _ptr(theta), ctypes.byref(dims), int(R), int(chunk), _ptr(out),
@@ -170,10 +210,26 @@ def m3_decode_step(state, x, dt, A, lam, B, C, theta, R, B_prev=None, x_prev=Non
     """One decode token; ``state`` [b,H,N,P] fp32 is updated in place. Returns out [b,H,P,R]."""
     import torch
     lib = load()
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [b,H,P,R] and B [b,G,N,R]")
     b, H, P, R_ = x.shape
     if R_ != R:
         raise ValueError("x.shape[-1] must equal R")
     G, N = B.shape[1], B.shape[2]
+    f32, act = torch.float32, x.dtype
+    _expect(state, "state", (b, H, N, P), f32)
+    _expect(x, "x", (b, H, P, R), act)
+    _expect(dt, "dt", (b, H), f32)
+    _expect(lam, "lam", (b, H), f32)
+    _expect(A, "A", (H,), f32)
+    _expect(B, "B", (b, G, N, R), act)
+    _expect(C, "C", (b, G, N, R), act)
+    _expect(theta, "theta", (b, G, N // 2), f32)
+    _expect(B_prev, "B_prev", (b, G, N, R), act, optional=True)
+    _expect(x_prev, "x_prev", (b, H, P, R), act, optional=True)
+    _expect(B_bias, "B_bias", (H, N, R), f32, optional=True)
+    _expect(C_bias, "C_bias", (H, N, R), f32, optional=True)
+    _expect(out, "out", (b, H, P, R), act, optional=True)
     if out is None:
         out = torch.empty_like(x)
     dims = make_dims(b, 1, H, G, P, N, _act_dtype(x), B_bias, C_bias)

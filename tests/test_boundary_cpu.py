@@ -143,3 +143,61 @@ def test_valid_call_without_a_device_reports_cuda_error(lib):
     assert _scan(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert _decode(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert lib.m3_device_status(None) == m3scan.M3_ERR_CUDA
+
+
+# ---------------------------------------------------------------- binding checks
+# The Python binding checks what a raw pointer cannot carry (device, dtype,
+# shape, contiguity) before any library call.
+def _prefill_args(torch, dev="cpu", b=1, L=4, H=2, G=1, P=8, N=8, R=1, act=None):
+    act = act or torch.bfloat16
+    f = dict(device=dev)
+    return dict(x=torch.zeros(b, L, H, P, R, dtype=act, **f),
+                dt=torch.zeros(b, L, H, **f), A=torch.zeros(H, **f), lam=torch.zeros(b, L, H, **f),
+                B=torch.zeros(b, L, G, N, R, dtype=act, **f),
+                C=torch.zeros(b, L, G, N, R, dtype=act, **f),
+                theta=torch.zeros(b, L, G, N // 2, **f), R=R, chunk=4)
+
+
+def test_binding_rejects_host_tensors():
+    torch = pytest.importorskip("torch")
+    from selective_state_space_129_b300 import m3scan
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        m3scan.m3_scan_fwd(**_prefill_args(torch))
+
+
+class _DeviceTensorStub:
+    """Stands in for a CUDA tensor (no GPU here): what the checks read."""
+
+    def __init__(self, shape, dtype, contiguous=True):
+        self.is_cuda, self.shape, self.dtype, self._c = True, shape, dtype, contiguous
+
+    def is_contiguous(self):
+        return self._c
+
+
+def test_binding_checks_shapes_dtypes_and_contiguity():
+    torch = pytest.importorskip("torch")
+    from selective_state_space_129_b300 import m3scan
+    ex = m3scan._expect
+    ex(_DeviceTensorStub((2, 3), torch.float32), "t", (2, 3), torch.float32)  # passes
+    ex(None, "opt", (1,), torch.float32, optional=True)                       # passes
+    with pytest.raises(ValueError, match="required"):
+        ex(None, "t", (1,), torch.float32)
+    with pytest.raises(ValueError, match="must have shape"):
+        ex(_DeviceTensorStub((2, 4), torch.float32), "t", (2, 3), torch.float32)
+    with pytest.raises(ValueError, match="must be torch.float32"):
+        ex(_DeviceTensorStub((2, 3), torch.bfloat16), "t", (2, 3), torch.float32)
+    with pytest.raises(ValueError, match="contiguous"):
+        ex(_DeviceTensorStub((2, 3), torch.float32, contiguous=False), "t", (2, 3), torch.float32)
+
+
+def test_decode_binding_rejects_host_state():
+    torch = pytest.importorskip("torch")
+    from selective_state_space_129_b300 import m3scan
+    b, H, G, P, N, R = 1, 2, 1, 8, 8, 1
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        m3scan.m3_decode_step(torch.zeros(b, H, N, P), torch.zeros(b, H, P, R, dtype=torch.bfloat16),
+                              torch.zeros(b, H), torch.zeros(H), torch.zeros(b, H),
+                              torch.zeros(b, G, N, R, dtype=torch.bfloat16),
+                              torch.zeros(b, G, N, R, dtype=torch.bfloat16),
+                              torch.zeros(b, G, N // 2), R=R)

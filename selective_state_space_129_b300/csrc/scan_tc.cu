@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_go[2];  // per-role broadcast of "continue" decisions
   __shared__ SlotScalars<KP> ss[2];
   __shared__ float s_dtraw[2][64], s_lamraw[2][64], s_bnx[2][64];
-  __shared__ float s_tot[2][TG][KP];   // per token group: angle total (hi, lo)
+  __shared__ __align__(16) float s_tot[2][TG][KP];   // per token group: angle total (hi, lo)
   __shared__ float s_carry[2][2][KP];  // [chunk parity][hi, lo][pair]
   __shared__ unsigned int s_max[2][3];  // per chunk parity: bounds of |B|, |C|, |x| (float bits)
   __shared__ float s_hred[kCoreWarps];
@@ -701,8 +701,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         float o0 = 0.f, o1 = 0.f;
         for (int q = 0; q < tg; ++q) {
-          o0 += s_tot[0][q][k0] + s_tot[1][q][k0];
-          o1 += s_tot[0][q][k0 + 1] + s_tot[1][q][k0 + 1];
+          const float2 hi = *reinterpret_cast<const float2*>(&s_tot[0][q][k0]);
+          const float2 lo = *reinterpret_cast<const float2*>(&s_tot[1][q][k0]);
+          const float2 o = add2(make_float2(o0, o1), add2(hi, lo));
+          o0 = o.x;
+          o1 = o.y;
         }
         float ch0 = 0.f, cl0 = 0.f, ch1 = 0.f, cl1 = 0.f;
         if (c > sch.c_begin) {
@@ -1060,17 +1063,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ph_[8], pl_[8];
 #pragma unroll
           for (int j = 0; j < 16; j += 2) {
-            float v2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int u = (j + e) / R, s_ = s0 + u;
-              const float moff = ex2(lt - lsv[u]) * wpv[u];
-              const float m = (s_ < t) ? moff : ((s_ == t) ? gdiag : 0.f);
-              v2[e] = m * __uint_as_float(sv[j + e]);
-            }
-            const uint32_t hw = pack_bf16(v2[0], v2[1]);
+            // two columns at a time (packed fp32 pairs; same roundings as scalar)
+            const int u0 = j / R, u1 = (j + 1) / R;
+            const float2 dl = sub2(make_float2(lt, lt), make_float2(lsv[u0], lsv[u1]));
+            const float2 mo = mul2(make_float2(ex2(dl.x), ex2(dl.y)), make_float2(wpv[u0], wpv[u1]));
+            const float m0 = (s0 + u0 < t) ? mo.x : ((s0 + u0 == t) ? gdiag : 0.f);
+            const float m1 = (s0 + u1 < t) ? mo.y : ((s0 + u1 == t) ? gdiag : 0.f);
+            const float2 v2 = mul2(make_float2(m0, m1),
+                                   make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])));
+            const uint32_t hw = pack_bf16(v2.x, v2.y);
             ph_[j >> 1] = hw;
-            pl_[j >> 1] = pack_bf16(v2[0] - bf_lo(hw), v2[1] - bf_hi(hw));
+            const float2 lo = sub2(v2, make_float2(bf_lo(hw), bf_hi(hw)));
+            pl_[j >> 1] = pack_bf16(lo.x, lo.y);
           }
           const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
           const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
@@ -1178,7 +1182,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tmem_ld16_16x32bx2<16>(tset + kColYo + ta, yo);
               ptx::tmem_ld_wait(yo);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) y[j] = fmaf(el, __uint_as_float(yo[j]), y[j]);
+              for (int j = 0; j < 16; j += 2) {
+                const float2 r2 = fma2(make_float2(el, el),
+                                       make_float2(__uint_as_float(yo[j]), __uint_as_float(yo[j + 1])),
+                                       make_float2(y[j], y[j + 1]));
+                y[j] = r2.x;
+                y[j + 1] = r2.y;
+              }
             }
             if constexpr (R == 1) {
               const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);

@@ -271,13 +271,27 @@ inline StreamLayout stream_layout(const DecodeArgs& a, int act) {
   return L;
 }
 
+// Per-unit coefficient tables: 3NR + N floats. R = 1: gamma (B + bias),
+// beta_hat (B_prev + bias), C + bias as [N][R] rows and alpha cos, alpha sin
+// as [N/2]. R > 1: the rotation is folded into the B_prev term (see the
+// kernel): U [N][2R] rows, C + bias [N][R] rows, (alpha cos, alpha sin) [N/2].
+__host__ __device__ inline size_t stream_coef_floats(size_t N, size_t R) { return 3 * N * R + N; }
+// Whether each warp prepares the coefficient rows of its own row pairs (no
+// block-wide barrier between preparation and items) or the whole CTA prepares
+// every row and meets at a barrier.
+__host__ __device__ constexpr bool stream_warp_prep(int R) { return R == 1; }
+// Two partial-y tables with per-warp preparation (no block-wide barrier
+// between one unit's final sum and the next unit's items), else one.
+__host__ __device__ inline int stream_yred_tables(int R) { return stream_warp_prep(R) ? 2 : 1; }
+
 // Partial y of warp w, column 4q + c, rank r at yred[(w 4R + c R + r)(P/4 + 1) + q]:
 // the lanes of a warp (consecutive q) store to consecutive words, and the
 // padding keeps the reads of the final sum (consecutive (p, r)) off shared banks.
 inline size_t stream_smem_bytes(const DecodeArgs& a, const StreamLayout& L) {
   const size_t N = a.N, P = a.P, R = a.R;
   return (size_t)kStages * L.bytes +
-         sizeof(float) * (3 * N * R + N + 2 * (size_t)kSWarps * R * (P + 4) + (size_t)a.H);
+         sizeof(float) * (stream_coef_floats(N, R) +
+                          stream_yred_tables(a.R) * (size_t)kSWarps * R * (P + 4) + (size_t)a.H);
 }
 
 // The 4 x R activations of one column quad (4 R consecutive elements of a
@@ -321,14 +335,18 @@ __global__ void __launch_bounds__(kSThreads, 2)
   const int N = (int)a.N, P = (int)a.P, K2 = N / 2, PQ = P / 4, H = (int)a.H;
   const int hpg = (int)(a.H / a.G);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float* bg = reinterpret_cast<float*>(dsm + (size_t)kStages * L.bytes);  // gamma (B + bias) [N][R]
-  float* bp = bg + N * R;        // beta_hat (B_prev + bias)  [N][R]
-  float* cc = bp + N * R;        // C + bias                  [N][R]
-  float* rc = cc + N * R;        // alpha cos                 [K2]
-  float* rs = rc + K2;           // alpha sin                 [K2]
-  float* yred0 = rs + K2;        // partial y per warp, two tables (padded layout above)
+  float* coef = reinterpret_cast<float*>(dsm + (size_t)kStages * L.bytes);
+  float* bg = coef;              // R = 1: gamma (B + bias)   [N][R]
+  float* bp = bg + N * R;        //        beta_hat (B_prev + bias)  [N][R]
+  float* cc = bp + N * R;        //        C + bias           [N][R]
+  float* rc = cc + N * R;        //        alpha cos          [K2]
+  float* rs = rc + K2;           //        alpha sin          [K2]
+  float* ud = coef;              // R > 1: U                  [N][2R]
+  float* cd = ud + 2 * N * R;    //        C + bias           [N][R]
+  float* rd = cd + N * R;        //        alpha (cos, sin)   [K2][2]
+  float* yred0 = coef + stream_coef_floats(N, R);  // partial y per warp (padded layout above)
   const int yred_floats = kSWarps * R * (P + 4);
-  float* sA = yred0 + 2 * yred_floats;  // A                  [H]
+  float* sA = yred0 + stream_yred_tables(R) * yred_floats;  // A [H]
   const bool has_prev = a.B_prev != nullptr;
   const int q = tid % PQ;  // this thread's column quad (PQ divides 32)
   const int items = K2 * PQ;
@@ -392,7 +410,7 @@ __global__ void __launch_bounds__(kSThreads, 2)
     // CTA prepares all rows and meets at a barrier, which measured faster
     // (b128 H32 P64 N128 R4: 58 us per step against 65 us per-warp; R1: 45 us
     // per-warp against 47 us).
-    constexpr bool kWarpPrep = (R == 1);
+    constexpr bool kWarpPrep = stream_warp_prep(R);
     const int kpw = 32 / PQ;                                  // row pairs per block of 32 items
     const int nj = (items - 32 * warp + kSThreads - 1) / kSThreads;  // this warp's blocks
     const int h = u % H;
@@ -406,23 +424,43 @@ __global__ void __launch_bounds__(kSThreads, 2)
     const float* sbb = reinterpret_cast<const float*>(stg + L.bb);
     const float* scb = reinterpret_cast<const float*>(stg + L.cb);
     const float* sth = reinterpret_cast<const float*>(stg + L.th);
+    // R > 1: the rotation is linear in the rows, so alpha Rot (beta_hat
+    // (B_prev + bias) x_prev^T) = (alpha Rot beta_hat (B_prev + bias)) x_prev^T:
+    // the rotated rows U[n][r] are formed once per unit, and the items apply
+    // the rotation to the state alone. Entry (row pair kq, rank r):
+    auto fold_prep = [&](int kq, int r) {
+      float sn, cs;
+      sincosf(d * sth[kq], &sn, &cs);
+      const float ac = alpha * cs, as = alpha * sn;
+      const int i0 = 2 * kq * R + r, i1 = i0 + R;  // (row 2kq, r), (row 2kq + 1, r)
+      const float bb0 = a.B_bias ? sbb[i0] : 0.f, bb1 = a.B_bias ? sbb[i1] : 0.f;
+      const float cb0 = a.C_bias ? scb[i0] : 0.f, cb1 = a.C_bias ? scb[i1] : 0.f;
+      float u0 = 0.f, u1 = 0.f;
+      if (has_prev) {
+        const float p0 = bhat * (ld_act(sBp + i0) + bb0), p1 = bhat * (ld_act(sBp + i1) + bb1);
+        u0 = fmaf(ac, p0, -as * p1);
+        u1 = fmaf(as, p0, ac * p1);
+      }
+      const float g0 = gamma * (ld_act(sB + i0) + bb0), g1 = gamma * (ld_act(sB + i1) + bb1);
+      float* U0 = ud + 2 * kq * 2 * R;  // row 2kq: U[n][r] = rotated B_prev term, U[n][R + r] = B term
+      U0[r] = u0;
+      U0[R + r] = g0;
+      U0[2 * R + r] = u1;  // row 2kq + 1
+      U0[3 * R + r] = g1;
+      cd[i0] = ld_act(sC + i0) + cb0;
+      cd[i1] = ld_act(sC + i1) + cb1;
+      if (r == 0) reinterpret_cast<float2*>(rd)[kq] = make_float2(ac, as);
+    };
     if (!kWarpPrep) {
-      // the whole CTA prepares every row, then one barrier
-      for (int i = tid; ok && i < N * R; i += kSThreads) {
-        const float bb = a.B_bias ? sbb[i] : 0.f;
-        const float cb = a.C_bias ? scb[i] : 0.f;
-        bg[i] = gamma * (ld_act(sB + i) + bb);
-        bp[i] = has_prev ? bhat * (ld_act(sBp + i) + bb) : 0.f;
-        cc[i] = ld_act(sC + i) + cb;
-      }
-      for (int kk = tid; ok && kk < K2; kk += kSThreads) {
-        float sn, cs;
-        sincosf(d * sth[kk], &sn, &cs);
-        rc[kk] = alpha * cs;
-        rs[kk] = alpha * sn;
-      }
+      for (int e = tid; ok && e < K2 * R; e += kSThreads) fold_prep(e / R, e % R);
       __syncthreads();
       if (abort_flag) break;  // uniform: read after the barrier
+    } else if (R > 1 && ok && nj > 0) {
+      for (int e = lane; e < nj * kpw * R; e += 32) {
+        const int jj = e / (kpw * R), rem = e - jj * kpw * R;
+        const int kq = (32 * warp + jj * kSThreads) / PQ + rem / R;
+        if (kq < K2) fold_prep(kq, rem % R);
+      }
     } else if (ok && nj > 0) {
       const int per_block = kpw * 2 * R;  // coefficient entries (row, rank) per block
       for (int e = lane; e < nj * per_block; e += 32) {
@@ -466,54 +504,75 @@ __global__ void __launch_bounds__(kSThreads, 2)
 
     const float* sst = reinterpret_cast<const float*>(stg + L.st);
     float* gst = a.state + (int64_t)u * N * P;
-    float* yred = yred0 + (k & 1) * yred_floats;  // alternates: the last unit's sum may still read the other
-    for (int it = tid; ok && it < items; it += kSThreads) {
-      const int kq = it / PQ;
-      float4 h0 = *reinterpret_cast<const float4*>(sst + (2 * kq) * P + 4 * q);
-      float4 h1 = *reinterpret_cast<const float4*>(sst + (2 * kq + 1) * P + 4 * q);
-      float bp0[R], bp1[R], bg0[R], bg1[R], c0[R], c1[R];
-      ld_row<R>(bp + (2 * kq) * R, bp0);
-      ld_row<R>(bp + (2 * kq + 1) * R, bp1);
-      ld_row<R>(bg + (2 * kq) * R, bg0);
-      ld_row<R>(bg + (2 * kq + 1) * R, bg1);
-      ld_row<R>(cc + (2 * kq) * R, c0);
-      ld_row<R>(cc + (2 * kq + 1) * R, c1);
-      const float ac = rc[kq], as = rs[kq];
-      float* v0 = reinterpret_cast<float*>(&h0);
-      float* v1 = reinterpret_cast<float*>(&h1);
-      if constexpr (R == 1) {
+    // with per-warp preparation two tables alternate: the last unit's sum may still read the other
+    float* yred = yred0 + (kWarpPrep ? (k & 1) * yred_floats : 0);
+    if constexpr (R == 1) {
+      for (int it = tid; ok && it < items; it += kSThreads) {
+        const int kq = it / PQ;
+        float4 h0 = *reinterpret_cast<const float4*>(sst + (2 * kq) * P + 4 * q);
+        float4 h1 = *reinterpret_cast<const float4*>(sst + (2 * kq + 1) * P + 4 * q);
+        const float bp0 = bp[2 * kq], bp1 = bp[2 * kq + 1], bg0 = bg[2 * kq], bg1 = bg[2 * kq + 1];
+        const float c0 = cc[2 * kq], c1 = cc[2 * kq + 1];
+        const float ac = rc[kq], as = rs[kq];
+        float* v0 = reinterpret_cast<float*>(&h0);
+        float* v1 = reinterpret_cast<float*>(&h1);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const float g0 = fmaf(bp0[0], xpr[c][0], v0[c]), g1 = fmaf(bp1[0], xpr[c][0], v1[c]);
-          const float u0 = bg0[0] * xr[c][0], u1 = bg1[0] * xr[c][0];
+          const float g0 = fmaf(bp0, xpr[c][0], v0[c]), g1 = fmaf(bp1, xpr[c][0], v1[c]);
+          const float u0 = bg0 * xr[c][0], u1 = bg1 * xr[c][0];
           const float n0 = fmaf(ac, g0, fmaf(-as, g1, u0));
           const float n1 = fmaf(as, g0, fmaf(ac, g1, u1));
           v0[c] = n0;
           v1[c] = n1;
-          yp[c][0] = fmaf(c0[0], n0, fmaf(c1[0], n1, yp[c][0]));
+          yp[c][0] = fmaf(c0, n0, fmaf(c1, n1, yp[c][0]));
         }
-      } else {
-        // rank sums on (r, r + 1) pairs: packed two-lane FMAs, operands straight
-        // from the coefficient rows and the activations
+        *reinterpret_cast<float4*>(gst + (2 * kq) * P + 4 * q) = h0;
+        *reinterpret_cast<float4*>(gst + (2 * kq + 1) * P + 4 * q) = h1;
+      }
+    } else {
+      // h' = alpha Rot h + U (x_prev | x)^T: the 2R-term row sums run on rank
+      // pairs as packed two-lane FMAs. X[c][j] = (x_prev | x)[column 4q + c]
+      // [ranks 2j, 2j + 1], j < R.
+      float2 X[4][R];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < R / 2; ++j) {
+          X[c][j] = make_float2(xpr[c][2 * j], xpr[c][2 * j + 1]);
+          X[c][R / 2 + j] = make_float2(xr[c][2 * j], xr[c][2 * j + 1]);
+        }
+      const float4* U4 = reinterpret_cast<const float4*>(ud);  // R / 2 float4 per row
+      const float2* R2 = reinterpret_cast<const float2*>(rd);
+      for (int it = tid; ok && it < items; it += kSThreads) {
+        const int kq = it / PQ;
+        float4 h0 = *reinterpret_cast<const float4*>(sst + (2 * kq) * P + 4 * q);
+        float4 h1 = *reinterpret_cast<const float4*>(sst + (2 * kq + 1) * P + 4 * q);
+        float2 w0[R], w1[R];
+#pragma unroll
+        for (int j = 0; j < R / 2; ++j) {
+          const float4 t0 = U4[2 * kq * (R / 2) + j], t1 = U4[(2 * kq + 1) * (R / 2) + j];
+          w0[2 * j] = make_float2(t0.x, t0.y);
+          w0[2 * j + 1] = make_float2(t0.z, t0.w);
+          w1[2 * j] = make_float2(t1.x, t1.y);
+          w1[2 * j + 1] = make_float2(t1.z, t1.w);
+        }
+        float c0[R], c1[R];
+        ld_row<R>(cd + (2 * kq) * R, c0);
+        ld_row<R>(cd + (2 * kq + 1) * R, c1);
+        const float2 rot = R2[kq];
+        const float ac = rot.x, as = rot.y;
+        float* v0 = reinterpret_cast<float*>(&h0);
+        float* v1 = reinterpret_cast<float*>(&h1);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float2 ag0 = ptx::mul2(make_float2(bp0[0], bp0[1]), make_float2(xpr[c][0], xpr[c][1]));
-          float2 ag1 = ptx::mul2(make_float2(bp1[0], bp1[1]), make_float2(xpr[c][0], xpr[c][1]));
-          float2 au0 = ptx::mul2(make_float2(bg0[0], bg0[1]), make_float2(xr[c][0], xr[c][1]));
-          float2 au1 = ptx::mul2(make_float2(bg1[0], bg1[1]), make_float2(xr[c][0], xr[c][1]));
+          float2 s0 = ptx::mul2(w0[0], X[c][0]), s1 = ptx::mul2(w1[0], X[c][0]);
 #pragma unroll
-          for (int r = 2; r < R; r += 2) {
-            const float2 xp2 = make_float2(xpr[c][r], xpr[c][r + 1]);
-            const float2 x2 = make_float2(xr[c][r], xr[c][r + 1]);
-            ag0 = ptx::fma2(make_float2(bp0[r], bp0[r + 1]), xp2, ag0);
-            ag1 = ptx::fma2(make_float2(bp1[r], bp1[r + 1]), xp2, ag1);
-            au0 = ptx::fma2(make_float2(bg0[r], bg0[r + 1]), x2, au0);
-            au1 = ptx::fma2(make_float2(bg1[r], bg1[r + 1]), x2, au1);
+          for (int j = 1; j < R; ++j) {
+            s0 = ptx::fma2(w0[j], X[c][j], s0);
+            s1 = ptx::fma2(w1[j], X[c][j], s1);
           }
-          const float g0 = v0[c] + (ag0.x + ag0.y), g1 = v1[c] + (ag1.x + ag1.y);
-          const float u0 = au0.x + au0.y, u1 = au1.x + au1.y;
-          const float n0 = fmaf(ac, g0, fmaf(-as, g1, u0));
-          const float n1 = fmaf(as, g0, fmaf(ac, g1, u1));
+          const float n0 = fmaf(ac, v0[c], fmaf(-as, v1[c], s0.x + s0.y));
+          const float n1 = fmaf(as, v0[c], fmaf(ac, v1[c], s1.x + s1.y));
           v0[c] = n0;
           v1[c] = n1;
           const float2 n02 = make_float2(n0, n0), n12 = make_float2(n1, n1);
@@ -526,9 +585,9 @@ __global__ void __launch_bounds__(kSThreads, 2)
             yp[c][r + 1] = y2.y;
           }
         }
+        *reinterpret_cast<float4*>(gst + (2 * kq) * P + 4 * q) = h0;
+        *reinterpret_cast<float4*>(gst + (2 * kq + 1) * P + 4 * q) = h1;
       }
-      *reinterpret_cast<float4*>(gst + (2 * kq) * P + 4 * q) = h0;
-      *reinterpret_cast<float4*>(gst + (2 * kq + 1) * P + 4 * q) = h1;
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c)

@@ -288,6 +288,34 @@ def test_decode_streaming_partial_item_block(orc, R):
     assert m3.m3_device_status() == m3.M3_OK
 
 
+@pytest.mark.parametrize("R", [2, 4])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_decode_streaming_mimo_without_bias(orc, R, bf16):
+    """Rank 2 and 4 through the streaming kernel with no B / C bias and four
+    heads sharing each of two B / C groups, three steps."""
+    shape = m3synth.ScanShape(3, 1, 8, 2, 64, 64, R=R, chunk=1, bf16=bf16)
+    b, H, N, P = shape.batch, shape.heads, shape.dstate, shape.headdim
+    st_ref = np.random.default_rng(11).standard_normal((b, H, N, P))
+    st = torch.from_numpy(st_ref.astype(np.float32)).cuda()
+    st_ref = st.cpu().numpy().astype(np.float64)
+    prev, prev_h = None, None
+    for i in range(3):
+        s_ = m3synth.decode_inputs(shape, seed=70 + R, step=i)
+        d = to_device(s_, bf16)
+        kw = dict(B_prev=prev["B"], x_prev=prev["x"]) if prev is not None else {}
+        out = m3.m3_decode_step(st, d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"],
+                                d["theta"], R=R, **kw)
+        okw = dict(B_prev=prev_h["B"], x_prev=prev_h["x"]) if prev_h is not None else {}
+        y_ref, st_ref = orc.decode_step(st_ref, s_["x"], s_["dt"], s_["A"], s_["lam"], s_["B"],
+                                        s_["C"], s_["theta"], **okw)
+        torch.cuda.synchronize()
+        (assert_bf16_out if bf16 else assert_f32)(out.float().cpu().numpy(), y_ref,
+                                                  "y step %d" % i)
+        prev, prev_h = d, s_
+    (assert_bf16 if bf16 else assert_f32)(st.cpu().numpy(), st_ref, "state")
+    assert m3.m3_device_status() == m3.M3_OK
+
+
 def test_decode_full_batch_mimo(orc):
     """The 128 x 32 decode batch at rank 4, bf16: two steps (every CTA of the
     streaming kernel walks several (batch, head) units through both stages)."""

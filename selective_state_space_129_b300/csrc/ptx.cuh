@@ -113,17 +113,6 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-// Named barrier that also returns the OR of one predicate over its threads.
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool p) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)p), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
 
 // Elementwise max of |a| and |b| over the two bf16 halves of each word (the
 // sign bits of the result are those of a xor b; callers clear them).

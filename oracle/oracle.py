@@ -149,6 +149,31 @@ def decode_step(state, x, dt, A, lam, B, C, theta, B_prev=None, x_prev=None,
     return y, st
 
 
+def decode_tokens(state, x, dt, A, lam, B, C, theta, B_prev=None, x_prev=None,
+                  B_bias=None, C_bias=None, nthreads=0):
+    """K consecutive decode tokens of every (batch, head): the decode step
+    applied to tokens t = 0 .. K-1 in order, token t's previous token being
+    token t-1 of the block (the given B_prev / x_prev for t = 0; None for the
+    first token of a sequence). Returns (y, new_state); ``state`` is not
+    modified.
+
+    Layouts: state [b,H,N,P]; x, y [b,K,H,P,R]; dt, lam [b,K,H];
+    B, C [b,K,G,N,R]; theta [b,K,G,N/2]; B_prev [b,G,N,R], x_prev [b,H,P,R].
+    """
+    x, dt, lam, B, C, theta = map(_f64, (x, dt, lam, B, C, theta))
+    K = x.shape[1]
+    st = _f64(state)
+    ys = []
+    for t in range(K):
+        bp, xp = (B_prev, x_prev) if t == 0 else (B[:, t - 1], x[:, t - 1])
+        y, st = decode_step(st, x[:, t], dt[:, t], A, lam[:, t], B[:, t], C[:, t], theta[:, t],
+                            B_prev=bp, x_prev=xp, B_bias=B_bias, C_bias=C_bias,
+                            nthreads=nthreads)
+        ys.append(y)
+    y = np.stack(ys, axis=1) if ys else np.zeros_like(x)
+    return y, st
+
+
 class Oracle:
     """The same entry points bound to a given build of ``m3oracle.c``.
 

@@ -310,6 +310,35 @@ def test_prefill_then_decode(orc, R):
 
 
 # ---------------------------------------------------------------------------
+# 10b. K decode tokens in one block continue a prefill exactly: prefill of
+#      L tokens, then tokens L .. L+K-1 decoded together, equals the prefill
+#      of L + K tokens (outputs of the decoded tokens and the final state);
+#      from a zero state with no previous token it equals a K-token prefill.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("R", [1, 4])
+def test_decode_tokens_continue_prefill(orc, R):
+    import oracle.oracle as om
+    L, K = 11, 5
+    d = _rand_inputs(12, b=2, L=L + K, H=4, G=2, P=3, N=6, R=R)
+    seq = ("x", "dt", "lam", "B", "C", "theta")
+    y_full, st_full = orc.scan_seq(**d)
+    _, stL = orc.scan_seq(**{k: (v[:, :L] if k in seq else v) for k, v in d.items()})
+    blk = {k: d[k][:, L:] for k in seq}
+    y, st = om.decode_tokens(stL, blk["x"], blk["dt"], d["A"], blk["lam"], blk["B"], blk["C"],
+                             blk["theta"], B_prev=d["B"][:, L - 1], x_prev=d["x"][:, L - 1],
+                             B_bias=d["B_bias"], C_bias=d["C_bias"])
+    assert y.shape == y_full[:, L:].shape
+    assert _rel(y, y_full[:, L:]) < 1e-12
+    assert _rel(st, st_full) < 1e-12
+    first = {k: d[k][:, :K] for k in seq}
+    y0, s0 = om.decode_tokens(np.zeros_like(stL), first["x"], first["dt"], d["A"], first["lam"],
+                              first["B"], first["C"], first["theta"], B_bias=d["B_bias"],
+                              C_bias=d["C_bias"])
+    y_pre, s_pre = orc.scan_seq(**{k: (v[:, :K] if k in seq else v) for k, v in d.items()})
+    assert _rel(y0, y_pre) < 1e-12 and _rel(s0, s_pre) < 1e-12
+
+
+# ---------------------------------------------------------------------------
 # 11. Hand-derived two-token example (fixture).
 # ---------------------------------------------------------------------------
 def _ev(expr):

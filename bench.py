@@ -15,6 +15,8 @@ Printed on rank 0: one JSON line. Besides the contract keys it carries
   roofline         HBM roof of the prefill kernel (algorithmic bytes / time)
   roofline_tensor  tensor-pipe roof of the same kernel (algorithmic FLOPs / time)
   decode           1024-step CUDA-graph decode, batch 128 x 32 heads, R = 1 and 4
+  decode_tokens    multi-token decode (8 tokens per call, state read and written
+                   once per call), same batch, R = 1 and 4
   prefill_mimo     the R = 4 prefill workload (chunk 16)
   e2e              through the C ABI from pinned host buffers, copies included
   cpu_baseline     the fp64 CPU oracle on a bounded sample of the workload
@@ -78,6 +80,16 @@ def decode_bytes(s: m3synth.ScanShape) -> int:
     act = 2
     return (2 * b * H * N * P * 4 + 3 * b * H * P * R * act + 3 * b * G * N * R * act
             + b * G * (N // 2) * 4 + 2 * b * H * 4)
+
+
+def decode_tokens_bytes(s: m3synth.ScanShape, K: int) -> int:
+    """Per multi-token call: the state read + written once, plus the K tokens'
+    activations (x, out, B, C, theta, dt, lambda) and the token before the block."""
+    b, H, G, P, N, R = s.batch, s.heads, s.groups, s.headdim, s.dstate, s.R
+    act = 2
+    per_token = (2 * b * H * P * R * act + 2 * b * G * N * R * act + b * G * (N // 2) * 4
+                 + 2 * b * H * 4)
+    return 2 * b * H * N * P * 4 + K * per_token + b * H * P * R * act + b * G * N * R * act
 
 
 class Clocks:
@@ -296,6 +308,12 @@ def run_ours(args, rank, world, local_rank):
             print(json.dumps(bench_decode(torch, m3, dev, args.only, peaks,
                                           steps=args.decode_steps)), flush=True)
         return
+    if args.only in ("decode_tokens_siso", "decode_tokens_mimo"):
+        if rank == 0:
+            name = args.only.replace("tokens_", "")
+            print(json.dumps(bench_decode_tokens(torch, m3, dev, name, peaks,
+                                                 calls=args.decode_steps)), flush=True)
+        return
     if args.only == "prefill_long":
         if rank == 0:
             print(json.dumps(bench_prefill_long(torch, m3, dev, args, peaks)), flush=True)
@@ -380,6 +398,9 @@ def run_ours(args, rank, world, local_rank):
     sis, mim = line["decode"]["siso"], line["decode"]["mimo_r4"]
     if sis.get("ms_per_step") and mim.get("ms_per_step"):
         line["decode"]["r4_over_r1_latency"] = mim["ms_per_step"] / sis["ms_per_step"]
+    line["decode_tokens"] = {
+        "siso_k%d" % DECODE_BLOCK: bench_decode_tokens(torch, m3, dev, "decode_siso", peaks),
+        "mimo_r4_k%d" % DECODE_BLOCK: bench_decode_tokens(torch, m3, dev, "decode_mimo", peaks)}
     line["e2e"] = e2e
     if not args.no_cpu_baseline:
         rate, cores, sample = oracle_rate(shape, inp)
@@ -547,6 +568,74 @@ def bench_decode(torch, m3, dev, name, peaks, n_sets=16, steps=m3synth.DECODE_ST
             "l2": "state 134 MB exceeds the 126 MB L2; no flush between steps"}
 
 
+DECODE_BLOCK = 8  # tokens per multi-token decode call
+# fp32 CUDA-core peak: 148 SMs x 128 FMA lanes x 2 flop x 2.032 GHz (maximum SM clock)
+FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def bench_decode_tokens(torch, m3, dev, name, peaks, K=DECODE_BLOCK, calls=128, n_sets=4):
+    """Multi-token decode: ``calls`` calls of K tokens each for the 128 x 32
+    decode batch, captured in one CUDA graph; the blocks cycle over ``n_sets``
+    seeded K-token sets (each block's B_prev / x_prev are the last token of
+    the block before). tok/s = 128 K calls / time."""
+    idx, base = m3synth.WORKLOADS[name]
+    shape = m3synth.ScanShape(base.batch, K, base.heads, base.groups, base.headdim, base.dstate,
+                              R=base.R, chunk=1)
+    raw = [m3synth.scan_inputs(shape, seed=100 * idx + i) for i in range(n_sets)]
+    for r in raw[1:]:  # one head's A and biases for the whole run
+        r["A"], r["B_bias"], r["C_bias"] = raw[0]["A"], raw[0]["B_bias"], raw[0]["C_bias"]
+    sets = [to_device(r, True, dev) for r in raw]
+    last = [{"B": s["B"][:, K - 1].contiguous(), "x": s["x"][:, K - 1].contiguous()} for s in sets]
+    st = torch.zeros((shape.batch, shape.heads, shape.dstate, shape.headdim),
+                     dtype=torch.float32, device=dev)
+    out = torch.empty_like(sets[0]["x"])
+    s = torch.cuda.Stream(device=dev)
+
+    def call(i, stream):
+        cur, prev = sets[i % n_sets], last[(i - 1) % n_sets]
+        m3.m3_decode_tokens(st, cur["x"], cur["dt"], cur["A"], cur["lam"], cur["B"], cur["C"],
+                            cur["theta"], R=shape.R, B_prev=prev["B"], x_prev=prev["x"],
+                            out=out, B_bias=cur["B_bias"], C_bias=cur["C_bias"], stream=stream)
+
+    with torch.cuda.stream(s):
+        for i in range(4):
+            call(i, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(calls):
+            call(i, s)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    reps = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for _ in range(reps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    ms_call = e0.elapsed_time(e1) / (reps * calls)
+    nbytes = decode_tokens_bytes(shape, K)
+    gbs = nbytes / (ms_call * 1e-3) / 1e9
+    # per state element and token: alpha Rot h (2 FMA), U (x_prev | x)^T (2R FMA), y (R FMA)
+    flops = (shape.batch * shape.heads * shape.dstate * shape.headdim * K * (4 + 6 * shape.R))
+    tfl = flops / (ms_call * 1e-3) / 1e12
+    return {"workload": "%s b%d H%d P%d N%d R%d, %d tokens per call, %d calls in one CUDA graph"
+                        % (name, shape.batch, shape.heads, shape.headdim, shape.dstate, shape.R,
+                           K, calls),
+            "tok_s": shape.batch * K / (ms_call * 1e-3), "ms_per_call": ms_call,
+            "ms_per_token_step": ms_call / K,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "algorithmic_bytes": nbytes},
+            "roofline_alu": {"bound": "alu", "achieved": tfl, "peak": FP32_PEAK_TFLOPS,
+                             "unit": "TFLOP/s", "frac": tfl / FP32_PEAK_TFLOPS,
+                             "algorithmic_flops": flops,
+                             "peak_source": "148 SMs x 128 fp32 FMA lanes x 2 x 2.032 GHz"},
+            "gpu_launches": calls * reps}
+
+
 def bench_e2e(torch, m3, dev, shape, inp, args, world=1):
     """Same workload through the public call from pinned host buffers: every
     step copies its inputs host->device, runs the scan and reads its outputs
@@ -622,10 +711,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="all",
                     choices=["all", "prefill_siso", "prefill_mimo", "decode_siso", "decode_mimo",
-                             "prefill_long"],
+                             "decode_tokens_siso", "decode_tokens_mimo", "prefill_long"],
                     help="run one workload alone (profiling); the default runs them all")
     ap.add_argument("--decode-steps", type=int, default=m3synth.DECODE_STEPS,
-                    help="decode steps per CUDA graph with --only decode_*")
+                    help="decode steps (or multi-token calls) per CUDA graph with --only decode_*")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     rank = int(os.environ.get("RANK", "0"))

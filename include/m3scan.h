@@ -58,7 +58,7 @@ typedef enum {
 
 typedef struct {
   int64_t batch;   /* b  >= 0                                             */
-  int64_t seqlen;  /* L  >= 0 (prefill); ignored by decode                 */
+  int64_t seqlen;  /* L  >= 0 (prefill); K (multi-token decode); ignored by decode */
   int64_t heads;   /* H  >= 1                                             */
   int64_t groups;  /* G  >= 1, divides H                                  */
   int64_t headdim; /* P  >= 1                                             */
@@ -121,6 +121,37 @@ m3_status m3_decode_step(float* state, const void* x, const float* dt, const flo
                          const float* lambda, const void* B_prev, const void* x_prev,
                          const void* B, const void* C, const float* theta, const m3_dims* dims,
                          int R, void* out, void* stream);
+
+/*
+ * Multi-token decode: K consecutive tokens of the recurrence for every (b, h)
+ * in one call, state updated in place; the result equals K calls of
+ * m3_decode_step in token order, token t's B_prev / x_prev being token t-1's
+ * raw B and x. The state is read once and written once per call (it stays on
+ * chip between the K tokens), so the state traffic per token falls by K --
+ * for a block of tokens that is known in advance (speculative drafts, a
+ * prompt's tail, several tokens per request).
+ *
+ *   state   [b, H, N, P]     fp32, h before the block on entry, after it on return
+ *   x, out  [b, K, H, P, R]  act_dtype
+ *   dt, lambda [b, K, H] fp32;  A [H] fp32
+ *   B, C    [b, K, G, N, R]  act_dtype (raw: the kernel adds the bias)
+ *   theta   [b, K, G, N/2]   fp32
+ *   B_prev  [b, G, N, R]     raw B, and
+ *   x_prev  [b, H, P, R]     x of the token before the block; both NULL when
+ *           the block starts a sequence. One NULL and one non-NULL is
+ *           M3_ERR_INVALID_ARG.
+ * K = dims->seqlen (1 ... 4096; K = 0 with b H > 0 is a no-op); workspace and
+ * workspace_bytes are ignored. Supported shapes: R in {1, 2, 4}, P a multiple
+ * of 4 with P/4 dividing 32, N/2 * P/4 <= 1024 (a state of at most 32 KB per
+ * head), every per-token block of x, B, C, theta and the biases a multiple of
+ * 16 bytes and 16-byte aligned, and the block's activations within 200 KB of
+ * shared memory; other valid shapes return M3_ERR_UNSUPPORTED (use
+ * m3_decode_step per token).
+ */
+m3_status m3_decode_tokens(float* state, const void* x, const float* dt, const float* A,
+                           const float* lambda, const void* B_prev, const void* x_prev,
+                           const void* B, const void* C, const float* theta,
+                           const m3_dims* dims, int R, void* out, void* stream);
 
 /*
  * Prefill that allocates no device memory: the same computation, arguments

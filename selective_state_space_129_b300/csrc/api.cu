@@ -199,6 +199,49 @@ m3_status m3_decode_step(float* state, const void* x, const float* dt, const flo
                                      static_cast<cudaStream_t>(stream)));
 }
 
+m3_status m3_decode_tokens(float* state, const void* x, const float* dt, const float* A,
+                           const float* lambda, const void* B_prev, const void* x_prev,
+                           const void* B, const void* C, const float* theta,
+                           const m3_dims* dims, int R, void* out, void* stream) {
+  m3_status st = check_dims(dims, R);
+  if (st != M3_OK) return st;
+  if (dims->seqlen < 0) return M3_ERR_INVALID_ARG;
+  if ((B_prev == nullptr) != (x_prev == nullptr)) return M3_ERR_INVALID_ARG;
+  const int64_t b = dims->batch, K = dims->seqlen, H = dims->heads, G = dims->groups,
+                P = dims->headdim, N = dims->dstate;
+  const size_t act = dims->act_dtype == M3_BF16 ? 2 : 4;
+  int64_t n_x, n_t, n_bc, n_th, n_st, n_xp, n_bp;
+  if (!count({b, K, H, P, R}, &n_x) || !count({b, K, H}, &n_t) || !count({b, K, G, N, R}, &n_bc) ||
+      !count({b, K, G, N / 2}, &n_th) || !count({b, H, N, P}, &n_st) ||
+      !count({b, H, P, R}, &n_xp) || !count({b, G, N, R}, &n_bp))
+    return M3_ERR_INVALID_ARG;
+  if (!ptr_ok(state, n_st, 16) || !ptr_ok(x, n_x, act) || !ptr_ok(out, n_x, act) ||
+      !ptr_ok(dt, n_t, 4) || !ptr_ok(lambda, n_t, 4) || !ptr_ok(A, H, 4) ||
+      !ptr_ok(B, n_bc, act) || !ptr_ok(C, n_bc, act) || !ptr_ok(theta, n_th, 4))
+    return M3_ERR_INVALID_ARG;
+  if (B_prev && (!ptr_ok(B_prev, n_bp, act) || !ptr_ok(x_prev, n_xp, act)))
+    return M3_ERR_INVALID_ARG;
+  if ((dims->B_bias && !aligned(dims->B_bias, 4)) || (dims->C_bias && !aligned(dims->C_bias, 4)))
+    return M3_ERR_INVALID_ARG;
+  m3::TokensArgs a;
+  a.state = state; a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B_prev = B_prev;
+  a.x_prev = x_prev; a.B = B; a.C = C; a.theta = theta; a.B_bias = dims->B_bias;
+  a.C_bias = dims->C_bias; a.out = out; a.batch = b; a.K = K; a.H = H; a.G = G; a.P = P;
+  a.N = N; a.R = R;
+  // the kernel moves every per-token block with 16-byte vectors
+  const void* vec[] = {x, B, C, theta, B_prev, x_prev, dims->B_bias, dims->C_bias};
+  for (const void* p : vec)
+    if (p != nullptr && !aligned(p, 16)) return M3_ERR_UNSUPPORTED;
+  if (K == 0 || n_st == 0) return M3_OK;  // nothing to compute
+  if (!m3::tokens_supported(a, (int)act)) return M3_ERR_UNSUPPORTED;
+  if (b * H > 0x7fffffff) return M3_ERR_UNSUPPORTED;
+
+  st = check_device();
+  if (st != M3_OK) return st;
+  return from_cuda(m3::launch_decode_tokens(a, dims->act_dtype == M3_BF16,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 m3_status m3_device_status(void* stream) {
   unsigned int v = 0;
   if (m3::read_clear_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess) {

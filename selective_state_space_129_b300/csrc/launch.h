@@ -44,6 +44,27 @@ struct DecodeArgs {
   int R;
 };
 
+// K consecutive decode tokens (x, out [b,K,H,P,R]; dt, lam [b,K,H];
+// B, C [b,K,G,N,R]; theta [b,K,G,N/2]; B_prev [b,G,N,R] and x_prev [b,H,P,R]
+// of the token before the block, or both NULL).
+struct TokensArgs {
+  float* state;
+  const void* x;
+  const float* dt;
+  const float* A;
+  const float* lam;
+  const void* B_prev;
+  const void* x_prev;
+  const void* B;
+  const void* C;
+  const float* theta;
+  const float* B_bias;
+  const float* C_bias;
+  void* out;
+  int64_t batch, K, H, G, P, N;
+  int R;
+};
+
 // CUDA-core chunked prefill (any shape whose tiles fit shared memory).
 size_t scan_simt_smem_bytes(int64_t N, int64_t P, int R, int Q);
 cudaError_t launch_scan_simt(const ScanArgs& a, bool bf16, cudaStream_t s);
@@ -57,6 +78,10 @@ cudaError_t launch_scan_tc(const ScanArgs& a, unsigned int* status, cudaStream_t
 // Decode step.
 bool decode_supported(int64_t N, int64_t P, int R);
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s);
+
+// K decode tokens in one launch, the state held on chip between them.
+bool tokens_supported(const TokensArgs& a, int act);
+cudaError_t launch_decode_tokens(const TokensArgs& a, bool bf16, cudaStream_t s);
 
 // Device address of this device's status word of expired waits.
 cudaError_t status_word(unsigned int** ptr);

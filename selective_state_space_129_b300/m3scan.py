@@ -18,7 +18,7 @@ M3_F32, M3_BF16 = 0, 1
 
 # Exported entry points (kept in step with include/m3scan.h).
 EXPORTS = ("m3_scan_fwd", "m3_scan_fwd_noalloc", "m3_decode_step", "m3_scan_workspace_bytes",
-           "m3_status_string", "m3_device_status", "m3_version")
+           "m3_status_string", "m3_device_status", "m3_version", "m3_decode_tokens")
 
 
 class M3Error(RuntimeError):
@@ -64,6 +64,8 @@ def load(path: str = LIB_PATH):
     lib.m3_scan_fwd_noalloc.restype = i32
     lib.m3_decode_step.argtypes = [vp] * 10 + [dims_p, i32, vp, vp]
     lib.m3_decode_step.restype = i32
+    lib.m3_decode_tokens.argtypes = [vp] * 10 + [dims_p, i32, vp, vp]
+    lib.m3_decode_tokens.restype = i32
     lib.m3_scan_workspace_bytes.argtypes = [dims_p, i32, i32]
     lib.m3_scan_workspace_bytes.restype = ctypes.c_size_t
     lib.m3_status_string.argtypes = [i32]
@@ -237,6 +239,45 @@ def m3_decode_step(state, x, dt, A, lam, B, C, theta, R, B_prev=None, x_prev=Non
                             _ptr(x_prev), _ptr(B), _ptr(C), _ptr(theta), ctypes.byref(dims),
                             int(R), _ptr(out), _stream_handle(stream))
     _check(st, "m3_decode_step")
+    return out
+
+
+def m3_decode_tokens(state, x, dt, A, lam, B, C, theta, R, B_prev=None, x_prev=None, out=None,
+                     B_bias=None, C_bias=None, stream=None):
+    """K consecutive decode tokens; ``state`` [b,H,N,P] fp32 is updated in place.
+
+    x [b,K,H,P,R], dt / lam [b,K,H], B / C [b,K,G,N,R], theta [b,K,G,N/2];
+    B_prev [b,G,N,R] / x_prev [b,H,P,R] are the token before the block (or
+    None). Returns out [b,K,H,P,R]."""
+    import torch
+    lib = load()
+    if x.dim() != 5 or B.dim() != 5:
+        raise ValueError("x must be [b,K,H,P,R] and B [b,K,G,N,R]")
+    b, K, H, P, R_ = x.shape
+    if R_ != R:
+        raise ValueError("x.shape[-1] must equal R")
+    G, N = B.shape[2], B.shape[3]
+    f32, act = torch.float32, x.dtype
+    _expect(state, "state", (b, H, N, P), f32)
+    _expect(x, "x", (b, K, H, P, R), act)
+    _expect(dt, "dt", (b, K, H), f32)
+    _expect(lam, "lam", (b, K, H), f32)
+    _expect(A, "A", (H,), f32)
+    _expect(B, "B", (b, K, G, N, R), act)
+    _expect(C, "C", (b, K, G, N, R), act)
+    _expect(theta, "theta", (b, K, G, N // 2), f32)
+    _expect(B_prev, "B_prev", (b, G, N, R), act, optional=True)
+    _expect(x_prev, "x_prev", (b, H, P, R), act, optional=True)
+    _expect(B_bias, "B_bias", (H, N, R), f32, optional=True)
+    _expect(C_bias, "C_bias", (H, N, R), f32, optional=True)
+    _expect(out, "out", (b, K, H, P, R), act, optional=True)
+    if out is None:
+        out = torch.empty_like(x)
+    dims = make_dims(b, K, H, G, P, N, _act_dtype(x), B_bias, C_bias)
+    st = lib.m3_decode_tokens(_ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B_prev),
+                              _ptr(x_prev), _ptr(B), _ptr(C), _ptr(theta), ctypes.byref(dims),
+                              int(R), _ptr(out), _stream_handle(stream))
+    _check(st, "m3_decode_tokens")
     return out
 
 

@@ -129,6 +129,39 @@ def test_decode_state_alignment(lib):
     assert _decode(lib, _dims(), state=FAKE + 4) == m3scan.M3_ERR_INVALID_ARG
 
 
+def _tokens(lib, dims, R=1, **ptrs):
+    p = dict(state=FAKE, x=FAKE, dt=FAKE, A=FAKE, lam=FAKE, Bp=0, xp=0, B=FAKE, C=FAKE,
+             theta=FAKE, out=FAKE)
+    p.update(ptrs)
+    v = lambda k: ctypes.c_void_p(p[k]) if p[k] else None
+    return lib.m3_decode_tokens(v("state"), v("x"), v("dt"), v("A"), v("lam"), v("Bp"), v("xp"),
+                                v("B"), v("C"), v("theta"), ctypes.byref(dims), R, v("out"), None)
+
+
+@pytest.mark.parametrize("missing", ["state", "x", "dt", "A", "lam", "B", "C", "theta", "out"])
+def test_tokens_null_pointer(lib, missing):
+    assert _tokens(lib, _dims(), **{missing: 0}) == m3scan.M3_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,R,ptrs,expect", [
+    (dict(headdim=6), 1, {}, m3scan.M3_ERR_UNSUPPORTED),           # P not a multiple of 4
+    (dict(), 3, {}, m3scan.M3_ERR_UNSUPPORTED),                    # R outside {1, 2, 4}
+    (dict(dstate=512, headdim=64), 1, {}, m3scan.M3_ERR_UNSUPPORTED),  # state above 32 KB
+    (dict(), 1, dict(x=FAKE + 4), m3scan.M3_ERR_UNSUPPORTED),      # not 16-byte aligned
+    (dict(seqlen=5000), 1, {}, m3scan.M3_ERR_UNSUPPORTED),         # K above 4096
+    (dict(dstate=5), 1, {}, m3scan.M3_ERR_INVALID_ARG),
+    (dict(seqlen=-1), 1, {}, m3scan.M3_ERR_INVALID_ARG),
+    (dict(), 1, dict(Bp=FAKE), m3scan.M3_ERR_INVALID_ARG),         # B_prev without x_prev
+    (dict(), 1, dict(state=FAKE + 4), m3scan.M3_ERR_INVALID_ARG),
+])
+def test_tokens_rejects(lib, kw, R, ptrs, expect):
+    assert _tokens(lib, _dims(**kw), R=R, **ptrs) == expect
+
+
+def test_tokens_empty_block_is_a_no_op(lib):
+    assert _tokens(lib, _dims(seqlen=0)) == m3scan.M3_OK
+
+
 def test_workspace_query(lib):
     d = _dims()
     assert m3scan.m3_scan_workspace_bytes(d, 1, 4) == 0
@@ -142,6 +175,7 @@ def test_valid_call_without_a_device_reports_cuda_error(lib):
         pytest.skip("a device is present; the no-device path is not reachable")
     assert _scan(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert _decode(lib, _dims()) == m3scan.M3_ERR_CUDA
+    assert _tokens(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert lib.m3_device_status(None) == m3scan.M3_ERR_CUDA
 
 

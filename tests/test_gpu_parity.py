@@ -342,6 +342,82 @@ def test_decode_full_batch_mimo(orc):
     assert m3.m3_device_status() == m3.M3_OK
 
 
+# ---------------------------------------------------------------- multi-token decode
+def _tokens_case(shape, seed, prev, bias=True):
+    """Inputs of a K-token block (K = shape.seqlen), a random entry state and,
+    with ``prev``, the raw B / x of the token before the block."""
+    inp = m3synth.scan_inputs(shape, seed=seed)
+    if not bias:
+        inp["B_bias"] = inp["C_bias"] = None
+    b, H, N, P = shape.batch, shape.heads, shape.dstate, shape.headdim
+    st0 = (0.5 * np.random.default_rng(seed).standard_normal((b, H, N, P))).astype(np.float32)
+    pv = m3synth.decode_inputs(shape, seed=seed + 1, step=0) if prev else None
+    return inp, st0, pv
+
+
+def _run_tokens(inp, st0, pv, shape):
+    d = to_device({k: v for k, v in inp.items() if v is not None}, shape.bf16)
+    kw = {}
+    if pv is not None:
+        dp = to_device(pv, shape.bf16)
+        kw = dict(B_prev=dp["B"], x_prev=dp["x"])
+    st = torch.from_numpy(st0).cuda()
+    out = m3.m3_decode_tokens(st, d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"],
+                              R=shape.R, B_bias=d.get("B_bias"), C_bias=d.get("C_bias"), **kw)
+    torch.cuda.synchronize()
+    assert m3.m3_device_status() == m3.M3_OK
+    return out.float().cpu().numpy(), st.cpu().numpy()
+
+
+def _oracle_tokens(orc, inp, st0, pv, bsel=None):
+    sel = (lambda a: a) if bsel is None else (lambda a: a[bsel])
+    kw = {}
+    if pv is not None:
+        kw = dict(B_prev=sel(pv["B"]), x_prev=sel(pv["x"]))
+    return orc.decode_tokens(sel(st0), sel(inp["x"]), sel(inp["dt"]), inp["A"], sel(inp["lam"]),
+                             sel(inp["B"]), sel(inp["C"]), sel(inp["theta"]),
+                             B_bias=inp["B_bias"], C_bias=inp["C_bias"], **kw)
+
+
+@pytest.mark.parametrize("R", [1, 2, 4])
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+@pytest.mark.parametrize("prev", [False, True], ids=["first", "continued"])
+def test_decode_tokens(orc, R, bf16, prev):
+    """Five tokens per call, b3 H8 G2 P64 N128: every thread holds four row
+    pairs of the state in registers across the tokens."""
+    shape = m3synth.ScanShape(3, 5, 8, 2, 64, 128, R=R, chunk=1, bf16=bf16)
+    inp, st0, pv = _tokens_case(shape, 80 + R, prev)
+    y, st = _run_tokens(inp, st0, pv, shape)
+    y_ref, st_ref = _oracle_tokens(orc, inp, st0, pv)
+    (assert_bf16_out if bf16 else assert_f32)(y, y_ref, "y")
+    (assert_bf16 if bf16 else assert_f32)(st, st_ref, "state")
+
+
+@pytest.mark.parametrize("P,N,R", [(8, 24, 1), (8, 24, 4), (32, 64, 2), (16, 16, 4)])
+def test_decode_tokens_small_shapes(orc, P, N, R):
+    """Fewer items than threads (N24 P8: 24), partial warps of column quads,
+    no bias, one token per call and a long block."""
+    for K, seed in ((1, 90), (13, 91)):
+        shape = m3synth.ScanShape(2, K, 4, 1, P, N, R=R, chunk=1, bf16=True)
+        inp, st0, pv = _tokens_case(shape, seed, prev=True, bias=False)
+        y, st = _run_tokens(inp, st0, pv, shape)
+        y_ref, st_ref = _oracle_tokens(orc, inp, st0, pv)
+        assert_bf16_out(y, y_ref, "y K=%d" % K)
+        assert_bf16(st, st_ref, "state K=%d" % K)
+
+
+def test_decode_tokens_full_batch_mimo(orc):
+    """The 128 x 32 decode batch at rank 4, eight tokens per call (the
+    benchmark's launch); batch rows 0, 77 and 127 checked against the oracle."""
+    shape = m3synth.ScanShape(128, 8, 32, 1, 64, 128, R=4, chunk=1, bf16=True)
+    inp, st0, pv = _tokens_case(shape, 95, prev=True)
+    y, st = _run_tokens(inp, st0, pv, shape)
+    bsel = np.array([0, 77, 127])
+    y_ref, st_ref = _oracle_tokens(orc, inp, st0, pv, bsel)
+    assert_bf16_out(y[bsel], y_ref, "y")
+    assert_bf16(st[bsel], st_ref, "state")
+
+
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 def test_prefill_then_decode_matches_longer_prefill(orc, bf16):
     shape = m3synth.ScanShape(2, 33, 4, 1, 64, 128, R=1, chunk=16, bf16=bf16)

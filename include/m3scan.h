@@ -102,6 +102,30 @@ m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const floa
                       int R, int chunk, void* out, float* final_state, void* stream);
 
 /*
+ * Prefill that continues a sequence (chunked prefill): the same computation,
+ * arguments and layouts as m3_scan_fwd over the block of L tokens, started
+ * from `state` instead of zero, with the state updated in place:
+ *
+ *   state   [b, H, N, P] fp32: h before the block on entry (explicit frame, as
+ *           returned by m3_scan_fwd's final_state, m3_decode_step or this
+ *           call), h after the block on return.
+ *   B_prev  [b, G, N, R] raw B and
+ *   x_prev  [b, H, P, R] x of the token before the block (act_dtype); both
+ *           NULL when the block starts the sequence (then the call equals
+ *           m3_scan_fwd from a zero state when `state` is zero). One NULL and
+ *           one non-NULL is M3_ERR_INVALID_ARG.
+ * Calling m3_scan_fwd on tokens [0, L1) and then this on [L1, L1 + L2) with
+ * the first call's final state and its last token as B_prev / x_prev gives
+ * the outputs and final state of one m3_scan_fwd over [0, L1 + L2). R must
+ * be 1, 2 or 4 (else M3_ERR_UNSUPPORTED). L = 0 leaves the state unchanged.
+ * The state must not alias any other argument. Scratch as for m3_scan_fwd.
+ */
+m3_status m3_scan_fwd_state(const void* x, const float* dt, const float* A, const float* lambda,
+                            const void* B, const void* C, const float* theta,
+                            const void* B_prev, const void* x_prev, const m3_dims* dims, int R,
+                            int chunk, void* out, float* state, void* stream);
+
+/*
  * Decode: one token of the recurrence for every (b, h), state updated in place.
  *
  *   state   [b, H, N, P]  fp32, h_{t-1} on entry, h_t on return (explicit frame)

@@ -96,9 +96,18 @@ size_t m3_scan_workspace_bytes(const m3_dims* dims, int R, int chunk) {
   return m3::scan_tc_workspace_bytes(a);
 }
 
-m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const float* lambda,
-                      const void* B, const void* C, const float* theta, const m3_dims* dims,
-                      int R, int chunk, void* out, float* final_state, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Prefill from a given entering state (continuation) or from zero. With
+// `state` (the m3_scan_fwd_state form) final_state is `state` itself: it is
+// read as the entering state, has the pending beta term of B_prev / x_prev
+// added first, and receives the state after the block.
+m3_status scan_impl(const void* x, const float* dt, const float* A, const float* lambda,
+                    const void* B, const void* C, const float* theta, const m3_dims* dims, int R,
+                    int chunk, void* out, float* final_state, bool continue_state,
+                    const void* B_prev, const void* x_prev, void* stream) {
   m3_status st = check_dims(dims, R);
   if (st != M3_OK) return st;
   if (chunk < 1 || dims->seqlen < 0) return M3_ERR_INVALID_ARG;
@@ -117,6 +126,15 @@ m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const floa
   if (final_state && !aligned(final_state, 4)) return M3_ERR_INVALID_ARG;
   if ((dims->B_bias && !aligned(dims->B_bias, 4)) || (dims->C_bias && !aligned(dims->C_bias, 4)))
     return M3_ERR_INVALID_ARG;
+  if (continue_state) {
+    int64_t n_bp, n_xp;
+    if (!count({b, G, N, R}, &n_bp) || !count({b, H, P, R}, &n_xp)) return M3_ERR_INVALID_ARG;
+    if (!ptr_ok(final_state, n_st, 4)) return M3_ERR_INVALID_ARG;
+    if ((B_prev == nullptr) != (x_prev == nullptr)) return M3_ERR_INVALID_ARG;
+    if (B_prev && (!ptr_ok(B_prev, n_bp, act) || !ptr_ok(x_prev, n_xp, act)))
+      return M3_ERR_INVALID_ARG;
+    if (!(R == 1 || R == 2 || R == 4)) return M3_ERR_UNSUPPORTED;
+  }
   if ((int64_t)chunk * R > 4096 || chunk > 4096) return M3_ERR_UNSUPPORTED;
 
   const bool bf16 = dims->act_dtype == M3_BF16;
@@ -136,13 +154,20 @@ m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const floa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (n_st == 0) return M3_OK;
   if (L == 0) {
+    if (continue_state) return M3_OK;  // no token: the state stays as it is
     if (final_state)
       return from_cuda(cudaMemsetAsync(final_state, 0, sizeof(float) * (size_t)n_st, s));
     return M3_OK;
   }
+  if (continue_state && B_prev) {
+    st = from_cuda(m3::launch_entry_state(final_state, B_prev, x_prev, dt, lambda, dims->B_bias,
+                                          b, L, H, G, P, N, R, bf16, s));
+    if (st != M3_OK) return st;
+  }
   m3::ScanArgs a;
   a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B = B; a.C = C; a.theta = theta;
   a.B_bias = dims->B_bias; a.C_bias = dims->C_bias; a.out = out; a.final_state = final_state;
+  a.h_init = continue_state ? final_state : nullptr;
   a.workspace = dims->workspace; a.workspace_bytes = dims->workspace_bytes;
   a.batch = b; a.L = L; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R; a.Q = chunk;
   if (use_tc) {
@@ -158,6 +183,25 @@ m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const floa
     return from_cuda(m3::launch_scan_tc(a, status, s));
   }
   return from_cuda(m3::launch_scan_simt(a, bf16, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+m3_status m3_scan_fwd(const void* x, const float* dt, const float* A, const float* lambda,
+                      const void* B, const void* C, const float* theta, const m3_dims* dims,
+                      int R, int chunk, void* out, float* final_state, void* stream) {
+  return scan_impl(x, dt, A, lambda, B, C, theta, dims, R, chunk, out, final_state, false,
+                   nullptr, nullptr, stream);
+}
+
+m3_status m3_scan_fwd_state(const void* x, const float* dt, const float* A, const float* lambda,
+                            const void* B, const void* C, const float* theta,
+                            const void* B_prev, const void* x_prev, const m3_dims* dims, int R,
+                            int chunk, void* out, float* state, void* stream) {
+  return scan_impl(x, dt, A, lambda, B, C, theta, dims, R, chunk, out, state, true, B_prev,
+                   x_prev, stream);
 }
 
 m3_status m3_decode_step(float* state, const void* x, const float* dt, const float* A,

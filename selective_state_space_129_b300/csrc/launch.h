@@ -19,6 +19,9 @@ struct ScanArgs {
   const float* C_bias;
   void* out;
   float* final_state;
+  // state entering the first token ([b,H,N,P] fp32, explicit frame, its
+  // pending beta term included), or NULL for zero; may alias final_state
+  const float* h_init;
   void* workspace;          // device scratch, or NULL (allocated stream-ordered when needed)
   size_t workspace_bytes;
   int64_t batch, L, H, G, P, N;
@@ -74,6 +77,14 @@ bool scan_tc_supported(int64_t N, int64_t P, int R, int Q);
 // Scratch the tensor-core prefill needs (segmented long sequences), 0 if none.
 size_t scan_tc_workspace_bytes(const ScanArgs& a);
 cudaError_t launch_scan_tc(const ScanArgs& a, unsigned int* status, cudaStream_t s);
+
+// Prefill continuation: state[b,h] += beta_hat_0 (B_prev + bias) x_prev^T, the
+// pending term of the block's first token (beta_hat_0 = (1 - lam_0) dt_0), in
+// place, so that the state becomes the explicit-frame entering state.
+cudaError_t launch_entry_state(float* state, const void* B_prev, const void* x_prev,
+                               const float* dt, const float* lam, const float* B_bias,
+                               int64_t batch, int64_t L, int64_t H, int64_t G, int64_t P,
+                               int64_t N, int R, bool bf16, cudaStream_t s);
 
 // Decode step.
 bool decode_supported(int64_t N, int64_t P, int R);

@@ -14,8 +14,9 @@
 //   y_t = sum_s S M x_s + exp(Lam_t) Ct_t^T H_in
 //   H_out = Rot(Phi_end)(exp(Lam_end) H_in + sum_s exp(Lam_end-Lam_s) w_s Bt_s x_s^T)
 //   w_s = gamma_s + beta_hat_{s+1}   (beta_hat of the token after s; 0 at the end)
-// H_in of the first chunk is zero. This is the path for the fp32 precision
-// mode and for bf16 shapes that the tensor-core kernel does not take.
+// H_in of the first chunk is zero, or the caller's entering state. This is
+// the path for the fp32 precision mode and for bf16 shapes that the
+// tensor-core kernel does not take.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -81,7 +82,13 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(ScanArgs a) {
   T* out = static_cast<T*>(a.out);
   const float A_h = a.A[h];
 
-  for (int i = tid; i < N * ldp; i += kThreads) Hs[i] = 0.f;
+  // the entering state (explicit frame, pending beta term included), or zero
+  if (a.h_init) {
+    const float* hi = a.h_init + bh * (int64_t)N * P;
+    for (int i = tid; i < N * P; i += kThreads) Hs[(i / P) * ldp + i % P] = hi[i];
+  } else {
+    for (int i = tid; i < N * ldp; i += kThreads) Hs[i] = 0.f;
+  }
 
   for (int64_t t0 = 0; t0 < L; t0 += Q) {
     const int q = (int)((L - t0 < Q) ? (L - t0) : Q);

@@ -1370,15 +1370,20 @@ int num_sms() {
 // the fast sincos is accurate.
 constexpr int kSegBatch = 8;
 __global__ void __launch_bounds__(256)
-    seg_combine_kernel(float* __restrict__ ws, const float* __restrict__ scal, int64_t nseq,
-                       int nseg, int N, int P) {
+    seg_combine_kernel(float* __restrict__ ws, const float* __restrict__ scal,
+                       const float* __restrict__ h_init, int64_t nseq, int nseg, int N, int P) {
   const int KP = N / 2;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= nseq * KP * P) return;
   const int64_t seq = i / ((int64_t)KP * P);
   const int k = (int)((i / P) % KP), pcol = (int)(i % P);
   const int64_t o0 = (int64_t)(2 * k) * P + pcol, o1 = o0 + P;
+  // the state entering segment 0: the caller's entering state, or zero
   float h0 = 0.f, h1 = 0.f;
+  if (h_init) {
+    h0 = h_init[seq * (int64_t)N * P + o0];
+    h1 = h_init[seq * (int64_t)N * P + o1];
+  }
   for (int j0 = 0; j0 < nseg; j0 += kSegBatch) {
     float g0[kSegBatch], g1[kSegBatch], lg[kSegBatch], ang[kSegBatch];
 #pragma unroll
@@ -1468,7 +1473,8 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   p.final_state = a.final_state; p.status = status;
   p.L = a.L; p.H = a.H; p.G = a.G; p.batch = a.batch;
   p.nchunks = (int)((a.L + a.Q - 1) / a.Q);
-  p.ws_state = nullptr; p.ws_scal = nullptr; p.ws_hin = nullptr;
+  p.ws_state = nullptr; p.ws_scal = nullptr;
+  p.ws_hin = a.h_init;  // unsegmented: unit u is sequence u
   const SegPlan pl = plan_segments(a, device_sms());
   p.nseg = pl.nseg;
   p.seg_chunks = pl.seg_chunks;
@@ -1495,11 +1501,12 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   p.ws_state = ws;
   p.ws_scal = ws + units * a.N * a.P;
   p.final_state = nullptr;
+  p.ws_hin = nullptr;  // the state-only pass starts every segment from zero
   cudaError_t e = launch_pass<R, NS, true>(maps, p, units, s);
   if (e == cudaSuccess) {
     const int64_t n = nseq * (a.N / 2) * a.P;
-    seg_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, p.ws_scal, nseq, pl.nseg,
-                                                                   (int)a.N, (int)a.P);
+    seg_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, p.ws_scal, a.h_init, nseq,
+                                                                   pl.nseg, (int)a.N, (int)a.P);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {

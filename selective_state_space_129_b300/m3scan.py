@@ -18,7 +18,8 @@ M3_F32, M3_BF16 = 0, 1
 
 # Exported entry points (kept in step with include/m3scan.h).
 EXPORTS = ("m3_scan_fwd", "m3_scan_fwd_noalloc", "m3_decode_step", "m3_scan_workspace_bytes",
-           "m3_status_string", "m3_device_status", "m3_version", "m3_decode_tokens")
+           "m3_status_string", "m3_device_status", "m3_version", "m3_decode_tokens",
+           "m3_scan_fwd_state")
 
 
 class M3Error(RuntimeError):
@@ -66,6 +67,8 @@ def load(path: str = LIB_PATH):
     lib.m3_decode_step.restype = i32
     lib.m3_decode_tokens.argtypes = [vp] * 10 + [dims_p, i32, vp, vp]
     lib.m3_decode_tokens.restype = i32
+    lib.m3_scan_fwd_state.argtypes = [vp] * 9 + [dims_p, i32, i32, vp, vp, vp]
+    lib.m3_scan_fwd_state.restype = i32
     lib.m3_scan_workspace_bytes.argtypes = [dims_p, i32, i32]
     lib.m3_scan_workspace_bytes.restype = ctypes.c_size_t
     lib.m3_status_string.argtypes = [i32]
@@ -187,6 +190,30 @@ def m3_scan_fwd(x, dt, A, lam, B, C, theta, R, chunk, out=None, final_state=None
                          _stream_handle(stream))
     _check(st, "m3_scan_fwd")
     return out, final_state
+
+
+def m3_scan_fwd_state(x, dt, A, lam, B, C, theta, R, chunk, state, B_prev=None, x_prev=None,
+                      out=None, B_bias=None, C_bias=None, workspace=None, stream=None):
+    """Prefill that continues a sequence from ``state`` [b,H,N,P] fp32, which is
+    updated in place to the state after the block; B_prev [b,G,N,R] / x_prev
+    [b,H,P,R] are the token before the block (or None). Returns out."""
+    import torch
+    lib = load()
+    if state is None:
+        raise ValueError("state is required")
+    b, L, H, P, G, N = _check_prefill(x, dt, A, lam, B, C, theta, R, out, state, B_bias, C_bias)
+    _expect(B_prev, "B_prev", (b, G, N, R), x.dtype, optional=True)
+    _expect(x_prev, "x_prev", (b, H, P, R), x.dtype, optional=True)
+    if workspace is not None and not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias, workspace)
+    st = lib.m3_scan_fwd_state(_ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B), _ptr(C),
+                               _ptr(theta), _ptr(B_prev), _ptr(x_prev), ctypes.byref(dims),
+                               int(R), int(chunk), _ptr(out), _ptr(state), _stream_handle(stream))
+    _check(st, "m3_scan_fwd_state")
+    return out
 
 
 def m3_scan_fwd_noalloc(x, dt, A, lam, B, C, theta, R, chunk, out, final_state, B_bias=None,

@@ -162,6 +162,35 @@ def test_tokens_empty_block_is_a_no_op(lib):
     assert _tokens(lib, _dims(seqlen=0)) == m3scan.M3_OK
 
 
+def _scan_state(lib, dims, R=1, chunk=4, **ptrs):
+    p = dict(x=FAKE, dt=FAKE, A=FAKE, lam=FAKE, B=FAKE, C=FAKE, theta=FAKE, Bp=0, xp=0,
+             out=FAKE, state=FAKE)
+    p.update(ptrs)
+    v = lambda k: ctypes.c_void_p(p[k]) if p[k] else None
+    return lib.m3_scan_fwd_state(v("x"), v("dt"), v("A"), v("lam"), v("B"), v("C"), v("theta"),
+                                 v("Bp"), v("xp"), ctypes.byref(dims), R, chunk, v("out"),
+                                 v("state"), None)
+
+
+@pytest.mark.parametrize("kw,R,ptrs,expect", [
+    (dict(), 1, dict(state=0), m3scan.M3_ERR_INVALID_ARG),        # the state is required
+    (dict(), 1, dict(Bp=FAKE), m3scan.M3_ERR_INVALID_ARG),        # B_prev without x_prev
+    (dict(), 1, dict(xp=FAKE), m3scan.M3_ERR_INVALID_ARG),
+    (dict(), 1, dict(x=0), m3scan.M3_ERR_INVALID_ARG),
+    (dict(), 3, {}, m3scan.M3_ERR_UNSUPPORTED),                    # R outside {1, 2, 4}
+    (dict(dstate=7), 1, {}, m3scan.M3_ERR_INVALID_ARG),
+])
+def test_scan_state_rejects(lib, kw, R, ptrs, expect):
+    assert _scan_state(lib, _dims(**kw), R=R, **ptrs) == expect
+
+
+def test_scan_state_empty_block_still_checks_the_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("checked without a device")
+    assert _scan_state(lib, _dims(seqlen=0)) == m3scan.M3_ERR_CUDA
+
+
 def test_workspace_query(lib):
     d = _dims()
     assert m3scan.m3_scan_workspace_bytes(d, 1, 4) == 0
@@ -176,6 +205,7 @@ def test_valid_call_without_a_device_reports_cuda_error(lib):
     assert _scan(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert _decode(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert _tokens(lib, _dims()) == m3scan.M3_ERR_CUDA
+    assert _scan_state(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert lib.m3_device_status(None) == m3scan.M3_ERR_CUDA
 
 

@@ -342,6 +342,83 @@ def test_decode_full_batch_mimo(orc):
     assert m3.m3_device_status() == m3.M3_OK
 
 
+# ---------------------------------------------------------------- prefill continuation
+def _continue_case(shape, seed, prev, bias=True):
+    inp = m3synth.scan_inputs(shape, seed=seed)
+    if not bias:
+        inp["B_bias"] = inp["C_bias"] = None
+    b, H, N, P = shape.batch, shape.heads, shape.dstate, shape.headdim
+    st0 = (0.5 * np.random.default_rng(seed).standard_normal((b, H, N, P))).astype(np.float32)
+    pv = m3synth.decode_inputs(shape, seed=seed + 1, step=0) if prev else None
+    return inp, st0, pv
+
+
+@pytest.mark.parametrize("case", [
+    # (b, L, H, G, P, N, R, chunk, bf16): tensor-core path, unsegmented (3 chunks)
+    (2, 150, 4, 2, 64, 128, 1, 64, True),
+    (2, 150, 4, 1, 64, 128, 4, 16, True),
+    # tensor-core path, segmented (few sequences, 16 chunks: four segments each)
+    (1, 1024, 2, 1, 64, 128, 1, 64, True),
+    (1, 300, 2, 1, 64, 64, 4, 16, True),
+    # CUDA-core path (fp32 mode; a bf16 shape the tensor cores do not take)
+    (2, 45, 4, 2, 32, 16, 2, 8, False),
+    (1, 37, 2, 1, 16, 24, 1, 16, True),
+], ids=lambda c: "b%d_L%d_H%d_P%d_N%d_R%d_Q%d_%s" % (c[0], c[1], c[2], c[4], c[5], c[6], c[7],
+                                                     "bf16" if c[8] else "f32"))
+@pytest.mark.parametrize("prev", [False, True], ids=["no_prev", "prev"])
+def test_prefill_continues_from_a_state(orc, case, prev):
+    b, L, H, G, P, N, R, Q, bf16 = case
+    shape = m3synth.ScanShape(b, L, H, G, P, N, R=R, chunk=Q, bf16=bf16)
+    inp, st0, pv = _continue_case(shape, 120 + R + (L % 7), prev)
+    d = to_device(inp, bf16)
+    kw = {}
+    if pv is not None:
+        dp = to_device(pv, bf16)
+        kw = dict(B_prev=dp["B"], x_prev=dp["x"])
+    st = torch.from_numpy(st0).cuda()
+    out = m3.m3_scan_fwd_state(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"], R=R,
+                               chunk=Q, state=st, B_bias=d["B_bias"], C_bias=d["C_bias"], **kw)
+    torch.cuda.synchronize()
+    assert m3.m3_device_status() == m3.M3_OK
+    okw = dict(B_prev=pv["B"], x_prev=pv["x"]) if pv is not None else {}
+    y_ref, st_ref = orc.decode_tokens(st0, inp["x"], inp["dt"], inp["A"], inp["lam"], inp["B"],
+                                      inp["C"], inp["theta"], B_bias=inp["B_bias"],
+                                      C_bias=inp["C_bias"], **okw)
+    y = out.float().cpu().numpy()
+    if bf16:
+        assert_bf16_out(y, y_ref, "y")
+        assert_bf16(st.cpu().numpy(), st_ref, "state")
+    else:
+        assert_f32(y, y_ref, "y")
+        assert_f32(st.cpu().numpy(), st_ref, "state")
+
+
+@pytest.mark.parametrize("R,Q", [(1, 64), (4, 16)])
+def test_chained_prefill_equals_one_prefill(orc, R, Q):
+    """m3_scan_fwd over the first 700 tokens, then m3_scan_fwd_state over the
+    remaining 324 with the first call's final state and last token, against
+    one sequential scan of all 1024 tokens."""
+    shape = m3synth.ScanShape(2, 1024, 4, 1, 64, 128, R=R, chunk=Q, bf16=True)
+    inp = m3synth.scan_inputs(shape, seed=140 + R)
+    d = to_device(inp, True)
+    L1 = 700
+    part = lambda t, lo, hi: t[:, lo:hi].contiguous()
+    seq = ("x", "dt", "lam", "B", "C", "theta")
+    a = {k: (part(v, 0, L1) if k in seq else v) for k, v in d.items()}
+    c = {k: (part(v, L1, 1024) if k in seq else v) for k, v in d.items()}
+    _, st = m3.m3_scan_fwd(a["x"], a["dt"], a["A"], a["lam"], a["B"], a["C"], a["theta"], R=R,
+                           chunk=Q, B_bias=a["B_bias"], C_bias=a["C_bias"])
+    y2 = m3.m3_scan_fwd_state(c["x"], c["dt"], c["A"], c["lam"], c["B"], c["C"], c["theta"], R=R,
+                              chunk=Q, state=st, B_prev=d["B"][:, L1 - 1].contiguous(),
+                              x_prev=d["x"][:, L1 - 1].contiguous(), B_bias=c["B_bias"],
+                              C_bias=c["C_bias"])
+    torch.cuda.synchronize()
+    y_ref, st_ref = orc.scan_seq(inp["x"], inp["dt"], inp["A"], inp["lam"], inp["B"], inp["C"],
+                                 inp["theta"], inp["B_bias"], inp["C_bias"])
+    assert_bf16_out(y2.float().cpu().numpy(), y_ref[:, L1:], "y of the second call")
+    assert_bf16(st.cpu().numpy(), st_ref, "final state")
+
+
 # ---------------------------------------------------------------- multi-token decode
 def _tokens_case(shape, seed, prev, bias=True):
     """Inputs of a K-token block (K = shape.seqlen), a random entry state and,

@@ -18,6 +18,7 @@ Printed on rank 0: one JSON line. Besides the contract keys it carries
   decode_tokens    multi-token decode (8 tokens per call, state read and written
                    once per call), same batch, R = 1 and 4
   prefill_mimo     the R = 4 prefill workload (chunk 16)
+  prefill_chunked  the headline workload as two calls of 1024 tokens (continuation)
   e2e              through the C ABI from pinned host buffers, copies included
   cpu_baseline     the fp64 CPU oracle on a bounded sample of the workload
 """
@@ -392,6 +393,7 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
         return
     line["prefill_mimo"] = bench_prefill_other(torch, m3, dev, "prefill_mimo", args, peaks)
+    line["prefill_chunked"] = bench_prefill_chunked(torch, m3, dev, args)
     line["prefill_long"] = bench_prefill_long(torch, m3, dev, args, peaks)
     line["decode"] = {"siso": bench_decode(torch, m3, dev, "decode_siso", peaks),
                       "mimo_r4": bench_decode(torch, m3, dev, "decode_mimo", peaks)}
@@ -444,6 +446,55 @@ def bench_prefill_other(torch, m3, dev, name, args, peaks):
             "tok_s": shape.tokens / (ms * 1e-3), "ms": ms,
             "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
             "tensor_frac": nflops / (ms * 1e-3) / 1e12 / peaks["bf16"]}
+
+
+def bench_prefill_chunked(torch, m3, dev, args, pieces=2):
+    """The headline prefill workload run as ``pieces`` consecutive calls (the
+    first m3_scan_fwd, the others m3_scan_fwd_state continuing from the state
+    and last token of the call before), timed like the single call."""
+    idx, shape = m3synth.WORKLOADS["prefill_siso"]
+    inp = m3synth.scan_inputs(shape, seed=idx)
+    d = to_device(inp, True, dev)
+    Lp = shape.seqlen // pieces
+    seq = ("x", "dt", "lam", "B", "C", "theta")
+    parts = [{k: (v[:, i * Lp:(i + 1) * Lp].contiguous() if k in seq else v) for k, v in d.items()}
+             for i in range(pieces)]
+    prevs = [None] + [{"B": parts[i]["B"][:, -1].contiguous(), "x": parts[i]["x"][:, -1].contiguous()}
+                      for i in range(pieces - 1)]
+    outs = [torch.empty_like(p["x"]) for p in parts]
+    st = torch.empty((shape.batch, shape.heads, shape.dstate, shape.headdim),
+                     dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def launch():
+        for i, (p, pv) in enumerate(zip(parts, prevs)):
+            if i == 0:
+                m3.m3_scan_fwd(p["x"], p["dt"], p["A"], p["lam"], p["B"], p["C"], p["theta"],
+                               R=shape.R, chunk=shape.chunk, out=outs[i], final_state=st,
+                               B_bias=p["B_bias"], C_bias=p["C_bias"], stream=stream)
+            else:
+                m3.m3_scan_fwd_state(p["x"], p["dt"], p["A"], p["lam"], p["B"], p["C"],
+                                     p["theta"], R=shape.R, chunk=shape.chunk, state=st,
+                                     B_prev=pv["B"], x_prev=pv["x"], out=outs[i],
+                                     B_bias=p["B_bias"], C_bias=p["C_bias"], stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = sum(times) / len(times)
+    return {"workload": "prefill_siso b%d L%d as %d calls of %d tokens (m3_scan_fwd, then "
+                        "m3_scan_fwd_state)" % (shape.batch, shape.seqlen, pieces, Lp),
+            "tok_s": shape.tokens / (ms * 1e-3), "ms": ms, "gpu_launches": pieces + pieces - 1}
 
 
 def device_inputs(torch, shape, dev, seed):

@@ -72,7 +72,7 @@ m3_status from_cuda(cudaError_t e) {
 
 extern "C" {
 
-int m3_version(void) { return 100; }
+int m3_version(void) { return 200; }  // 0.2.0: m3_decode_tokens, m3_scan_fwd_state
 
 const char* m3_status_string(m3_status s) {
   switch (s) {

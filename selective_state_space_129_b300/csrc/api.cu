@@ -2,6 +2,7 @@
 // The declarations, layouts and error behaviour are documented in m3scan.h.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "launch.h"
@@ -66,6 +67,41 @@ m3_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return M3_OK;
   cudaGetLastError();
   return M3_ERR_CUDA;
+}
+
+// Fault injection, for tests of the error paths, from the environment
+// variable M3_FAULT (read at every call; unset or any other value: none):
+//   arg      every valid compute call returns M3_ERR_INVALID_ARG before any
+//            device work;
+//   launch   the call returns M3_ERR_CUDA in place of its launches;
+//   alloc    the library's own scratch allocation (a segmented prefill
+//            without a caller workspace) fails: M3_ERR_CUDA before any launch;
+//   timeout  the work is replaced by a kernel whose bounded device wait runs
+//            out (1 ms), so that m3_device_status reports M3_ERR_TIMEOUT.
+// In every mode the call's outputs (and a decode's state) are left untouched.
+enum class Fault { kNone, kArg, kLaunch, kAlloc, kTimeout };
+
+Fault fault_mode() {
+  const char* v = getenv("M3_FAULT");
+  if (v == nullptr) return Fault::kNone;
+  if (strcmp(v, "arg") == 0) return Fault::kArg;
+  if (strcmp(v, "launch") == 0) return Fault::kLaunch;
+  if (strcmp(v, "alloc") == 0) return Fault::kAlloc;
+  if (strcmp(v, "timeout") == 0) return Fault::kTimeout;
+  return Fault::kNone;
+}
+
+constexpr uint64_t kInjectedWaitNs = 1000000ull;  // 1 ms
+
+// The launch-time faults: M3_OK to go on with the real work, else the status
+// to return (the timeout fault has launched its expiring wait by then).
+m3_status injected_launch_fault(Fault f, cudaStream_t s) {
+  if (f == Fault::kLaunch) return M3_ERR_CUDA;
+  if (f == Fault::kTimeout) {
+    const m3_status st = from_cuda(m3::launch_expired_wait(kInjectedWaitNs, s));
+    return st == M3_OK ? M3_ERR_TIMEOUT : st;
+  }
+  return M3_OK;
 }
 
 }  // namespace
@@ -148,16 +184,28 @@ m3_status scan_impl(const void* x, const float* dt, const float* A, const float*
     if (smem > 227 * 1024) return M3_ERR_UNSUPPORTED;
   }
   if (b * H > 0x7fffffff) return M3_ERR_UNSUPPORTED;
+  const Fault fault = fault_mode();
+  if (fault == Fault::kArg) return M3_ERR_INVALID_ARG;
 
   st = check_device();
   if (st != M3_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (n_st == 0) return M3_OK;
+  {
+    const m3_status f = injected_launch_fault(fault, s);
+    if (f == M3_ERR_TIMEOUT) return M3_OK;  // reported by m3_device_status
+    if (f != M3_OK) return f;
+  }
   if (L == 0) {
     if (continue_state) return M3_OK;  // no token: the state stays as it is
     if (final_state)
       return from_cuda(cudaMemsetAsync(final_state, 0, sizeof(float) * (size_t)n_st, s));
     return M3_OK;
+  }
+  if (fault == Fault::kAlloc && use_tc && dims->workspace == nullptr) {
+    m3::ScanArgs q = {};
+    q.batch = b; q.L = L; q.H = H; q.G = G; q.P = P; q.N = N; q.R = R; q.Q = chunk;
+    if (m3::scan_tc_workspace_bytes(q) > 0) return M3_ERR_CUDA;  // the allocation "failed"
   }
   if (continue_state && B_prev) {
     st = from_cuda(m3::launch_entry_state(final_state, B_prev, x_prev, dt, lambda, dims->B_bias,
@@ -228,10 +276,17 @@ m3_status m3_decode_step(float* state, const void* x, const float* dt, const flo
     return M3_ERR_INVALID_ARG;
   if (!m3::decode_supported(N, P, R)) return M3_ERR_UNSUPPORTED;
   if (b * H > 0x7fffffff) return M3_ERR_UNSUPPORTED;
+  const Fault fault = fault_mode();
+  if (fault == Fault::kArg) return M3_ERR_INVALID_ARG;
 
   st = check_device();
   if (st != M3_OK) return st;
   if (n_st == 0) return M3_OK;
+  {
+    const m3_status f = injected_launch_fault(fault, static_cast<cudaStream_t>(stream));
+    if (f == M3_ERR_TIMEOUT) return M3_OK;
+    if (f != M3_OK) return f;
+  }
   m3::DecodeArgs a;
   a.state = state; a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B_prev = B_prev;
   a.x_prev = x_prev; a.B = B; a.C = C; a.theta = theta; a.B_bias = dims->B_bias;
@@ -279,9 +334,16 @@ m3_status m3_decode_tokens(float* state, const void* x, const float* dt, const f
   if (K == 0 || n_st == 0) return M3_OK;  // nothing to compute
   if (!m3::tokens_supported(a, (int)act)) return M3_ERR_UNSUPPORTED;
   if (b * H > 0x7fffffff) return M3_ERR_UNSUPPORTED;
+  const Fault fault = fault_mode();
+  if (fault == Fault::kArg) return M3_ERR_INVALID_ARG;
 
   st = check_device();
   if (st != M3_OK) return st;
+  {
+    const m3_status f = injected_launch_fault(fault, static_cast<cudaStream_t>(stream));
+    if (f == M3_ERR_TIMEOUT) return M3_OK;
+    if (f != M3_OK) return f;
+  }
   return from_cuda(m3::launch_decode_tokens(a, dims->act_dtype == M3_BF16,
                                             static_cast<cudaStream_t>(stream)));
 }

@@ -94,6 +94,10 @@ cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s);
 bool tokens_supported(const TokensArgs& a, int act);
 cudaError_t launch_decode_tokens(const TokensArgs& a, bool bf16, cudaStream_t s);
 
+// Fault injection (M3_FAULT=timeout): a kernel whose bounded wait runs out
+// after limit_ns, recording the expiry in the status word.
+cudaError_t launch_expired_wait(uint64_t limit_ns, cudaStream_t s);
+
 // Device address of this device's status word of expired waits.
 cudaError_t status_word(unsigned int** ptr);
 cudaError_t read_clear_status(unsigned int* value, cudaStream_t s);

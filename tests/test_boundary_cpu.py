@@ -191,6 +191,22 @@ def test_scan_state_empty_block_still_checks_the_device(lib):
     assert _scan_state(lib, _dims(seqlen=0)) == m3scan.M3_ERR_CUDA
 
 
+def test_fault_injection_arg_rejects_valid_calls(lib, monkeypatch):
+    """M3_FAULT=arg: a valid call is refused on the host, before any device work."""
+    monkeypatch.setenv("M3_FAULT", "arg")
+    assert _scan(lib, _dims()) == m3scan.M3_ERR_INVALID_ARG
+    assert _decode(lib, _dims()) == m3scan.M3_ERR_INVALID_ARG
+    assert _tokens(lib, _dims()) == m3scan.M3_ERR_INVALID_ARG
+    assert _scan_state(lib, _dims()) == m3scan.M3_ERR_INVALID_ARG
+    # invalid calls still report their own status first
+    assert _scan(lib, _dims(dstate=7)) == m3scan.M3_ERR_INVALID_ARG
+    assert _decode(lib, _dims(), R=3) == m3scan.M3_ERR_UNSUPPORTED
+    monkeypatch.setenv("M3_FAULT", "no-such-mode")  # unknown values inject nothing
+    import torch
+    if not torch.cuda.is_available():
+        assert _scan(lib, _dims()) == m3scan.M3_ERR_CUDA
+
+
 def test_workspace_query(lib):
     d = _dims()
     assert m3scan.m3_scan_workspace_bytes(d, 1, 4) == 0

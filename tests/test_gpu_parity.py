@@ -342,6 +342,86 @@ def test_decode_full_batch_mimo(orc):
     assert m3.m3_device_status() == m3.M3_OK
 
 
+# ---------------------------------------------------------------- fault injection
+# M3_FAULT (host side, read at every call) forces the error paths; the
+# "timeout" mode runs a kernel whose bounded mbarrier wait runs out after 1 ms,
+# so the device-status path is exercised without any fault or hang.
+def _small_decode(bf16=True):
+    shape = m3synth.ScanShape(2, 1, 4, 1, 64, 128, R=1, chunk=1, bf16=bf16)
+    s0 = m3synth.decode_inputs(shape, seed=150, step=0)
+    st0 = (0.5 * np.random.default_rng(150).standard_normal((2, 4, 128, 64))).astype(np.float32)
+    return shape, s0, st0
+
+
+def _decode_call(d, st, out):
+    return m3.m3_decode_step(st, d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"],
+                             R=1, out=out, B_bias=d["B_bias"], C_bias=d["C_bias"])
+
+
+@pytest.mark.parametrize("mode", ["launch", "arg"])
+def test_fault_injection_leaves_outputs_untouched(monkeypatch, mode):
+    shape, s0, st0 = _small_decode()
+    d = to_device(s0, True)
+    st = torch.from_numpy(st0).cuda()
+    out = torch.full_like(d["x"], 7.0)
+    monkeypatch.setenv("M3_FAULT", mode)
+    with pytest.raises(m3.M3Error) as err:
+        _decode_call(d, st, out)
+    assert err.value.status == (m3.M3_ERR_CUDA if mode == "launch" else m3.M3_ERR_INVALID_ARG)
+    torch.cuda.synchronize()
+    assert torch.equal(st.cpu(), torch.from_numpy(st0))
+    assert bool((out.float() == 7.0).all())
+    monkeypatch.delenv("M3_FAULT")
+    _decode_call(d, st, out)  # the next call runs normally
+    torch.cuda.synchronize()
+    assert not torch.equal(st.cpu(), torch.from_numpy(st0))
+
+
+def test_injected_wait_expiry_is_reported_and_the_context_stays_usable(orc, monkeypatch):
+    shape, s0, st0 = _small_decode()
+    d = to_device(s0, True)
+    st = torch.from_numpy(st0).cuda()
+    out = torch.full_like(d["x"], 7.0)
+    assert m3.m3_device_status() == m3.M3_OK
+    monkeypatch.setenv("M3_FAULT", "timeout")
+    _decode_call(d, st, out)  # enqueued: the expiry is seen through the status
+    assert m3.m3_device_status() == m3.M3_ERR_TIMEOUT
+    assert m3.m3_device_status() == m3.M3_OK  # read and cleared
+    assert torch.equal(st.cpu(), torch.from_numpy(st0))
+    assert bool((out.float() == 7.0).all())
+    monkeypatch.delenv("M3_FAULT")
+    y = _decode_call(d, st, out)
+    y_ref, st_ref = orc.decode_step(st0, s0["x"], s0["dt"], s0["A"], s0["lam"], s0["B"], s0["C"],
+                                    s0["theta"], B_bias=s0["B_bias"], C_bias=s0["C_bias"])
+    torch.cuda.synchronize()
+    assert_bf16_out(y.float().cpu().numpy(), y_ref, "y after the injected expiry")
+    assert_bf16(st.cpu().numpy(), st_ref, "state after the injected expiry")
+    assert m3.m3_device_status() == m3.M3_OK
+
+
+def test_injected_allocation_failure(monkeypatch):
+    """A segmented prefill that would allocate its scratch fails cleanly; with a
+    caller workspace there is no allocation and the call runs."""
+    shape = m3synth.ScanShape(1, 1024, 2, 1, 64, 128, R=1, chunk=64, bf16=True)
+    inp = m3synth.scan_inputs(shape, seed=151)
+    d = to_device(inp, True)
+    out = torch.full_like(d["x"], 7.0)
+    fs = torch.full((1, 2, 128, 64), 7.0, device="cuda")
+    monkeypatch.setenv("M3_FAULT", "alloc")
+    with pytest.raises(m3.M3Error) as err:
+        m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"], R=1,
+                       chunk=64, out=out, final_state=fs, B_bias=d["B_bias"], C_bias=d["C_bias"])
+    assert err.value.status == m3.M3_ERR_CUDA
+    torch.cuda.synchronize()
+    assert bool((out.float() == 7.0).all()) and bool((fs == 7.0).all())
+    dims = m3.make_dims(1, 1024, 2, 1, 64, 128, m3.M3_BF16)
+    ws = torch.empty(m3.m3_scan_workspace_bytes(dims, 1, 64), dtype=torch.uint8, device="cuda")
+    m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"], R=1, chunk=64,
+                   out=out, final_state=fs, B_bias=d["B_bias"], C_bias=d["C_bias"], workspace=ws)
+    torch.cuda.synchronize()
+    assert not bool((fs == 7.0).all())
+
+
 # ---------------------------------------------------------------- prefill continuation
 def _continue_case(shape, seed, prev, bias=True):
     inp = m3synth.scan_inputs(shape, seed=seed)

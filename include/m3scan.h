@@ -32,6 +32,13 @@
  *   - Outputs must not alias inputs (decode's `state` is updated in place).
  *   - The library runs on compute capability 10.3 (B300) only; elsewhere the
  *     compute entry points return M3_ERR_UNSUPPORTED.
+ *   - Fault injection for tests: the environment variable M3_FAULT, read at
+ *     every call, makes a valid compute call return M3_ERR_INVALID_ARG before
+ *     any device work ("arg"), return M3_ERR_CUDA in place of its launches
+ *     ("launch") or of the library's own scratch allocation ("alloc"), or run
+ *     a kernel whose bounded device wait expires after 1 ms in place of the
+ *     work ("timeout"; m3_device_status then reports M3_ERR_TIMEOUT). Outputs
+ *     and state are left untouched in every mode.
  */
 #ifndef M3SCAN_H_
 #define M3SCAN_H_

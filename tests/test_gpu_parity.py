@@ -473,6 +473,23 @@ def test_prefill_continues_from_a_state(orc, case, prev):
         assert_f32(st.cpu().numpy(), st_ref, "state")
 
 
+def test_prefill_continuation_of_no_tokens_keeps_the_state():
+    shape = m3synth.ScanShape(2, 0, 4, 1, 64, 128, R=1, chunk=64, bf16=True)
+    x = torch.zeros((2, 0, 4, 64, 1), dtype=torch.bfloat16, device="cuda")
+    dt = torch.zeros((2, 0, 4), device="cuda")
+    B = torch.zeros((2, 0, 1, 128, 1), dtype=torch.bfloat16, device="cuda")
+    th = torch.zeros((2, 0, 1, 64), device="cuda")
+    A = torch.full((4,), -1.0, device="cuda")
+    st0 = torch.randn((2, 4, 128, 64), device="cuda")
+    st = st0.clone()
+    Bp = torch.ones((2, 1, 128, 1), dtype=torch.bfloat16, device="cuda")
+    xp = torch.ones((2, 4, 64, 1), dtype=torch.bfloat16, device="cuda")
+    m3.m3_scan_fwd_state(x, dt, A, dt, B, B, th, R=1, chunk=64, state=st, B_prev=Bp, x_prev=xp)
+    torch.cuda.synchronize()
+    assert torch.equal(st, st0)
+    assert shape.tokens == 0
+
+
 @pytest.mark.parametrize("R,Q", [(1, 64), (4, 16)])
 def test_chained_prefill_equals_one_prefill(orc, R, Q):
     """m3_scan_fwd over the first 700 tokens, then m3_scan_fwd_state over the

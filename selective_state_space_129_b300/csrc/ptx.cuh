@@ -144,14 +144,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
-                                            int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
                                             int c1, int c2, int c3) {
   asm volatile(
@@ -261,14 +253,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
   d |= (uint64_t)1 << 46;  // descriptor version for sm_100
   d |= (uint64_t)2 << 61;  // 128-byte swizzle
   return d;
-}
-
-// Byte offset of element (row, col) in a tile of 128-byte rows (64 bf16 per
-// row) laid out with the 128-byte swizzle: the 16-byte chunk index is XORed
-// with the row index modulo 8.
-__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col_bf16) {
-  const uint32_t chunk = (col_bf16 >> 3) ^ (row & 7u);
-  return row * 128u + chunk * 16u + (col_bf16 & 7u) * 2u;
 }
 
 // TMEM -> registers: 32 lanes x 32 bits, 16 consecutive columns per thread.

@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kSThreads, 2)
     // the rotation to the state alone. Entry (row pair kq, rank r):
     auto fold_prep = [&](int kq, int r) {
       float sn, cs;
-      sincosf(d * sth[kq], &sn, &cs);
+      __sincosf(wrap_angle(d * sth[kq]), &sn, &cs);
       const float ac = alpha * cs, as = alpha * sn;
       const int i0 = 2 * kq * R + r, i1 = i0 + R;  // (row 2kq, r), (row 2kq + 1, r)
       const float bb0 = a.B_bias ? sbb[i0] : 0.f, bb1 = a.B_bias ? sbb[i1] : 0.f;
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kSThreads, 2)
         const int kq = (32 * warp + jj * kSThreads) / PQ + (e - jj * kpw);
         if (kq >= K2) continue;
         float sn, cs;
-        sincosf(d * sth[kq], &sn, &cs);
+        __sincosf(wrap_angle(d * sth[kq]), &sn, &cs);
         rc[kq] = alpha * cs;
         rs[kq] = alpha * sn;
       }

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kTThreads, tok_ctas_per_sm(R))
       float2* cd = ud + 2 * NR;                                           // [N][R] pairs
       float4* rd = reinterpret_cast<float4*>(cd + NR);                    // [K2][2]
       float sn, cs;
-      sincosf(d * sth[kq], &sn, &cs);
+      __sincosf(wrap_angle(d * sth[kq]), &sn, &cs);
       const float ac = alpha * cs, as = alpha * sn;
       const int i0 = 2 * kq * R + r, i1 = i0 + R;  // (row 2kq, r), (row 2kq + 1, r)
       const float bb0 = a.B_bias ? sbb[i0] : 0.f, bb1 = a.B_bias ? sbb[i1] : 0.f;

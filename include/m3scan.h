@@ -133,6 +133,28 @@ m3_status m3_scan_fwd_state(const void* x, const float* dt, const float* A, cons
                             int chunk, void* out, float* state, void* stream);
 
 /*
+ * Backward pass of a prefill that starts from a zero state: the gradients of
+ * the scalar <y, dy> + <h_final, d_final> with respect to every input
+ * (training). Same inputs and layouts as m3_scan_fwd, plus
+ *   dy        [b, L, H, P, R]  act_dtype, the gradient of the outputs
+ *   d_final   [b, H, N, P]     fp32 (16-byte aligned), the gradient of the final
+ *                              state, or NULL for zero
+ * and fp32 gradients: dx [b,L,H,P,R], ddt and dlambda [b,L,H], dA [H],
+ * dB and dC [b,L,G,N,R] (summed over the heads of a group), dtheta
+ * [b,L,G,N/2], dB_bias and dC_bias [H,N,R] (each may be NULL: not computed).
+ * R in {1, 2, 4}, P a multiple of 4 with P/4 dividing 32, N/2 * P/4 <= 1024;
+ * other shapes return M3_ERR_UNSUPPORTED. The CUDA-core kernel walks each
+ * sequence forward to store a state checkpoint every 64 tokens, then backward
+ * chunk by chunk; its scratch ((L/64 + 64) N P floats per (b, h)) is
+ * allocated and freed on `stream` by the library. dims->workspace is ignored.
+ */
+m3_status m3_scan_bwd(const void* x, const float* dt, const float* A, const float* lambda,
+                      const void* B, const void* C, const float* theta, const void* dy,
+                      const float* d_final, const m3_dims* dims, int R, float* dx, float* ddt,
+                      float* dA, float* dlambda, float* dB, float* dC, float* dtheta,
+                      float* dB_bias, float* dC_bias, void* stream);
+
+/*
  * Decode: one token of the recurrence for every (b, h), state updated in place.
  *
  *   state   [b, H, N, P]  fp32, h_{t-1} on entry, h_t on return (explicit frame)

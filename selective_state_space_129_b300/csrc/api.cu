@@ -348,6 +348,55 @@ m3_status m3_decode_tokens(float* state, const void* x, const float* dt, const f
                                             static_cast<cudaStream_t>(stream)));
 }
 
+m3_status m3_scan_bwd(const void* x, const float* dt, const float* A, const float* lambda,
+                      const void* B, const void* C, const float* theta, const void* dy,
+                      const float* d_final, const m3_dims* dims, int R, float* dx, float* ddt,
+                      float* dA, float* dlambda, float* dB, float* dC, float* dtheta,
+                      float* dB_bias, float* dC_bias, void* stream) {
+  m3_status st = check_dims(dims, R);
+  if (st != M3_OK) return st;
+  if (dims->seqlen < 0) return M3_ERR_INVALID_ARG;
+  const int64_t b = dims->batch, L = dims->seqlen, H = dims->heads, G = dims->groups,
+                P = dims->headdim, N = dims->dstate;
+  const size_t act = dims->act_dtype == M3_BF16 ? 2 : 4;
+  int64_t n_x, n_t, n_bc, n_th, n_st, n_bias;
+  if (!count({b, L, H, P, R}, &n_x) || !count({b, L, H}, &n_t) ||
+      !count({b, L, G, N, R}, &n_bc) || !count({b, L, G, N / 2}, &n_th) ||
+      !count({b, H, N, P}, &n_st) || !count({H, N, R}, &n_bias))
+    return M3_ERR_INVALID_ARG;
+  if (!ptr_ok(x, n_x, act) || !ptr_ok(dy, n_x, act) || !ptr_ok(dt, n_t, 4) ||
+      !ptr_ok(lambda, n_t, 4) || !ptr_ok(A, H, 4) || !ptr_ok(B, n_bc, act) ||
+      !ptr_ok(C, n_bc, act) || !ptr_ok(theta, n_th, 4) || !ptr_ok(dx, n_x, 4) ||
+      !ptr_ok(ddt, n_t, 4) || !ptr_ok(dlambda, n_t, 4) || !ptr_ok(dA, H, 4) ||
+      !ptr_ok(dB, n_bc, 4) || !ptr_ok(dC, n_bc, 4) || !ptr_ok(dtheta, n_th, 4))
+    return M3_ERR_INVALID_ARG;
+  if ((d_final && !aligned(d_final, 16)) || (dB_bias && !aligned(dB_bias, 4)) ||
+      (dC_bias && !aligned(dC_bias, 4)))
+    return M3_ERR_INVALID_ARG;
+  if ((dims->B_bias && !aligned(dims->B_bias, 4)) || (dims->C_bias && !aligned(dims->C_bias, 4)))
+    return M3_ERR_INVALID_ARG;
+  if (!m3::scan_bwd_supported(N, P, R)) return M3_ERR_UNSUPPORTED;
+  if (b * H > 0x7fffffff) return M3_ERR_UNSUPPORTED;
+  const Fault fault = fault_mode();
+  if (fault == Fault::kArg) return M3_ERR_INVALID_ARG;
+
+  st = check_device();
+  if (st != M3_OK) return st;
+  {
+    const m3_status f = injected_launch_fault(fault, static_cast<cudaStream_t>(stream));
+    if (f == M3_ERR_TIMEOUT) return M3_OK;
+    if (f != M3_OK) return f;
+  }
+  m3::BwdArgs a;
+  a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B = B; a.C = C; a.theta = theta;
+  a.B_bias = dims->B_bias; a.C_bias = dims->C_bias; a.dy = dy; a.d_final = d_final;
+  a.dx = dx; a.ddt = ddt; a.dA = dA; a.dlam = dlambda; a.dB = dB; a.dC = dC; a.dtheta = dtheta;
+  a.dB_bias = dB_bias; a.dC_bias = dC_bias;
+  a.batch = b; a.L = L; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R;
+  return from_cuda(m3::launch_scan_bwd(a, dims->act_dtype == M3_BF16,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 m3_status m3_device_status(void* stream) {
   unsigned int v = 0;
   if (m3::read_clear_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess) {

@@ -68,6 +68,34 @@ struct TokensArgs {
   int R;
 };
 
+// Backward pass of the prefill from a zero state: gradients of
+// <y, dy> + <h_final, d_final>. Gradients are fp32; dA, dB, dC, dtheta and the
+// bias gradients are accumulated (zeroed by the launcher), the rest written.
+struct BwdArgs {
+  const void* x;
+  const float* dt;
+  const float* A;
+  const float* lam;
+  const void* B;
+  const void* C;
+  const float* theta;
+  const float* B_bias;
+  const float* C_bias;
+  const void* dy;          // [b,L,H,P,R], act dtype
+  const float* d_final;    // [b,H,N,P] or NULL
+  float* dx;               // [b,L,H,P,R]
+  float* ddt;              // [b,L,H]
+  float* dA;               // [H]
+  float* dlam;             // [b,L,H]
+  float* dB;               // [b,L,G,N,R]
+  float* dC;               // [b,L,G,N,R]
+  float* dtheta;           // [b,L,G,N/2]
+  float* dB_bias;          // [H,N,R] or NULL
+  float* dC_bias;          // [H,N,R] or NULL
+  int64_t batch, L, H, G, P, N;
+  int R;
+};
+
 // CUDA-core chunked prefill (any shape whose tiles fit shared memory).
 size_t scan_simt_smem_bytes(int64_t N, int64_t P, int R, int Q);
 cudaError_t launch_scan_simt(const ScanArgs& a, bool bf16, cudaStream_t s);
@@ -97,6 +125,10 @@ cudaError_t launch_decode_tokens(const TokensArgs& a, bool bf16, cudaStream_t s)
 // Fault injection (M3_FAULT=timeout): a kernel whose bounded wait runs out
 // after limit_ns, recording the expiry in the status word.
 cudaError_t launch_expired_wait(uint64_t limit_ns, cudaStream_t s);
+
+// Backward pass (CUDA cores, state checkpoints in a stream-ordered scratch).
+bool scan_bwd_supported(int64_t N, int64_t P, int R);
+cudaError_t launch_scan_bwd(const BwdArgs& a, bool bf16, cudaStream_t s);
 
 // Device address of this device's status word of expired waits.
 cudaError_t status_word(unsigned int** ptr);

@@ -19,7 +19,7 @@ M3_F32, M3_BF16 = 0, 1
 # Exported entry points (kept in step with include/m3scan.h).
 EXPORTS = ("m3_scan_fwd", "m3_scan_fwd_noalloc", "m3_decode_step", "m3_scan_workspace_bytes",
            "m3_status_string", "m3_device_status", "m3_version", "m3_decode_tokens",
-           "m3_scan_fwd_state")
+           "m3_scan_fwd_state", "m3_scan_bwd")
 
 
 class M3Error(RuntimeError):
@@ -69,6 +69,8 @@ def load(path: str = LIB_PATH):
     lib.m3_decode_tokens.restype = i32
     lib.m3_scan_fwd_state.argtypes = [vp] * 9 + [dims_p, i32, i32, vp, vp, vp]
     lib.m3_scan_fwd_state.restype = i32
+    lib.m3_scan_bwd.argtypes = [vp] * 9 + [dims_p, i32] + [vp] * 10
+    lib.m3_scan_bwd.restype = i32
     lib.m3_scan_workspace_bytes.argtypes = [dims_p, i32, i32]
     lib.m3_scan_workspace_bytes.restype = ctypes.c_size_t
     lib.m3_status_string.argtypes = [i32]
@@ -214,6 +216,34 @@ def m3_scan_fwd_state(x, dt, A, lam, B, C, theta, R, chunk, state, B_prev=None, 
                                int(R), int(chunk), _ptr(out), _ptr(state), _stream_handle(stream))
     _check(st, "m3_scan_fwd_state")
     return out
+
+
+def m3_scan_bwd(x, dt, A, lam, B, C, theta, dy, R, d_final=None, B_bias=None, C_bias=None,
+                stream=None):
+    """Gradients of <y, dy> + <h_final, d_final> of a prefill from a zero state.
+    Returns a dict of fp32 tensors: x, dt, A, lam, B, C, theta and, when the
+    biases are given, B_bias, C_bias."""
+    import torch
+    lib = load()
+    b, L, H, P, G, N = _check_prefill(x, dt, A, lam, B, C, theta, R, dy, None, B_bias, C_bias)
+    _expect(d_final, "d_final", (b, H, N, P), torch.float32, optional=True)
+    f = dict(dtype=torch.float32, device=x.device)
+    g = dict(x=torch.empty(b, L, H, P, R, **f), dt=torch.empty(b, L, H, **f),
+             A=torch.empty(H, **f), lam=torch.empty(b, L, H, **f),
+             B=torch.empty(b, L, G, N, R, **f), C=torch.empty(b, L, G, N, R, **f),
+             theta=torch.empty(b, L, G, N // 2, **f))
+    if B_bias is not None:
+        g["B_bias"] = torch.empty(H, N, R, **f)
+    if C_bias is not None:
+        g["C_bias"] = torch.empty(H, N, R, **f)
+    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias)
+    st = lib.m3_scan_bwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B), _ptr(C), _ptr(theta),
+                         _ptr(dy), _ptr(d_final), ctypes.byref(dims), int(R), _ptr(g["x"]),
+                         _ptr(g["dt"]), _ptr(g["A"]), _ptr(g["lam"]), _ptr(g["B"]), _ptr(g["C"]),
+                         _ptr(g["theta"]), _ptr(g.get("B_bias")), _ptr(g.get("C_bias")),
+                         _stream_handle(stream))
+    _check(st, "m3_scan_bwd")
+    return g
 
 
 def m3_scan_fwd_noalloc(x, dt, A, lam, B, C, theta, R, chunk, out, final_state, B_bias=None,

@@ -207,6 +207,31 @@ def test_fault_injection_arg_rejects_valid_calls(lib, monkeypatch):
         assert _scan(lib, _dims()) == m3scan.M3_ERR_CUDA
 
 
+def _bwd(lib, dims, R=1, **ptrs):
+    names = ("x", "dt", "A", "lam", "B", "C", "theta", "dy", "dfin", "gx", "gdt", "gA", "glam",
+             "gB", "gC", "gth", "gbb", "gcb")
+    p = {k: FAKE for k in names}
+    p.update(dfin=0, gbb=0, gcb=0)
+    p.update(ptrs)
+    v = lambda k: ctypes.c_void_p(p[k]) if p[k] else None
+    return lib.m3_scan_bwd(v("x"), v("dt"), v("A"), v("lam"), v("B"), v("C"), v("theta"), v("dy"),
+                           v("dfin"), ctypes.byref(dims), R, v("gx"), v("gdt"), v("gA"), v("glam"),
+                           v("gB"), v("gC"), v("gth"), v("gbb"), v("gcb"), None)
+
+
+@pytest.mark.parametrize("kw,R,ptrs,expect", [
+    (dict(), 1, dict(dy=0), m3scan.M3_ERR_INVALID_ARG),
+    (dict(), 1, dict(gx=0), m3scan.M3_ERR_INVALID_ARG),
+    (dict(), 1, dict(dfin=FAKE + 4), m3scan.M3_ERR_INVALID_ARG),   # d_final not 16-byte aligned
+    (dict(), 3, {}, m3scan.M3_ERR_UNSUPPORTED),
+    (dict(headdim=6), 1, {}, m3scan.M3_ERR_UNSUPPORTED),
+    (dict(dstate=512, headdim=64), 1, {}, m3scan.M3_ERR_UNSUPPORTED),
+    (dict(dstate=7), 1, {}, m3scan.M3_ERR_INVALID_ARG),
+])
+def test_bwd_rejects(lib, kw, R, ptrs, expect):
+    assert _bwd(lib, _dims(**kw), R=R, **ptrs) == expect
+
+
 def test_workspace_query(lib):
     d = _dims()
     assert m3scan.m3_scan_workspace_bytes(d, 1, 4) == 0
@@ -222,6 +247,7 @@ def test_valid_call_without_a_device_reports_cuda_error(lib):
     assert _decode(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert _tokens(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert _scan_state(lib, _dims()) == m3scan.M3_ERR_CUDA
+    assert _bwd(lib, _dims()) == m3scan.M3_ERR_CUDA
     assert lib.m3_device_status(None) == m3scan.M3_ERR_CUDA
 
 

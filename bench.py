@@ -19,6 +19,7 @@ Printed on rank 0: one JSON line. Besides the contract keys it carries
                    once per call), same batch, R = 1 and 4
   prefill_mimo     the R = 4 prefill workload (chunk 16)
   prefill_chunked  the headline workload as two calls of 1024 tokens (continuation)
+  prefill_backward the backward pass (all gradients) of the headline workload
   e2e              through the C ABI from pinned host buffers, copies included
   cpu_baseline     the fp64 CPU oracle on a bounded sample of the workload
 """
@@ -315,6 +316,10 @@ def run_ours(args, rank, world, local_rank):
             print(json.dumps(bench_decode_tokens(torch, m3, dev, name, peaks,
                                                  calls=args.decode_steps)), flush=True)
         return
+    if args.only == "prefill_backward":
+        if rank == 0:
+            print(json.dumps(bench_backward(torch, m3, dev)), flush=True)
+        return
     if args.only == "prefill_long":
         if rank == 0:
             print(json.dumps(bench_prefill_long(torch, m3, dev, args, peaks)), flush=True)
@@ -394,6 +399,7 @@ def run_ours(args, rank, world, local_rank):
         return
     line["prefill_mimo"] = bench_prefill_other(torch, m3, dev, "prefill_mimo", args, peaks)
     line["prefill_chunked"] = bench_prefill_chunked(torch, m3, dev, args)
+    line["prefill_backward"] = bench_backward(torch, m3, dev)
     line["prefill_long"] = bench_prefill_long(torch, m3, dev, args, peaks)
     line["decode"] = {"siso": bench_decode(torch, m3, dev, "decode_siso", peaks),
                       "mimo_r4": bench_decode(torch, m3, dev, "decode_mimo", peaks)}
@@ -495,6 +501,41 @@ def bench_prefill_chunked(torch, m3, dev, args, pieces=2):
     return {"workload": "prefill_siso b%d L%d as %d calls of %d tokens (m3_scan_fwd, then "
                         "m3_scan_fwd_state)" % (shape.batch, shape.seqlen, pieces, Lp),
             "tok_s": shape.tokens / (ms * 1e-3), "ms": ms, "gpu_launches": pieces + pieces - 1}
+
+
+def bench_backward(torch, m3, dev, reps=3):
+    """m3_scan_bwd on the headline prefill workload (gradients of <y, dy> +
+    <h_final, d_final>), timed like the forward call (L2 flushed first)."""
+    idx, shape = m3synth.WORKLOADS["prefill_siso"]
+    inp = m3synth.scan_inputs(shape, seed=idx)
+    d = to_device(inp, True, dev)
+    gen = torch.Generator(device=dev).manual_seed(idx)
+    dy = torch.randn(d["x"].shape, device=dev, generator=gen).to(torch.bfloat16)
+    dfin = torch.randn((shape.batch, shape.heads, shape.dstate, shape.headdim), device=dev,
+                       generator=gen)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def launch():
+        m3.m3_scan_bwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"], dy,
+                       R=shape.R, d_final=dfin, B_bias=d["B_bias"], C_bias=d["C_bias"],
+                       stream=stream)
+
+    launch()
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = sum(times) / len(times)
+    return {"workload": "prefill_siso b%d L%d H%d P%d N%d R%d, backward (all gradients)" % (
+                shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate, shape.R),
+            "tok_s": shape.tokens / (ms * 1e-3), "ms": ms,
+            "kernel": "CUDA cores, one CTA per (b, h), state checkpoints every 64 tokens"}
 
 
 def device_inputs(torch, shape, dev, seed):
@@ -762,7 +803,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="all",
                     choices=["all", "prefill_siso", "prefill_mimo", "decode_siso", "decode_mimo",
-                             "decode_tokens_siso", "decode_tokens_mimo", "prefill_long"],
+                             "decode_tokens_siso", "decode_tokens_mimo", "prefill_long",
+                             "prefill_backward"],
                     help="run one workload alone (profiling); the default runs them all")
     ap.add_argument("--decode-steps", type=int, default=m3synth.DECODE_STEPS,
                     help="decode steps (or multi-token calls) per CUDA graph with --only decode_*")

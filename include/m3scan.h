@@ -218,9 +218,11 @@ m3_status m3_decode_tokens(float* state, const void* x, const float* dt, const f
  * 32 MiB array of this library in device memory, held on every GPU that loads
  * the library until the process exits; dims->workspace is ignored. A call
  * that needs more than 32 MiB returns M3_ERR_UNSUPPORTED without launching
- * anything (use m3_scan_fwd with a caller workspace for those). The first call
- * on a device looks up that device's address of the array (a host-side
- * runtime query, no allocation); make that first call before any stream
+ * anything (use m3_scan_fwd with a caller workspace for those). Every call
+ * looks up the current device's address of the array (a host-side runtime
+ * query, no allocation), so the address stays right if the device's context
+ * is destroyed and created again; the first call on a device also loads the
+ * library's device code there, so make that first call before any stream
  * capture. All calls share the one array, so calls that can overlap on the
  * GPU (different streams, or different host threads, on the same device)
  * race on it; serialise them. The scan writes every scratch byte it reads, so

@@ -175,9 +175,13 @@ m3_status scan_impl(const void* x, const float* dt, const float* A, const float*
 
   const bool bf16 = dims->act_dtype == M3_BF16;
   // The tensor-core path moves tiles with TMA and 128-bit accesses: it takes
-  // 16-byte-aligned activations and final state; other calls use the CUDA cores.
+  // 16-byte-aligned activations, biases and final state and 8-byte-aligned
+  // theta; other calls use the CUDA cores.
   const bool use_tc = bf16 && m3::scan_tc_supported(N, P, R, chunk) && aligned(x, 16) &&
                       aligned(out, 16) && aligned(B, 16) && aligned(C, 16) &&
+                      aligned(theta, 8) &&
+                      (dims->B_bias == nullptr || aligned(dims->B_bias, 16)) &&
+                      (dims->C_bias == nullptr || aligned(dims->C_bias, 16)) &&
                       (final_state == nullptr || aligned(final_state, 16));
   if (!use_tc) {
     const size_t smem = m3::scan_simt_smem_bytes(N, P, R, chunk);

@@ -10,12 +10,15 @@
 //
 // The array lives in device memory for as long as the library is loaded, on
 // every GPU that loads it. Its host-side name is only a stand-in for the
-// symbol, not a device address, so the device address is looked up once per
-// device (with that device current) and passed on as the workspace pointer.
+// symbol, not a device address, so every call looks up the current device's
+// address of the array (cudaGetSymbolAddress, a host-side query that
+// allocates nothing; the first call on a device also loads the library's
+// device code there) and passes it on as the workspace pointer. Looking it up
+// each time, rather than remembering it per device, keeps the address right
+// if the device's context is destroyed and created again (cudaDeviceReset),
+// after which the array may sit elsewhere.
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "m3scan.h"
 
@@ -25,28 +28,14 @@ constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
-std::mutex g_scratch_mu;
-
 // Device address of the current device's copy of the scratch array.
 m3_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
     cudaGetLastError();
     return M3_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) return M3_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return M3_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return M3_OK;
 }
 

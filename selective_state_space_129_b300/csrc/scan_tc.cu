@@ -3,15 +3,17 @@
 // Scope: bf16 activations, head dim P = 64, state N in {64, 128}, MIMO rank
 // R in {1, 2, 4} with chunk Q = 64 / R, so that the flattened (token, rank)
 // tile of a chunk has QR = 64 rows (the MIMO chunk rule C_MIMO = C_SISO / R of
-// papernotes.org sec. 3).
+// "Mamba-3: Improved Sequence Modeling using State Space Principles",
+// papernotes.org, sec. 3 MIMO).
 //
 // Math (per batch row b and head h). The rotation of the complex-valued state
-// is folded into B and C as a cumulative data-dependent RoPE (aipaper.cc
+// is folded into B and C as a cumulative data-dependent RoPE ("MAMBA-3:
+// IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES", aipaper.cc,
 // sec. 4.2, Prop. 3): with Phi_t = sum_{u<=t} Delta_u theta_u (per state pair,
 // over the whole sequence) and Rot(-Phi_t) applied to B_t and C_t,
 //   g_t = alpha_t g_{t-1} + beta_t Bt_{t-1} x_{t-1}^T + gamma_t Bt_t x_t^T,
 //   y_t = Ct_t^T g_t,   h_t = Rot(Phi_t) g_t   (explicit frame).
-// The exponential-trapezoidal weights are those of Prop. 1 (aipaper.cc
+// The exponential-trapezoidal weights are those of Prop. 1 (same page,
 // sec. 4.1). The state g therefore needs no rotation between chunks. Within a
 // chunk of tokens t0..t1 (Lam = chunk-local inclusive cumsum of Delta A):
 //   S   = Ct Bt^T                                   (tcgen05, M=64 N=64 K=N)
@@ -22,7 +24,7 @@
 //   H_out = exp(Lam_t1) H_in + Bt^T diag(w) X,  w_s = exp(Lam_t1 - Lam_s)(gamma_s + bhat_{s+1})
 // where H_in is the chunk's entering state including the pending beta term of
 // its first token, and bhat_{s+1} = (1 - lambda_{s+1}) Delta_{s+1} (0 past the
-// end). H lives in fp32 registers.
+// end).
 //
 // Precision. The rotated operands are data derived in fp32, not inputs, and
 // the score matrix sums products much larger than y itself (|B|^2 = N for
@@ -30,35 +32,37 @@
 // therefore fp16 (11-bit significand, kind::f16 MMA with fp32 accumulation),
 // each scaled by a power of two chosen per chunk from a bound of its
 // magnitude, so fp16's range never limits the inputs. The scales are undone
-// exactly where a per-element factor is applied anyway (mask, state update,
+// exactly where a per-element factor is applied anyway (mask, state rescale,
 // output). P is split into bf16 high and low parts so that P X (X is an exact
 // bf16 input) keeps ~16 significant bits. The cumulative angle is carried
-// from chunk to chunk as a float-float pair fed by Kahan-compensated sums, so
-// it does not drift over long sequences.
+// from chunk to chunk as a float-float pair, so it does not drift over long
+// sequences.
 //
-// Organisation: a persistent, warp-specialised CTA (512 threads, one per SM)
-// walks work units (whole (b, h) sequences, or segments of them when there
-// are fewer sequences than SMs), chunk by chunk, as a software pipeline:
-//   warps 0-7    prologue: decay scan (warp 0), angles, RoPE fold of B/C into
-//                fp16 UMMA tiles, w X, into one of two operand slots per chunk;
-//                one thread issues the TMA of the next chunk's raw B, C,
-//                theta, x tiles (one raw slot), two others the chunk's S and D
-//                MMAs into one of two TMEM accumulator sets; one warp
-//                prefetches the next chunk's dt, lambda
-//   warps 8-15   core (two warps per TMEM lane quadrant, 32 columns each):
-//                mask S -> P, state H = exp(Lam_end) H + D and its fp16 copy,
-//                y = Y + exp(Lam_t) Yoff -> TMA store, final state; its thread
-//                0 issues Y = P X for chunk c and Yoff = Ct H for chunk c+1,
-//                overlapping chunk c's epilogue
-// so the prologue of chunk c+1 runs while the core finishes chunk c. Roles
-// hand off through mbarriers; a role synchronises internally with its own
-// named barrier. Operand tiles are 128-byte-swizzled rows of 64 16-bit
-// elements; a [rows][64k] tile is at once the K-major operand along its
-// columns and the MN-major operand along its rows, so Bt serves both S (K = N)
-// and the state GEMM (K = tokens).
+// Organisation: a persistent CTA of 256 threads (8 warps) walks work units
+// (whole (b, h) sequences, or segments of them when there are fewer sequences
+// than SMs) chunk by chunk; two CTAs share an SM (about 104 KB of shared
+// memory and 256 TMEM columns each), so one CTA's barriers and MMA waits are
+// covered by the other's work. Every warp takes part in every phase of a chunk:
+//   fold   raw B, C, x tiles (TMA, refilled with the next chunk as soon as they
+//          are read) -> magnitude bounds and per-token-group angle sums ->
+//          barrier -> fp16 scales, angle offsets, sincos, RoPE fold of B and C
+//          into 128-byte-swizzled fp16 UMMA tiles, w X, the bf16 X operand, and
+//          the rescale of the state held in TMEM by exp(Lam_end) and the change
+//          of scale -> barrier -> one thread issues D (accumulated onto the
+//          state), S and Yoff = Ct H_in
+//   mask   S -> P (bf16 high + low, over the Bt tile, which D and S no longer
+//          read) -> barrier -> one thread issues Y = P X
+//   state  the state after D (TMEM) -> its bound -> barrier -> its scaled fp16
+//          copy for the next chunk's Yoff
+//   output y = Y + exp(Lam_t) Yoff -> bf16 -> global memory (16-byte stores;
+//          a TMA store from a staging tile for R > 1); final state
+// The fp32 state lives in the TMEM columns of the D accumulator: each chunk
+// rescales it in place and the D MMA accumulates onto it. One warp computes
+// the next chunk's decay scan (warp shuffles) at the end of a chunk; theta is
+// read from global memory into registers one chunk ahead.
 // Every mbarrier wait is bounded; on expiry the CTA records the status word,
-// every role leaves its loop at the next chunk boundary, and the CTA still
-// frees its tensor memory.
+// every thread leaves the loop at the next block barrier, and the CTA still
+// waits for its copies in flight and frees its tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -71,16 +75,11 @@
 namespace m3 {
 namespace {
 
-constexpr int kProWarps = 8, kCoreWarps = 8;
-constexpr int kProThreads = kProWarps * 32;    // 256
-constexpr int kCoreThreads = kCoreWarps * 32;  // 256: two warps per TMEM lane quadrant
-constexpr int kThreads = kProThreads + kCoreThreads;  // 512 (128 registers per thread)
-constexpr int kWarpTmem = kProWarps;                  // allocates / frees TMEM
-constexpr uint32_t kBarPro = 1, kBarCore = 2;          // named barrier ids
+constexpr int kThreads = 256;  // 8 warps, two CTAs per SM (128 registers per thread)
+constexpr int kWarps = kThreads / 32;
 constexpr int kQR = 64;  // rows of the flattened (token, rank) tile
 constexpr int kP = 64;   // head dim of the tensor-core path
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemSlot = 256;          // columns per accumulator set
+constexpr uint32_t kTmemCols = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 constexpr uint32_t kTileBytes = 64 * 128;    // 64 rows x 128 B
 constexpr float kLog2e = 1.4426950408889634f;
@@ -94,7 +93,7 @@ constexpr float kPi2c = 1.0253131677e-11f;
 // angles beyond this bound are reduced first.
 constexpr float kAngleDirect = 300.f;
 
-// TMEM column offsets of the four fp32 accumulators within a set.
+// TMEM column offsets of the four fp32 accumulators. D holds the state.
 constexpr uint32_t kColS = 0, kColD = 64, kColY = 128, kColYo = 192;
 
 constexpr uint32_t align1k(uint32_t v) { return (v + 1023u) & ~1023u; }
@@ -103,48 +102,49 @@ template <int R, int NS>
 struct Cfg {
   static constexpr int Q = kQR / R;          // tokens per chunk
   static constexpr int KP = NS / 2;          // rotating state pairs
-  static constexpr int KP2 = KP / 2;         // pair-pairs: a prologue thread owns two pairs
-  static constexpr int TG = kProThreads / KP2;  // token groups in the prologue
-  static constexpr int TPG = Q / TG;         // tokens per prologue thread
+  static constexpr int KP2 = KP / 2;         // pair-pairs: a fold thread owns two pairs
+  static constexpr int TG = kThreads / KP2;  // token groups of the fold
+  static constexpr int TPG = Q / TG;         // tokens per fold thread
   static_assert(TPG >= 1 && Q % TG == 0, "token groups must divide the chunk");
-  static constexpr int HR = NS * kP / kCoreThreads;  // fp32 state values per core thread
-  static constexpr int BW = 2 * R;           // raw 32-bit words of B (or C) per token and thread
-  // raw slot (TMA destination): B, C [Q][NS*R] bf16, theta [Q][KP] fp32, x [Q][P*R] bf16
+  static constexpr int HR = NS * kP / kThreads;  // fp32 state values per thread
+  static constexpr int BW = 2 * R;  // raw 32-bit words of B (or C) per token and thread
+  // raw slot (TMA destination): B, C [Q][NS*R] bf16, x [Q][P*R] bf16
   static constexpr uint32_t kRawB = 0;
   static constexpr uint32_t kRawC = kRawB + Q * NS * R * 2;
-  static constexpr uint32_t kRawTh = kRawC + Q * NS * R * 2;
-  static constexpr uint32_t kRawX = align1k(kRawTh + Q * KP * 4);  // 128B-swizzled for R = 1
-  static constexpr uint32_t kRawBytes = kRawX + (uint32_t)(Q * kP * R * 2);
-  // two operand slots: Bt, Ct [64][NS] fp16, w X [64][64] fp16, X [64][64] bf16
-  static constexpr uint32_t kOpBt = 0;
-  static constexpr uint32_t kOpCt = 64 * NS * 2;
-  static constexpr uint32_t kOpXw = 2 * 64 * NS * 2;
-  static constexpr uint32_t kOpXo = kOpXw + kTileBytes;
-  static constexpr uint32_t kOpBytes = kOpXo + kTileBytes;
-  static constexpr uint32_t kOp0 = align1k(kRawBytes);
-  // core tiles: P high / low (bf16), fp16 state copy [NS][64], output staging
-  static constexpr uint32_t kPh = kOp0 + 2 * kOpBytes;
+  static constexpr uint32_t kRawX = align1k(kRawC + Q * NS * R * 2);  // 128B-swizzled for R = 1
+  static constexpr uint32_t kRawEnd = kRawX + (uint32_t)(Q * kP * R * 2);
+  // operand tiles: Bt, Ct [64][NS] fp16, w X [64][64] fp16, X [64][64] bf16,
+  // the fp16 state copy [NS][64]
+  static constexpr uint32_t kBt = align1k(kRawEnd);
+  static constexpr uint32_t kCt = kBt + 64 * NS * 2;
+  static constexpr uint32_t kXw = kCt + 64 * NS * 2;
+  static constexpr uint32_t kXo = kXw + kTileBytes;
+  static constexpr uint32_t kH = kXo + kTileBytes;
+  static constexpr uint32_t kHEnd = kH + NS * 128;
+  // masked scores P (bf16 high, low): over Bt when it is large enough
+  static constexpr uint32_t kPh = (NS == 128) ? kBt : kHEnd;
   static constexpr uint32_t kPl = kPh + kTileBytes;
-  static constexpr uint32_t kH = kPl + kTileBytes;
-  static constexpr uint32_t kYs = kH + NS * 128;
-  static constexpr uint32_t kBytes = kYs + kTileBytes;
+  // output staging (R > 1): over w X, which only D reads
+  static constexpr uint32_t kYs = kXw;
+  static constexpr uint32_t kBytes = (kPl + kTileBytes > kHEnd) ? kPl + kTileBytes : kHEnd;
   static constexpr uint32_t kSmem = kBytes + 1024;  // + alignment slack
-  // bytes landing on the raw barrier per chunk
+  // bytes landing on the raw barrier per chunk (full pass; state-only pass)
   static constexpr uint32_t kTxBytes =
-      2u * Q * NS * R * 2 + (uint32_t)(Q * KP * 4) + (uint32_t)(Q * kP * R * 2);
+      2u * Q * NS * R * 2 + (uint32_t)(Q * kP * R * 2);
+  static constexpr uint32_t kTxBytesSO = (uint32_t)Q * NS * R * 2 + (uint32_t)(Q * kP * R * 2);
 };
 
-// Per-chunk scalars handed from the prologue to the core (one set per slot).
-template <int KP>
-struct __align__(16) SlotScalars {
+// Per-chunk scalars (one set per chunk parity): the decay scan's results for
+// the chunk's tokens and the chunk's fp16 scales.
+struct __align__(16) Scal {
   float lam2[64];  // Lam_t in log2 units
   float gam[64];   // gamma_t
   float wp[64];    // gamma_t + bhat_{t+1}
   float eL[64];    // exp(Lam_t)
   float wend[64];  // exp(Lam_end - Lam_t) (gamma_t + bhat_{t+1})
-  float fang[KP];  // cumulative angle after the chunk (last chunk of a sequence)
-  float eLend, wmax, invB, invC, invX;
-  float lamend2;  // Lam_end in log2 units
+  float dt[64];    // Delta_t
+  float eLend, lamend2, wmax;  // exp(Lam_end), Lam_end (log2), max |wend|
+  float invB, invC, invX;      // inverse fp16 scales of Bt, Ct, w X
   float pad[2];
 };
 
@@ -152,8 +152,10 @@ struct TcParams {
   const float* dt;
   const float* A;
   const float* lam;
+  const float* theta;
   const float* B_bias;
   const float* C_bias;
+  __nv_bfloat16* out;
   float* final_state;
   unsigned int* status;
   int64_t L, H, G, batch;
@@ -172,10 +174,6 @@ struct TcParams {
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col) {
   return row * 128u + ((((col >> 3) ^ row) & 7u) << 4) + (col & 7u) * 2u;
-}
-// [rows][K] tile stored as K/64 blocks of [rows][64]: byte offset of (row, col).
-__device__ __forceinline__ uint32_t tile_off(uint32_t row, uint32_t col, uint32_t rows) {
-  return (col >> 6) * rows * 128u + sw128(row, col & 63u);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -210,7 +208,6 @@ __device__ __forceinline__ void pow2_scale(float M, float* sigma, float* inv) {
 using ptx::add2;
 using ptx::fma2;
 using ptx::mul2;
-using ptx::sub2;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -296,7 +293,9 @@ __host__ __device__ constexpr uint32_t koff_k(int kk, uint32_t rows) {
 __host__ __device__ constexpr uint32_t koff_mn(int kk) { return (uint32_t)kk * 2048u; }
 
 // Bounded wait on an mbarrier phase; on expiry record the status word and the
-// CTA's abort flag. Returns false if the CTA is (now) aborting.
+// CTA's abort flag. Returns false if the CTA is (now) aborting. Every thread
+// that needs the phase waits itself; threads leave the chunk loop only right
+// after a block barrier, where the flag reads the same for all of them.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag,
                                               unsigned int* status) {
   if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
@@ -308,10 +307,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
 
 // Position of a CTA in its schedule. Work units are (sequence, segment)
 // pairs, unit u = seq * nseg + segment, covering chunks [c_begin, c_end) of
-// the sequence; a CTA walks units blockIdx.x, +gridDim.x, ... chunk by chunk
-// (g counts its chunks; slots and mbarrier phases follow g).
+// the sequence; a CTA walks units blockIdx.x, +gridDim.x, ... chunk by chunk.
 // (32-bit indices, divided once per unit: 64-bit division is a long
-// software sequence that would sit on the per-chunk critical path).
+// software sequence.)
 struct Sched {
   int unit, b, h;
   int c, c_begin, c_end;
@@ -324,6 +322,9 @@ struct Sched {
     b = seq / p.heads;
     h = seq - b * p.heads;
   }
+  __device__ __forceinline__ bool has_next(const TcParams& p) const {
+    return c + 1 < c_end || unit + (int)gridDim.x < p.nunits;
+  }
   __device__ __forceinline__ bool next(const TcParams& p) {
     if (++c < c_end) return true;
     const int u = unit + (int)gridDim.x;
@@ -335,14 +336,13 @@ struct Sched {
 
 // Raw decay inputs of a chunk's tokens: dt, lambda of the token and of its
 // successor (zero past the end of the sequence); lane handles tokens lane and
-// lane + 32. Only loads: the arithmetic waits until the values are needed, so
-// that the load latency overlaps other work.
+// lane + 32. Only loads, so that their latency overlaps other work.
 struct DecayRaw {
-  float dt[2], lam[2], dtn[2], lamn[2];
+  float dt[2], lam[2], dtn[2], lamn[2], A;
 };
-__device__ __forceinline__ void load_decay_raw(const TcParams& p, int64_t b, int64_t h, int64_t t0,
-                                               int Q, int lane, DecayRaw& d) {
-  const int64_t L = p.L, H = p.H;
+__device__ __forceinline__ void load_decay_raw(const TcParams& p, const Sched& u, int Q, int lane,
+                                               DecayRaw& d) {
+  const int64_t L = p.L, H = p.H, b = u.b, h = u.h, t0 = (int64_t)u.c * Q;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int i = lane + 32 * j;
@@ -353,24 +353,72 @@ __device__ __forceinline__ void load_decay_raw(const TcParams& p, int64_t b, int
     d.dtn[j] = inn ? p.dt[(b * L + t + 1) * H + h] : 0.f;
     d.lamn[j] = inn ? p.lam[(b * L + t + 1) * H + h] : 1.f;
   }
+  d.A = p.A[u.h];
 }
-// dt, lambda and bhat of the successor into the chunk's decay-input buffer
-__device__ __forceinline__ void store_decay(const DecayRaw& d, int lane, float* sdt, float* slam,
-                                            float* sbn) {
+// The chunk's decay scan (one warp, shuffles): Lam_t = inclusive sum of
+// Delta A within the chunk, and the weights derived from it.
+__device__ __forceinline__ void decay_scan(const DecayRaw& d, int Q, int lane, Scal& sc) {
+  float a0 = d.dt[0] * d.A * kLog2e, a1 = d.dt[1] * d.A * kLog2e;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float v0 = __shfl_up_sync(0xffffffffu, a0, o);
+    const float v1 = __shfl_up_sync(0xffffffffu, a1, o);
+    if (lane >= o) {
+      a0 += v0;
+      a1 += v1;
+    }
+  }
+  a1 += __shfl_sync(0xffffffffu, a0, 31);
+  const float lam_end = (Q <= 32) ? __shfl_sync(0xffffffffu, a0, Q - 1)
+                                  : __shfl_sync(0xffffffffu, a1, (Q - 1) & 31);
+  const float lv[2] = {a0, a1};
+  float wm = 0.f;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    sdt[lane + 32 * j] = d.dt[j];
-    slam[lane + 32 * j] = d.lam[j];
-    sbn[lane + 32 * j] = (1.f - d.lamn[j]) * d.dtn[j];
+    const int i = lane + 32 * j;
+    if (i < Q) {
+      const float gam = d.lam[j] * d.dt[j];
+      const float wpv = gam + (1.f - d.lamn[j]) * d.dtn[j];
+      const float we = ex2(lam_end - lv[j]) * wpv;
+      sc.lam2[i] = lv[j];
+      sc.gam[i] = gam;
+      sc.wp[i] = wpv;
+      sc.wend[i] = we;
+      sc.eL[i] = ex2(lv[j]);
+      sc.dt[i] = d.dt[j];
+      wm = fmaxf(wm, fabsf(we));
+    }
+  }
+  wm = warp_max(wm);
+  if (lane == 0) {
+    sc.eLend = ex2(lam_end);
+    sc.lamend2 = lam_end;
+    sc.wmax = wm;
+  }
+}
+
+// theta of this fold thread's tokens (TPG consecutive tokens of group tg) and
+// pairs (k0, k0 + 1), straight from global memory (zero past the end).
+template <int KP, int TPG>
+__device__ __forceinline__ void load_theta(const TcParams& p, const Sched& u, int Q, int tg, int k0,
+                                           float2 (&th)[TPG]) {
+  const int64_t gi = u.h / p.hpg;
+  const int64_t t0 = (int64_t)u.c * Q + tg * TPG;
+#pragma unroll
+  for (int i = 0; i < TPG; ++i) {
+    const int64_t t = t0 + i;
+    th[i] = t < p.L ? __ldg(reinterpret_cast<const float2*>(
+                          p.theta + (((int64_t)u.b * p.L + t) * p.G + gi) * KP + k0))
+                    : make_float2(0.f, 0.f);
   }
 }
 
 // SO: the state-only pass of a segmented scan (no C, no outputs).
 template <int R, int NS, bool SO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
-                   const __grid_constant__ CUtensorMap tm_th, const __grid_constant__ CUtensorMap tm_x,
-                   const __grid_constant__ CUtensorMap tm_y, TcParams p) {
+                   const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+                   TcParams p) {
   using K = Cfg<R, NS>;
   constexpr int Q = K::Q, KP = K::KP, KP2 = K::KP2, TG = K::TG, TPG = K::TPG, HR = K::HR;
   constexpr uint32_t kIdS = ptx::idesc_f16_f32(64, 64, false, false);
@@ -382,607 +430,206 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
 
-  __shared__ uint64_t bar_raw_full;
-  __shared__ uint64_t bar_op_full[2], bar_slot_free[2], bar_acc_full[2], bar_y_full[2];
+  __shared__ uint64_t bar_raw, bar_ds, bar_yo, bar_y;
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
-  __shared__ int s_go[2];  // per-role broadcast of "continue" decisions
-  __shared__ SlotScalars<KP> ss[2];
-  __shared__ float s_dtraw[2][64], s_lamraw[2][64], s_bnx[2][64];
-  __shared__ __align__(16) float s_tot[2][TG][KP];   // per token group: angle total (hi, lo)
-  __shared__ float s_carry[2][2][KP];  // [chunk parity][hi, lo][pair]
-  __shared__ unsigned int s_max[2][3];  // per chunk parity: bounds of |B|, |C|, |x| (float bits)
-  __shared__ float s_hred[kCoreWarps];
-  __shared__ float s_bias_red[2][kProWarps];
-  // R > 1: the head's B / C bias transposed to [rank][row] (registers for R = 1)
-  __shared__ __align__(16) float s_biasT[2][R][NS];  // B, C bias of the head, [rank][n]
+  __shared__ Scal ss[2];
+  __shared__ __align__(16) float s_tot[TG][KP];  // per token group: angle total
+  __shared__ float s_carry[2][2][KP];            // [chunk parity][hi, lo][pair]
+  __shared__ float s_fang[KP];                   // angle after a unit's last chunk
+  __shared__ unsigned int s_max[2][3];  // per chunk parity: bounds of |B|, |C|, |x|
+  __shared__ float s_red[kWarps];
+  __shared__ float s_bias_red[2][kWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nC = p.nchunks;
+  // fold mapping: pairs k0, k0 + 1 (rows 4kk2 .. 4kk2 + 3), tokens tg*TPG ..
+  const int kk2 = tid % KP2, tg = tid / KP2, k0 = 2 * kk2;
+  // accumulator mapping: TMEM lane quadrant, 32-column half
+  const int quad = warp & 3, half = warp >> 2;
 
   // ---------------------------------------------------------------- setup
-  if (warp == kWarpTmem) {
+  if (warp == 0) {
     ptx::tmem_alloc(&tmem_holder, kTmemCols);
     ptx::tmem_relinquish();
   }
   if (tid == 0) {
     abort_flag = 0;
     for (int i = 0; i < 6; ++i) (&s_max[0][0])[i] = 0u;
-    ptx::mbar_init(&bar_raw_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&bar_op_full[s], 1);
-      ptx::mbar_init(&bar_slot_free[s], kCoreWarps);
-      ptx::mbar_init(&bar_acc_full[s], SO ? 1 : 2);  // the S and the D issuer commit
-      ptx::mbar_init(&bar_y_full[s], 1);
-    }
+    ptx::mbar_init(&bar_raw, 1);
+    ptx::mbar_init(&bar_ds, 1);
+    ptx::mbar_init(&bar_yo, 1);
+    ptx::mbar_init(&bar_y, 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&tm_B);
     ptx::prefetch_tensormap(&tm_C);
-    ptx::prefetch_tensormap(&tm_th);
     ptx::prefetch_tensormap(&tm_x);
-    ptx::prefetch_tensormap(&tm_y);
+    if (R > 1) ptx::prefetch_tensormap(&tm_y);
   }
-  // masked-score tiles: blocks above the diagonal are zero and never written again
-  for (uint32_t i = tid * 16; i < 2u * kTileBytes; i += kThreads * 16)
-    sts128(sbase + K::kPh + i, make_uint4(0, 0, 0, 0));
-  ptx::fence_proxy_async_smem();
   ptx::tc_fence_before_sync();
   __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem = tmem_holder;
+  const uint32_t tq = (uint32_t)(32 * quad) << 16;  // this warp's lane quadrant
 
-  // TMA of one chunk's raw tiles into the raw slot (one prologue thread)
+  // TMA of one chunk's raw tiles into the raw slot (one thread)
   auto issue_raw = [&](const Sched& u) {
-    const int b = u.b, h = u.h, gi = h / p.hpg;
+    const int gi = u.h / p.hpg;
     const int t0 = u.c * Q;
-    ptx::mbar_arrive_expect_tx(&bar_raw_full, SO ? K::kTxBytes - K::kRawC : K::kTxBytes);
-    ptx::tma_load_5d(smem + K::kRawB, &tm_B, &bar_raw_full, 0, 0, gi, t0, b);
-    if (!SO) ptx::tma_load_5d(smem + K::kRawC, &tm_C, &bar_raw_full, 0, 0, gi, t0, b);
-    ptx::tma_load_4d(smem + K::kRawTh, &tm_th, &bar_raw_full, 0, gi, t0, b);
-    ptx::tma_load_4d(smem + K::kRawX, &tm_x, &bar_raw_full, 0, h, t0, b);
+    ptx::mbar_arrive_expect_tx(&bar_raw, SO ? K::kTxBytesSO : K::kTxBytes);
+    ptx::tma_load_5d(smem + K::kRawB, &tm_B, &bar_raw, 0, 0, gi, t0, u.b);
+    if (!SO) ptx::tma_load_5d(smem + K::kRawC, &tm_C, &bar_raw, 0, 0, gi, t0, u.b);
+    ptx::tma_load_4d(smem + K::kRawX, &tm_x, &bar_raw, 0, u.h, t0, u.b);
   };
 
-  if (warp < kProWarps) {
-    // ============================================================ prologue
-    const int kk2 = tid % KP2, tg = tid / KP2;
-    const int k0 = 2 * kk2;  // this thread's pairs: k0, k0 + 1 (rows 4kk2 .. 4kk2 + 3)
-    int cur_h = -1;
-    float bmax_bias = 0.f, cmax_bias = 0.f;
-    int inflight = -1;  // phase parity of a raw load issued and not yet consumed
-    // the first chunk's inputs
-    Sched sch;
-    sch.start(blockIdx.x, p);
-    // one-off duties sit on warps without other extra work: TMA of the raw
-    // tiles (warp 4), S and D MMA issue (warps 2 and 3); warp 0 runs the decay
-    // scan, warp 1 loads the next chunk's decay inputs, warps 6 and 7 carry
-    // the angle totals
-    constexpr int kTmaTid = 128, kSTid = 64, kDTid = 96;
-    if (tid == kTmaTid) {
-      issue_raw(sch);
-      inflight = 0;
+  // state element (n, cb + j) of this thread's 16-column block `blk` is hv[16 blk + j]
+  auto hpos = [&](int blk, uint32_t& n, uint32_t& cb) {
+    if constexpr (NS == 128) {
+      n = (uint32_t)(32 * quad + lane);  // M=128 accumulator layout: lane = row
+      cb = 32u * half + 16u * blk;
+    } else {
+      n = (uint32_t)(16 * quad + (lane & 15));  // M=64 layout: 16 rows per quadrant
+      cb = 32u * half + 16u * (lane >> 4);
     }
-    if (warp == 1) {
-      DecayRaw d;
-      load_decay_raw(p, sch.b, sch.h, (int64_t)sch.c * Q, Q, lane, d);
-      store_decay(d, lane, s_dtraw[0], s_lamraw[0], s_bnx[0]);
+  };
+  auto state_ld = [&](float (&hv)[HR]) {
+#pragma unroll
+    for (int blk = 0; blk < HR / 16; ++blk) {
+      uint32_t d[16];
+      if constexpr (NS == 128)
+        ptx::tmem_ld16(tmem + kColD + tq + 32u * half + 16u * blk, d);
+      else
+        ptx::tmem_ld16_16x32bx2<16>(tmem + kColD + tq + 32u * half, d);
+      ptx::tmem_ld_wait(d);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) hv[16 * blk + j] = __uint_as_float(d[j]);
     }
-    // the first chunk's decay inputs are in place before warp 0 reads them
-    // (later chunks' are stored before the previous chunk's last barrier)
-    ptx::named_bar_sync(kBarPro, kProThreads);
-    float A_h = 0.f;
-    for (int g = 0;; ++g) {
-      const int h = sch.h;
-      const int c = sch.c, s = g & 1, db = g & 1;
-      const bool has_next = sch.c + 1 < sch.c_end || sch.unit + (int)gridDim.x < p.nunits;
-      SlotScalars<KP>& sc = ss[s];
-      if (h != cur_h) {
-        // per-head A, bias (fp32) and a block-wide bound of the bias magnitude
-        cur_h = h;
-        A_h = p.A[h];
-        float mb = 0.f, mc = 0.f;
-        // the previous head's bias was last read before the previous chunk's
-        // last barrier
-        for (int i = tid; i < NS * R; i += kProThreads) {
-          const float vb = p.B_bias ? p.B_bias[(int64_t)h * NS * R + i] : 0.f;
-          const float vc = p.C_bias ? p.C_bias[(int64_t)h * NS * R + i] : 0.f;
-          s_biasT[0][i % R][i / R] = vb;
-          s_biasT[1][i % R][i / R] = vc;
-          mb = fmaxf(mb, fabsf(vb));
-          mc = fmaxf(mc, fabsf(vc));
+  };
+  auto state_st = [&](const float (&hv)[HR]) {
+#pragma unroll
+    for (int blk = 0; blk < HR / 16; ++blk) {
+      uint32_t d[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) d[j] = __float_as_uint(hv[16 * blk + j]);
+      if constexpr (NS == 128)
+        ptx::tmem_st16(tmem + kColD + tq + 32u * half + 16u * blk, d);
+      else
+        ptx::tmem_st16_16x32bx2<16>(tmem + kColD + tq + 32u * half, d);
+    }
+    ptx::tmem_st_wait();
+  };
+  // fp16 copy of f * hv into the state tile (operand of the next Yoff)
+  auto write_hcopy = [&](const float (&hv)[HR], float f) {
+    const float2 f2 = make_float2(f, f);
+#pragma unroll
+    for (int blk = 0; blk < HR / 16; ++blk) {
+      uint32_t n, cb;
+      hpos(blk, n, cb);
+      uint32_t wv[8];
+#pragma unroll
+      for (int j = 0; j < 16; j += 2) {
+        const float2 v = mul2(f2, make_float2(hv[16 * blk + j], hv[16 * blk + j + 1]));
+        wv[j >> 1] = pack_f16(v.x, v.y);
+      }
+      sts128(sbase + K::kH + sw128(n, cb), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+      sts128(sbase + K::kH + sw128(n, cb + 8u), make_uint4(wv[4], wv[5], wv[6], wv[7]));
+    }
+  };
+  auto abs_max = [&](const float (&hv)[HR]) {
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < HR; ++i) m = fmaxf(m, fabsf(hv[i]));
+    return m;
+  };
+
+  // Fold stores: row l = i R + r of this thread's token rows (rows tg*TPG*R +
+  // l) at columns 4kk2 .. 4kk2 + 3 of Bt / Ct. The 128-byte swizzle XORs the
+  // 16-byte chunk index with the row's low three bits; those are rb7 ^ (l & 7)
+  // (rb7 = the first row's, 0 or 4), so every store address is the one base
+  // below XOR (l & 7) << 4 (bits 4-6, which nothing else in the base sets)
+  // plus the constant l * 128.
+  uint32_t fold_base;
+  {
+    const uint32_t col = 4u * (uint32_t)kk2, cl = col & 63u;
+    const uint32_t row0 = (uint32_t)(tg * TPG * R), rb7 = row0 & 7u;
+    fold_base = sbase + K::kBt + (col >> 6) * 64u * 128u + row0 * 128u +
+                ((((cl >> 3) ^ rb7) & 7u) << 4) + (cl & 7u) * 2u;
+  }
+
+  // ---------------------------------------------------------------- first chunk's inputs
+  Sched sch;
+  sch.start(blockIdx.x, p);
+  if (tid == 0) issue_raw(sch);
+  DecayRaw dr;
+  if (warp == 0) {
+    load_decay_raw(p, sch, Q, lane, dr);
+    decay_scan(dr, Q, lane, ss[0]);
+  }
+  float2 th[TPG];
+  load_theta<KP, TPG>(p, sch, Q, tg, k0, th);
+  __syncthreads();
+
+  // state bookkeeping (uniform over the CTA)
+  bool has_state = false;   // TMEM holds a state (else the first D MMA overwrites)
+  bool yoff_ready = false;  // the state tile holds H_in of this chunk (its Yoff is issued)
+  float u_prev = 1.f;       // the TMEM state is (state) / u_prev
+  float h_inv_prev = 1.f;   // inverse scale of the state tile read by this chunk's Yoff
+  float dsum = 0.f;         // log2 decay over the unit (state-only pass)
+  float bmax_bias = 0.f, cmax_bias = 0.f;  // bounds of the head's bias magnitudes
+  // (thread 0) parity of a raw load issued and not yet waited for, and the
+  // barrier and parity of its last MMA commit: what an early exit waits for
+  int raw_pending = 0;
+  uint64_t* last_commit = nullptr;
+  uint32_t last_parity = 0;
+  float hv[HR];
+
+  for (int g = 0;; ++g) {
+    const int b = sch.b, h = sch.h, c = sch.c;
+    const bool first = c == sch.c_begin, last = c == sch.c_end - 1;
+    const bool has_next = sch.has_next(p);
+    Scal& sc = ss[g & 1];
+    ptx::tc_fence_after_sync();
+
+    // ================================================= unit start: entering state
+    if (first) {
+      has_state = false;
+      yoff_ready = false;
+      u_prev = 1.f;
+      dsum = 0.f;
+      {
+        // bounds of the head's bias magnitudes (for the fp16 scales)
+        const int64_t o = ((int64_t)h * NS + 4 * kk2) * R;
+        float bm = 0.f, cm = 0.f;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+          const float4 vb = p.B_bias ? __ldg(reinterpret_cast<const float4*>(p.B_bias + o) + q)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 vc = (!SO && p.C_bias)
+                                ? __ldg(reinterpret_cast<const float4*>(p.C_bias + o) + q)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          bm = fmaxf(bm, fmaxf(fmaxf(fabsf(vb.x), fabsf(vb.y)), fmaxf(fabsf(vb.z), fabsf(vb.w))));
+          cm = fmaxf(cm, fmaxf(fmaxf(fabsf(vc.x), fabsf(vc.y)), fmaxf(fabsf(vc.z), fabsf(vc.w))));
         }
-        mb = warp_max(mb);
-        mc = warp_max(mc);
+        bm = warp_max(bm);
+        cm = warp_max(cm);
         if (lane == 0) {
-          s_bias_red[0][warp] = mb;
-          s_bias_red[1][warp] = mc;
+          s_bias_red[0][warp] = bm;
+          s_bias_red[1][warp] = cm;
         }
-        ptx::named_bar_sync(kBarPro, kProThreads);
+        __syncthreads();
         bmax_bias = 0.f;
         cmax_bias = 0.f;
 #pragma unroll
-        for (int w = 0; w < kProWarps; ++w) {
+        for (int w = 0; w < kWarps; ++w) {
           bmax_bias = fmaxf(bmax_bias, s_bias_red[0][w]);
           cmax_bias = fmaxf(cmax_bias, s_bias_red[1][w]);
         }
       }
-      // 1. every thread waits for this chunk's raw tiles itself (no block
-      // barrier here); an expired wait sets the abort flag, which every thread
-      // reads after the next barrier
-      if (wait_or_abort(&bar_raw_full, (uint32_t)(g & 1), &abort_flag, p.status) && tid == kTmaTid)
-        inflight = -1;
-      // 2b. raw tiles -> registers (loads issued first)
-      float2 th2[TPG];
-      uint32_t bw[TPG][K::BW], cw[TPG][K::BW];
-      uint32_t bacc = 0u, cacc = 0u;
-#pragma unroll
-      for (int i = 0; i < TPG; ++i) {
-        const int t = tg * TPG + i;
-        const uint2 tv = lds64(sbase + K::kRawTh + (uint32_t)(t * KP + k0) * 4u);
-        th2[i] = make_float2(__uint_as_float(tv.x), __uint_as_float(tv.y));
-        const uint32_t ob = (uint32_t)(t * NS * R + 4 * kk2 * R) * 2u;
-        if constexpr (R == 1) {
-          const uint2 vb = lds64(sbase + K::kRawB + ob);
-          bw[i][0] = vb.x; bw[i][1] = vb.y;
-          if constexpr (!SO) {
-            const uint2 vc = lds64(sbase + K::kRawC + ob);
-            cw[i][0] = vc.x; cw[i][1] = vc.y;
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < K::BW / 4; ++q) {
-            const uint4 vb = lds128(sbase + K::kRawB + ob + 16u * q);
-            bw[i][4 * q] = vb.x; bw[i][4 * q + 1] = vb.y; bw[i][4 * q + 2] = vb.z; bw[i][4 * q + 3] = vb.w;
-            if constexpr (!SO) {
-              const uint4 vc = lds128(sbase + K::kRawC + ob + 16u * q);
-              cw[i][4 * q] = vc.x; cw[i][4 * q + 1] = vc.y; cw[i][4 * q + 2] = vc.z; cw[i][4 * q + 3] = vc.w;
-            }
-          }
-        }
-      }
-      // 2a (while the tile loads above are in flight). Decay scan (warp 0, once
-      // operand slot s and its scalars are free:
-      // the rest of the slot is written after the next barrier); the next
-      // chunk's dt, lambda (warp 1, into registers)
-      DecayRaw nd;
-      int slot_ok = 1;
-      if (warp == 0 && g >= 2) {
-        if (lane == 0)
-          slot_ok = wait_or_abort(&bar_slot_free[s], (uint32_t)(((g >> 1) & 1) ^ 1), &abort_flag,
-                                  p.status) ? 1 : 0;
-        slot_ok = __shfl_sync(0xffffffffu, slot_ok, 0);
-      }
-      if (warp == 0 && slot_ok) {
-        float dtv[2], lmv[2], bnx[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int i = lane + 32 * j;
-          dtv[j] = s_dtraw[db][i];
-          lmv[j] = s_lamraw[db][i];
-          bnx[j] = s_bnx[db][i];
-        }
-        float a0 = dtv[0] * A_h * kLog2e, a1 = dtv[1] * A_h * kLog2e;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float v0 = __shfl_up_sync(0xffffffffu, a0, o);
-          const float v1 = __shfl_up_sync(0xffffffffu, a1, o);
-          if (lane >= o) { a0 += v0; a1 += v1; }
-        }
-        a1 += __shfl_sync(0xffffffffu, a0, 31);
-        const float lam_end = (Q <= 32) ? __shfl_sync(0xffffffffu, a0, Q - 1)
-                                        : __shfl_sync(0xffffffffu, a1, (Q - 1) & 31);
-        const float lv[2] = {a0, a1};
-        float wm = 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int i = lane + 32 * j;
-          if (i < Q) {
-            const float gam = lmv[j] * dtv[j];
-            const float wpv = gam + bnx[j];
-            const float we = ex2(lam_end - lv[j]) * wpv;
-            sc.lam2[i] = lv[j];
-            sc.gam[i] = gam;
-            sc.wp[i] = wpv;
-            sc.wend[i] = we;
-            sc.eL[i] = ex2(lv[j]);
-            wm = fmaxf(wm, fabsf(we));
-          }
-        }
-        wm = warp_max(wm);
-        if (lane == 0) {
-          sc.eLend = ex2(lam_end);
-          sc.lamend2 = lam_end;
-          sc.wmax = wm;
-        }
-      } else if (warp == 1 && has_next) {
-        Sched nxt = sch;
-        nxt.next(p);
-        load_decay_raw(p, nxt.b, nxt.h, (int64_t)nxt.c * Q, Q, lane, nd);
-      }
-      // 2c. magnitude bounds, Kahan-compensated angle sums
-#pragma unroll
-      for (int i = 0; i < TPG; ++i) {
-#pragma unroll
-        for (int q = 0; q < K::BW; ++q) {
-          bacc = ptx::bf16x2_absmax(bacc, bw[i][q]);
-          if constexpr (!SO) cacc = ptx::bf16x2_absmax(cacc, cw[i][q]);
-        }
-      }
-      float2 ph[TPG];
-      {
-        float2 run = make_float2(0.f, 0.f), comp = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < TPG; ++i) {
-          const float d = s_dtraw[db][tg * TPG + i];
-          const float2 yk = sub2(mul2(make_float2(d, d), th2[i]), comp);
-          const float2 tk = add2(run, yk);
-          comp = sub2(sub2(tk, run), yk);
-          run = tk;
-          ph[i] = run;
-        }
-        s_tot[0][tg][k0] = run.x;
-        s_tot[0][tg][k0 + 1] = run.y;
-        s_tot[1][tg][k0] = -comp.x;
-        s_tot[1][tg][k0 + 1] = -comp.y;
-      }
-      // x of this chunk -> registers (w X and the operand copy of X)
-      constexpr int kXItems = (R == 1) ? 2 : (Q * (kP / 4)) / kProThreads;
-      constexpr int kXVec = (R == 1) ? 1 : R / 2;
-      uint4 xv[kXItems][kXVec];
-      uint32_t xacc = 0u;
-      const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
-#pragma unroll
-      for (int j = 0; j < kXItems; ++j) {
-        const int it = tid + kProThreads * j;
-        if constexpr (R == 1) {
-          xv[j][0] = lds128(sbase + K::kRawX + (uint32_t)it * 16u);  // 16-byte chunk, row it / 8
-        } else {
-          const int sx = it / (kP / 4), pb = it % (kP / 4);
-          const uint32_t src = sbase + K::kRawX + (uint32_t)(sx * kP * R + 4 * pb * R) * 2u;
-#pragma unroll
-          for (int q = 0; q < kXVec; ++q) xv[j][q] = lds128(src + 16u * q);
-        }
-#pragma unroll
-        for (int q = 0; q < kXVec; ++q) {
-          xacc = ptx::bf16x2_absmax(xacc, xv[j][q].x);
-          xacc = ptx::bf16x2_absmax(xacc, xv[j][q].y);
-          xacc = ptx::bf16x2_absmax(xacc, xv[j][q].z);
-          xacc = ptx::bf16x2_absmax(xacc, xv[j][q].w);
-        }
-      }
-      {
-        // non-negative floats order like their bit patterns
-        const float bm = warp_max(bf_absmax(bacc)), cm = warp_max(bf_absmax(cacc));
-        const float xm = warp_max(bf_absmax(xacc));
-        if (lane == 0) {
-          atomicMax(&s_max[g & 1][0], __float_as_uint(bm));
-          atomicMax(&s_max[g & 1][1], __float_as_uint(cm));
-          atomicMax(&s_max[g & 1][2], __float_as_uint(xm));
-        }
-      }
-      ptx::named_bar_sync(kBarPro, kProThreads);
-      if (*reinterpret_cast<volatile int*>(&abort_flag)) break;  // uniform after the barrier
-      // every read of the raw slot is done: refill it with the next chunk
-      if (has_next) {
-        if (tid == kTmaTid) {
-          Sched nxt = sch;
-          nxt.next(p);
-          issue_raw(nxt);
-          inflight = (g + 1) & 1;
-        }
-        if (warp == 1) store_decay(nd, lane, s_dtraw[db ^ 1], s_lamraw[db ^ 1], s_bnx[db ^ 1]);
-      }
-      // 3. per-chunk fp16 scales of Bt, Ct and w X
-      float sigB, invB, sigC, invC, sigX, invX;
-      {
-        const float mb = __uint_as_float(s_max[g & 1][0]);
-        const float mc = __uint_as_float(s_max[g & 1][1]);
-        const float mx = __uint_as_float(s_max[g & 1][2]);
-        // the other parity's words are free (read last chunk): clear them for the next
-        if (tid == 0) {
-          s_max[(g + 1) & 1][0] = 0u;
-          s_max[(g + 1) & 1][1] = 0u;
-          s_max[(g + 1) & 1][2] = 0u;
-        }
-        // a rotated pair keeps its norm: |Rot(v)_i| <= sqrt(2) max|v| < 2 max|v|
-        pow2_scale(2.f * (mb + bmax_bias), &sigB, &invB);
-        pow2_scale(2.f * (mc + cmax_bias), &sigC, &invC);
-        pow2_scale(mx * sc.wmax, &sigX, &invX);
-        if (tid == 0) {
-          sc.invB = invB;
-          sc.invC = invC;
-          sc.invX = invX;
-        }
-      }
-      // 4. angle before this thread's first token: carry + earlier groups.
-      // Within the chunk an fp32 offset suffices; the carry to the next
-      // chunk is float-float so that it does not drift.
-      const int cpar = g & 1;
-      float2 off;
-      {
-        float o0 = 0.f, o1 = 0.f;
-        for (int q = 0; q < tg; ++q) {
-          const float2 hi = *reinterpret_cast<const float2*>(&s_tot[0][q][k0]);
-          const float2 lo = *reinterpret_cast<const float2*>(&s_tot[1][q][k0]);
-          const float2 o = add2(make_float2(o0, o1), add2(hi, lo));
-          o0 = o.x;
-          o1 = o.y;
-        }
-        float ch0 = 0.f, cl0 = 0.f, ch1 = 0.f, cl1 = 0.f;
-        if (c > sch.c_begin) {
-          ch0 = s_carry[cpar][0][k0];
-          cl0 = s_carry[cpar][1][k0];
-          ch1 = s_carry[cpar][0][k0 + 1];
-          cl1 = s_carry[cpar][1][k0 + 1];
-        }
-        off.x = wrap_rad(ch0 + (cl0 + o0));
-        off.y = wrap_rad(ch1 + (cl1 + o1));
-        // the carry of pair k0 is updated by group TG-1, that of k0+1 by TG-2
-        if (tg >= TG - 2) {
-          const int k = (tg == TG - 1) ? k0 : k0 + 1;
-          // float-float sum of the group totals as a tree, then the carry
-          float th[TG], tl[TG];
-#pragma unroll
-          for (int q = 0; q < TG; ++q) {
-            th[q] = s_tot[0][q][k];
-            tl[q] = s_tot[1][q][k];
-          }
-#pragma unroll
-          for (int w = 1; w < TG; w <<= 1)
-#pragma unroll
-            for (int q = 0; q + w < TG; q += 2 * w) ff_add(th[q], tl[q], th[q + w], tl[q + w]);
-          float eh = (tg == TG - 1) ? ch0 : ch1, el = (tg == TG - 1) ? cl0 : cl1;
-          ff_add(eh, el, th[0], tl[0]);
-          ff_wrap(eh, el);
-          s_carry[cpar ^ 1][0][k] = eh;
-          s_carry[cpar ^ 1][1][k] = el;
-          if (c == sch.c_end - 1) sc.fang[k] = eh + el;
-        }
-      }
-      // 5. RoPE fold: sigma Rot(-Phi) (B + bias), likewise C, into fp16 tiles
-      {
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < TPG; ++i) {
-          ph[i] = add2(off, ph[i]);
-          amax = fmaxf(amax, fmaxf(fabsf(ph[i].x), fabsf(ph[i].y)));
-        }
-        if (__any_sync(0xffffffffu, amax > kAngleDirect)) {
-#pragma unroll
-          for (int i = 0; i < TPG; ++i) ph[i] = make_float2(wrap_rad(ph[i].x), wrap_rad(ph[i].y));
-        }
-      }
-      const float2 sB2 = make_float2(sigB, sigB), sC2 = make_float2(sigC, sigC);
-      if constexpr (R == 1) {
-        // sigma (B + bias) = fma(sigma, B, sigma bias), exact for a power-of-two
-        // sigma, so the scale rides on the bias add instead of on cos and sin
-        const float4 bq = *reinterpret_cast<const float4*>(&s_biasT[0][0][4 * kk2]);
-        const float2 bs0 = mul2(sB2, make_float2(bq.x, bq.z)), bs1 = mul2(sB2, make_float2(bq.y, bq.w));
-        float2 cs0 = make_float2(0.f, 0.f), cs1 = cs0;
-        if constexpr (!SO) {
-          const float4 cq = *reinterpret_cast<const float4*>(&s_biasT[1][0][4 * kk2]);
-          cs0 = mul2(sC2, make_float2(cq.x, cq.z));
-          cs1 = mul2(sC2, make_float2(cq.y, cq.w));
-        }
-#pragma unroll
-        for (int i = 0; i < TPG; ++i) {
-          float2 sn, cs;
-          __sincosf(ph[i].x, &sn.x, &cs.x);
-          __sincosf(ph[i].y, &sn.y, &cs.y);
-          const float2 nsn = make_float2(-sn.x, -sn.y);
-          const int t = tg * TPG + i;
-          // .x holds pair k0 (rows 4kk2, 4kk2 + 1), .y pair k0 + 1
-          const float2 b0 = fma2(sB2, make_float2(bf_at(bw[i], 0), bf_at(bw[i], 2)), bs0);
-          const float2 b1 = fma2(sB2, make_float2(bf_at(bw[i], 1), bf_at(bw[i], 3)), bs1);
-          // Rot(-Phi) = [[cos, sin], [-sin, cos]]
-          const float2 bt0 = fma2(cs, b0, mul2(sn, b1)), bt1 = fma2(cs, b1, mul2(nsn, b0));
-          const uint32_t o = tile_off((uint32_t)t, 4u * kk2, 64u);
-          sts64(opb + K::kOpBt + o, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
-          if constexpr (!SO) {
-            const float2 c0 = fma2(sC2, make_float2(bf_at(cw[i], 0), bf_at(cw[i], 2)), cs0);
-            const float2 c1 = fma2(sC2, make_float2(bf_at(cw[i], 1), bf_at(cw[i], 3)), cs1);
-            const float2 ct0 = fma2(cs, c0, mul2(sn, c1)), ct1 = fma2(cs, c1, mul2(nsn, c0));
-            sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
-          }
-        }
-      } else if constexpr (TPG <= 2) {
-        // few tokens per thread (R = 4): every rank's bias row is loaded once
-        // and applied to the thread's tokens, whose cos / sin are kept
-        float2 csB[TPG], snB[TPG], nsnB[TPG], csC[TPG], snC[TPG], nsnC[TPG];
-#pragma unroll
-        for (int i = 0; i < TPG; ++i) {
-          float2 sn, cs;
-          __sincosf(ph[i].x, &sn.x, &cs.x);
-          __sincosf(ph[i].y, &sn.y, &cs.y);
-          csB[i] = mul2(cs, sB2);
-          snB[i] = mul2(sn, sB2);
-          nsnB[i] = make_float2(-snB[i].x, -snB[i].y);
-          csC[i] = mul2(cs, sC2);
-          snC[i] = mul2(sn, sC2);
-          nsnC[i] = make_float2(-snC[i].x, -snC[i].y);
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float4 bq = *reinterpret_cast<const float4*>(&s_biasT[0][r][4 * kk2]);
-          float4 cq = bq;
-          if constexpr (!SO) cq = *reinterpret_cast<const float4*>(&s_biasT[1][r][4 * kk2]);
-#pragma unroll
-          for (int i = 0; i < TPG; ++i) {
-            const int t = tg * TPG + i;
-            float2 b0 = make_float2(bf_at(bw[i], 0 * R + r), bf_at(bw[i], 2 * R + r));
-            float2 b1 = make_float2(bf_at(bw[i], 1 * R + r), bf_at(bw[i], 3 * R + r));
-            b0 = add2(b0, make_float2(bq.x, bq.z));
-            b1 = add2(b1, make_float2(bq.y, bq.w));
-            const float2 bt0 = fma2(csB[i], b0, mul2(snB[i], b1));
-            const float2 bt1 = fma2(csB[i], b1, mul2(nsnB[i], b0));
-            const uint32_t o = tile_off((uint32_t)(t * R + r), 4u * kk2, 64u);
-            sts64(opb + K::kOpBt + o, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
-            if constexpr (!SO) {
-              float2 c0 = make_float2(bf_at(cw[i], 0 * R + r), bf_at(cw[i], 2 * R + r));
-              float2 c1 = make_float2(bf_at(cw[i], 1 * R + r), bf_at(cw[i], 3 * R + r));
-              c0 = add2(c0, make_float2(cq.x, cq.z));
-              c1 = add2(c1, make_float2(cq.y, cq.w));
-              const float2 ct0 = fma2(csC[i], c0, mul2(snC[i], c1));
-              const float2 ct1 = fma2(csC[i], c1, mul2(nsnC[i], c0));
-              sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < TPG; ++i) {
-          float2 sn, cs;
-          __sincosf(ph[i].x, &sn.x, &cs.x);
-          __sincosf(ph[i].y, &sn.y, &cs.y);
-          const float2 csB = mul2(cs, sB2), snB = mul2(sn, sB2);
-          const float2 csC = mul2(cs, sC2), snC = mul2(sn, sC2);
-          const float2 nsnB = make_float2(-snB.x, -snB.y), nsnC = make_float2(-snC.x, -snC.y);
-          const int t = tg * TPG + i;
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            // elements (n, r) for n = 4kk2 + e; .x holds pair k0 (e = 0, 1), .y pair k0+1 (e = 2, 3)
-            const float4 bq = *reinterpret_cast<const float4*>(&s_biasT[0][r][4 * kk2]);
-            float2 b0 = make_float2(bf_at(bw[i], 0 * R + r), bf_at(bw[i], 2 * R + r));
-            float2 b1 = make_float2(bf_at(bw[i], 1 * R + r), bf_at(bw[i], 3 * R + r));
-            b0 = add2(b0, make_float2(bq.x, bq.z));
-            b1 = add2(b1, make_float2(bq.y, bq.w));
-            // Rot(-Phi) = [[cos, sin], [-sin, cos]]
-            const float2 bt0 = fma2(csB, b0, mul2(snB, b1)), bt1 = fma2(csB, b1, mul2(nsnB, b0));
-            const uint32_t o = tile_off((uint32_t)(t * R + r), 4u * kk2, 64u);
-            sts64(opb + K::kOpBt + o, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
-            if constexpr (!SO) {
-              const float4 cq = *reinterpret_cast<const float4*>(&s_biasT[1][r][4 * kk2]);
-              float2 c0 = make_float2(bf_at(cw[i], 0 * R + r), bf_at(cw[i], 2 * R + r));
-              float2 c1 = make_float2(bf_at(cw[i], 1 * R + r), bf_at(cw[i], 3 * R + r));
-              c0 = add2(c0, make_float2(cq.x, cq.z));
-              c1 = add2(c1, make_float2(cq.y, cq.w));
-              const float2 ct0 = fma2(csC, c0, mul2(snC, c1)), ct1 = fma2(csC, c1, mul2(nsnC, c0));
-              sts64(opb + K::kOpCt + o, pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
-            }
-          }
-        }
-      }
-      // 6. w X (fp16, scaled) and X as the [(token, rank)][p] bf16 operand
-#pragma unroll
-      for (int j = 0; j < kXItems; ++j) {
-        const int it = tid + kProThreads * j;
-        if constexpr (R == 1) {
-          // the raw tile is already 128-byte swizzled [token][p]: same offsets
-          const uint32_t row = (uint32_t)it >> 3;
-          const float w = sc.wend[row] * sigX;
-          const uint4 v = xv[j][0];
-          if constexpr (!SO) sts128(opb + K::kOpXo + (uint32_t)it * 16u, v);
-          sts128(opb + K::kOpXw + (uint32_t)it * 16u,
-                 make_uint4(pack_f16(w * bf_lo(v.x), w * bf_hi(v.x)),
-                            pack_f16(w * bf_lo(v.y), w * bf_hi(v.y)),
-                            pack_f16(w * bf_lo(v.z), w * bf_hi(v.z)),
-                            pack_f16(w * bf_lo(v.w), w * bf_hi(v.w))));
-        } else {
-          const int sx = it / (kP / 4), pb = it % (kP / 4);
-          uint32_t wv[2 * R];
-#pragma unroll
-          for (int q = 0; q < kXVec; ++q) {
-            wv[4 * q] = xv[j][q].x; wv[4 * q + 1] = xv[j][q].y;
-            wv[4 * q + 2] = xv[j][q].z; wv[4 * q + 3] = xv[j][q].w;
-          }
-          const float w = sc.wend[sx] * sigX;
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            float v4[4];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) v4[q4] = bf_at(wv, q4 * R + r);
-            const uint32_t o = sw128((uint32_t)(sx * R + r), 4u * pb);
-            if constexpr (!SO) sts64(opb + K::kOpXo + o, pack_bf16(v4[0], v4[1]), pack_bf16(v4[2], v4[3]));
-            sts64(opb + K::kOpXw + o, pack_f16(w * v4[0], w * v4[1]), pack_f16(w * v4[2], w * v4[3]));
-          }
-        }
-      }
-      // 7. S = Ct Bt^T and D = Bt^T (w X) of this chunk into TMEM set s (free
-      // since the core released slot s), then publish the slot to the core
-      ptx::fence_proxy_async_smem();
-      ptx::named_bar_sync(kBarPro, kProThreads);
-      // (S and D from two warps, so that the two issue sequences overlap)
-      if ((!SO && tid == kSTid) || tid == kDTid) {
-        const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
-        ptx::tc_fence_after_sync();
-        if (tid == kDTid) {
-          const Desc dBm = make_desc(opb + K::kOpBt, 64u * 128u);
-          const Desc dXw = make_desc(opb + K::kOpXw, 64u * 128u);
-#pragma unroll
-          for (int kk = 0; kk < kQR / 16; ++kk)
-            ptx::mma_bf16_ss(tset + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD,
-                             kk > 0);
-        } else {
-          const Desc dBk = make_desc(opb + K::kOpBt, 16u), dCk = make_desc(opb + K::kOpCt, 16u);
-#pragma unroll
-          for (int kk = 0; kk < NS / 16; ++kk)
-            ptx::mma_bf16_ss(tset + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
-                             kIdS, kk > 0);
-        }
-        ptx::mma_commit(&bar_acc_full[s]);
-        if (tid == kDTid) ptx::mbar_arrive(&bar_op_full[s]);
-      }
-      if (!has_next) break;
-      sch.next(p);  // = nxt, recomputed rather than kept live across the body
-    }
-    // on an early exit, let an issued load land before the CTA ends
-    if (tid == kTmaTid && inflight >= 0) ptx::mbar_wait(&bar_raw_full, (uint32_t)inflight, kWaitNs);
-  } else {
-    // ============================================================ core (+ MMA issue)
-    const int ct = tid - kProThreads;  // 0..127
-    const int quad = warp & 3;         // TMEM lane quadrant of this warp
-    const int half = (warp - kProWarps) >> 2;  // which 32-column half of the tiles it takes
-    const int cwarp = warp - kProWarps;        // 0 .. kCoreWarps - 1
-    float hreg[HR];
-    float h_inv_prev = 1.f;
-    float dsum = 0.f;  // log2 decay accumulated over the unit (state-only pass)
-    // state element (n, cb + j) of this thread's 16-column block `blk` is hreg[16 blk + j]
-    auto hpos = [&](int blk, uint32_t& n, uint32_t& cb) {
-      if constexpr (NS == 128) {
-        n = (uint32_t)(32 * quad + lane);  // M=128 accumulator layout: lane = row
-        cb = 32u * half + 16u * blk;
-      } else {
-        n = (uint32_t)(16 * quad + (lane & 15));  // M=64 layout: 16 rows per quadrant
-        cb = 32u * half + 16u * (lane >> 4);
-      }
-    };
-    // fp16 copy of sigma * hreg into the state tile (operand of the next Yoff)
-    auto write_hcopy = [&](float h_sig) {
-      const float2 hs2 = make_float2(h_sig, h_sig);
-#pragma unroll
-      for (int blk = 0; blk < HR / 16; ++blk) {
-        uint32_t n, cb;
-        hpos(blk, n, cb);
-        uint32_t wv[8];
-#pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const float2 v = mul2(hs2, make_float2(hreg[16 * blk + j], hreg[16 * blk + j + 1]));
-          wv[j >> 1] = pack_f16(v.x, v.y);
-        }
-        sts128(sbase + K::kH + sw128(n, cb), make_uint4(wv[0], wv[1], wv[2], wv[3]));
-        sts128(sbase + K::kH + sw128(n, cb + 8u), make_uint4(wv[4], wv[5], wv[6], wv[7]));
-      }
-    };
-    // Yoff = Ct H of chunk g into set g & 1 (this thread's next commit, after
-    // the chunk's Y, covers it)
-    auto issue_yoff = [&](int g) {
-      const int s = g & 1;
-      const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
-      const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
-      const Desc dCk = make_desc(opb + K::kOpCt, 16u), dH = make_desc(sbase + K::kH, (uint32_t)NS * 128u);
-      ptx::tc_fence_after_sync();
-#pragma unroll
-      for (int kk = 0; kk < NS / 16; ++kk)
-        ptx::mma_bf16_ss(tset + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)), kIdYo,
-                         kk > 0);
-    };
-    // State entering unit u: the given explicit-frame state (the unit's local
-    // angle frame starts at zero, so no rotation) or zero; in the full pass its
-    // fp16 copy feeds the unit's first Yoff.
-    auto enter_unit = [&](int64_t u) {
-      dsum = 0.f;
       if (p.ws_hin) {
-        const float* src = p.ws_hin + u * (int64_t)NS * kP;
-        float m = 0.f;
+        // the given explicit-frame state (the unit's angle frame starts at
+        // zero, so no rotation) goes into TMEM as it is; the full pass also
+        // writes its fp16 copy for the first chunk's Yoff
+        const float* src = p.ws_hin + (int64_t)sch.unit * NS * kP;
 #pragma unroll
         for (int blk = 0; blk < HR / 16; ++blk) {
           uint32_t n, cb;
@@ -991,301 +638,614 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float4 v = q4[j];
-            hreg[16 * blk + 4 * j] = v.x;
-            hreg[16 * blk + 4 * j + 1] = v.y;
-            hreg[16 * blk + 4 * j + 2] = v.z;
-            hreg[16 * blk + 4 * j + 3] = v.w;
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            hv[16 * blk + 4 * j] = v.x;
+            hv[16 * blk + 4 * j + 1] = v.y;
+            hv[16 * blk + 4 * j + 2] = v.z;
+            hv[16 * blk + 4 * j + 3] = v.w;
           }
         }
+        state_st(hv);
+        has_state = true;
         if constexpr (!SO) {
-          m = warp_max(m);
-          if (lane == 0) s_hred[cwarp] = m;
-          ptx::named_bar_sync(kBarCore, kCoreThreads);
+          const float m = warp_max(abs_max(hv));
+          if (lane == 0) s_red[warp] = m;
+          __syncthreads();
           float mm = 0.f;
 #pragma unroll
-          for (int w = 0; w < kCoreWarps; ++w) mm = fmaxf(mm, s_hred[w]);
+          for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_red[w]);
           float h_sig;
           pow2_scale(mm, &h_sig, &h_inv_prev);
-          write_hcopy(h_sig);
-          ptx::fence_proxy_async_smem();
-          ptx::tc_fence_before_sync();
-          ptx::named_bar_sync(kBarCore, kCoreThreads);
+          write_hcopy(hv, h_sig);
+          yoff_ready = true;
+          // the block barrier before the MMA issue orders these writes
+        }
+      }
+    }
+
+    // ================================================= fold, part 1
+    // every thread waits for this chunk's raw tiles itself
+    if (wait_or_abort(&bar_raw, (uint32_t)(g & 1), &abort_flag, p.status) && tid == 0)
+      raw_pending = -1;
+    // raw B, C tiles -> registers
+    uint32_t bw[TPG][K::BW], cw[TPG][K::BW];
+    uint32_t bacc = 0u, cacc = 0u;
+#pragma unroll
+    for (int i = 0; i < TPG; ++i) {
+      const int t = tg * TPG + i;
+      const uint32_t ob = (uint32_t)(t * NS * R + 4 * kk2 * R) * 2u;
+      if constexpr (R == 1) {
+        const uint2 vb = lds64(sbase + K::kRawB + ob);
+        bw[i][0] = vb.x;
+        bw[i][1] = vb.y;
+        if constexpr (!SO) {
+          const uint2 vc = lds64(sbase + K::kRawC + ob);
+          cw[i][0] = vc.x;
+          cw[i][1] = vc.y;
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < HR; ++i) hreg[i] = 0.f;
+        for (int q = 0; q < K::BW / 4; ++q) {
+          const uint4 vb = lds128(sbase + K::kRawB + ob + 16u * q);
+          bw[i][4 * q] = vb.x; bw[i][4 * q + 1] = vb.y; bw[i][4 * q + 2] = vb.z; bw[i][4 * q + 3] = vb.w;
+          if constexpr (!SO) {
+            const uint4 vc = lds128(sbase + K::kRawC + ob + 16u * q);
+            cw[i][4 * q] = vc.x; cw[i][4 * q + 1] = vc.y; cw[i][4 * q + 2] = vc.z; cw[i][4 * q + 3] = vc.w;
+          }
+        }
       }
-    };
-    Sched sch;
-    sch.start(blockIdx.x, p);
-    enter_unit(sch.unit);
-    if (!SO && p.ws_hin && ct == 0 && wait_or_abort(&bar_op_full[0], 0u, &abort_flag, p.status))
-      issue_yoff(0);
-    for (int g = 0;; ++g) {
-      const int b = sch.b, h = sch.h;
-      const int c = sch.c, s = g & 1;
-      const bool first = c == sch.c_begin, last = c == sch.c_end - 1;
-      const bool has_next = sch.c + 1 < sch.c_end || sch.unit + (int)gridDim.x < p.nunits;
-      const SlotScalars<KP>& sc = ss[s];
-      const uint32_t tset = tmem + (uint32_t)s * kTmemSlot;
-      if (ct == 0)
-        s_go[1] = wait_or_abort(&bar_acc_full[s], (uint32_t)((g >> 1) & 1), &abort_flag, p.status)
-                      ? 1 : 0;
-      ptx::named_bar_sync(kBarCore, kCoreThreads);
-      if (!s_go[1]) break;
+    }
+#pragma unroll
+    for (int i = 0; i < TPG; ++i) {
+#pragma unroll
+      for (int q = 0; q < K::BW; ++q) {
+        bacc = ptx::bf16x2_absmax(bacc, bw[i][q]);
+        if constexpr (!SO) cacc = ptx::bf16x2_absmax(cacc, cw[i][q]);
+      }
+    }
+    // x of this chunk -> registers (w X and the operand copy of X)
+    constexpr int kXItems = (R == 1) ? 2 : (Q * (kP / 4)) / kThreads;
+    constexpr int kXVec = (R == 1) ? 1 : R / 2;
+    uint4 xv[kXItems][kXVec];
+    uint32_t xacc = 0u;
+#pragma unroll
+    for (int j = 0; j < kXItems; ++j) {
+      const int it = tid + kThreads * j;
+      if constexpr (R == 1) {
+        xv[j][0] = lds128(sbase + K::kRawX + (uint32_t)it * 16u);  // 16-byte chunk, row it / 8
+      } else {
+        const int sx = it / (kP / 4), pb = it % (kP / 4);
+        const uint32_t src = sbase + K::kRawX + (uint32_t)(sx * kP * R + 4 * pb * R) * 2u;
+#pragma unroll
+        for (int q = 0; q < kXVec; ++q) xv[j][q] = lds128(src + 16u * q);
+      }
+#pragma unroll
+      for (int q = 0; q < kXVec; ++q) {
+        xacc = ptx::bf16x2_absmax(xacc, xv[j][q].x);
+        xacc = ptx::bf16x2_absmax(xacc, xv[j][q].y);
+        xacc = ptx::bf16x2_absmax(xacc, xv[j][q].z);
+        xacc = ptx::bf16x2_absmax(xacc, xv[j][q].w);
+      }
+    }
+    // per-token-group angle sums (pairs k0, k0 + 1)
+    float2 ph[TPG];
+    {
+      float2 run = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < TPG; ++i) {
+        const float d = sc.dt[tg * TPG + i];
+        run = fma2(make_float2(d, d), th[i], run);
+        ph[i] = run;
+      }
+      *reinterpret_cast<float2*>(&s_tot[tg][k0]) = run;
+    }
+    {
+      // non-negative floats order like their bit patterns
+      const float bm = warp_max(bf_absmax(bacc)), cm = warp_max(bf_absmax(cacc));
+      const float xm = warp_max(bf_absmax(xacc));
+      if (lane == 0) {
+        atomicMax(&s_max[g & 1][0], __float_as_uint(bm));
+        atomicMax(&s_max[g & 1][1], __float_as_uint(cm));
+        atomicMax(&s_max[g & 1][2], __float_as_uint(xm));
+      }
+    }
+    Sched nxt = sch;
+    if (has_next) nxt.next(p);
+    // the staging tile of the previous chunk's output (over w X) is free
+    if (!SO && R > 1 && tid == 0) ptx::tma_store_wait_read<0>();
+    __syncthreads();  // ------------------------------------------ fold A
+    if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+    ptx::tc_fence_after_sync();
+    // every read of the raw slot is done: refill it with the next chunk
+    if (has_next && tid == 0) {
+      issue_raw(nxt);
+      raw_pending = (g + 1) & 1;
+    }
+
+    // ================================================= fold, part 2
+    float sigB, invB, sigC, invC, sigX, invX;
+    {
+      const float mb = __uint_as_float(s_max[g & 1][0]);
+      const float mc = __uint_as_float(s_max[g & 1][1]);
+      const float mx = __uint_as_float(s_max[g & 1][2]);
+      // the other parity's words were read last chunk: clear them for the next
+      if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) s_max[(g + 1) & 1][i] = 0u;
+      }
+      // a rotated pair keeps its norm: |Rot(v)_i| <= sqrt(2) max|v| < 2 max|v|
+      pow2_scale(2.f * (mb + bmax_bias), &sigB, &invB);
+      pow2_scale(2.f * (mc + cmax_bias), &sigC, &invC);
+      pow2_scale(mx * sc.wmax, &sigX, &invX);
+      if (tid == 0) {
+        sc.invB = invB;
+        sc.invC = invC;
+        sc.invX = invX;
+      }
+    }
+    // angle before this thread's first token: carry + earlier groups. Within
+    // the chunk an fp32 offset suffices; the carry to the next chunk is
+    // float-float so that it does not drift.
+    const int cpar = g & 1;
+    {
+      float2 o = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < TG - 1; ++q) {
+        const float2 v = *reinterpret_cast<const float2*>(&s_tot[q][k0]);
+        if (q < tg) o = add2(o, v);
+      }
+      float ch0 = 0.f, cl0 = 0.f, ch1 = 0.f, cl1 = 0.f;
+      if (!first) {
+        ch0 = s_carry[cpar][0][k0];
+        cl0 = s_carry[cpar][1][k0];
+        ch1 = s_carry[cpar][0][k0 + 1];
+        cl1 = s_carry[cpar][1][k0 + 1];
+      }
+      const float2 off = make_float2(wrap_rad(ch0 + (cl0 + o.x)), wrap_rad(ch1 + (cl1 + o.y)));
+      // the carry of pair k0 is updated by group TG-1, that of k0+1 by TG-2
+      if (tg >= TG - 2) {
+        const int k = (tg == TG - 1) ? k0 : k0 + 1;
+        // float-float sum of the group totals as a tree, then the carry
+        float thh[TG], tll[TG];
+#pragma unroll
+        for (int q = 0; q < TG; ++q) {
+          thh[q] = s_tot[q][k];
+          tll[q] = 0.f;
+        }
+#pragma unroll
+        for (int w = 1; w < TG; w <<= 1)
+#pragma unroll
+          for (int q = 0; q + w < TG; q += 2 * w) ff_add(thh[q], tll[q], thh[q + w], tll[q + w]);
+        float eh = (tg == TG - 1) ? ch0 : ch1, el = (tg == TG - 1) ? cl0 : cl1;
+        ff_add(eh, el, thh[0], tll[0]);
+        ff_wrap(eh, el);
+        s_carry[cpar ^ 1][0][k] = eh;
+        s_carry[cpar ^ 1][1][k] = el;
+        if (last) s_fang[k] = eh + el;
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < TPG; ++i) {
+        ph[i] = add2(off, ph[i]);
+        amax = fmaxf(amax, fmaxf(fabsf(ph[i].x), fabsf(ph[i].y)));
+      }
+      if (__any_sync(0xffffffffu, amax > kAngleDirect)) {
+#pragma unroll
+        for (int i = 0; i < TPG; ++i) ph[i] = make_float2(wrap_rad(ph[i].x), wrap_rad(ph[i].y));
+      }
+    }
+    // RoPE fold: sigma Rot(-Phi) (B + bias), likewise C, into fp16 tiles
+    const uint32_t opBt = sbase + K::kBt, opCt = sbase + K::kCt;
+    const float2 sB2 = make_float2(sigB, sigB), sC2 = make_float2(sigC, sigC);
+    if constexpr (R == 1) {
+      // sigma (B + bias) = fma(sigma, B, sigma bias), exact for a power-of-two
+      // sigma, so the scale rides on the bias add instead of on cos and sin
+      const int64_t ob = (int64_t)h * NS + 4 * kk2;
+      float4 bq[1], cq[1];
+      bq[0] = p.B_bias ? __ldg(reinterpret_cast<const float4*>(p.B_bias + ob))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      cq[0] = (!SO && p.C_bias) ? __ldg(reinterpret_cast<const float4*>(p.C_bias + ob))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float2 bs0 = mul2(sB2, make_float2(bq[0].x, bq[0].z));
+      const float2 bs1 = mul2(sB2, make_float2(bq[0].y, bq[0].w));
+      const float2 cs0 = mul2(sC2, make_float2(cq[0].x, cq[0].z));
+      const float2 cs1 = mul2(sC2, make_float2(cq[0].y, cq[0].w));
+#pragma unroll
+      for (int i = 0; i < TPG; ++i) {
+        float2 sn, cs;
+        __sincosf(ph[i].x, &sn.x, &cs.x);
+        __sincosf(ph[i].y, &sn.y, &cs.y);
+        const float2 nsn = make_float2(-sn.x, -sn.y);
+        // .x holds pair k0 (rows 4kk2, 4kk2 + 1), .y pair k0 + 1
+        const float2 b0 = fma2(sB2, make_float2(bf_at(bw[i], 0), bf_at(bw[i], 2)), bs0);
+        const float2 b1 = fma2(sB2, make_float2(bf_at(bw[i], 1), bf_at(bw[i], 3)), bs1);
+        // Rot(-Phi) = [[cos, sin], [-sin, cos]]
+        const float2 bt0 = fma2(cs, b0, mul2(sn, b1)), bt1 = fma2(cs, b1, mul2(nsn, b0));
+        const uint32_t a = (fold_base ^ ((uint32_t)(i & 7) << 4)) + (uint32_t)i * 128u;
+        sts64(a, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
+        if constexpr (!SO) {
+          const float2 c0 = fma2(sC2, make_float2(bf_at(cw[i], 0), bf_at(cw[i], 2)), cs0);
+          const float2 c1 = fma2(sC2, make_float2(bf_at(cw[i], 1), bf_at(cw[i], 3)), cs1);
+          const float2 ct0 = fma2(cs, c0, mul2(sn, c1)), ct1 = fma2(cs, c1, mul2(nsn, c0));
+          sts64(a + (K::kCt - K::kBt), pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
+        }
+      }
+    } else {
+      // R > 1: B, then C (one bias run live at a time). The thread's rows
+      // 4kk2 + e carry the head's bias [n][r]: float4 e holds row 4kk2 + e's R
+      // ranks (R = 4; for R = 2 a float4 holds two rows).
+      float2 csv[TPG], snv[TPG];
+#pragma unroll
+      for (int i = 0; i < TPG; ++i) {
+        __sincosf(ph[i].x, &snv[i].x, &csv[i].x);
+        __sincosf(ph[i].y, &snv[i].y, &csv[i].y);
+      }
+      const int64_t ob = ((int64_t)h * NS + 4 * kk2) * R;
+#pragma unroll
+      for (int pass = 0; pass < (SO ? 1 : 2); ++pass) {
+        const float* bias = pass == 0 ? p.B_bias : p.C_bias;
+        const uint32_t(&raw)[TPG][K::BW] = pass == 0 ? bw : cw;
+        const float2 s2 = pass == 0 ? sB2 : sC2;
+        float bv[4 * R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+          const float4 v = bias ? __ldg(reinterpret_cast<const float4*>(bias + ob) + q)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          bv[4 * q] = v.x; bv[4 * q + 1] = v.y; bv[4 * q + 2] = v.z; bv[4 * q + 3] = v.w;
+        }
+        float2 cs[TPG], sn[TPG], nsn[TPG];
+#pragma unroll
+        for (int i = 0; i < TPG; ++i) {
+          cs[i] = mul2(csv[i], s2);
+          sn[i] = mul2(snv[i], s2);
+          nsn[i] = make_float2(-sn[i].x, -sn[i].y);
+        }
+        const uint32_t dst = fold_base + (pass == 0 ? 0u : K::kCt - K::kBt);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          // bias of rows 4kk2 + e, rank r: element e * R + r of the run
+          const float2 bb0 = make_float2(bv[0 * R + r], bv[2 * R + r]);
+          const float2 bb1 = make_float2(bv[1 * R + r], bv[3 * R + r]);
+#pragma unroll
+          for (int i = 0; i < TPG; ++i) {
+            const float2 b0 = add2(make_float2(bf_at(raw[i], 0 * R + r), bf_at(raw[i], 2 * R + r)), bb0);
+            const float2 b1 = add2(make_float2(bf_at(raw[i], 1 * R + r), bf_at(raw[i], 3 * R + r)), bb1);
+            const float2 t0 = fma2(cs[i], b0, mul2(sn[i], b1));
+            const float2 t1 = fma2(cs[i], b1, mul2(nsn[i], b0));
+            const int l = i * R + r;
+            const uint32_t a = (dst ^ ((uint32_t)(l & 7) << 4)) + (uint32_t)l * 128u;
+            sts64(a, pack_f16(t0.x, t1.x), pack_f16(t0.y, t1.y));
+          }
+        }
+      }
+    }
+    // w X (fp16, scaled) and X as the [(token, rank)][p] bf16 operand
+#pragma unroll
+    for (int j = 0; j < kXItems; ++j) {
+      const int it = tid + kThreads * j;
+      if constexpr (R == 1) {
+        // the raw tile is already 128-byte swizzled [token][p]: same offsets
+        const uint32_t row = (uint32_t)it >> 3;
+        const float w = sc.wend[row] * sigX;
+        const uint4 v = xv[j][0];
+        const float2 w2 = make_float2(w, w);
+        if constexpr (!SO) sts128(sbase + K::kXo + (uint32_t)it * 16u, v);
+        const float2 p0 = mul2(w2, make_float2(bf_lo(v.x), bf_hi(v.x)));
+        const float2 p1 = mul2(w2, make_float2(bf_lo(v.y), bf_hi(v.y)));
+        const float2 p2 = mul2(w2, make_float2(bf_lo(v.z), bf_hi(v.z)));
+        const float2 p3 = mul2(w2, make_float2(bf_lo(v.w), bf_hi(v.w)));
+        sts128(sbase + K::kXw + (uint32_t)it * 16u,
+               make_uint4(pack_f16(p0.x, p0.y), pack_f16(p1.x, p1.y), pack_f16(p2.x, p2.y),
+                          pack_f16(p3.x, p3.y)));
+      } else {
+        const int sx = it / (kP / 4), pb = it % (kP / 4);
+        uint32_t wv[2 * R];
+#pragma unroll
+        for (int q = 0; q < kXVec; ++q) {
+          wv[4 * q] = xv[j][q].x; wv[4 * q + 1] = xv[j][q].y;
+          wv[4 * q + 2] = xv[j][q].z; wv[4 * q + 3] = xv[j][q].w;
+        }
+        const float w = sc.wend[sx] * sigX;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          float v4[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) v4[q4] = bf_at(wv, q4 * R + r);
+          const uint32_t o = sw128((uint32_t)(sx * R + r), 4u * pb);
+          if constexpr (!SO)
+            sts64(sbase + K::kXo + o, pack_bf16(v4[0], v4[1]), pack_bf16(v4[2], v4[3]));
+          sts64(sbase + K::kXw + o, pack_f16(w * v4[0], w * v4[1]), pack_f16(w * v4[2], w * v4[3]));
+        }
+      }
+    }
+    // the state in TMEM: rescale by exp(Lam_end) and the change of scale, so
+    // that D (in units of 1 / (sigma_B sigma_X)) accumulates onto it
+    if (has_state) {
+      if constexpr (SO) {
+        // the previous chunk's D must be complete (in the full pass the
+        // previous chunk's mask phase waited for it)
+        if (g > 0) wait_or_abort(&bar_ds, (uint32_t)((g - 1) & 1), &abort_flag, p.status);
+        ptx::tc_fence_after_sync();
+      }
+      state_ld(hv);
+      const float f = sc.eLend * (sigB * sigX) * u_prev;
+      const float2 f2 = make_float2(f, f);
+#pragma unroll
+      for (int i = 0; i < HR; i += 2) {
+        const float2 v = mul2(f2, make_float2(hv[i], hv[i + 1]));
+        hv[i] = v.x;
+        hv[i + 1] = v.y;
+      }
+      state_st(hv);
+    }
+    u_prev = invB * invX;
+    // the next chunk's theta and decay inputs (loads only; used next chunk)
+    if (has_next) {
+      load_theta<KP, TPG>(p, nxt, Q, tg, k0, th);
+      if (warp == 0) load_decay_raw(p, nxt, Q, lane, dr);
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before_sync();
+    __syncthreads();  // ------------------------------------------ fold B
+    if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+    if (tid == 0) {
+      // D = Bt^T (w X) onto the state; S = Ct Bt^T; Yoff = Ct H_in
       ptx::tc_fence_after_sync();
-      const float invB = sc.invB, invC = sc.invC, invX = sc.invX;
+      const Desc dBm = make_desc(opBt, 64u * 128u), dXw = make_desc(sbase + K::kXw, 64u * 128u);
+#pragma unroll
+      for (int kk = 0; kk < kQR / 16; ++kk)
+        ptx::mma_bf16_ss(tmem + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD,
+                         (has_state || kk > 0) ? 1u : 0u);
       if constexpr (!SO) {
-        // ---- masked scores: thread -> row a, 16 consecutive columns per block
+        const Desc dBk = make_desc(opBt, 16u), dCk = make_desc(opCt, 16u);
+#pragma unroll
+        for (int kk = 0; kk < NS / 16; ++kk)
+          ptx::mma_bf16_ss(tmem + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
+                           kIdS, kk > 0);
+      }
+      ptx::mma_commit(&bar_ds);
+      last_commit = &bar_ds;
+      last_parity = (uint32_t)(g & 1);
+      if constexpr (!SO) {
+        if (yoff_ready) {
+          const Desc dCk = make_desc(opCt, 16u), dH = make_desc(sbase + K::kH, (uint32_t)NS * 128u);
+#pragma unroll
+          for (int kk = 0; kk < NS / 16; ++kk)
+            ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)),
+                             kIdYo, kk > 0);
+        }
+        ptx::mma_commit(&bar_yo);
+        last_commit = &bar_yo;
+      }
+    }
+    has_state = true;
+
+    if constexpr (!SO) {
+      // ================================================= mask: P = S o Mask
+      wait_or_abort(&bar_ds, (uint32_t)(g & 1), &abort_flag, p.status);
+      ptx::tc_fence_after_sync();
+      {
+        // thread -> row a, 16 consecutive columns c0 .. c0 + 15 of this warp's half
         const int a = 16 * quad + (lane & 15);
         const int t = a / R;
-        const float einv = (float)((int)((__float_as_uint(invB * invC) >> 23) & 0xffu) - 127);
-        const float lt = sc.lam2[t] + einv;
-        const float gdiag = sc.gam[t] * (invB * invC);
-        // this warp's 32-column block; skip it when its 16 rows x 32 columns lie
-        // wholly above the diagonal
-        for (int blk = half; blk == half; ++blk) {
-          if ((32 * blk) / R > (16 * quad + 15) / R) continue;
-          uint32_t sv[16];
-          ptx::tmem_ld16_16x32bx2<16>(tset + kColS + ((uint32_t)(32 * quad) << 16) + 32u * blk, sv);
-          ptx::tmem_ld_wait(sv);
-          const int c0 = 32 * blk + 16 * (lane >> 4);
-          if (c0 / R > t) continue;
-          constexpr int NT = 16 / R;  // distinct tokens among the 16 columns
-          const int s0 = c0 / R;
-          float lsv[NT], wpv[NT];  // s0 is a multiple of NT >= 4: 16-byte aligned
+        const int c0 = 32 * half + 16 * (lane >> 4);
+        uint32_t ph_[8], pl_[8];
+        // a warp whose 16 rows x 32 columns lie wholly above the diagonal
+        // only writes zeros; elsewhere the mask itself zeroes s > t
+        if ((32 * half) / R > (16 * quad + 15) / R) {
 #pragma unroll
-          for (int u = 0; u < NT; u += 4) {
-            *reinterpret_cast<float4*>(&lsv[u]) = *reinterpret_cast<const float4*>(&sc.lam2[s0 + u]);
-            *reinterpret_cast<float4*>(&wpv[u]) = *reinterpret_cast<const float4*>(&sc.wp[s0 + u]);
+          for (int j = 0; j < 8; ++j) ph_[j] = pl_[j] = 0u;
+        } else {
+          uint32_t sv[16];
+          ptx::tmem_ld16_16x32bx2<16>(tmem + kColS + tq + 32u * half, sv);
+          ptx::tmem_ld_wait(sv);
+          {
+            const float invBC = sc.invB * sc.invC;
+            const float einv = (float)((int)((__float_as_uint(invBC) >> 23) & 0xffu) - 127);
+            const float lt = sc.lam2[t] + einv;
+            const float gdiag = sc.gam[t] * invBC;
+            constexpr int NT = 16 / R;  // distinct tokens among the 16 columns
+            const int s0 = c0 / R;
+            float lsv[NT], wpv[NT];  // s0 is a multiple of NT >= 4: 16-byte aligned
+#pragma unroll
+            for (int u = 0; u < NT; u += 4) {
+              *reinterpret_cast<float4*>(&lsv[u]) = *reinterpret_cast<const float4*>(&sc.lam2[s0 + u]);
+              *reinterpret_cast<float4*>(&wpv[u]) = *reinterpret_cast<const float4*>(&sc.wp[s0 + u]);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              // two columns at a time (packed fp32 pairs; same roundings as scalar)
+              const int u0 = j / R, u1 = (j + 1) / R;
+              const float2 dl = ptx::sub2(make_float2(lt, lt), make_float2(lsv[u0], lsv[u1]));
+              const float2 mo = mul2(make_float2(ex2(dl.x), ex2(dl.y)), make_float2(wpv[u0], wpv[u1]));
+              const float m0 = (s0 + u0 < t) ? mo.x : ((s0 + u0 == t) ? gdiag : 0.f);
+              const float m1 = (s0 + u1 < t) ? mo.y : ((s0 + u1 == t) ? gdiag : 0.f);
+              const float2 v2 = mul2(make_float2(m0, m1),
+                                     make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])));
+              const uint32_t hw = pack_bf16(v2.x, v2.y);
+              ph_[j >> 1] = hw;
+              const float2 lo = ptx::sub2(v2, make_float2(bf_lo(hw), bf_hi(hw)));
+              pl_[j >> 1] = pack_bf16(lo.x, lo.y);
+            }
           }
-          uint32_t ph_[8], pl_[8];
+        }
+        const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
+        const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
+        sts128(sbase + K::kPh + o0, make_uint4(ph_[0], ph_[1], ph_[2], ph_[3]));
+        sts128(sbase + K::kPh + o1, make_uint4(ph_[4], ph_[5], ph_[6], ph_[7]));
+        sts128(sbase + K::kPl + o0, make_uint4(pl_[0], pl_[1], pl_[2], pl_[3]));
+        sts128(sbase + K::kPl + o1, make_uint4(pl_[4], pl_[5], pl_[6], pl_[7]));
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before_sync();
+      __syncthreads();  // ------------------------------------------ mask
+      if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+      if (tid == 0) {
+        // Y = P X (P = high + low parts)
+        ptx::tc_fence_after_sync();
+        const Desc dPh = make_desc(sbase + K::kPh, 16u), dPl = make_desc(sbase + K::kPl, 16u);
+        const Desc dX = make_desc(sbase + K::kXo, 64u * 128u);
+#pragma unroll
+        for (int kk = 0; kk < kQR / 16; ++kk)
+          ptx::mma_bf16_ss(tmem + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
+                           kIdY, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kQR / 16; ++kk)
+          ptx::mma_bf16_ss(tmem + kColY, desc_at(dPl, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
+                           kIdY, 1u);
+        ptx::mma_commit(&bar_y);
+        last_commit = &bar_y;
+      }
+
+      // ================================================= state: bound and fp16 copy
+      ptx::tc_fence_after_sync();
+      state_ld(hv);
+      {
+        const float m = warp_max(abs_max(hv));
+        if (lane == 0) s_red[warp] = m;
+      }
+      __syncthreads();  // ------------------------------------------ state bound
+      if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+      const float uBX = invB * invX;  // the TMEM state is sigma_B sigma_X h
+      float h_inv = h_inv_prev;
+      if (!last) {
+        float m = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) m = fmaxf(m, s_red[w]);
+        float h_sig;
+        pow2_scale(m * uBX, &h_sig, &h_inv);
+        // this chunk's Yoff read the previous copy
+        wait_or_abort(&bar_yo, (uint32_t)(g & 1), &abort_flag, p.status);
+        write_hcopy(hv, uBX * h_sig);
+        ptx::fence_proxy_async_smem();
+      }
+
+      // ================================================= output: y = Y + exp(Lam_t) Yoff
+      wait_or_abort(&bar_y, (uint32_t)(g & 1), &abort_flag, p.status);
+      ptx::tc_fence_after_sync();
+      {
+        const int a = 16 * quad + (lane & 15);
+        const int c0 = 32 * half + 16 * (lane >> 4);  // first p of this thread
+        const float el = sc.eL[a / R] * (sc.invC * h_inv_prev);
+        uint32_t yv[16];
+        ptx::tmem_ld16_16x32bx2<16>(tmem + kColY + tq + 32u * half, yv);
+        ptx::tmem_ld_wait(yv);
+        float y[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[j] = __uint_as_float(yv[j]);
+        if (yoff_ready) {
+          uint32_t yo[16];
+          ptx::tmem_ld16_16x32bx2<16>(tmem + kColYo + tq + 32u * half, yo);
+          ptx::tmem_ld_wait(yo);
 #pragma unroll
           for (int j = 0; j < 16; j += 2) {
-            // two columns at a time (packed fp32 pairs; same roundings as scalar)
-            const int u0 = j / R, u1 = (j + 1) / R;
-            const float2 dl = sub2(make_float2(lt, lt), make_float2(lsv[u0], lsv[u1]));
-            const float2 mo = mul2(make_float2(ex2(dl.x), ex2(dl.y)), make_float2(wpv[u0], wpv[u1]));
-            const float m0 = (s0 + u0 < t) ? mo.x : ((s0 + u0 == t) ? gdiag : 0.f);
-            const float m1 = (s0 + u1 < t) ? mo.y : ((s0 + u1 == t) ? gdiag : 0.f);
-            const float2 v2 = mul2(make_float2(m0, m1),
-                                   make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])));
-            const uint32_t hw = pack_bf16(v2.x, v2.y);
-            ph_[j >> 1] = hw;
-            const float2 lo = sub2(v2, make_float2(bf_lo(hw), bf_hi(hw)));
-            pl_[j >> 1] = pack_bf16(lo.x, lo.y);
+            const float2 r2 = fma2(make_float2(el, el),
+                                   make_float2(__uint_as_float(yo[j]), __uint_as_float(yo[j + 1])),
+                                   make_float2(y[j], y[j + 1]));
+            y[j] = r2.x;
+            y[j + 1] = r2.y;
           }
-          const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
-          const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
-          sts128(sbase + K::kPh + o0, make_uint4(ph_[0], ph_[1], ph_[2], ph_[3]));
-          sts128(sbase + K::kPh + o1, make_uint4(ph_[4], ph_[5], ph_[6], ph_[7]));
-          sts128(sbase + K::kPl + o0, make_uint4(pl_[0], pl_[1], pl_[2], pl_[3]));
-          sts128(sbase + K::kPl + o1, make_uint4(pl_[4], pl_[5], pl_[6], pl_[7]));
         }
-        ptx::fence_proxy_async_smem();
-        ptx::named_bar_sync(kBarCore, kCoreThreads);
-        if (ct == 0) {
-          // Y = P X (P = high + low parts) of this chunk
-          const uint32_t opb = sbase + K::kOp0 + (uint32_t)s * K::kOpBytes;
-          const Desc dPh = make_desc(sbase + K::kPh, 16u), dPl = make_desc(sbase + K::kPl, 16u);
-          const Desc dX = make_desc(opb + K::kOpXo, 64u * 128u);
-          ptx::tc_fence_after_sync();
+        if constexpr (R == 1) {
+          const int64_t t = (int64_t)c * Q + a;
+          if (t < p.L) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + ((((int64_t)b * p.L + t) * p.H + h) * kP + c0));
+            dst[0] = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                                pack_bf16(y[6], y[7]));
+            dst[1] = make_uint4(pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
+                                pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15]));
+          }
+        } else {
+          // staging in the global layout of one chunk: [token][p][r]
+          const int t = a / R, r = a % R;
 #pragma unroll
-          for (int kk = 0; kk < kQR / 16; ++kk)
-            ptx::mma_bf16_ss(tset + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
-                             kIdY, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < kQR / 16; ++kk)
-            ptx::mma_bf16_ss(tset + kColY, desc_at(dPl, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
-                             kIdY, 1u);
-          ptx::mma_commit(&bar_y_full[s]);
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat16 v = __float2bfloat16_rn(y[j]);
+            sts16(sbase + K::kYs + (uint32_t)((t * kP + c0 + j) * R + r) * 2u,
+                  *reinterpret_cast<uint16_t*>(&v));
+          }
+          ptx::fence_proxy_async_smem();
         }
       }
-      // ---- state: H = exp(Lam_end) H + D / (sigma_B sigma_X)
-      float hmax = 0.f;
-      {
-        const float2 e2 = make_float2(sc.eLend, sc.eLend);
-        const float iBX = invB * invX;
-        const float2 i2 = make_float2(iBX, iBX);
+      h_inv_prev = h_inv;
+      yoff_ready = !last;
+    } else {
+      dsum += sc.lamend2;
+    }
+
+    if (last) {
+      if constexpr (SO) {
+        // the unit's local end state and its (log2 decay, angle) totals
+        wait_or_abort(&bar_ds, (uint32_t)(g & 1), &abort_flag, p.status);
+        ptx::tc_fence_after_sync();
+        state_ld(hv);
+        const float uBX = invB * invX;
+        float* dst = p.ws_state + sch.unit * (int64_t)NS * kP;
 #pragma unroll
         for (int blk = 0; blk < HR / 16; ++blk) {
-          uint32_t d[16];
-          if constexpr (NS == 128) {
-            ptx::tmem_ld16(tset + kColD + ((uint32_t)(32 * quad) << 16) + 32u * half + 16u * blk, d);
-          } else {
-            ptx::tmem_ld16_16x32bx2<16>(tset + kColD + ((uint32_t)(32 * quad) << 16) + 32u * half, d);
-          }
-          ptx::tmem_ld_wait(d);
+          uint32_t n, cb;
+          hpos(blk, n, cb);
+          float4* q4 = reinterpret_cast<float4*>(dst + (int64_t)n * kP + cb);
 #pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            float2 hv = mul2(e2, make_float2(hreg[16 * blk + j], hreg[16 * blk + j + 1]));
-            hv = fma2(i2, make_float2(__uint_as_float(d[j]), __uint_as_float(d[j + 1])), hv);
-            hreg[16 * blk + j] = hv.x;
-            hreg[16 * blk + j + 1] = hv.y;
-            if constexpr (!SO) hmax = fmaxf(hmax, fmaxf(fabsf(hv.x), fabsf(hv.y)));
+          for (int j = 0; j < 4; ++j)
+            q4[j] = make_float4(uBX * hv[16 * blk + 4 * j], uBX * hv[16 * blk + 4 * j + 1],
+                                uBX * hv[16 * blk + 4 * j + 2], uBX * hv[16 * blk + 4 * j + 3]);
+        }
+        float* sd = p.ws_scal + sch.unit * (int64_t)(1 + KP);
+        if (tid == 0) sd[0] = dsum;
+        if (tid < KP) sd[1 + tid] = s_fang[tid];
+      } else if (c == nC - 1 && p.final_state) {
+        // final state of the sequence, explicit frame: h = Rot(Phi_{L-1}) g
+        const float uBX = invB * invX;
+        float* fs = p.final_state + ((int64_t)b * p.heads + h) * NS * kP;
+#pragma unroll
+        for (int blk = 0; blk < HR / 16; ++blk) {
+          uint32_t n, cb;
+          hpos(blk, n, cb);
+          // the carried angle is wrapped to [-pi, pi]: the fast sincos is accurate there
+          float sn, cs;
+          __sincosf(s_fang[n >> 1], &sn, &cs);
+          const bool odd = n & 1;
+          float o[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float hvj = uBX * hv[16 * blk + j];
+            const float other = __shfl_xor_sync(0xffffffffu, hvj, 1);
+            // even row: c g0 - s g1 ; odd row: s g0 + c g1
+            o[j] = odd ? fmaf(sn, other, cs * hvj) : fmaf(-sn, other, cs * hvj);
           }
+          float4* dst = reinterpret_cast<float4*>(fs + (int64_t)n * kP + cb);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
         }
       }
-      if constexpr (SO) dsum += sc.lamend2;
-      bool next_issued = false;
-      if constexpr (!SO) {
-        hmax = warp_max(hmax);
-        if (lane == 0) s_hred[cwarp] = hmax;
-        // Y (and this chunk's Yoff, which read the previous state copy) complete;
-        // the output staging tile is free again
-        if (ct == 0) {
-          s_go[1] = wait_or_abort(&bar_y_full[s], (uint32_t)((g >> 1) & 1), &abort_flag, p.status)
-                        ? 1 : 0;
-          ptx::tma_store_wait_read<0>();
-        }
-        ptx::named_bar_sync(kBarCore, kCoreThreads);
-        if (!s_go[1]) break;
-        ptx::tc_fence_after_sync();
-        float h_inv = h_inv_prev;
-        if (!last) {
-          // fp16 copy of the new state for the next chunk's Ct H product
-          float m = 0.f;
-#pragma unroll
-          for (int w = 0; w < kCoreWarps; ++w) m = fmaxf(m, s_hred[w]);
-          float h_sig;
-          pow2_scale(m, &h_sig, &h_inv);
-          write_hcopy(h_sig);
-          ptx::fence_proxy_async_smem();
-          ptx::tc_fence_before_sync();
-          ptx::named_bar_sync(kBarCore, kCoreThreads);
-          // the next chunk's Yoff, if its operands are ready already
-          if (ct == 0 &&
-              ptx::mbar_try_wait(&bar_op_full[(g + 1) & 1], (uint32_t)(((g + 1) >> 1) & 1))) {
-            issue_yoff(g + 1);
-            next_issued = true;
-          }
-        }
-        // ---- outputs: y = Y + exp(Lam_t) Yoff
-        {
-          const int a = 16 * quad + (lane & 15);
-          const float el = sc.eL[a / R] * (invC * h_inv_prev);
-          const bool has_yoff = !first || p.ws_hin != nullptr;
-          for (int blk = half; blk == half; ++blk) {
-            uint32_t yv[16];
-            const uint32_t ta = ((uint32_t)(32 * quad) << 16) + 32u * blk;
-            ptx::tmem_ld16_16x32bx2<16>(tset + kColY + ta, yv);
-            ptx::tmem_ld_wait(yv);
-            const int c0 = 32 * blk + 16 * (lane >> 4);  // first p of this thread
-            float y[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = __uint_as_float(yv[j]);
-            if (has_yoff) {
-              // a unit that starts from a zero state has no Yoff for its first
-              // chunk (that accumulator was not written)
-              uint32_t yo[16];
-              ptx::tmem_ld16_16x32bx2<16>(tset + kColYo + ta, yo);
-              ptx::tmem_ld_wait(yo);
-#pragma unroll
-              for (int j = 0; j < 16; j += 2) {
-                const float2 r2 = fma2(make_float2(el, el),
-                                       make_float2(__uint_as_float(yo[j]), __uint_as_float(yo[j + 1])),
-                                       make_float2(y[j], y[j + 1]));
-                y[j] = r2.x;
-                y[j + 1] = r2.y;
-              }
-            }
-            if constexpr (R == 1) {
-              const uint32_t o0 = sw128((uint32_t)a, (uint32_t)c0);
-              const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
-              sts128(sbase + K::kYs + o0, make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
-                                                     pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7])));
-              sts128(sbase + K::kYs + o1,
-                     make_uint4(pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
-                                pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15])));
-            } else {
-              // staging in the global layout of one chunk: [token][p][r]
-              const int t = a / R, r = a % R;
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                __nv_bfloat16 v = __float2bfloat16_rn(y[j]);
-                sts16(sbase + K::kYs + (uint32_t)((t * kP + c0 + j) * R + r) * 2u,
-                      *reinterpret_cast<uint16_t*>(&v));
-              }
-            }
-          }
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before_sync();
-        ptx::named_bar_sync(kBarCore, kCoreThreads);
-        if (ct == 0) {
-          ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, h, c * Q, b);
-          ptx::tma_store_commit();
-        }
-        h_inv_prev = h_inv;
-      }
-      if (last) {
-        if constexpr (SO) {
-          // the unit's local end state and its (log2 decay, angle) totals
-          float* dst = p.ws_state + sch.unit * (int64_t)NS * kP;
-#pragma unroll
-          for (int blk = 0; blk < HR / 16; ++blk) {
-            uint32_t n, cb;
-            hpos(blk, n, cb);
-            float4* q4 = reinterpret_cast<float4*>(dst + (int64_t)n * kP + cb);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              q4[j] = make_float4(hreg[16 * blk + 4 * j], hreg[16 * blk + 4 * j + 1],
-                                  hreg[16 * blk + 4 * j + 2], hreg[16 * blk + 4 * j + 3]);
-          }
-          float* sd = p.ws_scal + sch.unit * (int64_t)(1 + KP);
-          if (ct == 0) sd[0] = dsum;
-          if (ct < KP) sd[1 + ct] = sc.fang[ct];
-        } else if (c == nC - 1 && p.final_state) {
-          // final state of the sequence, explicit frame: h = Rot(Phi_{L-1}) g
-          float* fs = p.final_state + ((int64_t)b * p.heads + h) * NS * kP;
-#pragma unroll
-          for (int blk = 0; blk < HR / 16; ++blk) {
-            uint32_t n, cb;
-            hpos(blk, n, cb);
-            // the carried angle is wrapped to [-pi, pi]: the fast sincos is
-            // accurate there (and keeps the accurate version's large slow path
-            // out of the loop's code)
-            float sn, cs;
-            __sincosf(sc.fang[n >> 1], &sn, &cs);
-            const bool odd = n & 1;
-            float o[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float hv = hreg[16 * blk + j];
-              const float other = __shfl_xor_sync(0xffffffffu, hv, 1);
-              // even row: c g0 - s g1 ; odd row: s g0 + c g1
-              o[j] = odd ? fmaf(sn, other, cs * hv) : fmaf(-sn, other, cs * hv);
-            }
-            float4* dst = reinterpret_cast<float4*>(fs + (int64_t)n * kP + cb);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-          }
-        }
-        if (has_next) enter_unit(sch.unit + (int)gridDim.x);
-      }
-      ptx::tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bar_slot_free[s]);
-      if constexpr (!SO) {
-        // the next chunk's Yoff if it could not go out above
-        const bool want_yoff = has_next && (!last || p.ws_hin != nullptr);
-        if (ct == 0 && want_yoff && !next_issued &&
-            wait_or_abort(&bar_op_full[(g + 1) & 1], (uint32_t)(((g + 1) >> 1) & 1), &abort_flag,
-                          p.status))
-          issue_yoff(g + 1);
-      }
-      if (!has_next) break;
-      sch.next(p);
     }
-    if (ct == 0) ptx::tma_store_wait_all<0>();
+    // the next chunk's decay scan
+    if (warp == 0 && has_next) decay_scan(dr, Q, lane, ss[(g + 1) & 1]);
+    ptx::tc_fence_before_sync();
+    __syncthreads();  // ------------------------------------------ end of chunk
+    if (!SO && R > 1 && tid == 0) {
+      ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, h, c * Q, b);
+      ptx::tma_store_commit();
+    }
+    if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+    if (!has_next) break;
+    sch = nxt;
   }
 
   // ---------------------------------------------------------------- teardown
+  if (tid == 0) {
+    // after an early exit, let issued copies and MMAs finish before the CTA
+    // ends (bounded waits): a load still in flight would land in shared
+    // memory the CTA no longer owns. After a normal exit these phases are
+    // complete already.
+    if (raw_pending >= 0) ptx::mbar_wait(&bar_raw, (uint32_t)raw_pending, kWaitNs);
+    if (last_commit) ptx::mbar_wait(last_commit, last_parity, kWaitNs);
+    if (!SO && R > 1) ptx::tma_store_wait_all<0>();
+  }
   ptx::tc_fence_before_sync();
   __syncthreads();
-  if (warp == kWarpTmem) {
+  if (warp == 0) {
     ptx::tc_fence_after_sync();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
@@ -1339,16 +1299,6 @@ bool make_bc_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
   cuuint64_t strides[4] = {d0 * 2, NR * 2, NR * 2 * a.G, NR * 2 * a.G * a.L};
   cuuint32_t box[5] = {(cuuint32_t)d0, (cuuint32_t)d1, 1, (cuuint32_t)a.Q, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, ptr, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-// theta [b, L, G, N/2] fp32 as {N/2, G, L, b}.
-bool make_theta_map(CUtensorMap* m, const float* ptr, const ScanArgs& a) {
-  const uint64_t KP = (uint64_t)a.N / 2;
-  cuuint64_t dims[4] = {KP, (cuuint64_t)a.G, (cuuint64_t)a.L, (cuuint64_t)a.batch};
-  cuuint64_t strides[3] = {KP * 4, KP * 4 * a.G, KP * 4 * a.G * a.L};
-  cuuint32_t box[4] = {(cuuint32_t)KP, 1, (cuuint32_t)a.Q, 1};
-  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -1449,26 +1399,50 @@ int device_sms() {
 template <int R, int NS, bool SO>
 cudaError_t launch_pass(const CUtensorMap* maps, const TcParams& p, int64_t units, cudaStream_t s) {
   constexpr uint32_t smem = Cfg<R, NS>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel<R, NS, SO>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = scan_tc_kernel<R, NS, SO>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // as much shared memory as the SM has, so that two CTAs fit
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   const int sms = num_sms();
   if (sms <= 0) return cudaErrorInvalidValue;
-  const unsigned grid = (unsigned)(units < sms ? units : sms);
-  scan_tc_kernel<R, NS, SO><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3],
-                                                          maps[4], p);
+  // CTAs per SM from the device's limits (shared memory with its per-CTA
+  // reservation, registers); each CTA holds 256 of the SM's 512 TMEM
+  // columns, so never more than two. Any count is correct: CTAs do not wait
+  // on one another.
+  int dev = 0, smem_sm = 0, smem_rsv = 0, regs_sm = 0;
+  cudaFuncAttributes fa;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+          cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+          cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) !=
+          cudaSuccess ||
+      (e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess)
+    return e;
+  const int64_t per_cta_smem = (int64_t)smem + (int64_t)fa.sharedSizeBytes + smem_rsv;
+  const int64_t per_cta_regs = (int64_t)((fa.numRegs + 7) / 8 * 8) * kThreads;
+  int64_t per_sm = per_cta_smem > 0 ? smem_sm / per_cta_smem : 1;
+  if (per_cta_regs > 0 && regs_sm / per_cta_regs < per_sm) per_sm = regs_sm / per_cta_regs;
+  per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
+  const int64_t slots = (int64_t)per_sm * sms;
+  const unsigned grid = (unsigned)(units < slots ? units : slots);
+  kern<<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
 }
 
 template <int R, int NS>
 cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
-  CUtensorMap maps[5];
+  // B, C, x and (R > 1: the output is stored by TMA) y
+  CUtensorMap maps[4];
   if (!make_bc_map(&maps[0], a.B, a) || !make_bc_map(&maps[1], a.C, a) ||
-      !make_theta_map(&maps[2], a.theta, a) || !make_act_map(&maps[3], a.x, a) ||
-      !make_act_map(&maps[4], a.out, a))
+      !make_act_map(&maps[2], a.x, a) || !make_act_map(&maps[3], R > 1 ? a.out : a.x, a))
     return cudaErrorInvalidValue;
   TcParams p;
-  p.dt = a.dt; p.A = a.A; p.lam = a.lam;
+  p.dt = a.dt; p.A = a.A; p.lam = a.lam; p.theta = a.theta;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
   p.B_bias = a.B_bias; p.C_bias = a.C_bias;
   p.final_state = a.final_state; p.status = status;
   p.L = a.L; p.H = a.H; p.G = a.G; p.batch = a.batch;

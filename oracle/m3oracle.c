@@ -41,6 +41,8 @@
  *                    metaphor-xennon blog, sec. 1.3 / 6.3; mask = decay x
  *                    2-band, papernotes.org sec. 1)
  * and a single decode step m3o_decode_step (the recurrence body for one t).
+ * m3o_bc_norm is BCNorm, the weightless RMS normalisation of B and C over N
+ * that the scan can apply to its raw B / C inputs before the bias.
  */
 #include <math.h>
 #include <stdint.h>
@@ -424,5 +426,31 @@ int m3o_decode_step(int64_t batch, int64_t H, int64_t G, int64_t P, int64_t N, i
       }
     free(Gm);
   }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* BCNorm: RMS normalisation of B (or C) over the state dimension N, per     */
+/* (batch, token, group, rank), with no learned weight:                      */
+/*   out[b,t,g,n,r] = in[b,t,g,n,r] / sqrt(mean_n in[b,t,g,n,r]^2 + eps)      */
+/* (papernotes.org, sec. 4: BC normalisation applied to the projected B and  */
+/* C, before the per-head B/C bias; bud-325 notes, key claims: BCNorm is an  */
+/* RMSNorm on the B/C activations). The scan then takes out as its B / C.    */
+/* ------------------------------------------------------------------------ */
+int m3o_bc_norm(int64_t batch, int64_t L, int64_t G, int64_t N, int64_t R, const double* in,
+                double* out, double eps) {
+  if (batch < 0 || L < 0 || G <= 0 || N <= 0 || R <= 0 || !(eps >= 0.0)) return 1;
+  for (int64_t b = 0; b < batch; ++b)
+    for (int64_t t = 0; t < L; ++t)
+      for (int64_t g = 0; g < G; ++g)
+        for (int64_t r = 0; r < R; ++r) {
+          double ss = 0.0;
+          for (int64_t n = 0; n < N; ++n) {
+            const double v = in[IX_BC(b, t, g, n, r)];
+            ss += v * v;
+          }
+          const double inv = 1.0 / sqrt(ss / (double)N + eps);
+          for (int64_t n = 0; n < N; ++n) out[IX_BC(b, t, g, n, r)] = in[IX_BC(b, t, g, n, r)] * inv;
+        }
   return 0;
 }

@@ -57,6 +57,8 @@ def _bind(path):
     lib.m3o_scan_chunked.restype = ctypes.c_int
     lib.m3o_decode_step.argtypes = [i64] * 6 + [dp] * 12 + [dp, ctypes.c_int]
     lib.m3o_decode_step.restype = ctypes.c_int
+    lib.m3o_bc_norm.argtypes = [i64] * 5 + [dp, dp, ctypes.c_double]
+    lib.m3o_bc_norm.restype = ctypes.c_int
     lib.m3o_max_threads.argtypes = []
     lib.m3o_max_threads.restype = ctypes.c_int
     return lib
@@ -125,6 +127,22 @@ def scan_chunked(x, dt, A, lam, B, C, theta, chunk, B_bias=None, C_bias=None, nt
     """Chunked SSD form with materialised intra-chunk mask; returns (y, final_state)."""
     return _scan("m3o_scan_chunked", x, dt, A, lam, B, C, theta, B_bias, C_bias,
                  chunk=int(chunk), nthreads=nthreads)
+
+
+BC_NORM_EPS = 1e-6
+
+
+def bc_norm(Bm, eps=BC_NORM_EPS, lib=None):
+    """BCNorm of B or C [b, L, G, N, R]: each (b, t, g, r) vector over N divided
+    by its root mean square (plus eps under the root), no weight. Returns a new
+    fp64 array; the scan with BCNorm is the scan of these normalised B and C."""
+    a = _f64(Bm)
+    b, L, G, N, R = a.shape
+    out = np.zeros_like(a)
+    rc = (lib or _load()).m3o_bc_norm(b, L, G, N, R, _ptr(a), _ptr(out), float(eps))
+    if rc != 0:
+        raise ValueError("m3o_bc_norm rejected its arguments")
+    return out
 
 
 def decode_step(state, x, dt, A, lam, B, C, theta, B_prev=None, x_prev=None,
@@ -196,6 +214,9 @@ class Oracle:
                      nthreads=0):
         return _scan("m3o_scan_chunked", x, dt, A, lam, B, C, theta, B_bias, C_bias,
                      chunk=int(chunk), nthreads=nthreads, lib=self._lib)
+
+    def bc_norm(self, Bm, eps=BC_NORM_EPS):
+        return bc_norm(Bm, eps, lib=self._lib)
 
 
 def build_variant(src_text: str, out_path: str) -> str:

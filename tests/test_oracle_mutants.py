@@ -14,6 +14,7 @@ from oracle import oracle
 
 SEQ_BEGIN = "int m3o_scan_seq("
 SEQ_END = "int m3o_scan_rope("
+BC_BEGIN = "int m3o_bc_norm("
 
 MUTANTS = {
     "beta_term_not_rotated": [
@@ -61,9 +62,29 @@ MUTANTS = {
     ],
 }
 
+# Mistakes planted in BCNorm (the normalisation of B and C over N).
+BC_MUTANTS = {
+    "bc_norm_without_root": [
+        ("const double inv = 1.0 / sqrt(ss / (double)N + eps);",
+         "const double inv = 1.0 / (ss / (double)N + eps);"),
+    ],
+    "bc_norm_sum_not_mean": [
+        ("const double inv = 1.0 / sqrt(ss / (double)N + eps);",
+         "const double inv = 1.0 / sqrt(ss + eps);"),
+    ],
+    "bc_norm_over_ranks": [
+        ("const double v = in[IX_BC(b, t, g, n, r)];", "const double v = in[IX_BC(b, t, g, n, 0)];"),
+    ],
+    "bc_norm_eps_outside_root": [
+        ("const double inv = 1.0 / sqrt(ss / (double)N + eps);",
+         "const double inv = 1.0 / (sqrt(ss / (double)N) + eps);"),
+    ],
+}
 
-def _mutate(src, edits):
-    i0, i1 = src.index(SEQ_BEGIN), src.index(SEQ_END)
+
+def _mutate(src, edits, begin=SEQ_BEGIN, end=SEQ_END):
+    i0 = src.index(begin)
+    i1 = src.index(end) if end else len(src)
     body = src[i0:i1]
     for old, new in edits:
         assert body.count(old) == 1, old
@@ -102,6 +123,26 @@ def test_mutant_is_caught(tmp_path, name):
     assert failed >= 1, "planted mistake %r passed every pin" % name
 
 
+def _run_bc_pins(orc):
+    failed = 0
+    for c in (pins.test_bc_norm_hand_fixture, pins.test_bc_norm_invariants,
+              pins.test_bc_norm_matches_the_input_recipe):
+        try:
+            c(orc)
+        except AssertionError:
+            failed += 1
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(BC_MUTANTS))
+def test_bc_norm_mutant_is_caught(tmp_path, name):
+    src = _mutate(oracle.source_text(), BC_MUTANTS[name], BC_BEGIN, None)
+    path = oracle.build_variant(src, os.path.join(str(tmp_path), "libmut_%s.so" % name))
+    assert _run_bc_pins(oracle.Oracle(path)) >= 1, "planted mistake %r passed every pin" % name
+
+
 def test_unmutated_source_passes_every_pin(tmp_path):
     path = oracle.build_variant(oracle.source_text(), os.path.join(str(tmp_path), "libsame.so"))
-    assert _run_pins(oracle.Oracle(path)) == 0
+    orc = oracle.Oracle(path)
+    assert _run_pins(orc) == 0
+    assert _run_bc_pins(orc) == 0

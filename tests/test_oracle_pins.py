@@ -398,3 +398,54 @@ def test_generator_is_bf16_exact_and_seeded():
     # ties to even: 1 + 2^-8 lies halfway between two bf16 values -> rounds to 1
     v = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8], np.float32)
     assert m3synth.to_bf16(v).tolist() == [1.0, 1.0 + 2.0 ** -6]
+
+
+# ---------------------------------------------------------------------------
+# BCNorm (papernotes.org sec. 4; bud-325 notes, key claims): RMS normalisation
+# over N per (b, t, g, r) with no weight, eps = 1e-6 under the root.
+# ---------------------------------------------------------------------------
+def _read_bc_fixture():
+    import math as m
+    vals = {}
+    with open(os.path.join(GOLDEN, "bc_norm_hand.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rhs = line.partition("=")
+            rows = [[eval(v, {"sqrt": m.sqrt}) for v in row.split(",")] for row in rhs.split(";")]
+            vals[key.strip()] = np.array(rows, dtype=np.float64)
+    return vals
+
+
+def test_bc_norm_hand_fixture(orc):
+    fx = _read_bc_fixture()
+    got = orc.bc_norm(fx["in"].reshape(1, 1, 1, 4, 2))
+    assert np.allclose(got.reshape(4, 2), fx["out"], rtol=1e-14, atol=0)
+
+
+def test_bc_norm_invariants(orc):
+    rng = np.random.default_rng(7)
+    v = rng.standard_normal((2, 5, 3, 16, 4)) * rng.uniform(0.01, 10.0, (2, 5, 3, 1, 4))
+    out = orc.bc_norm(v)
+    ms = np.mean(v * v, axis=3, keepdims=True)
+    # mean square of every normalised vector over N is ms / (ms + eps)
+    assert np.allclose(np.mean(out * out, axis=3, keepdims=True), ms / (ms + 1e-6), rtol=1e-12)
+    # direction is kept and each vector is normalised on its own: the ratio
+    # out / in is one positive constant per (b, t, g, r)
+    ratio = out / v
+    assert np.all(ratio > 0)
+    assert np.allclose(ratio, ratio[:, :, :, :1, :], rtol=1e-12)
+    # every rank is normalised on its own: R = 4 equals four R = 1 calls
+    for r in range(4):
+        assert np.allclose(orc.bc_norm(v[..., r:r + 1])[..., 0], out[..., r], rtol=1e-14)
+
+
+def test_bc_norm_matches_the_input_recipe(orc):
+    """The input generator's RMS normalisation (the workloads' recipe, written
+    separately) and the oracle's agree on the same raw draw."""
+    rng = np.random.Generator(np.random.PCG64(11))
+    raw = rng.standard_normal((2, 9, 1, 128, 4), dtype=np.float32)
+    rng = np.random.Generator(np.random.PCG64(11))
+    recipe = m3synth._bc(rng, (2, 9, 1, 128, 4), 128, rms=True)
+    assert np.allclose(orc.bc_norm(raw), recipe, rtol=2e-7, atol=0)

@@ -26,6 +26,7 @@ Printed on rank 0: one JSON line. Besides the contract keys it carries
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -76,10 +77,10 @@ def prefill_flops(s: m3synth.ScanShape) -> int:
     return s.batch * s.seqlen * s.heads * (2 * Q * R * R * (N + P) + 4 * R * N * P)
 
 
-def decode_bytes(s: m3synth.ScanShape) -> int:
-    """Per decode step: state read + write, plus the token's activations."""
+def decode_bytes(s: m3synth.ScanShape, act: int = 2) -> int:
+    """Per decode step: state read + write, plus the token's activations
+    (``act`` bytes per activation element)."""
     b, H, G, P, N, R = s.batch, s.heads, s.groups, s.headdim, s.dstate, s.R
-    act = 2
     return (2 * b * H * N * P * 4 + 3 * b * H * P * R * act + 3 * b * G * N * R * act
             + b * G * (N // 2) * 4 + 2 * b * H * 4)
 
@@ -324,6 +325,21 @@ def run_ours(args, rank, world, local_rank):
         if rank == 0:
             print(json.dumps(bench_prefill_long(torch, m3, dev, args, peaks)), flush=True)
         return
+    if args.only == "prefill_bcnorm":
+        if rank == 0:
+            print(json.dumps({k: bench_prefill_other(torch, m3, dev, w, args, peaks, bc_norm=True)
+                              for k, w in (("siso", "prefill_siso"),
+                                           ("mimo_r4", "prefill_mimo"))}), flush=True)
+        return
+    if args.only == "fp32_mode":
+        if rank == 0:
+            print(json.dumps({
+                "prefill_siso": bench_prefill_other(torch, m3, dev, "prefill_siso", args, peaks,
+                                                    fp32=True),
+                "decode_siso": bench_decode(torch, m3, dev, "decode_siso", peaks, fp32=True),
+                "decode_mimo_r4": bench_decode(torch, m3, dev, "decode_mimo", peaks,
+                                               fp32=True)}), flush=True)
+        return
     name = args.only if args.only in ("prefill_siso", "prefill_mimo") else "prefill_siso"
     idx, shape = m3synth.WORKLOADS[name]
     inp = m3synth.scan_inputs(shape, seed=rank_seed(idx, rank))
@@ -398,6 +414,15 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
         return
     line["prefill_mimo"] = bench_prefill_other(torch, m3, dev, "prefill_mimo", args, peaks)
+    line["prefill_bcnorm"] = {
+        "siso": bench_prefill_other(torch, m3, dev, "prefill_siso", args, peaks, bc_norm=True),
+        "mimo_r4": bench_prefill_other(torch, m3, dev, "prefill_mimo", args, peaks,
+                                       bc_norm=True)}
+    line["fp32_mode"] = {
+        "prefill_siso": bench_prefill_other(torch, m3, dev, "prefill_siso", args, peaks,
+                                            fp32=True),
+        "decode_siso": bench_decode(torch, m3, dev, "decode_siso", peaks, fp32=True),
+        "decode_mimo_r4": bench_decode(torch, m3, dev, "decode_mimo", peaks, fp32=True)}
     line["prefill_chunked"] = bench_prefill_chunked(torch, m3, dev, args)
     line["prefill_backward"] = bench_backward(torch, m3, dev)
     line["prefill_long"] = bench_prefill_long(torch, m3, dev, args, peaks)
@@ -417,10 +442,22 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def bench_prefill_other(torch, m3, dev, name, args, peaks):
+def bench_prefill_other(torch, m3, dev, name, args, peaks, bc_norm=False, fp32=False):
+    """One prefill workload timed like the headline. ``bc_norm``: B and C are
+    un-normalised (the recipe's vectors times a seeded per-vector scale) and
+    the call fuses BCNorm (M3_FLAG_BC_NORM). ``fp32``: fp32 activations, the
+    fp32 precision mode (CUDA-core kernel)."""
     idx, shape = m3synth.WORKLOADS[name]
+    if fp32:
+        shape = dataclasses.replace(shape, bf16=False)
     inp = m3synth.scan_inputs(shape, seed=idx)
-    d = to_device(inp, True, dev)
+    if bc_norm:
+        rng = np.random.default_rng(idx)
+        for k in ("B", "C"):
+            v = inp[k]
+            sc = rng.uniform(0.05, 20.0, size=v.shape[:3] + (1,) + v.shape[4:]).astype(np.float32)
+            inp[k] = m3synth.to_bf16(v * sc)
+    d = to_device(inp, not fp32, dev)
     out = torch.empty_like(d["x"])
     fs = torch.empty((shape.batch, shape.heads, shape.dstate, shape.headdim),
                      dtype=torch.float32, device=dev)
@@ -430,13 +467,14 @@ def bench_prefill_other(torch, m3, dev, name, args, peaks):
     def launch():
         m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"], R=shape.R,
                        chunk=shape.chunk, out=out, final_state=fs, B_bias=d["B_bias"],
-                       C_bias=d["C_bias"], stream=stream)
+                       C_bias=d["C_bias"], stream=stream, bc_norm=bc_norm)
 
+    steps = min(args.steps, 5) if fp32 else args.steps
     for _ in range(args.warmup):
         flush.zero_()
         launch()
     times = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -446,12 +484,19 @@ def bench_prefill_other(torch, m3, dev, name, args, peaks):
         times.append(e0.elapsed_time(e1))
     ms = sum(times) / len(times)
     nbytes, nflops = prefill_bytes(shape), prefill_flops(shape)
-    return {"workload": "%s b%d L%d H%d P%d N%d R%d chunk%d" % (
-                name, shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate,
-                shape.R, shape.chunk),
-            "tok_s": shape.tokens / (ms * 1e-3), "ms": ms,
-            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
-            "tensor_frac": nflops / (ms * 1e-3) / 1e12 / peaks["bf16"]}
+    r = {"workload": "%s b%d L%d H%d P%d N%d R%d chunk%d%s%s" % (
+             name, shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate,
+             shape.R, shape.chunk, ", fp32 activations" if fp32 else "",
+             ", un-normalised B/C with BCNorm fused" if bc_norm else ""),
+         "tok_s": shape.tokens / (ms * 1e-3), "ms": ms,
+         "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"]}
+    if fp32:
+        # the fp32 mode runs on the CUDA cores: its compute roof is the fp32 FMA peak
+        r["fp32_alu_frac"] = nflops / (ms * 1e-3) / 1e12 / FP32_PEAK_TFLOPS
+        r["kernel"] = "CUDA cores (fp32 arithmetic), one CTA per (b, h)"
+    else:
+        r["tensor_frac"] = nflops / (ms * 1e-3) / 1e12 / peaks["bf16"]
+    return r
 
 
 def bench_prefill_chunked(torch, m3, dev, args, pieces=2):
@@ -612,11 +657,15 @@ def bench_prefill_long(torch, m3, dev, args, peaks):
     return res
 
 
-def bench_decode(torch, m3, dev, name, peaks, n_sets=16, steps=m3synth.DECODE_STEPS):
+def bench_decode(torch, m3, dev, name, peaks, n_sets=16, steps=m3synth.DECODE_STEPS,
+                 fp32=False):
     """1024 decode steps captured in one CUDA graph; per-step inputs cycle over
-    ``n_sets`` seeded token sets (B_prev/x_prev are the previous set's)."""
+    ``n_sets`` seeded token sets (B_prev/x_prev are the previous set's).
+    ``fp32``: fp32 activations (the fp32 precision mode)."""
     idx, shape = m3synth.WORKLOADS[name]
-    sets = [to_device(m3synth.decode_inputs(shape, seed=idx, step=i), True, dev)
+    if fp32:
+        shape = dataclasses.replace(shape, bf16=False)
+    sets = [to_device(m3synth.decode_inputs(shape, seed=idx, step=i), not fp32, dev)
             for i in range(n_sets)]
     st = torch.zeros((shape.batch, shape.heads, shape.dstate, shape.headdim),
                      dtype=torch.float32, device=dev)
@@ -649,10 +698,11 @@ def bench_decode(torch, m3, dev, name, peaks, n_sets=16, steps=m3synth.DECODE_ST
     e1.record(cur)
     torch.cuda.synchronize()
     ms_step = e0.elapsed_time(e1) / (reps * steps)
-    nbytes = decode_bytes(shape)
+    nbytes = decode_bytes(shape, 4 if fp32 else 2)
     gbs = nbytes / (ms_step * 1e-3) / 1e9
-    return {"workload": "%s b%d H%d P%d N%d R%d, %d steps in one CUDA graph" % (
-                name, shape.batch, shape.heads, shape.headdim, shape.dstate, shape.R, steps),
+    return {"workload": "%s b%d H%d P%d N%d R%d, %d steps in one CUDA graph%s" % (
+                name, shape.batch, shape.heads, shape.headdim, shape.dstate, shape.R, steps,
+                ", fp32 activations" if fp32 else ""),
             "tok_s": shape.batch / (ms_step * 1e-3), "ms_per_step": ms_step,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm"], "algorithmic_bytes": nbytes},
@@ -804,7 +854,7 @@ def main():
     ap.add_argument("--only", default="all",
                     choices=["all", "prefill_siso", "prefill_mimo", "decode_siso", "decode_mimo",
                              "decode_tokens_siso", "decode_tokens_mimo", "prefill_long",
-                             "prefill_backward"],
+                             "prefill_backward", "prefill_bcnorm", "fp32_mode"],
                     help="run one workload alone (profiling); the default runs them all")
     ap.add_argument("--decode-steps", type=int, default=m3synth.DECODE_STEPS,
                     help="decode steps (or multi-token calls) per CUDA graph with --only decode_*")

@@ -63,6 +63,24 @@ typedef enum {
   M3_BF16 = 1 /* ... are bfloat16; dt, lambda, theta, A, biases and state stay fp32 */
 } m3_dtype;
 
+/*
+ * m3_dims.flags. Any other bit set is M3_ERR_INVALID_ARG.
+ *
+ * M3_FLAG_BC_NORM: B and C arrive un-normalised, and the prefill applies
+ * BCNorm to them itself, fused into its prologue: every (b, t, g, r) vector
+ * of B (and of C) over the N state rows is divided by its root mean square,
+ *   B[b,t,g,:,r] / sqrt(mean_n B[b,t,g,n,r]^2 + 1e-6),
+ * with no learned weight, before the per-head bias and the rotation
+ * (papernotes.org "Mamba-3: Improved Sequence Modeling using State Space
+ * Principles", sec. 4, BC normalisation and B/C bias; bud-325 notes, key
+ * claims). Supported by m3_scan_fwd and m3_scan_fwd_noalloc on the tensor-core
+ * path (bf16, P = 64, N in {64, 128}, chunk * R = 64, the alignments given
+ * there); every other call with it returns M3_ERR_UNSUPPORTED, as do
+ * m3_scan_fwd_state, the decode calls and m3_scan_bwd (normalise B and C
+ * before calling those).
+ */
+#define M3_FLAG_BC_NORM 1
+
 typedef struct {
   int64_t batch;   /* b  >= 0                                             */
   int64_t seqlen;  /* L  >= 0 (prefill); K (multi-token decode); ignored by decode */
@@ -71,7 +89,7 @@ typedef struct {
   int64_t headdim; /* P  >= 1                                             */
   int64_t dstate;  /* N  >= 2, even (N/2 rotating pairs)                  */
   int32_t act_dtype;  /* an m3_dtype                                      */
-  int32_t reserved;   /* must be 0                                        */
+  int32_t flags;      /* 0, or M3_FLAG_BC_NORM (prefill only, see below)  */
   const float* B_bias; /* [H, N, R] fp32 device pointer, or NULL (zero bias) */
   const float* C_bias; /* [H, N, R] fp32 device pointer, or NULL            */
   void* workspace;        /* device scratch for long sequences, or NULL     */

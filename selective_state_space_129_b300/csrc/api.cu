@@ -40,7 +40,7 @@ m3_status check_dims(const m3_dims* d, int R) {
   if (d->batch < 0 || d->heads < 1 || d->groups < 1 || d->headdim < 1 || d->dstate < 2)
     return M3_ERR_INVALID_ARG;
   if (d->dstate % 2 != 0 || d->heads % d->groups != 0) return M3_ERR_INVALID_ARG;
-  if (d->reserved != 0 || R < 1) return M3_ERR_INVALID_ARG;
+  if ((d->flags & ~M3_FLAG_BC_NORM) != 0 || R < 1) return M3_ERR_INVALID_ARG;
   if (d->act_dtype != M3_F32 && d->act_dtype != M3_BF16) return M3_ERR_UNSUPPORTED;
   if (d->heads > (1 << 20) || d->headdim > (1 << 20) || d->dstate > (1 << 20) || R > 1024)
     return M3_ERR_UNSUPPORTED;
@@ -183,6 +183,8 @@ m3_status scan_impl(const void* x, const float* dt, const float* A, const float*
                       (dims->B_bias == nullptr || aligned(dims->B_bias, 16)) &&
                       (dims->C_bias == nullptr || aligned(dims->C_bias, 16)) &&
                       (final_state == nullptr || aligned(final_state, 16));
+  const bool bc_norm = (dims->flags & M3_FLAG_BC_NORM) != 0;
+  if (bc_norm && (!use_tc || continue_state)) return M3_ERR_UNSUPPORTED;
   if (!use_tc) {
     const size_t smem = m3::scan_simt_smem_bytes(N, P, R, chunk);
     if (smem > 227 * 1024) return M3_ERR_UNSUPPORTED;
@@ -222,6 +224,7 @@ m3_status scan_impl(const void* x, const float* dt, const float* A, const float*
   a.h_init = continue_state ? final_state : nullptr;
   a.workspace = dims->workspace; a.workspace_bytes = dims->workspace_bytes;
   a.batch = b; a.L = L; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R; a.Q = chunk;
+  a.bc_norm = bc_norm;
   if (use_tc) {
     // a caller-provided workspace must be large enough; NULL means the
     // library allocates (stream-ordered) what it needs
@@ -262,6 +265,7 @@ m3_status m3_decode_step(float* state, const void* x, const float* dt, const flo
                          int R, void* out, void* stream) {
   m3_status st = check_dims(dims, R);
   if (st != M3_OK) return st;
+  if (dims->flags & M3_FLAG_BC_NORM) return M3_ERR_UNSUPPORTED;
   if ((B_prev == nullptr) != (x_prev == nullptr)) return M3_ERR_INVALID_ARG;
   const int64_t b = dims->batch, H = dims->heads, G = dims->groups, P = dims->headdim,
                 N = dims->dstate;
@@ -308,6 +312,7 @@ m3_status m3_decode_tokens(float* state, const void* x, const float* dt, const f
                            const m3_dims* dims, int R, void* out, void* stream) {
   m3_status st = check_dims(dims, R);
   if (st != M3_OK) return st;
+  if (dims->flags & M3_FLAG_BC_NORM) return M3_ERR_UNSUPPORTED;
   if (dims->seqlen < 0) return M3_ERR_INVALID_ARG;
   if ((B_prev == nullptr) != (x_prev == nullptr)) return M3_ERR_INVALID_ARG;
   const int64_t b = dims->batch, K = dims->seqlen, H = dims->heads, G = dims->groups,
@@ -359,6 +364,7 @@ m3_status m3_scan_bwd(const void* x, const float* dt, const float* A, const floa
                       float* dB_bias, float* dC_bias, void* stream) {
   m3_status st = check_dims(dims, R);
   if (st != M3_OK) return st;
+  if (dims->flags & M3_FLAG_BC_NORM) return M3_ERR_UNSUPPORTED;
   if (dims->seqlen < 0) return M3_ERR_INVALID_ARG;
   const int64_t b = dims->batch, L = dims->seqlen, H = dims->heads, G = dims->groups,
                 P = dims->headdim, N = dims->dstate;

@@ -26,6 +26,7 @@ struct ScanArgs {
   size_t workspace_bytes;
   int64_t batch, L, H, G, P, N;
   int R, Q;
+  bool bc_norm;  // B and C arrive un-normalised: BCNorm them in the prologue
 };
 
 struct DecodeArgs {

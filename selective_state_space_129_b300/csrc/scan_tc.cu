@@ -197,10 +197,12 @@ __device__ __forceinline__ float bf_absmax(uint32_t w) {
   return fmaxf(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
 }
 
-// Power of two sigma with M * sigma < 2^15 (inside fp16's range), and 1/sigma.
+// Power of two sigma with M * sigma < 2^15 (inside fp16's range), and 1/sigma;
+// sigma is at most 2^(14 - EMIN).
+template <int EMIN = -100>
 __device__ __forceinline__ void pow2_scale(float M, float* sigma, float* inv) {
   int e = (int)((__float_as_uint(M) >> 23) & 0xffu) - 127;  // M in [2^e, 2^(e+1))
-  e = e < -100 ? -100 : (e > 127 ? 127 : e);
+  e = e < EMIN ? EMIN : (e > 127 ? 127 : e);
   *sigma = __uint_as_float((uint32_t)(127 + 14 - e) << 23);
   *inv = __uint_as_float((uint32_t)(127 - 14 + e) << 23);
 }
@@ -413,8 +415,33 @@ __device__ __forceinline__ void load_theta(const TcParams& p, const Sched& u, in
   }
 }
 
+// Sum over the KP2 lanes that hold one token row (a whole warp for N = 128,
+// a half warp for N = 64).
+template <int KP2>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+  for (int o = KP2 / 2; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// BCNorm: the inverse root mean square over the N rows of element rank r of
+// one token's raw B (or C) words, this thread holding rows 4kk2 .. 4kk2 + 3.
+template <int R, int NS, int BW>
+__device__ __forceinline__ float bc_inv_rms(const uint32_t (&w)[BW], int r) {
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float v = bf_at(w, e * R + r);
+    ss = fmaf(v, v, ss);
+  }
+  ss = row_sum<NS / 4>(ss);
+  return rsqrtf(fmaf(ss, 1.f / NS, 1e-6f));
+}
+
 // SO: the state-only pass of a segmented scan (no C, no outputs).
-template <int R, int NS, bool SO>
+// NORM: B and C arrive un-normalised; BCNorm them here (each token's and
+// rank's vector over N divided by its root mean square), before the bias.
+template <int R, int NS, bool SO, bool NORM>
 __global__ void __launch_bounds__(kThreads, 2)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
                    const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
@@ -694,12 +721,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
+    if constexpr (!NORM) {
 #pragma unroll
-    for (int i = 0; i < TPG; ++i) {
+      for (int i = 0; i < TPG; ++i) {
 #pragma unroll
-      for (int q = 0; q < K::BW; ++q) {
-        bacc = ptx::bf16x2_absmax(bacc, bw[i][q]);
-        if constexpr (!SO) cacc = ptx::bf16x2_absmax(cacc, cw[i][q]);
+        for (int q = 0; q < K::BW; ++q) {
+          bacc = ptx::bf16x2_absmax(bacc, bw[i][q]);
+          if constexpr (!SO) cacc = ptx::bf16x2_absmax(cacc, cw[i][q]);
+        }
       }
     }
     // x of this chunk -> registers (w X and the operand copy of X)
@@ -772,10 +801,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int i = 0; i < 3; ++i) s_max[(g + 1) & 1][i] = 0u;
       }
-      // a rotated pair keeps its norm: |Rot(v)_i| <= sqrt(2) max|v| < 2 max|v|
-      pow2_scale(2.f * (mb + bmax_bias), &sigB, &invB);
-      pow2_scale(2.f * (mc + cmax_bias), &sigC, &invC);
-      pow2_scale(mx * sc.wmax, &sigX, &invX);
+      // a rotated pair keeps its norm: |Rot(v)_i| <= sqrt(2) max|v| < 2 max|v|;
+      // a BCNormed vector has every element below sqrt(N) in magnitude
+      constexpr float kNormBound = (NS == 128) ? 11.3137085f : 8.f;
+      // The state in TMEM is held in units of sigma_B sigma_X (the D MMA's):
+      // the tile scales are capped at 2^40, so that a chunk of zero or tiny
+      // inputs after large ones cannot inflate it beyond fp32's range (with
+      // the cap, elements above 2^-54 still keep fp16's full precision).
+      pow2_scale<-26>(2.f * ((NORM ? kNormBound : mb) + bmax_bias), &sigB, &invB);
+      pow2_scale<-26>(2.f * ((NORM ? kNormBound : mc) + cmax_bias), &sigC, &invC);
+      pow2_scale<-26>(mx * sc.wmax, &sigX, &invX);
       if (tid == 0) {
         sc.invB = invB;
         sc.invC = invC;
@@ -856,15 +891,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         __sincosf(ph[i].y, &sn.y, &cs.y);
         const float2 nsn = make_float2(-sn.x, -sn.y);
         // .x holds pair k0 (rows 4kk2, 4kk2 + 1), .y pair k0 + 1
-        const float2 b0 = fma2(sB2, make_float2(bf_at(bw[i], 0), bf_at(bw[i], 2)), bs0);
-        const float2 b1 = fma2(sB2, make_float2(bf_at(bw[i], 1), bf_at(bw[i], 3)), bs1);
+        float2 sBi = sB2;
+        if constexpr (NORM) {
+          const float v = sigB * bc_inv_rms<R, NS, K::BW>(bw[i], 0);
+          sBi = make_float2(v, v);
+        }
+        const float2 b0 = fma2(sBi, make_float2(bf_at(bw[i], 0), bf_at(bw[i], 2)), bs0);
+        const float2 b1 = fma2(sBi, make_float2(bf_at(bw[i], 1), bf_at(bw[i], 3)), bs1);
         // Rot(-Phi) = [[cos, sin], [-sin, cos]]
         const float2 bt0 = fma2(cs, b0, mul2(sn, b1)), bt1 = fma2(cs, b1, mul2(nsn, b0));
         const uint32_t a = (fold_base ^ ((uint32_t)(i & 7) << 4)) + (uint32_t)i * 128u;
         sts64(a, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
         if constexpr (!SO) {
-          const float2 c0 = fma2(sC2, make_float2(bf_at(cw[i], 0), bf_at(cw[i], 2)), cs0);
-          const float2 c1 = fma2(sC2, make_float2(bf_at(cw[i], 1), bf_at(cw[i], 3)), cs1);
+          float2 sCi = sC2;
+          if constexpr (NORM) {
+            const float v = sigC * bc_inv_rms<R, NS, K::BW>(cw[i], 0);
+            sCi = make_float2(v, v);
+          }
+          const float2 c0 = fma2(sCi, make_float2(bf_at(cw[i], 0), bf_at(cw[i], 2)), cs0);
+          const float2 c1 = fma2(sCi, make_float2(bf_at(cw[i], 1), bf_at(cw[i], 3)), cs1);
           const float2 ct0 = fma2(cs, c0, mul2(sn, c1)), ct1 = fma2(cs, c1, mul2(nsn, c0));
           sts64(a + (K::kCt - K::kBt), pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
         }
@@ -907,8 +952,17 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float2 bb1 = make_float2(bv[1 * R + r], bv[3 * R + r]);
 #pragma unroll
           for (int i = 0; i < TPG; ++i) {
-            const float2 b0 = add2(make_float2(bf_at(raw[i], 0 * R + r), bf_at(raw[i], 2 * R + r)), bb0);
-            const float2 b1 = add2(make_float2(bf_at(raw[i], 1 * R + r), bf_at(raw[i], 3 * R + r)), bb1);
+            const float2 v0 = make_float2(bf_at(raw[i], 0 * R + r), bf_at(raw[i], 2 * R + r));
+            const float2 v1 = make_float2(bf_at(raw[i], 1 * R + r), bf_at(raw[i], 3 * R + r));
+            float2 b0, b1;
+            if constexpr (NORM) {
+              const float rs = bc_inv_rms<R, NS, K::BW>(raw[i], r);
+              b0 = fma2(make_float2(rs, rs), v0, bb0);
+              b1 = fma2(make_float2(rs, rs), v1, bb1);
+            } else {
+              b0 = add2(v0, bb0);
+              b1 = add2(v1, bb1);
+            }
             const float2 t0 = fma2(cs[i], b0, mul2(sn[i], b1));
             const float2 t1 = fma2(cs[i], b1, mul2(nsn[i], b0));
             const int l = i * R + r;
@@ -1396,10 +1450,10 @@ int device_sms() {
   return n > 0 ? n : 148;
 }
 
-template <int R, int NS, bool SO>
+template <int R, int NS, bool SO, bool NORM>
 cudaError_t launch_pass(const CUtensorMap* maps, const TcParams& p, int64_t units, cudaStream_t s) {
   constexpr uint32_t smem = Cfg<R, NS>::kSmem;
-  auto kern = scan_tc_kernel<R, NS, SO>;
+  auto kern = scan_tc_kernel<R, NS, SO, NORM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // as much shared memory as the SM has, so that two CTAs fit
@@ -1433,7 +1487,7 @@ cudaError_t launch_pass(const CUtensorMap* maps, const TcParams& p, int64_t unit
   return cudaGetLastError();
 }
 
-template <int R, int NS>
+template <int R, int NS, bool NORM>
 cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   // B, C, x and (R > 1: the output is stored by TMA) y
   CUtensorMap maps[4];
@@ -1459,7 +1513,7 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   p.nunits = (int)(nseq * pl.nseg);
   p.heads = (int)a.H;
   p.hpg = (int)(a.H / a.G);
-  if (pl.nseg <= 1) return launch_pass<R, NS, false>(maps, p, nseq, s);
+  if (pl.nseg <= 1) return launch_pass<R, NS, false, NORM>(maps, p, nseq, s);
   // segmented: state-only pass, combine, full pass from the entering states
   const size_t need = seg_ws_bytes(a, pl);
   float* ws = static_cast<float*>(a.workspace);
@@ -1476,7 +1530,7 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   p.ws_scal = ws + units * a.N * a.P;
   p.final_state = nullptr;
   p.ws_hin = nullptr;  // the state-only pass starts every segment from zero
-  cudaError_t e = launch_pass<R, NS, true>(maps, p, units, s);
+  cudaError_t e = launch_pass<R, NS, true, NORM>(maps, p, units, s);
   if (e == cudaSuccess) {
     const int64_t n = nseq * (a.N / 2) * a.P;
     seg_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, p.ws_scal, a.h_init, nseq,
@@ -1487,7 +1541,7 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
     p.ws_state = nullptr;
     p.ws_hin = ws;
     p.final_state = a.final_state;
-    e = launch_pass<R, NS, false>(maps, p, units, s);
+    e = launch_pass<R, NS, false, NORM>(maps, p, units, s);
   }
   if (owned) {
     const cudaError_t f = cudaFreeAsync(ws, s);
@@ -1513,13 +1567,24 @@ bool scan_tc_supported(int64_t N, int64_t P, int R, int Q) {
 cudaError_t launch_scan_tc(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   if (a.L > 0x7fffffffLL - 2 * kQR || a.batch > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int key = a.R * 1000 + (int)a.N;
+  if (a.bc_norm) {
+    switch (key) {
+      case 1064: return launch_rn<1, 64, true>(a, status, s);
+      case 1128: return launch_rn<1, 128, true>(a, status, s);
+      case 2064: return launch_rn<2, 64, true>(a, status, s);
+      case 2128: return launch_rn<2, 128, true>(a, status, s);
+      case 4064: return launch_rn<4, 64, true>(a, status, s);
+      case 4128: return launch_rn<4, 128, true>(a, status, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (key) {
-    case 1064: return launch_rn<1, 64>(a, status, s);
-    case 1128: return launch_rn<1, 128>(a, status, s);
-    case 2064: return launch_rn<2, 64>(a, status, s);
-    case 2128: return launch_rn<2, 128>(a, status, s);
-    case 4064: return launch_rn<4, 64>(a, status, s);
-    case 4128: return launch_rn<4, 128>(a, status, s);
+    case 1064: return launch_rn<1, 64, false>(a, status, s);
+    case 1128: return launch_rn<1, 128, false>(a, status, s);
+    case 2064: return launch_rn<2, 64, false>(a, status, s);
+    case 2128: return launch_rn<2, 128, false>(a, status, s);
+    case 4064: return launch_rn<4, 64, false>(a, status, s);
+    case 4128: return launch_rn<4, 128, false>(a, status, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(HERE, "libm3scan.so")
 
 M3_OK, M3_ERR_INVALID_ARG, M3_ERR_UNSUPPORTED, M3_ERR_CUDA, M3_ERR_TIMEOUT = range(5)
 M3_F32, M3_BF16 = 0, 1
+M3_FLAG_BC_NORM = 1  # m3_dims.flags: BCNorm B and C inside the prefill
 
 # Exported entry points (kept in step with include/m3scan.h).
 EXPORTS = ("m3_scan_fwd", "m3_scan_fwd_noalloc", "m3_decode_step", "m3_scan_workspace_bytes",
@@ -37,7 +38,7 @@ class m3_dims(ctypes.Structure):
         ("headdim", ctypes.c_int64),
         ("dstate", ctypes.c_int64),
         ("act_dtype", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
         ("B_bias", ctypes.c_void_p),
         ("C_bias", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p),
@@ -150,12 +151,12 @@ def _act_dtype(t):
 
 
 def make_dims(batch, seqlen, heads, groups, headdim, dstate, act_dtype, B_bias=None,
-              C_bias=None, workspace=None):
+              C_bias=None, workspace=None, flags=0):
     d = m3_dims()
     d.batch, d.seqlen, d.heads, d.groups, d.headdim, d.dstate = (
         int(batch), int(seqlen), int(heads), int(groups), int(headdim), int(dstate))
     d.act_dtype = int(act_dtype)
-    d.reserved = 0
+    d.flags = int(flags)
     d.B_bias = None if B_bias is None else B_bias.data_ptr()
     d.C_bias = None if C_bias is None else C_bias.data_ptr()
     d.workspace = None if workspace is None else workspace.data_ptr()
@@ -173,9 +174,11 @@ def m3_scan_workspace_bytes(dims: m3_dims, R: int, chunk: int) -> int:
 
 
 def m3_scan_fwd(x, dt, A, lam, B, C, theta, R, chunk, out=None, final_state=None,
-                B_bias=None, C_bias=None, workspace=None, stream=None, want_state=True):
+                B_bias=None, C_bias=None, workspace=None, stream=None, want_state=True,
+                bc_norm=False):
     """Prefill. Shapes: x [b,L,H,P,R], dt/lam [b,L,H], A [H], B/C [b,L,G,N,R],
-    theta [b,L,G,N/2]. Returns (out, final_state)."""
+    theta [b,L,G,N/2]. Returns (out, final_state). ``bc_norm``: B and C are
+    un-normalised and the kernel applies BCNorm to them (M3_FLAG_BC_NORM)."""
     import torch
     lib = load()
     b, L, H, P, G, N = _check_prefill(x, dt, A, lam, B, C, theta, R, out, final_state, B_bias,
@@ -186,7 +189,8 @@ def m3_scan_fwd(x, dt, A, lam, B, C, theta, R, chunk, out=None, final_state=None
         out = torch.empty_like(x)
     if final_state is None and want_state:
         final_state = torch.empty((b, H, N, P), dtype=torch.float32, device=x.device)
-    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias, workspace)
+    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias, workspace,
+                     flags=M3_FLAG_BC_NORM if bc_norm else 0)
     st = lib.m3_scan_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B), _ptr(C), _ptr(theta),
                          ctypes.byref(dims), int(R), int(chunk), _ptr(out), _ptr(final_state),
                          _stream_handle(stream))
@@ -247,7 +251,7 @@ def m3_scan_bwd(x, dt, A, lam, B, C, theta, dy, R, d_final=None, B_bias=None, C_
 
 
 def m3_scan_fwd_noalloc(x, dt, A, lam, B, C, theta, R, chunk, out, final_state, B_bias=None,
-                        C_bias=None, stream=None):
+                        C_bias=None, stream=None, bc_norm=False):
     """Prefill like m3_scan_fwd into caller-allocated ``out`` / ``final_state``
     (``final_state`` may be None); the library allocates no device memory (its
     scratch is a fixed 32 MiB array; larger needs raise M3Error)."""
@@ -256,7 +260,8 @@ def m3_scan_fwd_noalloc(x, dt, A, lam, B, C, theta, R, chunk, out, final_state, 
         raise ValueError("out is required")
     b, L, H, P, G, N = _check_prefill(x, dt, A, lam, B, C, theta, R, out, final_state, B_bias,
                                       C_bias)
-    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias)
+    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias,
+                     flags=M3_FLAG_BC_NORM if bc_norm else 0)
     st = lib.m3_scan_fwd_noalloc(_ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B), _ptr(C),
                                  _ptr(theta), ctypes.byref(dims), int(R), int(chunk), _ptr(out),
                                  _ptr(final_state), _stream_handle(stream))

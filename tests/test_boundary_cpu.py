@@ -99,10 +99,38 @@ def test_scan_misaligned_pointer(lib):
     assert _scan(lib, d, x=FAKE + 1) == m3scan.M3_ERR_INVALID_ARG
 
 
-def test_scan_reserved_field_must_be_zero(lib):
+def test_scan_unknown_flags_are_rejected(lib):
+    for bit in (2, 4, 1 << 30):
+        d = _dims()
+        d.flags = bit
+        assert _scan(lib, d) == m3scan.M3_ERR_INVALID_ARG
+        d.flags = bit | m3scan.M3_FLAG_BC_NORM
+        assert _scan(lib, d) == m3scan.M3_ERR_INVALID_ARG
+
+
+def test_bc_norm_outside_the_tensor_core_prefill_is_unsupported(lib):
+    # fp32 activations take the CUDA-core path, which has no fused BCNorm
+    d = _dims(act_dtype=m3scan.M3_F32)
+    d.flags = m3scan.M3_FLAG_BC_NORM
+    assert _scan(lib, d) == m3scan.M3_ERR_UNSUPPORTED
+    # a bf16 shape outside the tensor-core scope (P = 16) likewise
+    d = _dims(act_dtype=m3scan.M3_BF16)
+    d.flags = m3scan.M3_FLAG_BC_NORM
+    assert _scan(lib, d) == m3scan.M3_ERR_UNSUPPORTED
+
+
+def test_bc_norm_is_unsupported_by_decode_continuation_and_backward(lib):
+    v = ctypes.c_void_p(FAKE)
     d = _dims()
-    d.reserved = 1
-    assert _scan(lib, d) == m3scan.M3_ERR_INVALID_ARG
+    d.flags = m3scan.M3_FLAG_BC_NORM
+    assert lib.m3_decode_step(v, v, v, v, v, None, None, v, v, v, ctypes.byref(d), 1, v,
+                              None) == m3scan.M3_ERR_UNSUPPORTED
+    assert lib.m3_decode_tokens(v, v, v, v, v, None, None, v, v, v, ctypes.byref(d), 1, v,
+                                None) == m3scan.M3_ERR_UNSUPPORTED
+    assert lib.m3_scan_fwd_state(v, v, v, v, v, v, v, None, None, ctypes.byref(d), 1, 4, v, v,
+                                 None) == m3scan.M3_ERR_UNSUPPORTED
+    assert lib.m3_scan_bwd(v, v, v, v, v, v, v, v, None, ctypes.byref(d), 1, v, v, v, v, v, v, v,
+                           None, None, None) == m3scan.M3_ERR_UNSUPPORTED
 
 
 def test_scan_null_dims(lib):

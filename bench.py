@@ -490,12 +490,13 @@ def bench_prefill_other(torch, m3, dev, name, args, peaks, bc_norm=False, fp32=F
              ", un-normalised B/C with BCNorm fused" if bc_norm else ""),
          "tok_s": shape.tokens / (ms * 1e-3), "ms": ms,
          "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"]}
+    r["tensor_frac"] = nflops / (ms * 1e-3) / 1e12 / peaks["bf16"]
     if fp32:
-        # the fp32 mode runs on the CUDA cores: its compute roof is the fp32 FMA peak
-        r["fp32_alu_frac"] = nflops / (ms * 1e-3) / 1e12 / FP32_PEAK_TFLOPS
-        r["kernel"] = "CUDA cores (fp32 arithmetic), one CTA per (b, h)"
-    else:
-        r["tensor_frac"] = nflops / (ms * 1e-3) / 1e12 / peaks["bf16"]
+        # the fp32 mode runs on the tensor cores with split fp16 operands (three
+        # MMAs per product): tensor_frac counts the algorithm's FLOPs once
+        r["kernel"] = ("tensor cores, fp32 activations as fp16 high + residual tiles, "
+                       "three products per contraction")
+        r["tensor_issued_frac"] = 3 * r["tensor_frac"]
     return r
 
 

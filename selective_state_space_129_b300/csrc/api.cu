@@ -124,7 +124,6 @@ const char* m3_status_string(m3_status s) {
 size_t m3_scan_workspace_bytes(const m3_dims* dims, int R, int chunk) {
   if (check_dims(dims, R) == M3_ERR_INVALID_ARG || chunk < 1 || dims->seqlen < 0)
     return (size_t)-1;
-  if (dims->act_dtype != M3_BF16) return 0;
   m3::ScanArgs a = {};
   a.batch = dims->batch; a.L = dims->seqlen; a.H = dims->heads; a.G = dims->groups;
   a.P = dims->headdim; a.N = dims->dstate; a.R = R; a.Q = chunk;
@@ -177,14 +176,16 @@ m3_status scan_impl(const void* x, const float* dt, const float* A, const float*
   // The tensor-core path moves tiles with TMA and 128-bit accesses: it takes
   // 16-byte-aligned activations, biases and final state and 8-byte-aligned
   // theta; other calls use the CUDA cores.
-  const bool use_tc = bf16 && m3::scan_tc_supported(N, P, R, chunk) && aligned(x, 16) &&
+  // (fp32 activations take the split-fp16 tensor-core mode when the shape and
+  // alignment allow, with the same conditions)
+  const bool use_tc = m3::scan_tc_supported(N, P, R, chunk) && aligned(x, 16) &&
                       aligned(out, 16) && aligned(B, 16) && aligned(C, 16) &&
                       aligned(theta, 8) &&
                       (dims->B_bias == nullptr || aligned(dims->B_bias, 16)) &&
                       (dims->C_bias == nullptr || aligned(dims->C_bias, 16)) &&
                       (final_state == nullptr || aligned(final_state, 16));
   const bool bc_norm = (dims->flags & M3_FLAG_BC_NORM) != 0;
-  if (bc_norm && (!use_tc || continue_state)) return M3_ERR_UNSUPPORTED;
+  if (bc_norm && (!use_tc || !bf16 || continue_state)) return M3_ERR_UNSUPPORTED;
   if (!use_tc) {
     const size_t smem = m3::scan_simt_smem_bytes(N, P, R, chunk);
     if (smem > 227 * 1024) return M3_ERR_UNSUPPORTED;
@@ -225,6 +226,7 @@ m3_status scan_impl(const void* x, const float* dt, const float* A, const float*
   a.workspace = dims->workspace; a.workspace_bytes = dims->workspace_bytes;
   a.batch = b; a.L = L; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R; a.Q = chunk;
   a.bc_norm = bc_norm;
+  a.f32 = !bf16;
   if (use_tc) {
     // a caller-provided workspace must be large enough; NULL means the
     // library allocates (stream-ordered) what it needs

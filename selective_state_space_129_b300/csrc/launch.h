@@ -27,6 +27,7 @@ struct ScanArgs {
   int64_t batch, L, H, G, P, N;
   int R, Q;
   bool bc_norm;  // B and C arrive un-normalised: BCNorm them in the prologue
+  bool f32;      // fp32 activations (the tensor-core fp32 mode), else bf16
 };
 
 struct DecodeArgs {

@@ -98,7 +98,10 @@ constexpr uint32_t kColS = 0, kColD = 64, kColY = 128, kColYo = 192;
 
 constexpr uint32_t align1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 
-template <int R, int NS>
+// F32: the fp32 precision mode. Activations arrive as fp32; every operand
+// tile is a pair of fp16 tiles, high part and residual (v = hi + lo to ~22
+// bits), and each product is formed from three MMAs (hi hi + hi lo + lo hi).
+template <int R, int NS, bool F32 = false>
 struct Cfg {
   static constexpr int Q = kQR / R;          // tokens per chunk
   static constexpr int KP = NS / 2;          // rotating state pairs
@@ -107,31 +110,38 @@ struct Cfg {
   static constexpr int TPG = Q / TG;         // tokens per fold thread
   static_assert(TPG >= 1 && Q % TG == 0, "token groups must divide the chunk");
   static constexpr int HR = NS * kP / kThreads;  // fp32 state values per thread
-  static constexpr int BW = 2 * R;  // raw 32-bit words of B (or C) per token and thread
-  // raw slot (TMA destination): B, C [Q][NS*R] bf16, x [Q][P*R] bf16
+  static constexpr int AB = F32 ? 4 : 2;           // bytes per raw activation element
+  static constexpr int BW = 4 * R * AB / 4;  // raw 32-bit words of B (or C) per token and thread
+  static constexpr int XW = (R == 1 ? 8 : 4 * R) * AB / 4;  // raw x words per item
+  static constexpr int OPS = F32 ? 2 : 1;  // fp16 tiles per operand (hi, lo)
+  // raw slot (TMA destination): B, C [Q][NS*R], x [Q][P*R] (bf16: x 128B-swizzled for R = 1)
   static constexpr uint32_t kRawB = 0;
-  static constexpr uint32_t kRawC = kRawB + Q * NS * R * 2;
-  static constexpr uint32_t kRawX = align1k(kRawC + Q * NS * R * 2);  // 128B-swizzled for R = 1
-  static constexpr uint32_t kRawEnd = kRawX + (uint32_t)(Q * kP * R * 2);
-  // operand tiles: Bt, Ct [64][NS] fp16, w X [64][64] fp16, X [64][64] bf16,
-  // the fp16 state copy [NS][64]
+  static constexpr uint32_t kRawC = kRawB + Q * NS * R * AB;
+  static constexpr uint32_t kRawX = align1k(kRawC + Q * NS * R * AB);
+  static constexpr uint32_t kRawEnd = kRawX + (uint32_t)(Q * kP * R * AB);
+  // operand tiles: Bt, Ct [64][NS] fp16, w X [64][64] fp16, X [64][64] (bf16;
+  // F32: fp16), the fp16 state copy [NS][64]; F32: each followed by its residual
+  static constexpr uint32_t kBtLo = 64 * NS * 2;   // hi -> lo offset of Bt, Ct
+  static constexpr uint32_t kXLo = kTileBytes;     // ... of w X, X, P
+  static constexpr uint32_t kHLo = NS * 128;       // ... of the state copy
+  static_assert(kBtLo % 1024 == 0 && kXLo % 1024 == 0 && kHLo % 1024 == 0,
+                "residual tiles keep the 1024-byte alignment of the swizzle atom");
   static constexpr uint32_t kBt = align1k(kRawEnd);
-  static constexpr uint32_t kCt = kBt + 64 * NS * 2;
-  static constexpr uint32_t kXw = kCt + 64 * NS * 2;
-  static constexpr uint32_t kXo = kXw + kTileBytes;
-  static constexpr uint32_t kH = kXo + kTileBytes;
-  static constexpr uint32_t kHEnd = kH + NS * 128;
-  // masked scores P (bf16 high, low): over Bt when it is large enough
-  static constexpr uint32_t kPh = (NS == 128) ? kBt : kHEnd;
+  static constexpr uint32_t kCt = kBt + OPS * 64 * NS * 2;
+  static constexpr uint32_t kXw = kCt + OPS * 64 * NS * 2;
+  static constexpr uint32_t kXo = kXw + OPS * kTileBytes;
+  static constexpr uint32_t kH = kXo + OPS * kTileBytes;
+  static constexpr uint32_t kHEnd = kH + OPS * NS * 128;
+  // masked scores P (high, low parts): over Bt (hi, lo) when it is large enough
+  static constexpr uint32_t kPh = (NS == 128 || F32) ? kBt : kHEnd;
   static constexpr uint32_t kPl = kPh + kTileBytes;
-  // output staging (R > 1): over w X, which only D reads
+  // output staging (R > 1): over w X (hi, lo), which only D reads
   static constexpr uint32_t kYs = kXw;
   static constexpr uint32_t kBytes = (kPl + kTileBytes > kHEnd) ? kPl + kTileBytes : kHEnd;
   static constexpr uint32_t kSmem = kBytes + 1024;  // + alignment slack
   // bytes landing on the raw barrier per chunk (full pass; state-only pass)
-  static constexpr uint32_t kTxBytes =
-      2u * Q * NS * R * 2 + (uint32_t)(Q * kP * R * 2);
-  static constexpr uint32_t kTxBytesSO = (uint32_t)Q * NS * R * 2 + (uint32_t)(Q * kP * R * 2);
+  static constexpr uint32_t kTxBytes = 2u * Q * NS * R * AB + (uint32_t)(Q * kP * R * AB);
+  static constexpr uint32_t kTxBytesSO = (uint32_t)Q * NS * R * AB + (uint32_t)(Q * kP * R * AB);
 };
 
 // Per-chunk scalars (one set per chunk parity): the decay scan's results for
@@ -145,7 +155,8 @@ struct __align__(16) Scal {
   float dt[64];    // Delta_t
   float eLend, lamend2, wmax;  // exp(Lam_end), Lam_end (log2), max |wend|
   float invB, invC, invX;      // inverse fp16 scales of Bt, Ct, w X
-  float pad[2];
+  float pmul;                  // S -> P units: invB invC (F32: times P's scale)
+  float wpmax;                 // max over the chunk of |gamma_t|, |gamma_t + bhat_{t+1}|
 };
 
 struct TcParams {
@@ -155,7 +166,7 @@ struct TcParams {
   const float* theta;
   const float* B_bias;
   const float* C_bias;
-  __nv_bfloat16* out;
+  void* out;  // bf16, or fp32 in the fp32 mode
   float* final_state;
   unsigned int* status;
   int64_t L, H, G, batch;
@@ -190,6 +201,19 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 template <int N>
 __device__ __forceinline__ float bf_at(const uint32_t (&w)[N], int e) {
   return (e & 1) ? bf_hi(w[e >> 1]) : bf_lo(w[e >> 1]);
+}
+// element e of a token's raw activation words: bf16 pairs, or fp32 (F32)
+template <bool F32, int N>
+__device__ __forceinline__ float act_at(const uint32_t (&w)[N], int e) {
+  if constexpr (F32)
+    return __uint_as_float(w[e]);
+  else
+    return bf_at(w, e);
+}
+// the fp16 residual pair (a, b) - hi, hi the fp16 pair already formed from (a, b)
+__device__ __forceinline__ uint32_t f16_residual(uint32_t hi, float a, float b) {
+  const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  return pack_f16(a - h.x, b - h.y);
 }
 // largest magnitude held in an accumulator of bf16x2 abs-maxima, as a float
 __device__ __forceinline__ float bf_absmax(uint32_t w) {
@@ -374,13 +398,14 @@ __device__ __forceinline__ void decay_scan(const DecayRaw& d, int Q, int lane, S
   const float lam_end = (Q <= 32) ? __shfl_sync(0xffffffffu, a0, Q - 1)
                                   : __shfl_sync(0xffffffffu, a1, (Q - 1) & 31);
   const float lv[2] = {a0, a1};
-  float wm = 0.f;
+  float wm = 0.f, wpm = 0.f;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int i = lane + 32 * j;
     if (i < Q) {
       const float gam = d.lam[j] * d.dt[j];
       const float wpv = gam + (1.f - d.lamn[j]) * d.dtn[j];
+      wpm = fmaxf(wpm, fmaxf(fabsf(gam), fabsf(wpv)));
       const float we = ex2(lam_end - lv[j]) * wpv;
       sc.lam2[i] = lv[j];
       sc.gam[i] = gam;
@@ -392,10 +417,12 @@ __device__ __forceinline__ void decay_scan(const DecayRaw& d, int Q, int lane, S
     }
   }
   wm = warp_max(wm);
+  wpm = warp_max(wpm);
   if (lane == 0) {
     sc.eLend = ex2(lam_end);
     sc.lamend2 = lam_end;
     sc.wmax = wm;
+    sc.wpmax = wpm;
   }
 }
 
@@ -441,17 +468,22 @@ __device__ __forceinline__ float bc_inv_rms(const uint32_t (&w)[BW], int r) {
 // SO: the state-only pass of a segmented scan (no C, no outputs).
 // NORM: B and C arrive un-normalised; BCNorm them here (each token's and
 // rank's vector over N divided by its root mean square), before the bias.
-template <int R, int NS, bool SO, bool NORM>
-__global__ void __launch_bounds__(kThreads, 2)
+// F32: the fp32 precision mode (see Cfg): one CTA per SM (its tiles take
+// about 210 KB of shared memory).
+template <int R, int NS, bool SO, bool NORM, bool F32>
+__global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
                    const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                    TcParams p) {
-  using K = Cfg<R, NS>;
+  using K = Cfg<R, NS, F32>;
+  static_assert(!(F32 && NORM), "BCNorm is fused on the bf16 path only");
   constexpr int Q = K::Q, KP = K::KP, KP2 = K::KP2, TG = K::TG, TPG = K::TPG, HR = K::HR;
   constexpr uint32_t kIdS = ptx::idesc_f16_f32(64, 64, false, false);
   constexpr uint32_t kIdD = ptx::idesc_f16_f32(NS, 64, true, true);
   constexpr uint32_t kIdYo = ptx::idesc_f16_f32(64, 64, false, true);
-  constexpr uint32_t kIdY = ptx::idesc_bf16_f32(64, 64, false, true);
+  // Y = P X: bf16 parts of P times the exact bf16 X, or (F32) fp16 parts
+  constexpr uint32_t kIdY =
+      F32 ? ptx::idesc_f16_f32(64, 64, false, true) : ptx::idesc_bf16_f32(64, 64, false, true);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -462,6 +494,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int abort_flag;
   __shared__ Scal ss[2];
   __shared__ __align__(16) float s_tot[TG][KP];  // per token group: angle total
+  // F32: its Kahan compensation (the angle sums are compensated in fp32 mode)
+  __shared__ __align__(16) float s_totlo[F32 ? TG : 1][F32 ? KP : 2];
   __shared__ float s_carry[2][2][KP];            // [chunk parity][hi, lo][pair]
   __shared__ float s_fang[KP];                   // angle after a unit's last chunk
   __shared__ unsigned int s_max[2][3];  // per chunk parity: bounds of |B|, |C|, |x|
@@ -552,14 +586,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int blk = 0; blk < HR / 16; ++blk) {
       uint32_t n, cb;
       hpos(blk, n, cb);
-      uint32_t wv[8];
+      uint32_t wv[8], wl[8];
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
         const float2 v = mul2(f2, make_float2(hv[16 * blk + j], hv[16 * blk + j + 1]));
         wv[j >> 1] = pack_f16(v.x, v.y);
+        if constexpr (F32) wl[j >> 1] = f16_residual(wv[j >> 1], v.x, v.y);
       }
       sts128(sbase + K::kH + sw128(n, cb), make_uint4(wv[0], wv[1], wv[2], wv[3]));
       sts128(sbase + K::kH + sw128(n, cb + 8u), make_uint4(wv[4], wv[5], wv[6], wv[7]));
+      if constexpr (F32) {
+        sts128(sbase + K::kH + K::kHLo + sw128(n, cb), make_uint4(wl[0], wl[1], wl[2], wl[3]));
+        sts128(sbase + K::kH + K::kHLo + sw128(n, cb + 8u), make_uint4(wl[4], wl[5], wl[6], wl[7]));
+      }
     }
   };
   auto abs_max = [&](const float (&hv)[HR]) {
@@ -696,11 +735,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     // raw B, C tiles -> registers
     uint32_t bw[TPG][K::BW], cw[TPG][K::BW];
     uint32_t bacc = 0u, cacc = 0u;
+    float bfm = 0.f, cfm = 0.f;  // F32: magnitude bounds
 #pragma unroll
     for (int i = 0; i < TPG; ++i) {
       const int t = tg * TPG + i;
-      const uint32_t ob = (uint32_t)(t * NS * R + 4 * kk2 * R) * 2u;
-      if constexpr (R == 1) {
+      const uint32_t ob = (uint32_t)(t * NS * R + 4 * kk2 * R) * (uint32_t)K::AB;
+      if constexpr (F32) {
+#pragma unroll
+        for (int q = 0; q < K::BW / 4; ++q) {
+          const uint4 vb = lds128(sbase + K::kRawB + ob + 16u * q);
+          bw[i][4 * q] = vb.x; bw[i][4 * q + 1] = vb.y; bw[i][4 * q + 2] = vb.z; bw[i][4 * q + 3] = vb.w;
+          if constexpr (!SO) {
+            const uint4 vc = lds128(sbase + K::kRawC + ob + 16u * q);
+            cw[i][4 * q] = vc.x; cw[i][4 * q + 1] = vc.y; cw[i][4 * q + 2] = vc.z; cw[i][4 * q + 3] = vc.w;
+          }
+        }
+      } else if constexpr (R == 1) {
         const uint2 vb = lds64(sbase + K::kRawB + ob);
         bw[i][0] = vb.x;
         bw[i][1] = vb.y;
@@ -721,7 +771,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
-    if constexpr (!NORM) {
+    if constexpr (F32) {
+#pragma unroll
+      for (int i = 0; i < TPG; ++i) {
+#pragma unroll
+        for (int q = 0; q < K::BW; ++q) {
+          bfm = fmaxf(bfm, fabsf(__uint_as_float(bw[i][q])));
+          if constexpr (!SO) cfm = fmaxf(cfm, fabsf(__uint_as_float(cw[i][q])));
+        }
+      }
+    } else if constexpr (!NORM) {
 #pragma unroll
       for (int i = 0; i < TPG; ++i) {
 #pragma unroll
@@ -731,46 +790,64 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
-    // x of this chunk -> registers (w X and the operand copy of X)
+    // x of this chunk -> registers (w X and the operand copy of X). An item
+    // is 8 consecutive p of one token row (R = 1; bf16: the 16-byte chunk at
+    // the same place of the 128B-swizzled raw tile) or 4 p x R ranks (R > 1).
     constexpr int kXItems = (R == 1) ? 2 : (Q * (kP / 4)) / kThreads;
-    constexpr int kXVec = (R == 1) ? 1 : R / 2;
-    uint4 xv[kXItems][kXVec];
+    uint32_t xw[kXItems][K::XW];
     uint32_t xacc = 0u;
+    float xfm = 0.f;
 #pragma unroll
     for (int j = 0; j < kXItems; ++j) {
       const int it = tid + kThreads * j;
+      uint32_t src;
       if constexpr (R == 1) {
-        xv[j][0] = lds128(sbase + K::kRawX + (uint32_t)it * 16u);  // 16-byte chunk, row it / 8
+        src = F32 ? sbase + K::kRawX + (uint32_t)it * 32u   // fp32 row-major: 8 floats
+                  : sbase + K::kRawX + (uint32_t)it * 16u;  // physical 16-byte chunk
       } else {
         const int sx = it / (kP / 4), pb = it % (kP / 4);
-        const uint32_t src = sbase + K::kRawX + (uint32_t)(sx * kP * R + 4 * pb * R) * 2u;
-#pragma unroll
-        for (int q = 0; q < kXVec; ++q) xv[j][q] = lds128(src + 16u * q);
+        src = sbase + K::kRawX + (uint32_t)(sx * kP * R + 4 * pb * R) * (uint32_t)K::AB;
       }
 #pragma unroll
-      for (int q = 0; q < kXVec; ++q) {
-        xacc = ptx::bf16x2_absmax(xacc, xv[j][q].x);
-        xacc = ptx::bf16x2_absmax(xacc, xv[j][q].y);
-        xacc = ptx::bf16x2_absmax(xacc, xv[j][q].z);
-        xacc = ptx::bf16x2_absmax(xacc, xv[j][q].w);
+      for (int q = 0; q < K::XW / 4; ++q) {
+        const uint4 v = lds128(src + 16u * q);
+        xw[j][4 * q] = v.x; xw[j][4 * q + 1] = v.y; xw[j][4 * q + 2] = v.z; xw[j][4 * q + 3] = v.w;
+      }
+#pragma unroll
+      for (int q = 0; q < K::XW; ++q) {
+        if constexpr (F32)
+          xfm = fmaxf(xfm, fabsf(__uint_as_float(xw[j][q])));
+        else
+          xacc = ptx::bf16x2_absmax(xacc, xw[j][q]);
       }
     }
     // per-token-group angle sums (pairs k0, k0 + 1)
     float2 ph[TPG];
     {
-      float2 run = make_float2(0.f, 0.f);
+      float2 run = make_float2(0.f, 0.f), comp = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < TPG; ++i) {
         const float d = sc.dt[tg * TPG + i];
-        run = fma2(make_float2(d, d), th[i], run);
+        if constexpr (F32) {
+          // Kahan-compensated: the fp32 mode's angles stay exact to ~2^-24
+          const float2 yk = ptx::sub2(mul2(make_float2(d, d), th[i]), comp);
+          const float2 tk = add2(run, yk);
+          comp = ptx::sub2(ptx::sub2(tk, run), yk);
+          run = tk;
+        } else {
+          run = fma2(make_float2(d, d), th[i], run);
+        }
         ph[i] = run;
       }
       *reinterpret_cast<float2*>(&s_tot[tg][k0]) = run;
+      if constexpr (F32)
+        *reinterpret_cast<float2*>(&s_totlo[tg][k0]) = make_float2(-comp.x, -comp.y);
     }
     {
       // non-negative floats order like their bit patterns
-      const float bm = warp_max(bf_absmax(bacc)), cm = warp_max(bf_absmax(cacc));
-      const float xm = warp_max(bf_absmax(xacc));
+      const float bm = warp_max(F32 ? bfm : bf_absmax(bacc));
+      const float cm = warp_max(F32 ? cfm : bf_absmax(cacc));
+      const float xm = warp_max(F32 ? xfm : bf_absmax(xacc));
       if (lane == 0) {
         atomicMax(&s_max[g & 1][0], __float_as_uint(bm));
         atomicMax(&s_max[g & 1][1], __float_as_uint(cm));
@@ -792,6 +869,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ================================================= fold, part 2
     float sigB, invB, sigC, invC, sigX, invX;
+    float sigXo = 1.f, ykY = 1.f;  // F32: scale of the X tile; Y units -> y
     {
       const float mb = __uint_as_float(s_max[g & 1][0]);
       const float mc = __uint_as_float(s_max[g & 1][1]);
@@ -811,10 +889,22 @@ __global__ void __launch_bounds__(kThreads, 2)
       pow2_scale<-26>(2.f * ((NORM ? kNormBound : mb) + bmax_bias), &sigB, &invB);
       pow2_scale<-26>(2.f * ((NORM ? kNormBound : mc) + cmax_bias), &sigC, &invC);
       pow2_scale<-26>(mx * sc.wmax, &sigX, &invX);
+      float pmul = invB * invC;
+      if constexpr (F32) {
+        // X (fp16 hi + lo) by its own scale; P by one from a bound of |P|:
+        // |S| <= N max|Bt| max|Ct|, the mask <= max(|gamma|, |gamma + bhat|)
+        float invXo, sigP, invP;
+        pow2_scale(mx, &sigXo, &invXo);
+        pow2_scale((float)NS * (2.f * (mb + bmax_bias)) * (2.f * (mc + cmax_bias)) * sc.wpmax,
+                   &sigP, &invP);
+        pmul *= sigP;
+        ykY = invP * invXo;
+      }
       if (tid == 0) {
         sc.invB = invB;
         sc.invC = invC;
         sc.invX = invX;
+        sc.pmul = pmul;
       }
     }
     // angle before this thread's first token: carry + earlier groups. Within
@@ -825,7 +915,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       float2 o = make_float2(0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < TG - 1; ++q) {
-        const float2 v = *reinterpret_cast<const float2*>(&s_tot[q][k0]);
+        float2 v = *reinterpret_cast<const float2*>(&s_tot[q][k0]);
+        if constexpr (F32) v = add2(v, *reinterpret_cast<const float2*>(&s_totlo[q][k0]));
         if (q < tg) o = add2(o, v);
       }
       float ch0 = 0.f, cl0 = 0.f, ch1 = 0.f, cl1 = 0.f;
@@ -844,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int q = 0; q < TG; ++q) {
           thh[q] = s_tot[q][k];
-          tll[q] = 0.f;
+          tll[q] = F32 ? s_totlo[q][k] : 0.f;
         }
 #pragma unroll
         for (int w = 1; w < TG; w <<= 1)
@@ -863,9 +954,84 @@ __global__ void __launch_bounds__(kThreads, 2)
         ph[i] = add2(off, ph[i]);
         amax = fmaxf(amax, fmaxf(fabsf(ph[i].x), fabsf(ph[i].y)));
       }
-      if (__any_sync(0xffffffffu, amax > kAngleDirect)) {
+      // (the fp32 mode always reduces: sin.approx / cos.approx are exact to
+      // ~2^-21 in absolute terms only on [-pi, pi])
+      if (F32 || __any_sync(0xffffffffu, amax > kAngleDirect)) {
 #pragma unroll
         for (int i = 0; i < TPG; ++i) ph[i] = make_float2(wrap_rad(ph[i].x), wrap_rad(ph[i].y));
+      }
+    }
+    // w X (fp16, scaled) and X as the [(token, rank)][p] operand: the exact
+    // bf16 input, or (F32) fp16 hi + lo of sigXo x
+#pragma unroll
+    for (int j = 0; j < kXItems; ++j) {
+      const int it = tid + kThreads * j;
+      if constexpr (R == 1 && !F32) {
+        // the raw tile is already 128-byte swizzled [token][p]: same offsets
+        const uint32_t row = (uint32_t)it >> 3;
+        const float w = sc.wend[row] * sigX;
+        const float2 w2 = make_float2(w, w);
+        const uint4 v = make_uint4(xw[j][0], xw[j][1], xw[j][2], xw[j][3]);
+        if constexpr (!SO) sts128(sbase + K::kXo + (uint32_t)it * 16u, v);
+        const float2 p0 = mul2(w2, make_float2(bf_lo(v.x), bf_hi(v.x)));
+        const float2 p1 = mul2(w2, make_float2(bf_lo(v.y), bf_hi(v.y)));
+        const float2 p2 = mul2(w2, make_float2(bf_lo(v.z), bf_hi(v.z)));
+        const float2 p3 = mul2(w2, make_float2(bf_lo(v.w), bf_hi(v.w)));
+        sts128(sbase + K::kXw + (uint32_t)it * 16u,
+               make_uint4(pack_f16(p0.x, p0.y), pack_f16(p1.x, p1.y), pack_f16(p2.x, p2.y),
+                          pack_f16(p3.x, p3.y)));
+      } else if constexpr (R == 1) {
+        // F32: item it holds p = 8 (it & 7) .. + 7 of row it / 8 (row-major raw)
+        const uint32_t row = (uint32_t)it >> 3;
+        const float w = sc.wend[row] * sigX;
+        const float2 w2 = make_float2(w, w);
+        const uint32_t o = sw128(row, 8u * ((uint32_t)it & 7u));
+        uint32_t hw[4], hl[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const float2 pw = mul2(w2, make_float2(act_at<F32>(xw[j], e), act_at<F32>(xw[j], e + 1)));
+          hw[e >> 1] = pack_f16(pw.x, pw.y);
+          hl[e >> 1] = f16_residual(hw[e >> 1], pw.x, pw.y);
+        }
+        sts128(sbase + K::kXw + o, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+        sts128(sbase + K::kXw + K::kXLo + o, make_uint4(hl[0], hl[1], hl[2], hl[3]));
+        if constexpr (!SO) {
+          const float2 s2 = make_float2(sigXo, sigXo);
+          uint32_t ph4[4], pl4[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float2 px = mul2(s2, make_float2(act_at<F32>(xw[j], e), act_at<F32>(xw[j], e + 1)));
+            ph4[e >> 1] = pack_f16(px.x, px.y);
+            pl4[e >> 1] = f16_residual(ph4[e >> 1], px.x, px.y);
+          }
+          sts128(sbase + K::kXo + o, make_uint4(ph4[0], ph4[1], ph4[2], ph4[3]));
+          sts128(sbase + K::kXo + K::kXLo + o, make_uint4(pl4[0], pl4[1], pl4[2], pl4[3]));
+        }
+      } else {
+        const int sx = it / (kP / 4), pb = it % (kP / 4);
+        const float w = sc.wend[sx] * sigX;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          float v4[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) v4[q4] = act_at<F32>(xw[j], q4 * R + r);
+          const uint32_t o = sw128((uint32_t)(sx * R + r), 4u * pb);
+          const uint32_t w0 = pack_f16(w * v4[0], w * v4[1]), w1 = pack_f16(w * v4[2], w * v4[3]);
+          sts64(sbase + K::kXw + o, w0, w1);
+          if constexpr (F32) {
+            sts64(sbase + K::kXw + K::kXLo + o, f16_residual(w0, w * v4[0], w * v4[1]),
+                  f16_residual(w1, w * v4[2], w * v4[3]));
+            if constexpr (!SO) {
+              const float a0 = sigXo * v4[0], a1 = sigXo * v4[1], a2 = sigXo * v4[2],
+                          a3 = sigXo * v4[3];
+              const uint32_t x0 = pack_f16(a0, a1), x1 = pack_f16(a2, a3);
+              sts64(sbase + K::kXo + o, x0, x1);
+              sts64(sbase + K::kXo + K::kXLo + o, f16_residual(x0, a0, a1), f16_residual(x1, a2, a3));
+            }
+          } else if constexpr (!SO) {
+            sts64(sbase + K::kXo + o, pack_bf16(v4[0], v4[1]), pack_bf16(v4[2], v4[3]));
+          }
+        }
       }
     }
     // RoPE fold: sigma Rot(-Phi) (B + bias), likewise C, into fp16 tiles
@@ -896,22 +1062,31 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float v = sigB * bc_inv_rms<R, NS, K::BW>(bw[i], 0);
           sBi = make_float2(v, v);
         }
-        const float2 b0 = fma2(sBi, make_float2(bf_at(bw[i], 0), bf_at(bw[i], 2)), bs0);
-        const float2 b1 = fma2(sBi, make_float2(bf_at(bw[i], 1), bf_at(bw[i], 3)), bs1);
+        const float2 b0 = fma2(sBi, make_float2(act_at<F32>(bw[i], 0), act_at<F32>(bw[i], 2)), bs0);
+        const float2 b1 = fma2(sBi, make_float2(act_at<F32>(bw[i], 1), act_at<F32>(bw[i], 3)), bs1);
         // Rot(-Phi) = [[cos, sin], [-sin, cos]]
         const float2 bt0 = fma2(cs, b0, mul2(sn, b1)), bt1 = fma2(cs, b1, mul2(nsn, b0));
         const uint32_t a = (fold_base ^ ((uint32_t)(i & 7) << 4)) + (uint32_t)i * 128u;
-        sts64(a, pack_f16(bt0.x, bt1.x), pack_f16(bt0.y, bt1.y));
+        {
+          const uint32_t h0 = pack_f16(bt0.x, bt1.x), h1 = pack_f16(bt0.y, bt1.y);
+          sts64(a, h0, h1);
+          if constexpr (F32)
+            sts64(a + K::kBtLo, f16_residual(h0, bt0.x, bt1.x), f16_residual(h1, bt0.y, bt1.y));
+        }
         if constexpr (!SO) {
           float2 sCi = sC2;
           if constexpr (NORM) {
             const float v = sigC * bc_inv_rms<R, NS, K::BW>(cw[i], 0);
             sCi = make_float2(v, v);
           }
-          const float2 c0 = fma2(sCi, make_float2(bf_at(cw[i], 0), bf_at(cw[i], 2)), cs0);
-          const float2 c1 = fma2(sCi, make_float2(bf_at(cw[i], 1), bf_at(cw[i], 3)), cs1);
+          const float2 c0 = fma2(sCi, make_float2(act_at<F32>(cw[i], 0), act_at<F32>(cw[i], 2)), cs0);
+          const float2 c1 = fma2(sCi, make_float2(act_at<F32>(cw[i], 1), act_at<F32>(cw[i], 3)), cs1);
           const float2 ct0 = fma2(cs, c0, mul2(sn, c1)), ct1 = fma2(cs, c1, mul2(nsn, c0));
-          sts64(a + (K::kCt - K::kBt), pack_f16(ct0.x, ct1.x), pack_f16(ct0.y, ct1.y));
+          const uint32_t h0 = pack_f16(ct0.x, ct1.x), h1 = pack_f16(ct0.y, ct1.y);
+          sts64(a + (K::kCt - K::kBt), h0, h1);
+          if constexpr (F32)
+            sts64(a + (K::kCt - K::kBt) + K::kBtLo, f16_residual(h0, ct0.x, ct1.x),
+                  f16_residual(h1, ct0.y, ct1.y));
         }
       }
     } else {
@@ -952,8 +1127,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float2 bb1 = make_float2(bv[1 * R + r], bv[3 * R + r]);
 #pragma unroll
           for (int i = 0; i < TPG; ++i) {
-            const float2 v0 = make_float2(bf_at(raw[i], 0 * R + r), bf_at(raw[i], 2 * R + r));
-            const float2 v1 = make_float2(bf_at(raw[i], 1 * R + r), bf_at(raw[i], 3 * R + r));
+            const float2 v0 = make_float2(act_at<F32>(raw[i], 0 * R + r), act_at<F32>(raw[i], 2 * R + r));
+            const float2 v1 = make_float2(act_at<F32>(raw[i], 1 * R + r), act_at<F32>(raw[i], 3 * R + r));
             float2 b0, b1;
             if constexpr (NORM) {
               const float rs = bc_inv_rms<R, NS, K::BW>(raw[i], r);
@@ -967,47 +1142,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float2 t1 = fma2(cs[i], b1, mul2(nsn[i], b0));
             const int l = i * R + r;
             const uint32_t a = (dst ^ ((uint32_t)(l & 7) << 4)) + (uint32_t)l * 128u;
-            sts64(a, pack_f16(t0.x, t1.x), pack_f16(t0.y, t1.y));
+            const uint32_t h0 = pack_f16(t0.x, t1.x), h1 = pack_f16(t0.y, t1.y);
+            sts64(a, h0, h1);
+            if constexpr (F32)
+              sts64(a + K::kBtLo, f16_residual(h0, t0.x, t1.x), f16_residual(h1, t0.y, t1.y));
           }
-        }
-      }
-    }
-    // w X (fp16, scaled) and X as the [(token, rank)][p] bf16 operand
-#pragma unroll
-    for (int j = 0; j < kXItems; ++j) {
-      const int it = tid + kThreads * j;
-      if constexpr (R == 1) {
-        // the raw tile is already 128-byte swizzled [token][p]: same offsets
-        const uint32_t row = (uint32_t)it >> 3;
-        const float w = sc.wend[row] * sigX;
-        const uint4 v = xv[j][0];
-        const float2 w2 = make_float2(w, w);
-        if constexpr (!SO) sts128(sbase + K::kXo + (uint32_t)it * 16u, v);
-        const float2 p0 = mul2(w2, make_float2(bf_lo(v.x), bf_hi(v.x)));
-        const float2 p1 = mul2(w2, make_float2(bf_lo(v.y), bf_hi(v.y)));
-        const float2 p2 = mul2(w2, make_float2(bf_lo(v.z), bf_hi(v.z)));
-        const float2 p3 = mul2(w2, make_float2(bf_lo(v.w), bf_hi(v.w)));
-        sts128(sbase + K::kXw + (uint32_t)it * 16u,
-               make_uint4(pack_f16(p0.x, p0.y), pack_f16(p1.x, p1.y), pack_f16(p2.x, p2.y),
-                          pack_f16(p3.x, p3.y)));
-      } else {
-        const int sx = it / (kP / 4), pb = it % (kP / 4);
-        uint32_t wv[2 * R];
-#pragma unroll
-        for (int q = 0; q < kXVec; ++q) {
-          wv[4 * q] = xv[j][q].x; wv[4 * q + 1] = xv[j][q].y;
-          wv[4 * q + 2] = xv[j][q].z; wv[4 * q + 3] = xv[j][q].w;
-        }
-        const float w = sc.wend[sx] * sigX;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          float v4[4];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) v4[q4] = bf_at(wv, q4 * R + r);
-          const uint32_t o = sw128((uint32_t)(sx * R + r), 4u * pb);
-          if constexpr (!SO)
-            sts64(sbase + K::kXo + o, pack_bf16(v4[0], v4[1]), pack_bf16(v4[2], v4[3]));
-          sts64(sbase + K::kXw + o, pack_f16(w * v4[0], w * v4[1]), pack_f16(w * v4[2], w * v4[3]));
         }
       }
     }
@@ -1044,17 +1183,37 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid == 0) {
       // D = Bt^T (w X) onto the state; S = Ct Bt^T; Yoff = Ct H_in
       ptx::tc_fence_after_sync();
+      // (F32: every product is hi hi + hi lo + lo hi of the split operands)
       const Desc dBm = make_desc(opBt, 64u * 128u), dXw = make_desc(sbase + K::kXw, 64u * 128u);
 #pragma unroll
       for (int kk = 0; kk < kQR / 16; ++kk)
         ptx::mma_bf16_ss(tmem + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD,
                          (has_state || kk > 0) ? 1u : 0u);
+      if constexpr (F32) {
+        const Desc dBml = make_desc(opBt + K::kBtLo, 64u * 128u);
+        const Desc dXwl = make_desc(sbase + K::kXw + K::kXLo, 64u * 128u);
+#pragma unroll
+        for (int kk = 0; kk < kQR / 16; ++kk) {
+          ptx::mma_bf16_ss(tmem + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXwl, koff_mn(kk)), kIdD, 1u);
+          ptx::mma_bf16_ss(tmem + kColD, desc_at(dBml, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD, 1u);
+        }
+      }
       if constexpr (!SO) {
         const Desc dBk = make_desc(opBt, 16u), dCk = make_desc(opCt, 16u);
 #pragma unroll
         for (int kk = 0; kk < NS / 16; ++kk)
           ptx::mma_bf16_ss(tmem + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
                            kIdS, kk > 0);
+        if constexpr (F32) {
+          const Desc dBkl = make_desc(opBt + K::kBtLo, 16u), dCkl = make_desc(opCt + K::kBtLo, 16u);
+#pragma unroll
+          for (int kk = 0; kk < NS / 16; ++kk) {
+            ptx::mma_bf16_ss(tmem + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBkl, koff_k(kk, 64)),
+                             kIdS, 1u);
+            ptx::mma_bf16_ss(tmem + kColS, desc_at(dCkl, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
+                             kIdS, 1u);
+          }
+        }
       }
       ptx::mma_commit(&bar_ds);
       last_commit = &bar_ds;
@@ -1066,6 +1225,17 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int kk = 0; kk < NS / 16; ++kk)
             ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)),
                              kIdYo, kk > 0);
+          if constexpr (F32) {
+            const Desc dCkl = make_desc(opCt + K::kBtLo, 16u);
+            const Desc dHl = make_desc(sbase + K::kH + K::kHLo, (uint32_t)NS * 128u);
+#pragma unroll
+            for (int kk = 0; kk < NS / 16; ++kk) {
+              ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dHl, koff_mn(kk)),
+                               kIdYo, 1u);
+              ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCkl, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)),
+                               kIdYo, 1u);
+            }
+          }
         }
         ptx::mma_commit(&bar_yo);
         last_commit = &bar_yo;
@@ -1093,32 +1263,42 @@ __global__ void __launch_bounds__(kThreads, 2)
           ptx::tmem_ld16_16x32bx2<16>(tmem + kColS + tq + 32u * half, sv);
           ptx::tmem_ld_wait(sv);
           {
-            const float invBC = sc.invB * sc.invC;
+            // S -> P units (a power of two: invB invC, times P's scale in F32)
+            const float invBC = sc.pmul;
             const float einv = (float)((int)((__float_as_uint(invBC) >> 23) & 0xffu) - 127);
             const float lt = sc.lam2[t] + einv;
             const float gdiag = sc.gam[t] * invBC;
-            constexpr int NT = 16 / R;  // distinct tokens among the 16 columns
             const int s0 = c0 / R;
-            float lsv[NT], wpv[NT];  // s0 is a multiple of NT >= 4: 16-byte aligned
-#pragma unroll
-            for (int u = 0; u < NT; u += 4) {
-              *reinterpret_cast<float4*>(&lsv[u]) = *reinterpret_cast<const float4*>(&sc.lam2[s0 + u]);
-              *reinterpret_cast<float4*>(&wpv[u]) = *reinterpret_cast<const float4*>(&sc.wp[s0 + u]);
-            }
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
-              // two columns at a time (packed fp32 pairs; same roundings as scalar)
+              // two columns at a time (packed fp32 pairs; same roundings as
+              // scalar), their decay terms read as they are needed
               const int u0 = j / R, u1 = (j + 1) / R;
-              const float2 dl = ptx::sub2(make_float2(lt, lt), make_float2(lsv[u0], lsv[u1]));
-              const float2 mo = mul2(make_float2(ex2(dl.x), ex2(dl.y)), make_float2(wpv[u0], wpv[u1]));
+              float2 lsp, wpp;
+              if constexpr (R == 1) {
+                lsp = *reinterpret_cast<const float2*>(&sc.lam2[s0 + u0]);
+                wpp = *reinterpret_cast<const float2*>(&sc.wp[s0 + u0]);
+              } else {
+                lsp = make_float2(sc.lam2[s0 + u0], sc.lam2[s0 + u1]);
+                wpp = make_float2(sc.wp[s0 + u0], sc.wp[s0 + u1]);
+              }
+              const float2 dl = ptx::sub2(make_float2(lt, lt), lsp);
+              const float2 mo = mul2(make_float2(ex2(dl.x), ex2(dl.y)), wpp);
               const float m0 = (s0 + u0 < t) ? mo.x : ((s0 + u0 == t) ? gdiag : 0.f);
               const float m1 = (s0 + u1 < t) ? mo.y : ((s0 + u1 == t) ? gdiag : 0.f);
               const float2 v2 = mul2(make_float2(m0, m1),
                                      make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])));
-              const uint32_t hw = pack_bf16(v2.x, v2.y);
-              ph_[j >> 1] = hw;
-              const float2 lo = ptx::sub2(v2, make_float2(bf_lo(hw), bf_hi(hw)));
-              pl_[j >> 1] = pack_bf16(lo.x, lo.y);
+              if constexpr (F32) {
+                // fp16 high part and residual (P is in units of its own scale)
+                const uint32_t hw = pack_f16(v2.x, v2.y);
+                ph_[j >> 1] = hw;
+                pl_[j >> 1] = f16_residual(hw, v2.x, v2.y);
+              } else {
+                const uint32_t hw = pack_bf16(v2.x, v2.y);
+                ph_[j >> 1] = hw;
+                const float2 lo = ptx::sub2(v2, make_float2(bf_lo(hw), bf_hi(hw)));
+                pl_[j >> 1] = pack_bf16(lo.x, lo.y);
+              }
             }
           }
         }
@@ -1146,6 +1326,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int kk = 0; kk < kQR / 16; ++kk)
           ptx::mma_bf16_ss(tmem + kColY, desc_at(dPl, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
                            kIdY, 1u);
+        if constexpr (F32) {
+          // ... + P_hi X_lo (the X tile is split too)
+          const Desc dXl = make_desc(sbase + K::kXo + K::kXLo, 64u * 128u);
+#pragma unroll
+          for (int kk = 0; kk < kQR / 16; ++kk)
+            ptx::mma_bf16_ss(tmem + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dXl, koff_mn(kk)),
+                             kIdY, 1u);
+        }
         ptx::mma_commit(&bar_y);
         last_commit = &bar_y;
       }
@@ -1185,7 +1373,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         ptx::tmem_ld_wait(yv);
         float y[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) y[j] = __uint_as_float(yv[j]);
+        for (int j = 0; j < 16; ++j) y[j] = F32 ? ykY * __uint_as_float(yv[j]) : __uint_as_float(yv[j]);
         if (yoff_ready) {
           uint32_t yo[16];
           ptx::tmem_ld16_16x32bx2<16>(tmem + kColYo + tq + 32u * half, yo);
@@ -1202,20 +1390,33 @@ __global__ void __launch_bounds__(kThreads, 2)
         if constexpr (R == 1) {
           const int64_t t = (int64_t)c * Q + a;
           if (t < p.L) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + ((((int64_t)b * p.L + t) * p.H + h) * kP + c0));
-            dst[0] = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                                pack_bf16(y[6], y[7]));
-            dst[1] = make_uint4(pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
-                                pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15]));
+            const int64_t e0 = (((int64_t)b * p.L + t) * p.H + h) * kP + c0;
+            if constexpr (F32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + e0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + e0);
+              dst[0] = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                                  pack_bf16(y[6], y[7]));
+              dst[1] = make_uint4(pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]),
+                                  pack_bf16(y[12], y[13]), pack_bf16(y[14], y[15]));
+            }
           }
         } else {
           // staging in the global layout of one chunk: [token][p][r]
           const int t = a / R, r = a % R;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            __nv_bfloat16 v = __float2bfloat16_rn(y[j]);
-            sts16(sbase + K::kYs + (uint32_t)((t * kP + c0 + j) * R + r) * 2u,
-                  *reinterpret_cast<uint16_t*>(&v));
+            const uint32_t e = (uint32_t)((t * kP + c0 + j) * R + r);
+            if constexpr (F32) {
+              asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + K::kYs + e * 4u), "f"(y[j])
+                           : "memory");
+            } else {
+              __nv_bfloat16 v = __float2bfloat16_rn(y[j]);
+              sts16(sbase + K::kYs + e * 2u, *reinterpret_cast<uint16_t*>(&v));
+            }
           }
           ptx::fence_proxy_async_smem();
         }
@@ -1249,6 +1450,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (tid < KP) sd[1 + tid] = s_fang[tid];
       } else if (c == nC - 1 && p.final_state) {
         // final state of the sequence, explicit frame: h = Rot(Phi_{L-1}) g
+        // (read from TMEM again rather than kept live through the output phase)
+        state_ld(hv);
         const float uBX = invB * invX;
         float* fs = p.final_state + ((int64_t)b * p.heads + h) * NS * kP;
 #pragma unroll
@@ -1335,25 +1538,27 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, c
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// x / out as a 4-D tensor {P*R, H, L, b}; the box is one head's chunk.
+// x / out as a 4-D tensor {P*R, H, L, b}; the box is one head's chunk
+// (bf16 with R = 1: 128-byte swizzled, the layout of the X operand).
 bool make_act_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
-  const uint64_t PR = (uint64_t)a.P * a.R;
+  const uint64_t PR = (uint64_t)a.P * a.R, es = a.f32 ? 4 : 2;
   cuuint64_t dims[4] = {PR, (cuuint64_t)a.H, (cuuint64_t)a.L, (cuuint64_t)a.batch};
-  cuuint64_t strides[3] = {PR * 2, PR * 2 * a.H, PR * 2 * a.H * a.L};
+  cuuint64_t strides[3] = {PR * es, PR * es * a.H, PR * es * a.H * a.L};
   cuuint32_t box[4] = {(cuuint32_t)PR, 1, (cuuint32_t)a.Q, 1};
-  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box,
-                a.R == 1 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+  return encode(m, a.f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                ptr, dims, strides, box,
+                (a.R == 1 && !a.f32) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // B / C [b, L, G, N, R] as a 5-D tensor {d0, N*R/d0, G, L, b} with d0 <= 256.
 bool make_bc_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
-  const uint64_t NR = (uint64_t)a.N * a.R;
+  const uint64_t NR = (uint64_t)a.N * a.R, es = a.f32 ? 4 : 2;
   const uint64_t d0 = NR < 256 ? NR : 256, d1 = NR / d0;
   cuuint64_t dims[5] = {d0, d1, (cuuint64_t)a.G, (cuuint64_t)a.L, (cuuint64_t)a.batch};
-  cuuint64_t strides[4] = {d0 * 2, NR * 2, NR * 2 * a.G, NR * 2 * a.G * a.L};
+  cuuint64_t strides[4] = {d0 * es, NR * es, NR * es * a.G, NR * es * a.G * a.L};
   cuuint32_t box[5] = {(cuuint32_t)d0, (cuuint32_t)d1, 1, (cuuint32_t)a.Q, 1};
-  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, ptr, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_NONE);
+  return encode(m, a.f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int num_sms() {
@@ -1450,10 +1655,10 @@ int device_sms() {
   return n > 0 ? n : 148;
 }
 
-template <int R, int NS, bool SO, bool NORM>
+template <int R, int NS, bool SO, bool NORM, bool F32>
 cudaError_t launch_pass(const CUtensorMap* maps, const TcParams& p, int64_t units, cudaStream_t s) {
-  constexpr uint32_t smem = Cfg<R, NS>::kSmem;
-  auto kern = scan_tc_kernel<R, NS, SO, NORM>;
+  constexpr uint32_t smem = Cfg<R, NS, F32>::kSmem;
+  auto kern = scan_tc_kernel<R, NS, SO, NORM, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // as much shared memory as the SM has, so that two CTAs fit
@@ -1487,7 +1692,7 @@ cudaError_t launch_pass(const CUtensorMap* maps, const TcParams& p, int64_t unit
   return cudaGetLastError();
 }
 
-template <int R, int NS, bool NORM>
+template <int R, int NS, bool NORM, bool F32>
 cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   // B, C, x and (R > 1: the output is stored by TMA) y
   CUtensorMap maps[4];
@@ -1496,7 +1701,7 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
     return cudaErrorInvalidValue;
   TcParams p;
   p.dt = a.dt; p.A = a.A; p.lam = a.lam; p.theta = a.theta;
-  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.out = a.out;
   p.B_bias = a.B_bias; p.C_bias = a.C_bias;
   p.final_state = a.final_state; p.status = status;
   p.L = a.L; p.H = a.H; p.G = a.G; p.batch = a.batch;
@@ -1513,7 +1718,7 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   p.nunits = (int)(nseq * pl.nseg);
   p.heads = (int)a.H;
   p.hpg = (int)(a.H / a.G);
-  if (pl.nseg <= 1) return launch_pass<R, NS, false, NORM>(maps, p, nseq, s);
+  if (pl.nseg <= 1) return launch_pass<R, NS, false, NORM, F32>(maps, p, nseq, s);
   // segmented: state-only pass, combine, full pass from the entering states
   const size_t need = seg_ws_bytes(a, pl);
   float* ws = static_cast<float*>(a.workspace);
@@ -1530,7 +1735,7 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   p.ws_scal = ws + units * a.N * a.P;
   p.final_state = nullptr;
   p.ws_hin = nullptr;  // the state-only pass starts every segment from zero
-  cudaError_t e = launch_pass<R, NS, true, NORM>(maps, p, units, s);
+  cudaError_t e = launch_pass<R, NS, true, NORM, F32>(maps, p, units, s);
   if (e == cudaSuccess) {
     const int64_t n = nseq * (a.N / 2) * a.P;
     seg_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws, p.ws_scal, a.h_init, nseq,
@@ -1541,7 +1746,7 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
     p.ws_state = nullptr;
     p.ws_hin = ws;
     p.final_state = a.final_state;
-    e = launch_pass<R, NS, false, NORM>(maps, p, units, s);
+    e = launch_pass<R, NS, false, NORM, F32>(maps, p, units, s);
   }
   if (owned) {
     const cudaError_t f = cudaFreeAsync(ws, s);
@@ -1567,24 +1772,31 @@ bool scan_tc_supported(int64_t N, int64_t P, int R, int Q) {
 cudaError_t launch_scan_tc(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   if (a.L > 0x7fffffffLL - 2 * kQR || a.batch > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int key = a.R * 1000 + (int)a.N;
+  if (a.bc_norm && a.f32) return cudaErrorInvalidValue;  // BCNorm is fused on the bf16 path only
   if (a.bc_norm) {
     switch (key) {
-      case 1064: return launch_rn<1, 64, true>(a, status, s);
-      case 1128: return launch_rn<1, 128, true>(a, status, s);
-      case 2064: return launch_rn<2, 64, true>(a, status, s);
-      case 2128: return launch_rn<2, 128, true>(a, status, s);
-      case 4064: return launch_rn<4, 64, true>(a, status, s);
-      case 4128: return launch_rn<4, 128, true>(a, status, s);
+      case 1064: return launch_rn<1, 64, true, false>(a, status, s);
+      case 1128: return launch_rn<1, 128, true, false>(a, status, s);
+      case 2064: return launch_rn<2, 64, true, false>(a, status, s);
+      case 2128: return launch_rn<2, 128, true, false>(a, status, s);
+      case 4064: return launch_rn<4, 64, true, false>(a, status, s);
+      case 4128: return launch_rn<4, 128, true, false>(a, status, s);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (key) {
-    case 1064: return launch_rn<1, 64, false>(a, status, s);
-    case 1128: return launch_rn<1, 128, false>(a, status, s);
-    case 2064: return launch_rn<2, 64, false>(a, status, s);
-    case 2128: return launch_rn<2, 128, false>(a, status, s);
-    case 4064: return launch_rn<4, 64, false>(a, status, s);
-    case 4128: return launch_rn<4, 128, false>(a, status, s);
+    case 1064: return a.f32 ? launch_rn<1, 64, false, true>(a, status, s)
+                      : launch_rn<1, 64, false, false>(a, status, s);
+    case 1128: return a.f32 ? launch_rn<1, 128, false, true>(a, status, s)
+                      : launch_rn<1, 128, false, false>(a, status, s);
+    case 2064: return a.f32 ? launch_rn<2, 64, false, true>(a, status, s)
+                      : launch_rn<2, 64, false, false>(a, status, s);
+    case 2128: return a.f32 ? launch_rn<2, 128, false, true>(a, status, s)
+                      : launch_rn<2, 128, false, false>(a, status, s);
+    case 4064: return a.f32 ? launch_rn<4, 64, false, true>(a, status, s)
+                      : launch_rn<4, 64, false, false>(a, status, s);
+    case 4128: return a.f32 ? launch_rn<4, 128, false, true>(a, status, s)
+                      : launch_rn<4, 128, false, false>(a, status, s);
     default: return cudaErrorInvalidValue;
   }
 }

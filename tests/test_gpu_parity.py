@@ -91,6 +91,31 @@ def test_tensor_core_shapes_bf16(orc, case):
     assert_bf16(fs, fs_ref, "final_state")
 
 
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: "L%d_Q%d_R%d_G%d_H%d_N%d_P%d" % c)
+def test_tensor_core_shapes_f32(orc, case):
+    """The fp32 mode on the tensor cores (split fp16 operands, three products
+    per contraction) at every tensor-core shape: relative L2 <= 1e-5."""
+    L, Q, R, G, H, N, P = case
+    shape = m3synth.ScanShape(2, L, H, G, P, N, R=R, chunk=Q, bf16=False, rms_bc=True)
+    inp = m3synth.scan_inputs(shape, seed=900 + L + R)
+    y, fs = _gpu_scan(inp, shape)
+    y_ref, fs_ref = _oracle(orc, inp)
+    assert_f32(y, y_ref, "y")
+    assert_f32(fs, fs_ref, "final_state")
+
+
+def test_segmented_prefill_f32(orc):
+    """Few sequences in the fp32 mode: the segmented tensor-core passes."""
+    shape = m3synth.ScanShape(1, 2000, 2, 1, 64, 128, R=1, chunk=64, bf16=False, rms_bc=True)
+    dims = m3.make_dims(1, 2000, 2, 1, 64, 128, m3.M3_F32)
+    assert m3.m3_scan_workspace_bytes(dims, 1, 64) > 0, "expected a segmented launch"
+    inp = m3synth.scan_inputs(shape, seed=41)
+    y, fs = _gpu_scan(inp, shape)
+    y_ref, fs_ref = _oracle(orc, inp)
+    assert_f32(y, y_ref, "y")
+    assert_f32(fs, fs_ref, "final_state")
+
+
 @pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: "L%d_Q%d_R%d_G%d_H%d_N%d_P%d" % c)
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 def test_small_shapes(orc, case, bf16):

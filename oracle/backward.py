@@ -2,14 +2,15 @@
 
 TEST INFRASTRUCTURE ONLY, like the rest of ``oracle/``: the tests are its only
 callers; the product library never imports it and it never imports the
-product library. It is the checker a backward kernel of the scan will be
-compared with; no such kernel exists yet.
+product library. It is the checker of the library's backward kernel
+(m3_scan_bwd; tests/test_gpu_parity.py, test_backward_matches_the_gradient_oracle).
 
 The forward is the sequential recurrence with explicit 2x2 rotations of the
-state (Prop. 1 of the aipaper.cc summary, sec. 4.1; the rotation of sec. 4.2,
-rotation matrix from the metaphor-xennon blog, sec. 2.2; MIMO rank R from
-papernotes.org, sec. 3), written here with torch tensor operations so that
-autograd differentiates it:
+state (Prop. 1 and the rotation, sec. 4.1 and 4.2 of the page
+"MAMBA-3: IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc); the rotation
+matrix, sec. 2.2 of "State Space Models 家族对比分析：S4 → Mamba → Mamba-2 → Mamba-3" (metaphor-xennon blog);
+MIMO rank R, sec. 3 of "Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org)),
+written here with torch tensor operations so that autograd differentiates it:
 
     U_t = (B_t + B_bias) x_t^T,  G_t = h_{t-1} + beta_hat_t U_{t-1}
     h_t = alpha_t Rot(Delta_t theta_t) G_t + gamma_t U_t,  y_t = (C_t + C_bias)^T h_t

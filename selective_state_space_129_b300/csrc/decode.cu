@@ -4,9 +4,12 @@
 //   G   = h + beta_hat (B_prev + bias) x_prev^T
 //   h' = alpha Rot(Delta theta) G + gamma (B + bias) x^T
 //   y   = (C + bias)^T h'                                   (P x R, stored [P][R])
-// which is the recurrence of Prop. 1 (aipaper.cc sec. 4.1) with the state
-// rotation of the complex-valued SSM (sec. 4.2; rotation matrix from the
-// metaphor-xennon blog sec. 2.2), MIMO rank R (papernotes.org sec. 3).
+// which is the recurrence of Prop. 1 with the state rotation of the
+// complex-valued SSM (sec. 4.1 and 4.2 of the page
+// "MAMBA-3: IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc); the
+// rotation matrix of sec. 2.2 of
+// "State Space Models 家族对比分析：S4 → Mamba → Mamba-2 → Mamba-3" (metaphor-xennon blog)),
+// with MIMO rank R (sec. 3 of "Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org)).
 //
 // The step is bound by HBM traffic: the fp32 state (N x P per head) is read
 // and written once, everything else is a few KB per head. The rank-R

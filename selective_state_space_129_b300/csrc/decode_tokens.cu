@@ -2,8 +2,9 @@
 // kept on chip between them.
 //
 // For every (batch, head) and t = 0 .. K-1 the step is the decode recurrence
-// (Prop. 1 of aipaper.cc sec. 4.1, rotation of sec. 4.2, MIMO rank R of
-// papernotes.org sec. 3):
+// (Prop. 1 and the rotation, sec. 4.1 and 4.2 of
+// "MAMBA-3: IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc); MIMO
+// rank R, sec. 3 of "Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org)):
 //   h_t = alpha_t Rot(Delta_t theta_t) (h_{t-1} + beta_hat_t B_{t-1} x_{t-1}^T)
 //         + gamma_t B_t x_t^T,        y_t = C_t^T h_t
 // where B_{t-1}, x_{t-1} is the previous token of the block (the caller's

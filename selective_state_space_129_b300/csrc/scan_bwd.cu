@@ -1,9 +1,10 @@
 // Backward pass of the Mamba-3 scan: the gradients of <y, dy> + <h_final,
 // d_final> for a prefill that starts from a zero state, on the CUDA cores.
 //
-// Forward (Prop. 1 of aipaper.cc sec. 4.1, the rotation of sec. 4.2, MIMO rank
-// R of papernotes.org sec. 3), per (batch, head), with Bb = B + B_bias and
-// Cb = C + C_bias:
+// Forward (Prop. 1 and the rotation, sec. 4.1 and 4.2 of
+// "MAMBA-3: IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc); MIMO
+// rank R, sec. 3 of "Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org)),
+// per (batch, head), with Bb = B + B_bias and Cb = C + C_bias:
 //   U_t = Bb_t x_t^T,  G_t = h_{t-1} + beta_hat_t U_{t-1},
 //   h_t = alpha_t Rot(phi_t) G_t + gamma_t U_t,  y_t = Cb_t^T h_t,
 //   phi_t = dt_t theta_t,  alpha = exp(dt A),  gamma = lambda dt,  beta_hat = (1 - lambda) dt.
@@ -27,7 +28,9 @@
 // registers. Reductions: over the 16 (P/4) lanes of a row pair by warp
 // shuffles, over row pairs through shared-memory atomics, and into the
 // gradients shared by heads, batches or tokens (dB, dC, dtheta, dA, the bias
-// gradients) by global atomics.
+// gradients) by global atomics. The order in which those atomics land varies
+// from run to run, so these gradients vary in their last bits between runs
+// (they are not bit-reproducible); the others are.
 #include <cuda_bf16.h>
 
 #include "common.cuh"

@@ -1,6 +1,7 @@
 // Entering state of a prefill that continues a sequence.
 //
-// The recurrence (Prop. 1 of aipaper.cc sec. 4.1) carries, besides the state
+// The recurrence (Prop. 1, sec. 4.1 of
+// "MAMBA-3: IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc)) carries, besides the state
 // h_{-1}, the previous token's B_{-1} x_{-1}^T into the first token through
 // its beta term: h_0 = alpha_0 R_0 (h_{-1} + beta_hat_0 B_{-1} x_{-1}^T) +
 // gamma_0 B_0 x_0^T. Both prefill kernels take the state entering their first

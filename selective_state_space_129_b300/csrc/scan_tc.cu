@@ -58,7 +58,7 @@
 //          a TMA store from a staging tile for R > 1); final state
 // The fp32 state lives in the TMEM columns of the D accumulator: each chunk
 // rescales it in place and the D MMA accumulates onto it. One warp computes
-// the next chunk's decay scan (warp shuffles) at the end of a chunk; theta is
+// the next chunk's decay scan (warp shuffles), in the mask phase; theta is
 // read from global memory into registers one chunk ahead.
 // Every mbarrier wait is bounded; on expiry the CTA records the status word,
 // every thread leaves the loop at the next block barrier, and the CTA still
@@ -500,12 +500,18 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
   __shared__ float s_fang[KP];                   // angle after a unit's last chunk
   __shared__ unsigned int s_max[2][3];  // per chunk parity: bounds of |B|, |C|, |x|
   __shared__ float s_red[kWarps];
+  __shared__ float s_red_unit[kWarps];  // the entering state's bound at a unit start
   __shared__ float s_bias_red[2][kWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nC = p.nchunks;
   // fold mapping: pairs k0, k0 + 1 (rows 4kk2 .. 4kk2 + 3), tokens tg*TPG ..
   const int kk2 = tid % KP2, tg = tid / KP2, k0 = 2 * kk2;
+  // The next chunk's decay scan: in the full pass by warp 4 during the mask
+  // phase (warp 4's 16 rows x 32 columns of S lie above the diagonal for
+  // every R, so it only writes zeros there); in the state-only pass by warp 0
+  // at the end of the chunk.
+  constexpr int kDecayWarp = SO ? 0 : 4;
   // accumulator mapping: TMEM lane quadrant, 32-column half
   const int quad = warp & 3, half = warp >> 2;
 
@@ -627,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
   sch.start(blockIdx.x, p);
   if (tid == 0) issue_raw(sch);
   DecayRaw dr;
-  if (warp == 0) {
+  if (warp == kDecayWarp) {
     load_decay_raw(p, sch, Q, lane, dr);
     decay_scan(dr, Q, lane, ss[0]);
   }
@@ -714,11 +720,11 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         has_state = true;
         if constexpr (!SO) {
           const float m = warp_max(abs_max(hv));
-          if (lane == 0) s_red[warp] = m;
+          if (lane == 0) s_red_unit[warp] = m;
           __syncthreads();
           float mm = 0.f;
 #pragma unroll
-          for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_red[w]);
+          for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_red_unit[w]);
           float h_sig;
           pow2_scale(mm, &h_sig, &h_inv_prev);
           write_hcopy(hv, h_sig);
@@ -1174,7 +1180,7 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
     // the next chunk's theta and decay inputs (loads only; used next chunk)
     if (has_next) {
       load_theta<KP, TPG>(p, nxt, Q, tg, k0, th);
-      if (warp == 0) load_decay_raw(p, nxt, Q, lane, dr);
+      if (warp == kDecayWarp) load_decay_raw(p, nxt, Q, lane, dr);
     }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before_sync();
@@ -1247,6 +1253,15 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       // ================================================= mask: P = S o Mask
       wait_or_abort(&bar_ds, (uint32_t)(g & 1), &abort_flag, p.status);
       ptx::tc_fence_after_sync();
+      // the bound of the state after D (for its fp16 copy below), published
+      // before the mask barrier so that the state phase needs no barrier of
+      // its own
+      state_ld(hv);
+      {
+        const float m = warp_max(abs_max(hv));
+        if (lane == 0) s_red[warp] = m;
+      }
+      if (warp == kDecayWarp && has_next) decay_scan(dr, Q, lane, ss[(g + 1) & 1]);
       {
         // thread -> row a, 16 consecutive columns c0 .. c0 + 15 of this warp's half
         const int a = 16 * quad + (lane & 15);
@@ -1338,18 +1353,13 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         last_commit = &bar_y;
       }
 
-      // ================================================= state: bound and fp16 copy
-      ptx::tc_fence_after_sync();
-      state_ld(hv);
-      {
-        const float m = warp_max(abs_max(hv));
-        if (lane == 0) s_red[warp] = m;
-      }
-      __syncthreads();  // ------------------------------------------ state bound
-      if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+      // ================================================= state: fp16 copy
+      // (the bound was published before the mask barrier)
       const float uBX = invB * invX;  // the TMEM state is sigma_B sigma_X h
       float h_inv = h_inv_prev;
       if (!last) {
+        ptx::tc_fence_after_sync();
+        state_ld(hv);
         float m = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) m = fmaxf(m, s_red[w]);
@@ -1477,15 +1487,24 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         }
       }
     }
-    // the next chunk's decay scan
-    if (warp == 0 && has_next) decay_scan(dr, Q, lane, ss[(g + 1) & 1]);
     ptx::tc_fence_before_sync();
-    __syncthreads();  // ------------------------------------------ end of chunk
-    if (!SO && R > 1 && tid == 0) {
-      ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, h, c * Q, b);
-      ptx::tma_store_commit();
+    // End of the chunk. The full pass at R = 1 needs no barrier here: every
+    // shared tile the next chunk overwrites was last read by this chunk's
+    // MMAs, whose completion each thread has waited for itself, and the next
+    // chunk's first barrier comes before any of its MMAs or TMEM reuse. The
+    // state-only pass (decay scan at the end) and R > 1 (the output staging
+    // lies over w X, and its TMA store reads it) meet here.
+    if constexpr (SO || R > 1) {
+      if constexpr (SO) {
+        if (warp == kDecayWarp && has_next) decay_scan(dr, Q, lane, ss[(g + 1) & 1]);
+      }
+      __syncthreads();  // ------------------------------------------ end of chunk
+      if (!SO && R > 1 && tid == 0) {
+        ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, h, c * Q, b);
+        ptx::tma_store_commit();
+      }
+      if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
     }
-    if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
     if (!has_next) break;
     sch = nxt;
   }

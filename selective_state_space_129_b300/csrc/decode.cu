@@ -711,6 +711,7 @@ bool decode_supported(int64_t N, int64_t P, int R) {
 
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s) {
   size_t smem = 0;
+  if (decode_mma_ok(a, bf16)) return launch_decode_mma(a, s);
   if (a.status != nullptr && stream_ok(a, bf16 ? 2 : 4, &smem))
     return bf16 ? launch_stream_t<__nv_bfloat16>(a, smem, s) : launch_stream_t<float>(a, smem, s);
   return bf16 ? launch_t<__nv_bfloat16>(a, s) : launch_t<float>(a, s);

@@ -119,6 +119,9 @@ cudaError_t launch_entry_state(float* state, const void* B_prev, const void* x_p
 // Decode step.
 bool decode_supported(int64_t N, int64_t P, int R);
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s);
+// bf16, R = 4, P = 64: the rank-R update on the tensor cores (mma.sync).
+bool decode_mma_ok(const DecodeArgs& a, bool bf16);
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 
 // K decode tokens in one launch, the state held on chip between them.
 bool tokens_supported(const TokensArgs& a, int act);

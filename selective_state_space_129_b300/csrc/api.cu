@@ -336,8 +336,8 @@ m3_status m3_decode_tokens(float* state, const void* x, const float* dt, const f
   m3::TokensArgs a;
   a.state = state; a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B_prev = B_prev;
   a.x_prev = x_prev; a.B = B; a.C = C; a.theta = theta; a.B_bias = dims->B_bias;
-  a.C_bias = dims->C_bias; a.out = out; a.batch = b; a.K = K; a.H = H; a.G = G; a.P = P;
-  a.N = N; a.R = R;
+  a.C_bias = dims->C_bias; a.out = out; a.status = nullptr; a.batch = b; a.K = K; a.H = H;
+  a.G = G; a.P = P; a.N = N; a.R = R;
   // the kernel moves every per-token block with 16-byte vectors
   const void* vec[] = {x, B, C, theta, B_prev, x_prev, dims->B_bias, dims->C_bias};
   for (const void* p : vec)
@@ -355,6 +355,9 @@ m3_status m3_decode_tokens(float* state, const void* x, const float* dt, const f
     if (f == M3_ERR_TIMEOUT) return M3_OK;
     if (f != M3_OK) return f;
   }
+  a.status = nullptr;
+  st = from_cuda(m3::status_word(&a.status));
+  if (st != M3_OK) return st;
   return from_cuda(m3::launch_decode_tokens(a, dims->act_dtype == M3_BF16,
                                             static_cast<cudaStream_t>(stream)));
 }

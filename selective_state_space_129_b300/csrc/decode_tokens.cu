@@ -395,6 +395,7 @@ bool tokens_supported(const TokensArgs& a, int act) {
 }
 
 cudaError_t launch_decode_tokens(const TokensArgs& a, bool bf16, cudaStream_t s) {
+  if (tokens_mma_ok(a, bf16)) return launch_tokens_mma(a, s);
   return bf16 ? launch_t<__nv_bfloat16>(a, s) : launch_t<float>(a, s);
 }
 

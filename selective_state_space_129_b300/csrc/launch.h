@@ -66,6 +66,7 @@ struct TokensArgs {
   const float* B_bias;
   const float* C_bias;
   void* out;
+  unsigned int* status;  // device word for expired waits (tensor-core kernel)
   int64_t batch, K, H, G, P, N;
   int R;
 };
@@ -126,6 +127,9 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 // K decode tokens in one launch, the state held on chip between them.
 bool tokens_supported(const TokensArgs& a, int act);
 cudaError_t launch_decode_tokens(const TokensArgs& a, bool bf16, cudaStream_t s);
+// bf16, R = 4, P = 64: the rank-R updates on the tensor cores (mma.sync).
+bool tokens_mma_ok(const TokensArgs& a, bool bf16);
+cudaError_t launch_tokens_mma(const TokensArgs& a, cudaStream_t s);
 
 // Fault injection (M3_FAULT=timeout): a kernel whose bounded wait runs out
 // after limit_ns, recording the expiry in the status word.

@@ -81,3 +81,43 @@ def test_decode_rank4_other_state_sizes_fall_back(orc, N):
     """N = 40 (not a multiple of 16), 144 and 256 (above 128) take the FMA
     streaming kernel, to the same bar."""
     _run(orc, 2, 4, 1, N, True, 2, seed=98)
+
+
+# ---------------------------------------------------------------- K tokens per call
+def _run_tokens(orc, batch, K, H, G, N, bias, prev, seed):
+    shape = m3synth.ScanShape(batch, K, H, G, 64, N, R=4, chunk=1, bf16=True)
+    inp = m3synth.scan_inputs(shape, seed=seed)
+    if not bias:
+        inp["B_bias"] = inp["C_bias"] = None
+    st0 = (0.5 * np.random.default_rng(seed).standard_normal((batch, H, N, 64))).astype(np.float32)
+    pv = m3synth.decode_inputs(shape, seed=seed + 1, step=0) if prev else None
+    d = to_device({k: v for k, v in inp.items() if v is not None}, True)
+    kw = {}
+    if pv is not None:
+        dp = to_device(pv, True)
+        kw = dict(B_prev=dp["B"], x_prev=dp["x"])
+    st = torch.from_numpy(st0).cuda()
+    out = m3.m3_decode_tokens(st, d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"],
+                              R=4, B_bias=d.get("B_bias"), C_bias=d.get("C_bias"), **kw)
+    torch.cuda.synchronize()
+    assert m3.m3_device_status() == m3.M3_OK
+    okw = dict(B_prev=pv["B"], x_prev=pv["x"]) if pv is not None else {}
+    y_ref, st_ref = orc.decode_tokens(st0, inp["x"], inp["dt"], inp["A"], inp["lam"], inp["B"],
+                                      inp["C"], inp["theta"], B_bias=inp["B_bias"],
+                                      C_bias=inp["C_bias"], **okw)
+    assert_bf16_out(out.float().cpu().numpy(), y_ref, "y")
+    e = max_over_rms(st.cpu().numpy(), st_ref)
+    assert e <= STATE_TOL, "state after %d tokens: max|err|/RMS %.3e" % (K, e)
+    return e
+
+
+@pytest.mark.parametrize("N,K,bias,prev", [
+    (16, 1, True, True),     # one token through the K-token kernel
+    (48, 5, False, False),   # no bias, no token before the block
+    (128, 8, True, True),    # the serving block: one window of eight tokens
+    (128, 16, True, True),   # three windows of tables (7, 7, 2 tokens)
+    (64, 24, True, False),   # two windows at N = 64
+])
+def test_decode_tokens_rank4_mma(orc, N, K, bias, prev):
+    e = _run_tokens(orc, 3, K, 8, 2, N, bias, prev, seed=200 + N + K)
+    print("decode tokens R=4 N=%d K=%d: state max|err|/RMS %.2e" % (N, K, e))

@@ -653,6 +653,14 @@ def bench_prefill_long(torch, m3, dev, args, peaks):
                      "tensor_frac": nflops / (ms * 1e-3) / 1e12 / peaks["bf16"],
                      "workspace_bytes": ws_bytes,
                      "inputs": "recipe distributions drawn on the device (torch RNG)"}
+        # the most the tensor pipe could be busy with the scan at the HBM
+        # roof: algorithmic FLOPs over the time the algorithmic bytes take
+        ceil = (nflops / 1e12 / peaks["bf16"]) / (nbytes / 1e9 / peaks["hbm"])
+        res[name]["tensor_frac_ceiling_at_hbm_roof"] = ceil
+        if ceil < 0.5:
+            res[name]["note"] = ("a 50%% tensor target is out of reach at this shape: even at "
+                                 "the HBM roof the tensor pipe could be at most %.0f%% busy"
+                                 % (100 * ceil))
         del d, out, fs, ws
         torch.cuda.empty_cache()
     return res

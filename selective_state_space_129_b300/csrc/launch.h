@@ -136,6 +136,11 @@ cudaError_t launch_tokens_mma(const TokensArgs& a, cudaStream_t s);
 cudaError_t launch_expired_wait(uint64_t limit_ns, cudaStream_t s);
 
 // Backward pass (CUDA cores, state checkpoints in a stream-ordered scratch).
+// bf16, P = 64, N in {64, 128}: the chunked backward on the tensor cores
+// (mma.sync TF32), with its workspace (bytes) given by the caller.
+bool scan_bwd_tc_ok(const BwdArgs& a, bool bf16);
+size_t scan_bwd_tc_workspace(const BwdArgs& a);
+cudaError_t launch_scan_bwd_tc(const BwdArgs& a, float* ws, cudaStream_t s);
 bool scan_bwd_supported(int64_t N, int64_t P, int R);
 cudaError_t launch_scan_bwd(const BwdArgs& a, bool bf16, cudaStream_t s);
 

@@ -418,6 +418,20 @@ cudaError_t launch_scan_bwd(const BwdArgs& a, bool bf16, cudaStream_t s) {
   if (e == cudaSuccess && a.dC_bias)
     e = cudaMemsetAsync(a.dC_bias, 0, sizeof(float) * a.H * a.N * a.R, s);
   if (e != cudaSuccess || nseq == 0 || a.L == 0) return e;
+  if (scan_bwd_tc_ok(a, bf16)) {
+    // the tensor-core path accumulates ddt and dlambda too (a chunk adds the
+    // trapezoid term of the token after it)
+    const size_t nt = (size_t)a.batch * a.L * a.H;
+    e = cudaMemsetAsync(a.ddt, 0, sizeof(float) * nt, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.dlam, 0, sizeof(float) * nt, s);
+    if (e != cudaSuccess) return e;
+    float* tws = nullptr;
+    e = cudaMallocAsync(reinterpret_cast<void**>(&tws), scan_bwd_tc_workspace(a), s);
+    if (e != cudaSuccess) return e;
+    e = launch_scan_bwd_tc(a, tws, s);
+    const cudaError_t f = cudaFreeAsync(tws, s);
+    return e == cudaSuccess ? f : e;
+  }
   float* ws = nullptr;
   e = cudaMallocAsync(reinterpret_cast<void**>(&ws), sizeof(float) * per * nseq, s);
   if (e != cudaSuccess) return e;

@@ -1,0 +1,846 @@
+// Backward pass of the Mamba-3 scan on the tensor cores: the gradients of
+// <y, dy> + <h_final, d_final> for a prefill from a zero state, bf16
+// activations, P = 64, N in {64, 128}, R in {1, 2, 4}.
+//
+// Forward (Prop. 1 and the rotation, sec. 4.1 and 4.2 of "MAMBA-3: IMPROVED
+// SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc); MIMO rank R,
+// sec. 3 of "Mamba-3: Improved Sequence Modeling using State Space
+// Principles" (papernotes.org)), written per chunk of Q = 64 / R tokens in the
+// chunk's own rotation frame. With chunk-local sums Lam_t = sum_{u<=t} dt_u A
+// and Phi_t[k] = sum_{u<=t} dt_u theta_u[k] (from the chunk's first token),
+// Bt_t = Rot(-Phi_t)(B_t + bias), Ct_t likewise, and H_in the explicit-frame
+// state entering the chunk (with the pending trapezoid term of its first token):
+//   y_t   = e^{Lam_t} Ct_t^T H_in + sum_{s<=t} W_ts (Ct_t . Bt_s) x_s,
+//   W_ts  = e^{Lam_t - Lam_s} (gamma_s + [s<t] bhat_{s+1}),
+//   H_out = Rot(Phi_end) (e^{Lam_end} H_in + sum_s w_s Bt_s x_s^T),
+//   w_s   = e^{Lam_end - Lam_s} (gamma_s + bhat_{s+1})
+// (bhat of the token after the chunk; 0 past the end). Flattening (token, rank)
+// into QR = 64 rows, S = Ct Bt^T, P = S o W and Y = P X + diag(e^Lam) Ct H_in
+// is the chunked form of the scan (papernotes.org sec. 1; SSD form
+// Y = (L o C B^T) X).
+//
+// Backward, per chunk, with dG = Rot(-Phi_end) dH_out (dH_out = d_final for
+// the last chunk) and H_in from a forward pass over the chunk boundaries:
+//   dP = dY X^T,  dS = dP o W,  dW_ts = sum over the rank block of S o dP
+//   dX  = P^T dY + diag(w) Bt dG
+//   dCt = dS Bt + diag(e^Lam) dY H_in^T,     dBt = dS^T Ct + diag(w) X dG^T
+//   dH_in = e^{Lam_end} dG + Ct^T diag(e^Lam) dY
+//   d e^{Lam_t} = rows of Ct . (dY H_in^T),  dw_s = rows of Bt . (X dG^T)
+// then the decay, trapezoid and rotation gradients:
+//   dl_u = sum_{s<u<=t} dW_ts W_ts + sum_{t>=u} d(e^Lam_t) e^Lam_t
+//          + sum_{s<u} dw_s w_s + e^{Lam_end} <dG, H_in>      (l_u = dt_u A)
+//   (the first sum is the exclusive prefix over v < u of column minus row
+//   sums of dW o W), dgamma_s, dbhat_{s+1} from column sums of dW o e^{Lam_t -
+//   Lam_s} and from dw_s; dB = Rot(Phi_t) dBt, dPhi_t = sum_r (dBt_0 Bt_1 -
+//   dBt_1 Bt_0) + the same for C + (at the chunk's last token) the rotation at
+//   its end; dphi_u = sum_{t>=u} dPhi_t within the chunk.
+//
+// Three launches:
+//   bwd_parts  one CTA per chunk: the chunk's contributions sum_s w_s Bt_s x_s^T
+//              and Ct^T diag(e^Lam) dY to the two state recurrences, and the
+//              chunk's Lam_end and Phi_end;
+//   bwd_scan   per (b, h, pair, column): the forward recurrence over chunks
+//              (H_in of every chunk) and the reverse one (dG of every chunk),
+//              elementwise, with the chunk-end rotation and decay gradients;
+//   bwd_chunk  one CTA per chunk: everything else.
+// Every contraction is mma.sync m16n8k8 TF32 (fp32 accumulation) from fp32
+// tiles in shared memory (x and dy are bf16 and exact in TF32). Gradients shared
+// by heads, batch rows or tokens (dB, dC, dtheta, dA, the biases, and ddt /
+// dlambda, which the next chunk's boundary term also adds to) are accumulated
+// with atomics, so their last bits vary between runs.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace m3 {
+namespace {
+
+constexpr int kBT = 512;  // threads of the chunk kernels
+constexpr int kRows = 64;  // flattened (token, rank) rows per chunk
+constexpr int kPd = 64;    // head dim
+constexpr int kSX = kPd + 4;  // word stride of the [64][P] tiles and of the [N][P] state tile
+
+template <int R, int NS>
+struct BCfg {
+  static constexpr int Q = kRows / R;
+  static constexpr int K2 = NS / 2;
+  static constexpr int SB = NS + 4;   // word stride of the [64][N] tiles
+  static constexpr int TG = kBT / K2;  // token groups of the fold
+  static constexpr int TPG = Q / TG;   // tokens per fold thread
+  static_assert(TPG >= 1 && Q % TG == 0, "token groups must divide the chunk");
+};
+
+// Per-token values of one chunk (index t < Q; bh has one more entry, the
+// token after the chunk).
+struct TokTab {
+  float lc[kRows];   // Lam_t, chunk-local inclusive sum of dt A
+  float dt[kRows], lm[kRows], gam[kRows];
+  float bh[kRows + 1];
+  float w[kRows], el[kRows];
+  float dtn, lmn;    // dt and lambda of the token after the chunk (0 past the end)
+};
+
+__device__ __forceinline__ float tf32r(float v) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+  return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// acc[nt] += A (rows m0 .. m0+15, K columns) x B (K rows, columns n0 + 8 nt ..),
+// operands fp32 (TF32-rounded) in shared memory. AT: A is stored transposed
+// (A[m][k] at A[k sa + m]), else row-major (A[m sa + k]). BKN: B is stored
+// row-major K x N (B[k sb + n]), else as its transpose (B[n sb + k]).
+template <int NT, bool AT, bool BKN>
+__device__ __forceinline__ void wgemm(float (&acc)[NT][4], const float* A, int sa, int m0,
+                                      const float* B, int sb, int n0, int K, int g, int tq) {
+#pragma unroll 2
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t a0, a1, a2, a3;
+    if (AT) {
+      a0 = __float_as_uint(A[(k0 + tq) * sa + m0 + g]);
+      a1 = __float_as_uint(A[(k0 + tq) * sa + m0 + g + 8]);
+      a2 = __float_as_uint(A[(k0 + tq + 4) * sa + m0 + g]);
+      a3 = __float_as_uint(A[(k0 + tq + 4) * sa + m0 + g + 8]);
+    } else {
+      a0 = __float_as_uint(A[(m0 + g) * sa + k0 + tq]);
+      a1 = __float_as_uint(A[(m0 + g + 8) * sa + k0 + tq]);
+      a2 = __float_as_uint(A[(m0 + g) * sa + k0 + tq + 4]);
+      a3 = __float_as_uint(A[(m0 + g + 8) * sa + k0 + tq + 4]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = n0 + 8 * nt + g;
+      uint32_t b0, b1;
+      if (BKN) {
+        b0 = __float_as_uint(B[(k0 + tq) * sb + n]);
+        b1 = __float_as_uint(B[(k0 + tq + 4) * sb + n]);
+      } else {
+        b0 = __float_as_uint(B[n * sb + k0 + tq]);
+        b1 = __float_as_uint(B[n * sb + k0 + tq + 4]);
+      }
+      mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
+#pragma unroll
+  for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+}
+
+// The chunk's per-token values, chunk-local angles, and the rotated Bt, Ct
+// tiles ([64][N] rows (t, r), TF32-rounded; zero past the sequence end).
+// Ph (optional): the angle table [Q][N/2]. s_gt: [TG][N/2] scratch.
+template <int R, int NS>
+__device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t h, int64_t gi,
+                                           int c0, int nv, float A_h, float* Bt, float* Ct,
+                                           float* Ph, TokTab& tk, float* s_gt, float* phi_end) {
+  using K = BCfg<R, NS>;
+  constexpr int Q = K::Q, K2 = K::K2, SB = K::SB, TPG = K::TPG;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t L = a.L, H = a.H, G = a.G;
+  if (tid <= Q) {
+    const int t = tid;
+    float d = 0.f, lm = 0.f;
+    if (c0 + t < L && (t < nv || t == Q)) {
+      const int64_t o = (b * L + c0 + t) * H + h;
+      d = a.dt[o];
+      lm = a.lam[o];
+    }
+    if (t < Q) {
+      tk.dt[t] = d;
+      tk.lm[t] = lm;
+      tk.gam[t] = lm * d;
+      tk.lc[t] = d * A_h;
+    } else {
+      tk.dtn = d;
+      tk.lmn = lm;
+    }
+    tk.bh[t] = (1.f - lm) * d;
+  }
+  __syncthreads();
+  // warp 0: the inclusive sum of dt A over the chunk, then w and e^Lam
+  if (tid < 32) {
+    float v0 = 2 * lane < Q ? tk.lc[2 * lane] : 0.f;
+    float v1 = 2 * lane + 1 < Q ? tk.lc[2 * lane + 1] : 0.f;
+    v1 += v0;
+    float s = v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += u;
+    }
+    const float excl = s - v1;
+    const float l0 = excl + v0, l1 = excl + v1;
+    const float lend = __shfl_sync(0xffffffffu, s, (Q - 1) / 2);
+    if (2 * lane < Q) tk.lc[2 * lane] = l0;
+    if (2 * lane + 1 < Q) tk.lc[2 * lane + 1] = l1;
+    __syncwarp();
+    if (2 * lane < Q) {
+      const int t = 2 * lane;
+      tk.el[t] = __expf(l0);
+      tk.w[t] = __expf(lend - l0) * (tk.gam[t] + tk.bh[t + 1]);
+    }
+    if (2 * lane + 1 < Q) {
+      const int t = 2 * lane + 1;
+      tk.el[t] = __expf(l1);
+      tk.w[t] = __expf(lend - l1) * (tk.gam[t] + tk.bh[t + 1]);
+    }
+  }
+  // the fold: thread (pair kk, token group tg), tokens tg TPG .. + TPG - 1
+  const int kk = tid % K2, tg = tid / K2;
+  float ang[TPG];
+  {
+    float run = 0.f;
+#pragma unroll
+    for (int j = 0; j < TPG; ++j) {
+      const int t = tg * TPG + j;
+      float phi = 0.f;
+      if (t < nv) phi = tk.dt[t] * a.theta[((b * L + c0 + t) * G + gi) * K2 + kk];
+      run += phi;
+      ang[j] = run;
+    }
+    s_gt[tg * K2 + kk] = run;
+  }
+  __syncthreads();
+  float off = 0.f;
+  for (int q = 0; q < tg; ++q) off += s_gt[q * K2 + kk];
+  const float* bbias = a.B_bias ? a.B_bias + (h * NS + 2 * kk) * R : nullptr;
+  const float* cbias = a.C_bias ? a.C_bias + (h * NS + 2 * kk) * R : nullptr;
+  const __nv_bfloat16* Bg = static_cast<const __nv_bfloat16*>(a.B);
+  const __nv_bfloat16* Cg = static_cast<const __nv_bfloat16*>(a.C);
+#pragma unroll
+  for (int j = 0; j < TPG; ++j) {
+    const int t = tg * TPG + j;
+    const float phi = off + ang[j];
+    if (Ph) Ph[t * K2 + kk] = phi;
+    if (phi_end && t == Q - 1) phi_end[kk] = phi;
+    float sn, cs;
+    __sincosf(wrap_angle(phi), &sn, &cs);
+    const int64_t bc = ((b * L + c0 + t) * G + gi) * NS * R + 2 * kk * R;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float b0 = 0.f, b1 = 0.f, q0 = 0.f, q1 = 0.f;
+      if (t < nv) {
+        b0 = __bfloat162float(Bg[bc + r]) + (bbias ? bbias[r] : 0.f);
+        b1 = __bfloat162float(Bg[bc + R + r]) + (bbias ? bbias[R + r] : 0.f);
+        q0 = __bfloat162float(Cg[bc + r]) + (cbias ? cbias[r] : 0.f);
+        q1 = __bfloat162float(Cg[bc + R + r]) + (cbias ? cbias[R + r] : 0.f);
+      }
+      const int row = t * R + r;
+      *reinterpret_cast<float2*>(Bt + row * SB + 2 * kk) =
+          make_float2(tf32r(cs * b0 + sn * b1), tf32r(cs * b1 - sn * b0));
+      *reinterpret_cast<float2*>(Ct + row * SB + 2 * kk) =
+          make_float2(tf32r(cs * q0 + sn * q1), tf32r(cs * q1 - sn * q0));
+    }
+  }
+  __syncthreads();
+}
+
+// A [64][P] activation tile (rows (t, r)) from x-like [b,L,H,P,R] bf16, each
+// row scaled by scale[t] (or not), zero past the sequence end.
+template <int R>
+__device__ __forceinline__ void load_act_tile(float* T, const __nv_bfloat16* src, int64_t b,
+                                              int64_t h, int64_t L, int64_t H, int c0, int nv,
+                                              const float* scale) {
+  constexpr int Q = kRows / R;
+  constexpr int PR = kPd * R;
+  for (int e = threadIdx.x * 8; e < Q * PR; e += kBT * 8) {
+    const int t = e / PR, rem = e - t * PR;
+    float v[8];
+    if (t < nv) {
+      const uint4 u = *reinterpret_cast<const uint4*>(src + ((b * L + c0 + t) * H + h) * PR + rem);
+      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(p2[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    const float sc = scale ? scale[t] : 1.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int p = (rem + i) / R, r = (rem + i) % R;
+      T[(t * R + r) * kSX + p] = scale ? tf32r(sc * v[i]) : v[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- parts
+
+template <int R, int NS>
+constexpr size_t parts_smem() {
+  using K = BCfg<R, NS>;
+  return sizeof(float) * (2 * kRows * K::SB + 2 * kRows * kSX + K::TG * K::K2) + sizeof(TokTab);
+}
+
+template <int R, int NS>
+__global__ void __launch_bounds__(kBT, 1)
+    bwd_parts_kernel(BwdArgs a, float* wsA, float* wsB, float* lam_end, float* phi_end, int nC) {
+  using K = BCfg<R, NS>;
+  constexpr int Q = K::Q, K2 = K::K2, SB = K::SB;
+  extern __shared__ float4 smf4[];
+  float* sm = reinterpret_cast<float*>(smf4);
+  float* Bt = sm;
+  float* Ct = Bt + kRows * SB;
+  float* Xw = Ct + kRows * SB;
+  float* Ye = Xw + kRows * kSX;
+  float* s_gt = Ye + kRows * kSX;
+  TokTab& tk = *reinterpret_cast<TokTab*>(s_gt + K::TG * K2);
+  const int c = blockIdx.x;
+  const int64_t bhi = blockIdx.y, b = bhi / a.H, h = bhi % a.H, gi = h / (a.H / a.G);
+  const int c0 = c * Q;
+  const int nv = (int)(a.L - c0 < Q ? a.L - c0 : Q);
+  const float A_h = a.A[h];
+  float* pe = phi_end + (bhi * nC + c) * K2;
+  chunk_prep<R, NS>(a, b, h, gi, c0, nv, A_h, Bt, Ct, nullptr, tk, s_gt, pe);
+  load_act_tile<R>(Xw, static_cast<const __nv_bfloat16*>(a.x), b, h, a.L, a.H, c0, nv, tk.w);
+  load_act_tile<R>(Ye, static_cast<const __nv_bfloat16*>(a.dy), b, h, a.L, a.H, c0, nv, tk.el);
+  if (threadIdx.x == 0) lam_end[bhi * nC + c] = tk.lc[Q - 1];
+  __syncthreads();
+  // [N][P] = Bt^T Xw and Ct^T Ye: warp tile 16 rows x (8 NT) columns
+  constexpr int MT = NS / 16, WPM = 16 / MT, NT = 8 / WPM;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+  const int m0 = 16 * (warp / WPM), n0 = 8 * NT * (warp % WPM);
+  float acc[NT][4];
+  const size_t slot = (size_t)(bhi * nC + c) * NS * kPd;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    zero_acc(acc);
+    wgemm<NT, true, true>(acc, pass ? Ct : Bt, SB, m0, pass ? Ye : Xw, kSX, n0, kRows, g, tq);
+    float* dst = (pass ? wsB : wsA) + slot;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = n0 + 8 * nt + 2 * tq;
+      *reinterpret_cast<float2*>(dst + (m0 + g) * kPd + col) = make_float2(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<float2*>(dst + (m0 + g + 8) * kPd + col) =
+          make_float2(acc[nt][2], acc[nt][3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- scan
+
+// One thread per (b, h, pair k, column p): the forward recurrence over the
+// chunk boundaries (wsA: the parts on entry, H_in of every chunk on exit) and
+// the reverse one (wsB: the parts on entry, dG of every chunk on exit), with
+// the chunk-end rotation's angle gradient (dphiB) and <dG, H_in> (dotgh).
+template <int NS>
+__global__ void __launch_bounds__(256)
+    bwd_scan_kernel(const float* __restrict__ lam_end, const float* __restrict__ phi_end,
+                    float* __restrict__ wsA, float* __restrict__ wsB,
+                    const float* __restrict__ d_final, float* __restrict__ dphiB,
+                    float* __restrict__ dotgh, int nC) {
+  constexpr int K2 = NS / 2;
+  constexpr int kB = 8;  // chunks whose loads are issued together
+  const int64_t bhi = blockIdx.x;
+  const int k = blockIdx.y * 4 + (int)(threadIdx.x >> 6), p = threadIdx.x & 63;
+  const int lane = threadIdx.x & 31;
+  const float* le = lam_end + bhi * nC;
+  const float* pe = phi_end + bhi * nC * K2 + k;
+  float* A0 = wsA + (size_t)bhi * nC * NS * kPd + (2 * k) * kPd + p;
+  float* B0 = wsB + (size_t)bhi * nC * NS * kPd + (2 * k) * kPd + p;
+  constexpr size_t kSlot = (size_t)NS * kPd;
+  float h0 = 0.f, h1 = 0.f;
+  for (int c1 = 0; c1 < nC; c1 += kB) {
+    const int n = nC - c1 < kB ? nC - c1 : kB;
+    float g0[kB], g1[kB], e[kB], ph[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j)
+      if (j < n) {
+        const float* q = A0 + (c1 + j) * kSlot;
+        g0[j] = q[0];
+        g1[j] = q[kPd];
+        e[j] = le[c1 + j];
+        ph[j] = pe[(c1 + j) * K2];
+      }
+#pragma unroll
+    for (int j = 0; j < kB; ++j)
+      if (j < n) {
+        float* q = A0 + (c1 + j) * kSlot;
+        q[0] = h0;
+        q[kPd] = h1;
+        float sn, cs;
+        __sincosf(wrap_angle(ph[j]), &sn, &cs);
+        const float ee = __expf(e[j]);
+        const float G0 = fmaf(ee, h0, g0[j]), G1 = fmaf(ee, h1, g1[j]);
+        h0 = cs * G0 - sn * G1;
+        h1 = sn * G0 + cs * G1;
+      }
+  }
+  float dh0 = 0.f, dh1 = 0.f;
+  if (d_final) {
+    const float* df = d_final + (size_t)bhi * NS * kPd + (2 * k) * kPd + p;
+    dh0 = df[0];
+    dh1 = df[kPd];
+  }
+  float o0 = h0, o1 = h1;  // the state leaving chunk c
+  for (int c1 = nC - 1; c1 >= 0; c1 -= kB) {
+    const int n = c1 + 1 < kB ? c1 + 1 : kB;  // chunks c1, c1 - 1, .., c1 - n + 1
+    float i0[kB], i1[kB], d0[kB], d1[kB], e[kB], ph[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j)
+      if (j < n) {
+        const int c = c1 - j;
+        i0[j] = A0[c * kSlot];
+        i1[j] = A0[c * kSlot + kPd];
+        d0[j] = B0[c * kSlot];
+        d1[j] = B0[c * kSlot + kPd];
+        e[j] = le[c];
+        ph[j] = pe[c * K2];
+      }
+#pragma unroll
+    for (int j = 0; j < kB; ++j)
+      if (j < n) {
+        const int c = c1 - j;
+        float sn, cs;
+        __sincosf(wrap_angle(ph[j]), &sn, &cs);
+        const float dg0 = cs * dh0 + sn * dh1, dg1 = cs * dh1 - sn * dh0;
+        float dp = dh1 * o0 - dh0 * o1;
+        float dot = dg0 * i0[j] + dg1 * i1[j];
+        B0[c * kSlot] = dg0;
+        B0[c * kSlot + kPd] = dg1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          dp += __shfl_xor_sync(0xffffffffu, dp, o);
+          dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        }
+        if (lane == 0) {
+          atomicAdd(dphiB + (bhi * nC + c) * K2 + k, dp);
+          atomicAdd(dotgh + bhi * nC + c, dot);
+        }
+        const float ee = __expf(e[j]);
+        dh0 = fmaf(ee, dg0, d0[j]);
+        dh1 = fmaf(ee, dg1, d1[j]);
+        o0 = i0[j];
+        o1 = i1[j];
+      }
+  }
+}
+
+// ---------------------------------------------------------------- chunk
+
+template <int R, int NS>
+constexpr size_t chunk_smem() {
+  using K = BCfg<R, NS>;
+  return sizeof(float) * (2 * kRows * K::SB + 4 * kRows * kSX + NS * kSX + 2 * K::Q * K::K2 +
+                          K::TG * K::K2 + 8 * kRows) +
+         sizeof(TokTab);
+}
+
+template <int R, int NS>
+__global__ void __launch_bounds__(kBT, 1)
+    bwd_chunk_kernel(BwdArgs a, const float* wsA, const float* wsB, const float* dphiB,
+                     const float* dotgh, int nC) {
+  using K = BCfg<R, NS>;
+  constexpr int Q = K::Q, K2 = K::K2, SB = K::SB;
+  extern __shared__ float4 smf4[];
+  float* sm = reinterpret_cast<float*>(smf4);
+  float* Bt = sm;
+  float* Ct = Bt + kRows * SB;
+  float* Xs = Ct + kRows * SB;
+  float* Ys = Xs + kRows * kSX;
+  float* Ps = Ys + kRows * kSX;
+  float* dSs = Ps + kRows * kSX;
+  float* St = dSs + kRows * kSX;  // [N][P]: H_in, then dG
+  float* Ph = St + NS * kSX;      // [Q][K2] angles
+  float* dPh = Ph + Q * K2;       // [Q][K2] angle gradients
+  float* s_gt = dPh + Q * K2;
+  float* colVi = s_gt + K::TG * K2;  // per token: column sums and row sums (64 each)
+  float* colVs = colVi + kRows;
+  float* colZ = colVs + kRows;
+  float* rowZ = colZ + kRows;
+  float* elg = rowZ + kRows;
+  float* dwv = elg + kRows;
+  float* ths = dwv + kRows;
+  float* dlv = ths + kRows;
+  TokTab& tk = *reinterpret_cast<TokTab*>(dlv + kRows);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
+  const int c = blockIdx.x;
+  const int64_t bhi = blockIdx.y, b = bhi / a.H, h = bhi % a.H, gi = h / (a.H / a.G);
+  const int64_t L = a.L, H = a.H, G = a.G;
+  const int c0 = c * Q;
+  const int nv = (int)(L - c0 < Q ? L - c0 : Q);
+  const float A_h = a.A[h];
+  const size_t slot = (size_t)(bhi * nC + c) * NS * kPd;
+
+  for (int i = tid; i < 8 * kRows; i += kBT) colVi[i] = 0.f;
+  for (int i = tid; i < Q * K2; i += kBT) dPh[i] = 0.f;
+  chunk_prep<R, NS>(a, b, h, gi, c0, nv, A_h, Bt, Ct, Ph, tk, s_gt, nullptr);
+  load_act_tile<R>(Xs, static_cast<const __nv_bfloat16*>(a.x), b, h, L, H, c0, nv, nullptr);
+  load_act_tile<R>(Ys, static_cast<const __nv_bfloat16*>(a.dy), b, h, L, H, c0, nv, nullptr);
+  for (int e = tid * 4; e < NS * kPd; e += kBT * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(wsA + slot + e);
+    const int n = e / kPd, p = e - n * kPd;
+    *reinterpret_cast<float4*>(St + n * kSX + p) =
+        make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
+  }
+  __syncthreads();
+
+  // ---- S = Ct Bt^T, dP = dY X^T (64 x 64; warp tile 16 x 16), the masks
+  {
+    const int m0 = 16 * (warp >> 2), n0 = 16 * (warp & 3);
+    float aS[2][4], aP[2][4];
+    zero_acc(aS);
+    zero_acc(aP);
+    wgemm<2, false, false>(aS, Ct, SB, m0, Bt, SB, n0, NS, g, tq);
+    wgemm<2, false, false>(aP, Ys, kSX, m0, Xs, kSX, n0, kPd, g, tq);
+    float rz[2] = {0.f, 0.f};
+    float cvi[2][2], cvs[2][2], cz[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) cvi[nt][q] = cvs[nt][q] = cz[nt][q] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + g + 8 * (e >> 1), j = n0 + 8 * nt + 2 * tq + (e & 1);
+        const int t = i / R, s = j / R;
+        float pv = 0.f, dsv = 0.f;
+        if (t >= s) {
+          const float D = __expf(tk.lc[t] - tk.lc[s]);
+          const float f = tk.gam[s] + (s < t ? tk.bh[s + 1] : 0.f);
+          const float M = D * f;
+          pv = aS[nt][e] * M;
+          dsv = aP[nt][e] * M;
+          const float sd = aS[nt][e] * aP[nt][e] * D;
+          cvi[nt][e & 1] += sd;
+          if (s < t) {
+            const float z = sd * f;
+            cvs[nt][e & 1] += sd;
+            cz[nt][e & 1] += z;
+            rz[e >> 1] += z;
+          }
+        }
+        Ps[i * kSX + j] = tf32r(pv);
+        dSs[i * kSX + j] = tf32r(dsv);
+      }
+    // column sums over the warp's 16 rows (lanes that differ in g)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          cvi[nt][q] += __shfl_xor_sync(0xffffffffu, cvi[nt][q], o);
+          cvs[nt][q] += __shfl_xor_sync(0xffffffffu, cvs[nt][q], o);
+          cz[nt][q] += __shfl_xor_sync(0xffffffffu, cz[nt][q], o);
+        }
+        if (g == 0) {
+          const int s = (n0 + 8 * nt + 2 * tq + q) / R;
+          atomicAdd(&colVi[s], cvi[nt][q]);
+          atomicAdd(&colVs[s], cvs[nt][q]);
+          atomicAdd(&colZ[s], cz[nt][q]);
+        }
+      }
+    // row sums over the warp's 16 columns (lanes that differ in tq)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      rz[q] += __shfl_xor_sync(0xffffffffu, rz[q], 1);
+      rz[q] += __shfl_xor_sync(0xffffffffu, rz[q], 2);
+      if (tq == 0) atomicAdd(&rowZ[(m0 + g + 8 * q) / R], rz[q]);
+    }
+  }
+  __syncthreads();
+
+  // ---- dCt = diag(e^Lam) dY H_in^T + dS Bt, and dBt = diag(w) X dG^T + dS^T Ct
+  //      (64 x N; warp tile 16 x N/4), each followed by the rotation backward
+  constexpr int NT3 = NS / 32;
+  const int m0 = 16 * (warp >> 2), n0 = (NS / 4) * (warp & 3);
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1) {
+      // the state tile: H_in -> dG
+      __syncthreads();
+      for (int e = tid * 4; e < NS * kPd; e += kBT * 4) {
+        const float4 v = *reinterpret_cast<const float4*>(wsB + slot + e);
+        const int n = e / kPd, p = e - n * kPd;
+        *reinterpret_cast<float4*>(St + n * kSX + p) =
+            make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
+      }
+      __syncthreads();
+    }
+    const float* Own = pass ? Bt : Ct;   // the tile whose gradient this is
+    const float* Oth = pass ? Ct : Bt;   // the other factor of S
+    float acc[NT3][4];
+    zero_acc(acc);
+    // E = (pass 0) dY H_in^T, (pass 1) X dG^T
+    wgemm<NT3, false, false>(acc, pass ? Xs : Ys, kSX, m0, St, kSX, n0, kPd, g, tq);
+    // row dots with the own tile: d e^Lam_t (pass 0), dw_s (pass 1)
+    {
+      float rd[2] = {0.f, 0.f};
+#pragma unroll
+      for (int nt = 0; nt < NT3; ++nt) {
+        const int col = n0 + 8 * nt + 2 * tq;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float2 o = *reinterpret_cast<const float2*>(Own + (m0 + g + 8 * q) * SB + col);
+          rd[q] = fmaf(o.x, acc[nt][2 * q], fmaf(o.y, acc[nt][2 * q + 1], rd[q]));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        rd[q] += __shfl_xor_sync(0xffffffffu, rd[q], 1);
+        rd[q] += __shfl_xor_sync(0xffffffffu, rd[q], 2);
+        if (tq == 0) atomicAdd(&(pass ? dwv : elg)[(m0 + g + 8 * q) / R], rd[q]);
+      }
+    }
+    // scale the rows: e^Lam_t (pass 0), w_s (pass 1)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int t = (m0 + g + 8 * q) / R;
+      const float sc = pass ? tk.w[t] : tk.el[t];
+#pragma unroll
+      for (int nt = 0; nt < NT3; ++nt) {
+        acc[nt][2 * q] *= sc;
+        acc[nt][2 * q + 1] *= sc;
+      }
+    }
+    // + dS Oth (pass 0) or dS^T Oth (pass 1)
+    if (pass == 0)
+      wgemm<NT3, false, true>(acc, dSs, kSX, m0, Oth, SB, n0, kRows, g, tq);
+    else
+      wgemm<NT3, true, true>(acc, dSs, kSX, m0, Oth, SB, n0, kRows, g, tq);
+    // rotation backward: the raw gradient Rot(Phi_t) d, the angle gradient,
+    // and the bias gradient (summed over the warp's rows of equal rank)
+    float* graw = pass ? a.dB : a.dC;
+    float* gbias = pass ? a.dB_bias : a.dC_bias;
+#pragma unroll
+    for (int nt = 0; nt < NT3; ++nt) {
+      const int col = n0 + 8 * nt + 2 * tq, k = col >> 1;
+      float bs0 = 0.f, bs1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int i = m0 + g + 8 * q, t = i / R, r = i % R;
+        const float d0 = acc[nt][2 * q], d1 = acc[nt][2 * q + 1];
+        const float2 o = *reinterpret_cast<const float2*>(Own + i * SB + col);
+        atomicAdd(&dPh[t * K2 + k], d0 * o.y - d1 * o.x);
+        float sn, cs;
+        __sincosf(wrap_angle(Ph[t * K2 + k]), &sn, &cs);
+        const float r0 = cs * d0 - sn * d1, r1 = sn * d0 + cs * d1;
+        if (t < nv) {
+          float* dst = graw + ((b * L + c0 + t) * G + gi) * NS * R + col * R + r;
+          if (R == 1) {
+            atomicAdd(reinterpret_cast<float2*>(dst), make_float2(r0, r1));
+          } else {
+            atomicAdd(dst, r0);
+            atomicAdd(dst + R, r1);
+          }
+        }
+        bs0 += r0;
+        bs1 += r1;
+      }
+      if (gbias) {
+        // rows m0 + g and m0 + g + 8 have rank g % R: sum over the lanes of equal rank
+#pragma unroll
+        for (int o = 4 * R; o < 32; o <<= 1) {
+          bs0 += __shfl_xor_sync(0xffffffffu, bs0, o);
+          bs1 += __shfl_xor_sync(0xffffffffu, bs1, o);
+        }
+        if (g < R) {
+          atomicAdd(gbias + (h * NS + col) * R + g, bs0);
+          atomicAdd(gbias + (h * NS + col + 1) * R + g, bs1);
+        }
+      }
+    }
+  }
+
+  // ---- dX = P^T dY + diag(w) Bt dG (64 x 64; warp tile 16 x 16)
+  {
+    const int xm0 = 16 * (warp >> 2), xn0 = 16 * (warp & 3);
+    float a1[2][4], a2[2][4];
+    zero_acc(a1);
+    zero_acc(a2);
+    wgemm<2, true, true>(a1, Ps, kSX, xm0, Ys, kSX, xn0, kRows, g, tq);
+    wgemm<2, false, true>(a2, Bt, SB, xm0, St, kSX, xn0, NS, g, tq);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int j = xm0 + g + 8 * q, s = j / R, r = j % R;
+      if (s >= nv) continue;
+      const float ws = tk.w[s];
+      float* dst = a.dx + ((b * L + c0 + s) * H + h) * kPd * R + r;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int p = xn0 + 8 * nt + 2 * tq;
+        dst[p * R] = fmaf(ws, a2[nt][2 * q], a1[nt][2 * q]);
+        dst[(p + 1) * R] = fmaf(ws, a2[nt][2 * q + 1], a1[nt][2 * q + 1]);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- the angle gradients: the chunk-end rotation at the last token, the
+  //      reverse sum over the chunk's tokens, dtheta, and theta . dphi per
+  //      token; thread (pair kk, token group tg) as in the fold
+  {
+    constexpr int TG = K::TG, TPG = K::TPG;
+    const int kk = tid % K2, tg = tid / K2;
+    float th[TPG], run[TPG];
+    float acc = (tg == TG - 1) ? dphiB[(bhi * nC + c) * K2 + kk] : 0.f;
+#pragma unroll
+    for (int j = TPG - 1; j >= 0; --j) {
+      const int t = tg * TPG + j;
+      th[j] = t < nv ? a.theta[((b * L + c0 + t) * G + gi) * K2 + kk] : 0.f;
+      acc += dPh[t * K2 + kk];
+      run[j] = acc;
+    }
+    s_gt[tg * K2 + kk] = acc;
+    __syncthreads();
+    float off = 0.f;
+    for (int q = tg + 1; q < TG; ++q) off += s_gt[q * K2 + kk];
+#pragma unroll
+    for (int j = 0; j < TPG; ++j) {
+      const int t = tg * TPG + j;
+      const float dphi = off + run[j];
+      if (t < nv) atomicAdd(a.dtheta + ((b * L + c0 + t) * G + gi) * K2 + kk, tk.dt[t] * dphi);
+      // theta . dphi over the pairs: a warp holds 32 pairs of one token
+      float v = th[j] * dphi;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) atomicAdd(&ths[t], v);
+    }
+  }
+  __syncthreads();
+
+  // ---- decay and trapezoid gradients per token (warp 0, two tokens a lane)
+  if (warp == 0) {
+    const float lend = tk.lc[Q - 1];
+    const float eend = __expf(lend) * dotgh[bhi * nC + c];
+    float fz[2], fe[2], fw[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int u = 2 * lane + q;
+      fz[q] = u < Q ? colZ[u] - rowZ[u] : 0.f;
+      fe[q] = u < Q ? elg[u] * tk.el[u] : 0.f;
+      fw[q] = u < Q ? dwv[u] * tk.w[u] : 0.f;
+    }
+    // exclusive prefix of fz and fw, inclusive suffix of fe (over u = 2 lane + q)
+    float pz = fz[0] + fz[1], pw = fw[0] + fw[1], se = fe[0] + fe[1];
+    float iz = pz, iw = pw, is = se;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float uz = __shfl_up_sync(0xffffffffu, iz, o);
+      const float uw = __shfl_up_sync(0xffffffffu, iw, o);
+      const float us = __shfl_down_sync(0xffffffffu, is, o);
+      if (lane >= o) {
+        iz += uz;
+        iw += uw;
+      }
+      if (lane + o < 32) is += us;
+    }
+    const float ez = iz - pz, ew = iw - pw;  // sums over u' < 2 lane
+    const float es = is - se;                // sum over u' > 2 lane + 1
+    float dA_part = 0.f;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int u = 2 * lane + q;
+      const float F = ez + (q ? fz[0] : 0.f);
+      const float Sw = ew + (q ? fw[0] : 0.f);
+      const float Se = es + fe[1] + (q ? 0.f : fe[0]);
+      if (u < nv) {
+        const float dl = F + Se + Sw + eend;
+        const float dgam = colVi[u] + dwv[u] * __expf(lend - tk.lc[u]);
+        const float dbh = u >= 1 ? colVs[u - 1] + dwv[u - 1] * __expf(lend - tk.lc[u - 1]) : 0.f;
+        const float d = tk.dt[u], lm = tk.lm[u];
+        const int64_t o = (b * L + c0 + u) * H + h;
+        atomicAdd(a.ddt + o, A_h * dl + lm * dgam + (1.f - lm) * dbh + ths[u]);
+        atomicAdd(a.dlam + o, d * (dgam - dbh));
+        dA_part = fmaf(d, dl, dA_part);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dA_part += __shfl_xor_sync(0xffffffffu, dA_part, o);
+    if (lane == 0) {
+      atomicAdd(a.dA + h, dA_part);
+      // the trapezoid weight of the token after the chunk enters this chunk's w
+      if (c0 + Q < L) {
+        const float dbn = dwv[Q - 1];
+        const int64_t o = (b * L + c0 + Q) * H + h;
+        atomicAdd(a.ddt + o, (1.f - tk.lmn) * dbn);
+        atomicAdd(a.dlam + o, -tk.dtn * dbn);
+      }
+    }
+  }
+}
+
+template <int R, int NS>
+cudaError_t launch_rn(const BwdArgs& a, float* ws, int nC, cudaStream_t s) {
+  constexpr int K2 = NS / 2;
+  const int64_t nbh = a.batch * a.H;
+  const size_t big = (size_t)nbh * nC * NS * kPd;
+  float* wsA = ws;
+  float* wsB = wsA + big;
+  float* lam_end = wsB + big;
+  float* phi_end = lam_end + (size_t)nbh * nC;
+  float* dphiB = phi_end + (size_t)nbh * nC * K2;
+  float* dotgh = dphiB + (size_t)nbh * nC * K2;
+  cudaError_t e = cudaMemsetAsync(dphiB, 0, sizeof(float) * (size_t)nbh * nC * (K2 + 1), s);
+  if (e != cudaSuccess) return e;
+  const size_t sp = parts_smem<R, NS>(), sc = chunk_smem<R, NS>();
+  e = cudaFuncSetAttribute(bwd_parts_kernel<R, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sp);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_chunk_kernel<R, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sc);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)nC, (unsigned)nbh);
+  bwd_parts_kernel<R, NS><<<grid, kBT, sp, s>>>(a, wsA, wsB, lam_end, phi_end, nC);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_scan_kernel<NS><<<dim3((unsigned)nbh, (unsigned)(K2 / 4)), 256, 0, s>>>(
+      lam_end, phi_end, wsA, wsB, a.d_final, dphiB, dotgh, nC);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_chunk_kernel<R, NS><<<grid, kBT, sc, s>>>(a, wsA, wsB, dphiB, dotgh, nC);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool scan_bwd_tc_ok(const BwdArgs& a, bool bf16) {
+  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!bf16 || a.P != kPd || !(a.N == 64 || a.N == 128)) return false;
+  if (!(a.R == 1 || a.R == 2 || a.R == 4)) return false;
+  if (a.batch * a.H > 65535) return false;  // grid y
+  const int64_t Q = kRows / a.R, nC = (a.L + Q - 1) / Q;
+  if (nC > 0x7fffffffLL) return false;
+  // 16-byte vectors of x / dy rows, 8-byte atomics of dB / dC at R = 1
+  if (!al(a.x) || !al(a.dy) || !al(a.dB) || !al(a.dC)) return false;
+  return true;
+}
+
+size_t scan_bwd_tc_workspace(const BwdArgs& a) {
+  const int64_t Q = kRows / a.R, nC = (a.L + Q - 1) / Q, nbh = a.batch * a.H;
+  return sizeof(float) * ((size_t)nbh * nC * (2 * a.N * kPd + 1 + a.N + 1));
+}
+
+cudaError_t launch_scan_bwd_tc(const BwdArgs& a, float* ws, cudaStream_t s) {
+  const int nC = (int)((a.L + kRows / a.R - 1) / (kRows / a.R));
+  switch (a.R * 1000 + (int)a.N) {
+    case 1064: return launch_rn<1, 64>(a, ws, nC, s);
+    case 1128: return launch_rn<1, 128>(a, ws, nC, s);
+    case 2064: return launch_rn<2, 64>(a, ws, nC, s);
+    case 2128: return launch_rn<2, 128>(a, ws, nC, s);
+    case 4064: return launch_rn<4, 64>(a, ws, nC, s);
+    case 4128: return launch_rn<4, 128>(a, ws, nC, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace m3

@@ -425,6 +425,7 @@ def run_ours(args, rank, world, local_rank):
         "decode_mimo_r4": bench_decode(torch, m3, dev, "decode_mimo", peaks, fp32=True)}
     line["prefill_chunked"] = bench_prefill_chunked(torch, m3, dev, args)
     line["prefill_backward"] = bench_backward(torch, m3, dev)
+    line["prefill_backward"]["over_forward"] = line["prefill_backward"]["ms"] / ms
     line["prefill_long"] = bench_prefill_long(torch, m3, dev, args, peaks)
     line["decode"] = {"siso": bench_decode(torch, m3, dev, "decode_siso", peaks),
                       "mimo_r4": bench_decode(torch, m3, dev, "decode_mimo", peaks)}
@@ -561,11 +562,16 @@ def bench_backward(torch, m3, dev, reps=3):
                        generator=gen)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    # the scratch a training loop allocates once and passes to every call
+    dims = m3.make_dims(shape.batch, shape.seqlen, shape.heads, shape.groups, shape.headdim,
+                        shape.dstate, m3.M3_BF16)
+    ws_bytes = m3.m3_scan_bwd_workspace_bytes(dims, shape.R)
+    ws = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device=dev)
 
     def launch():
         m3.m3_scan_bwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"], dy,
                        R=shape.R, d_final=dfin, B_bias=d["B_bias"], C_bias=d["C_bias"],
-                       stream=stream)
+                       stream=stream, workspace=ws)
 
     launch()
     times = []
@@ -580,8 +586,9 @@ def bench_backward(torch, m3, dev, reps=3):
     ms = sum(times) / len(times)
     return {"workload": "prefill_siso b%d L%d H%d P%d N%d R%d, backward (all gradients)" % (
                 shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate, shape.R),
-            "tok_s": shape.tokens / (ms * 1e-3), "ms": ms,
-            "kernel": "CUDA cores, one CTA per (b, h), state checkpoints every 64 tokens"}
+            "tok_s": shape.tokens / (ms * 1e-3), "ms": ms, "workspace_bytes": ws_bytes,
+            "kernel": "chunked on the tensor cores (mma.sync TF32): chunk contributions, "
+                      "boundary-state scans, per-chunk gradients"}
 
 
 def device_inputs(torch, shape, dev, seed):

@@ -161,10 +161,16 @@ m3_status m3_scan_fwd_state(const void* x, const float* dt, const float* A, cons
  * dB and dC [b,L,G,N,R] (summed over the heads of a group), dtheta
  * [b,L,G,N/2], dB_bias and dC_bias [H,N,R] (each may be NULL: not computed).
  * R in {1, 2, 4}, P a multiple of 4 with P/4 dividing 32, N/2 * P/4 <= 1024;
- * other shapes return M3_ERR_UNSUPPORTED. The CUDA-core kernel walks each
- * sequence forward to store a state checkpoint every 64 tokens, then backward
- * chunk by chunk; its scratch ((L/64 + 64) N P floats per (b, h)) is
- * allocated and freed on `stream` by the library. dims->workspace is ignored.
+ * other shapes return M3_ERR_UNSUPPORTED. bf16 shapes with P = 64 and
+ * N in {64, 128} (x, dy, dB, dC 16-byte aligned) run a chunked backward on
+ * the tensor cores (chunks of 64 / R tokens); the others a CUDA-core kernel
+ * that walks each sequence forward to store a state checkpoint every 64
+ * tokens, then backward chunk by chunk. Gradients shared by heads, batch rows
+ * or tokens are accumulated with atomics, so their last bits can vary from
+ * run to run. Scratch: dims->workspace, at least
+ * m3_scan_bwd_workspace_bytes(dims, R) bytes and 16-byte aligned (smaller or
+ * misaligned: M3_ERR_INVALID_ARG), or NULL, in which case the library
+ * allocates and frees it on `stream` (cudaMallocAsync / cudaFreeAsync).
  */
 m3_status m3_scan_bwd(const void* x, const float* dt, const float* A, const float* lambda,
                       const void* B, const void* C, const float* theta, const void* dy,
@@ -256,6 +262,14 @@ m3_status m3_scan_fwd_noalloc(const void* x, const float* dt, const float* A, co
  * invalid. Host function: reads the current device's SM count when a device
  * is present (assumes 148, a B300, otherwise); launches nothing. */
 size_t m3_scan_workspace_bytes(const m3_dims* dims, int R, int chunk);
+
+/*
+ * The device scratch (bytes) m3_scan_bwd needs for these dims and R, whichever
+ * of its two kernels runs (0 when there is nothing to compute); (size_t)-1
+ * for invalid dims. Callers that run the backward pass repeatedly pass it
+ * once allocated in dims->workspace.
+ */
+size_t m3_scan_bwd_workspace_bytes(const m3_dims* dims, int R);
 
 /* Static, human-readable name of a status. Pure host function. */
 const char* m3_status_string(m3_status status);

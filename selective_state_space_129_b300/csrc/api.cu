@@ -121,6 +121,14 @@ const char* m3_status_string(m3_status s) {
   return "M3_ERR_UNKNOWN";
 }
 
+size_t m3_scan_bwd_workspace_bytes(const m3_dims* dims, int R) {
+  if (check_dims(dims, R) == M3_ERR_INVALID_ARG || dims->seqlen < 0) return (size_t)-1;
+  m3::BwdArgs a = {};
+  a.batch = dims->batch; a.L = dims->seqlen; a.H = dims->heads; a.G = dims->groups;
+  a.P = dims->headdim; a.N = dims->dstate; a.R = R;
+  return m3::scan_bwd_workspace_bytes(a, dims->act_dtype == M3_BF16);
+}
+
 size_t m3_scan_workspace_bytes(const m3_dims* dims, int R, int chunk) {
   if (check_dims(dims, R) == M3_ERR_INVALID_ARG || chunk < 1 || dims->seqlen < 0)
     return (size_t)-1;
@@ -392,6 +400,17 @@ m3_status m3_scan_bwd(const void* x, const float* dt, const float* A, const floa
     return M3_ERR_INVALID_ARG;
   if (!m3::scan_bwd_supported(N, P, R)) return M3_ERR_UNSUPPORTED;
   if (b * H > 0x7fffffff) return M3_ERR_UNSUPPORTED;
+  m3::BwdArgs a;
+  a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B = B; a.C = C; a.theta = theta;
+  a.B_bias = dims->B_bias; a.C_bias = dims->C_bias; a.dy = dy; a.d_final = d_final;
+  a.dx = dx; a.ddt = ddt; a.dA = dA; a.dlam = dlambda; a.dB = dB; a.dC = dC; a.dtheta = dtheta;
+  a.dB_bias = dB_bias; a.dC_bias = dC_bias;
+  a.batch = b; a.L = L; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R;
+  const bool bf16 = dims->act_dtype == M3_BF16;
+  if (dims->workspace != nullptr &&
+      (!aligned(dims->workspace, 16) ||
+       dims->workspace_bytes < m3::scan_bwd_workspace_bytes(a, bf16)))
+    return M3_ERR_INVALID_ARG;
   const Fault fault = fault_mode();
   if (fault == Fault::kArg) return M3_ERR_INVALID_ARG;
 
@@ -402,13 +421,7 @@ m3_status m3_scan_bwd(const void* x, const float* dt, const float* A, const floa
     if (f == M3_ERR_TIMEOUT) return M3_OK;
     if (f != M3_OK) return f;
   }
-  m3::BwdArgs a;
-  a.x = x; a.dt = dt; a.A = A; a.lam = lambda; a.B = B; a.C = C; a.theta = theta;
-  a.B_bias = dims->B_bias; a.C_bias = dims->C_bias; a.dy = dy; a.d_final = d_final;
-  a.dx = dx; a.ddt = ddt; a.dA = dA; a.dlam = dlambda; a.dB = dB; a.dC = dC; a.dtheta = dtheta;
-  a.dB_bias = dB_bias; a.dC_bias = dC_bias;
-  a.batch = b; a.L = L; a.H = H; a.G = G; a.P = P; a.N = N; a.R = R;
-  return from_cuda(m3::launch_scan_bwd(a, dims->act_dtype == M3_BF16,
+  return from_cuda(m3::launch_scan_bwd(a, bf16, dims->workspace,
                                        static_cast<cudaStream_t>(stream)));
 }
 

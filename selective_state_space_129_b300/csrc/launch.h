@@ -142,7 +142,10 @@ bool scan_bwd_tc_ok(const BwdArgs& a, bool bf16);
 size_t scan_bwd_tc_workspace(const BwdArgs& a);
 cudaError_t launch_scan_bwd_tc(const BwdArgs& a, float* ws, cudaStream_t s);
 bool scan_bwd_supported(int64_t N, int64_t P, int R);
-cudaError_t launch_scan_bwd(const BwdArgs& a, bool bf16, cudaStream_t s);
+// ws: device scratch of scan_bwd_workspace_bytes() bytes (16-byte aligned),
+// or NULL: allocated and freed on the stream.
+size_t scan_bwd_workspace_bytes(const BwdArgs& a, bool bf16);
+cudaError_t launch_scan_bwd(const BwdArgs& a, bool bf16, void* ws, cudaStream_t s);
 
 // Device address of this device's status word of expired waits.
 cudaError_t status_word(unsigned int** ptr);

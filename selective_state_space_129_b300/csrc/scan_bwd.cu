@@ -402,10 +402,23 @@ bool scan_bwd_supported(int64_t N, int64_t P, int R) {
   return sizeof(float) * (5 * N * R + N + P * R + 8) <= 48 * 1024;
 }
 
-cudaError_t launch_scan_bwd(const BwdArgs& a, bool bf16, cudaStream_t s) {
+// The larger of the two paths' scratch where the shape allows both (which
+// one runs depends on the pointers' alignment too), so that one size serves.
+size_t scan_bwd_workspace_bytes(const BwdArgs& a, bool bf16) {
+  if (a.batch * a.H == 0 || a.L == 0) return 0;
+  const int64_t nC = (a.L + kBChunk - 1) / kBChunk;
+  const size_t simt = sizeof(float) * (size_t)(nC + kBChunk) * a.N * a.P * (size_t)(a.batch * a.H);
+  BwdArgs shape = a;
+  shape.x = shape.dy = nullptr;
+  shape.dB = shape.dC = nullptr;
+  if (!scan_bwd_tc_ok(shape, bf16)) return simt;
+  const size_t tc = scan_bwd_tc_workspace(a);
+  return tc > simt ? tc : simt;
+}
+
+cudaError_t launch_scan_bwd(const BwdArgs& a, bool bf16, void* ws, cudaStream_t s) {
   const int64_t nseq = a.batch * a.H;
   const int64_t nC = (a.L + kBChunk - 1) / kBChunk;
-  const size_t per = (size_t)(nC + kBChunk) * a.N * a.P;
   // the accumulated gradients start from zero
   cudaError_t e = cudaMemsetAsync(a.dA, 0, sizeof(float) * a.H, s);
   const size_t nbc = (size_t)a.batch * a.L * a.G * a.N * a.R;
@@ -418,28 +431,32 @@ cudaError_t launch_scan_bwd(const BwdArgs& a, bool bf16, cudaStream_t s) {
   if (e == cudaSuccess && a.dC_bias)
     e = cudaMemsetAsync(a.dC_bias, 0, sizeof(float) * a.H * a.N * a.R, s);
   if (e != cudaSuccess || nseq == 0 || a.L == 0) return e;
-  if (scan_bwd_tc_ok(a, bf16)) {
+  const bool tc = scan_bwd_tc_ok(a, bf16);
+  if (tc) {
     // the tensor-core path accumulates ddt and dlambda too (a chunk adds the
     // trapezoid term of the token after it)
     const size_t nt = (size_t)a.batch * a.L * a.H;
     e = cudaMemsetAsync(a.ddt, 0, sizeof(float) * nt, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(a.dlam, 0, sizeof(float) * nt, s);
     if (e != cudaSuccess) return e;
-    float* tws = nullptr;
-    e = cudaMallocAsync(reinterpret_cast<void**>(&tws), scan_bwd_tc_workspace(a), s);
-    if (e != cudaSuccess) return e;
-    e = launch_scan_bwd_tc(a, tws, s);
-    const cudaError_t f = cudaFreeAsync(tws, s);
-    return e == cudaSuccess ? f : e;
   }
-  float* ws = nullptr;
-  e = cudaMallocAsync(reinterpret_cast<void**>(&ws), sizeof(float) * per * nseq, s);
-  if (e != cudaSuccess) return e;
-  float* ckpt = ws;
-  float* scr = ws + (size_t)nC * a.N * a.P * nseq;
-  e = bf16 ? launch_t<__nv_bfloat16>(a, ckpt, scr, s) : launch_t<float>(a, ckpt, scr, s);
-  const cudaError_t f = cudaFreeAsync(ws, s);
-  return e == cudaSuccess ? f : e;
+  float* w = static_cast<float*>(ws);
+  if (w == nullptr) {
+    e = cudaMallocAsync(reinterpret_cast<void**>(&w), scan_bwd_workspace_bytes(a, bf16), s);
+    if (e != cudaSuccess) return e;
+  }
+  if (tc) {
+    e = launch_scan_bwd_tc(a, w, s);
+  } else {
+    float* ckpt = w;
+    float* scr = w + (size_t)nC * a.N * a.P * nseq;
+    e = bf16 ? launch_t<__nv_bfloat16>(a, ckpt, scr, s) : launch_t<float>(a, ckpt, scr, s);
+  }
+  if (ws == nullptr) {
+    const cudaError_t f = cudaFreeAsync(w, s);
+    if (e == cudaSuccess) e = f;
+  }
+  return e;
 }
 
 }  // namespace m3

@@ -97,39 +97,71 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// acc[nt] += A (rows m0 .. m0+15, K columns) x B (K rows, columns n0 + 8 nt ..),
-// operands fp32 (TF32-rounded) in shared memory. AT: A is stored transposed
-// (A[m][k] at A[k sa + m]), else row-major (A[m sa + k]). BKN: B is stored
-// row-major K x N (B[k sb + n]), else as its transpose (B[n sb + k]).
-template <int NT, bool AT, bool BKN>
-__device__ __forceinline__ void wgemm(float (&acc)[NT][4], const float* A, int sa, int m0,
-                                      const float* B, int sb, int n0, int K, int g, int tq) {
-#pragma unroll 2
+// acc[nt] += A x B with both operands stored k-major: A[m][k] at A[k SA + m]
+// (rows m0 .. m0+15) and B[k][n] at B[k SBS + n] (columns n0 + 8 nt ..), fp32
+// (TF32-rounded) in shared memory; each fragment word is loaded alone.
+template <int NT, int K, int SA, int SBS>
+__device__ __forceinline__ void wgemm_kk(float (&acc)[NT][4], const float* A, int m0,
+                                         const float* B, int n0, int lane) {
+  const int g = lane >> 2, tq = lane & 3;
+  const float* ap = A + tq * SA + m0 + g;
+  const float* bp = B + tq * SBS + n0 + g;
+#pragma unroll
   for (int k0 = 0; k0 < K; k0 += 8) {
-    uint32_t a0, a1, a2, a3;
-    if (AT) {
-      a0 = __float_as_uint(A[(k0 + tq) * sa + m0 + g]);
-      a1 = __float_as_uint(A[(k0 + tq) * sa + m0 + g + 8]);
-      a2 = __float_as_uint(A[(k0 + tq + 4) * sa + m0 + g]);
-      a3 = __float_as_uint(A[(k0 + tq + 4) * sa + m0 + g + 8]);
-    } else {
-      a0 = __float_as_uint(A[(m0 + g) * sa + k0 + tq]);
-      a1 = __float_as_uint(A[(m0 + g + 8) * sa + k0 + tq]);
-      a2 = __float_as_uint(A[(m0 + g) * sa + k0 + tq + 4]);
-      a3 = __float_as_uint(A[(m0 + g + 8) * sa + k0 + tq + 4]);
-    }
+    const uint32_t a0 = __float_as_uint(ap[k0 * SA]);
+    const uint32_t a1 = __float_as_uint(ap[k0 * SA + 8]);
+    const uint32_t a2 = __float_as_uint(ap[(k0 + 4) * SA]);
+    const uint32_t a3 = __float_as_uint(ap[(k0 + 4) * SA + 8]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int n = n0 + 8 * nt + g;
-      uint32_t b0, b1;
-      if (BKN) {
-        b0 = __float_as_uint(B[(k0 + tq) * sb + n]);
-        b1 = __float_as_uint(B[(k0 + tq + 4) * sb + n]);
-      } else {
-        b0 = __float_as_uint(B[n * sb + k0 + tq]);
-        b1 = __float_as_uint(B[n * sb + k0 + tq + 4]);
-      }
+      const uint32_t b0 = __float_as_uint(bp[k0 * SBS + 8 * nt]);
+      const uint32_t b1 = __float_as_uint(bp[(k0 + 4) * SBS + 8 * nt]);
       mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+    }
+  }
+}
+
+__device__ __forceinline__ void ldm4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                     uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// acc[nt] += A (rows m0 .. m0+15 of a row-major [m][k] fp32 tile, word stride
+// SA, at shared address a_tile) x B (K x 8 NT, columns n0 + 8 nt ..). The A
+// fragments come by ldmatrix: an 8 x 4 block of 32-bit words is the b16 8 x 8
+// matrix whose distribution (thread t: row t / 4, word t % 4) is the TF32
+// fragment's. BL: B is stored [n][k] (word stride SBS, at b_tile) and comes by
+// ldmatrix, two n-tiles at a time; else B is stored [k][n] (Bp) and each
+// fragment word is loaded alone.
+template <int NT, int K, int SA, int SBS, bool BL>
+__device__ __forceinline__ void wgemm_l(float (&acc)[NT][4], uint32_t a_tile, int m0,
+                                        uint32_t b_tile, const float* Bp, int n0, int lane) {
+  const int g = lane >> 2, tq = lane & 3, mi = lane >> 3, rr = lane & 7;
+  const uint32_t a_lane = a_tile + 4u * (uint32_t)((m0 + rr + 8 * (mi & 1)) * SA + 4 * (mi >> 1));
+  const uint32_t b_lane = b_tile + 4u * (uint32_t)((n0 + rr + 8 * (mi >> 1)) * SBS + 4 * (mi & 1));
+  const float* bp = Bp + tq * SBS + n0 + g;
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t a0, a1, a2, a3;
+    ldm4(a_lane + 4u * k0, a0, a1, a2, a3);
+    if constexpr (BL) {
+      static_assert(NT % 2 == 0, "n-tiles come in pairs");
+#pragma unroll
+      for (int nt = 0; nt < NT; nt += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldm4(b_lane + 4u * (8 * nt * SBS + k0), b0, b1, b2, b3);
+        mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+        mma_tf32(acc[nt + 1], a0, a1, a2, a3, b2, b3);
+      }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t b0 = __float_as_uint(bp[k0 * SBS + 8 * nt]);
+        const uint32_t b1 = __float_as_uint(bp[(k0 + 4) * SBS + 8 * nt]);
+        mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+      }
     }
   }
 }
@@ -142,13 +174,13 @@ __device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
 
 // The chunk's per-token values, chunk-local angles, and the rotated Bt, Ct
 // tiles ([64][N] rows (t, r), TF32-rounded; zero past the sequence end).
-// Ph (optional): the angle table [Q][N/2]. s_gt: [TG][N/2] scratch.
-template <int R, int NS>
+// Rt (optional): the rotation table [Q][N/2] of (cos, sin). s_gt: [TG][N/2] scratch.
+template <int R, int NS, int SB>
 __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t h, int64_t gi,
                                            int c0, int nv, float A_h, float* Bt, float* Ct,
-                                           float* Ph, TokTab& tk, float* s_gt, float* phi_end) {
+                                           float2* Rt, TokTab& tk, float* s_gt, float* phi_end) {
   using K = BCfg<R, NS>;
-  constexpr int Q = K::Q, K2 = K::K2, SB = K::SB, TPG = K::TPG;
+  constexpr int Q = K::Q, K2 = K::K2, TPG = K::TPG;
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t L = a.L, H = a.H, G = a.G;
   if (tid <= Q) {
@@ -225,10 +257,10 @@ __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t 
   for (int j = 0; j < TPG; ++j) {
     const int t = tg * TPG + j;
     const float phi = off + ang[j];
-    if (Ph) Ph[t * K2 + kk] = phi;
     if (phi_end && t == Q - 1) phi_end[kk] = phi;
     float sn, cs;
     __sincosf(wrap_angle(phi), &sn, &cs);
+    if (Rt) Rt[t * K2 + kk] = make_float2(cs, sn);
     const int64_t bc = ((b * L + c0 + t) * G + gi) * NS * R + 2 * kk * R;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -249,12 +281,41 @@ __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t 
   __syncthreads();
 }
 
-// A [64][P] activation tile (rows (t, r)) from x-like [b,L,H,P,R] bf16, each
-// row scaled by scale[t] (or not), zero past the sequence end.
-template <int R>
+// A [64][P] activation tile (rows (t, r), word stride ST) from x-like
+// [b,L,H,P,R] bf16, each row scaled by scale[t] (or not), zero past the
+// sequence end. A warp reads 64 consecutive elements of one token (bf16 pairs),
+// so its stores fill rows without bank conflicts for ST = 4 or 8 (mod 32).
+template <int R, int ST>
 __device__ __forceinline__ void load_act_tile(float* T, const __nv_bfloat16* src, int64_t b,
                                               int64_t h, int64_t L, int64_t H, int c0, int nv,
                                               const float* scale) {
+  constexpr int Q = kRows / R;
+  constexpr int PR = kPd * R;
+  for (int e = threadIdx.x * 2; e < Q * PR; e += kBT * 2) {
+    const int t = e / PR, rem = e - t * PR;
+    float2 v = make_float2(0.f, 0.f);
+    if (t < nv)
+      v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
+          src + ((b * L + c0 + t) * H + h) * PR + rem));
+    if (scale) {
+      const float sc = scale[t];
+      v = make_float2(tf32r(sc * v.x), tf32r(sc * v.y));
+    }
+    if (R == 1) {
+      *reinterpret_cast<float2*>(T + t * ST + rem) = v;
+    } else {
+      const int p = rem / R, r = rem % R;
+      T[(t * R + r) * ST + p] = v.x;
+      T[(t * R + r + 1) * ST + p] = v.y;
+    }
+  }
+}
+
+// The same tile, each thread reading 8 consecutive elements of a token (one
+// 16-byte load) and storing them one by one.
+template <int R, int ST>
+__device__ __forceinline__ void load_act_tile8(float* T, const __nv_bfloat16* src, int64_t b,
+                                               int64_t h, int64_t L, int64_t H, int c0, int nv) {
   constexpr int Q = kRows / R;
   constexpr int PR = kPd * R;
   for (int e = threadIdx.x * 8; e < Q * PR; e += kBT * 8) {
@@ -273,11 +334,10 @@ __device__ __forceinline__ void load_act_tile(float* T, const __nv_bfloat16* src
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = 0.f;
     }
-    const float sc = scale ? scale[t] : 1.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int p = (rem + i) / R, r = (rem + i) % R;
-      T[(t * R + r) * kSX + p] = scale ? tf32r(sc * v[i]) : v[i];
+      T[(t * R + r) * ST + p] = v[i];
     }
   }
 }
@@ -287,21 +347,25 @@ __device__ __forceinline__ void load_act_tile(float* T, const __nv_bfloat16* src
 template <int R, int NS>
 constexpr size_t parts_smem() {
   using K = BCfg<R, NS>;
-  return sizeof(float) * (2 * kRows * K::SB + 2 * kRows * kSX + K::TG * K::K2) + sizeof(TokTab);
+  return sizeof(float) * (2 * kRows * (NS + 8) + 2 * kRows * (kPd + 8) + K::TG * K::K2) +
+         sizeof(TokTab);
 }
 
 template <int R, int NS>
-__global__ void __launch_bounds__(kBT, 1)
+__global__ void __launch_bounds__(kBT, 2)
     bwd_parts_kernel(BwdArgs a, float* wsA, float* wsB, float* lam_end, float* phi_end, int nC) {
   using K = BCfg<R, NS>;
-  constexpr int Q = K::Q, K2 = K::K2, SB = K::SB;
+  constexpr int Q = K::Q, K2 = K::K2;
+  // word strides 8 (mod 32): every tile here is read k-major (lanes tq rows
+  // apart, g columns apart), which then touches 32 different banks
+  constexpr int SBP = NS + 8, SXP = kPd + 8;
   extern __shared__ float4 smf4[];
   float* sm = reinterpret_cast<float*>(smf4);
   float* Bt = sm;
-  float* Ct = Bt + kRows * SB;
-  float* Xw = Ct + kRows * SB;
-  float* Ye = Xw + kRows * kSX;
-  float* s_gt = Ye + kRows * kSX;
+  float* Ct = Bt + kRows * SBP;
+  float* Xw = Ct + kRows * SBP;
+  float* Ye = Xw + kRows * SXP;
+  float* s_gt = Ye + kRows * SXP;
   TokTab& tk = *reinterpret_cast<TokTab*>(s_gt + K::TG * K2);
   const int c = blockIdx.x;
   const int64_t bhi = blockIdx.y, b = bhi / a.H, h = bhi % a.H, gi = h / (a.H / a.G);
@@ -309,9 +373,10 @@ __global__ void __launch_bounds__(kBT, 1)
   const int nv = (int)(a.L - c0 < Q ? a.L - c0 : Q);
   const float A_h = a.A[h];
   float* pe = phi_end + (bhi * nC + c) * K2;
-  chunk_prep<R, NS>(a, b, h, gi, c0, nv, A_h, Bt, Ct, nullptr, tk, s_gt, pe);
-  load_act_tile<R>(Xw, static_cast<const __nv_bfloat16*>(a.x), b, h, a.L, a.H, c0, nv, tk.w);
-  load_act_tile<R>(Ye, static_cast<const __nv_bfloat16*>(a.dy), b, h, a.L, a.H, c0, nv, tk.el);
+  chunk_prep<R, NS, SBP>(a, b, h, gi, c0, nv, A_h, Bt, Ct, nullptr, tk, s_gt, pe);
+  load_act_tile<R, SXP>(Xw, static_cast<const __nv_bfloat16*>(a.x), b, h, a.L, a.H, c0, nv, tk.w);
+  load_act_tile<R, SXP>(Ye, static_cast<const __nv_bfloat16*>(a.dy), b, h, a.L, a.H, c0, nv,
+                        tk.el);
   if (threadIdx.x == 0) lam_end[bhi * nC + c] = tk.lc[Q - 1];
   __syncthreads();
   // [N][P] = Bt^T Xw and Ct^T Ye: warp tile 16 rows x (8 NT) columns
@@ -323,7 +388,7 @@ __global__ void __launch_bounds__(kBT, 1)
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
     zero_acc(acc);
-    wgemm<NT, true, true>(acc, pass ? Ct : Bt, SB, m0, pass ? Ye : Xw, kSX, n0, kRows, g, tq);
+    wgemm_kk<NT, kRows, SBP, SXP>(acc, pass ? Ct : Bt, m0, pass ? Ye : Xw, n0, lane);
     float* dst = (pass ? wsB : wsA) + slot;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -439,7 +504,7 @@ __global__ void __launch_bounds__(256)
 template <int R, int NS>
 constexpr size_t chunk_smem() {
   using K = BCfg<R, NS>;
-  return sizeof(float) * (2 * kRows * K::SB + 4 * kRows * kSX + NS * kSX + 2 * K::Q * K::K2 +
+  return sizeof(float) * (2 * kRows * K::SB + 5 * kRows * kSX + NS * kSX + 2 * K::Q * K::K2 +
                           K::TG * K::K2 + 8 * kRows) +
          sizeof(TokTab);
 }
@@ -456,12 +521,13 @@ __global__ void __launch_bounds__(kBT, 1)
   float* Ct = Bt + kRows * SB;
   float* Xs = Ct + kRows * SB;
   float* Ys = Xs + kRows * kSX;
-  float* Ps = Ys + kRows * kSX;
-  float* dSs = Ps + kRows * kSX;
-  float* St = dSs + kRows * kSX;  // [N][P]: H_in, then dG
-  float* Ph = St + NS * kSX;      // [Q][K2] angles
-  float* dPh = Ph + Q * K2;       // [Q][K2] angle gradients
-  float* s_gt = dPh + Q * K2;
+  float* PT = Ys + kRows * kSX;   // P transposed: [s row][t row]
+  float* dSs = PT + kRows * kSX;  // dS
+  float* dST = dSs + kRows * kSX; // dS transposed
+  float* St = dST + kRows * kSX;  // [N][P]: H_in, then dG
+  float2* Rt = reinterpret_cast<float2*>(St + NS * kSX);  // [Q][K2] (cos, sin) of the angles
+  float* dPh = Xs;  // [Q][K2] angle gradients, once X is no longer read
+  float* s_gt = reinterpret_cast<float*>(Rt + Q * K2);
   float* colVi = s_gt + K::TG * K2;  // per token: column sums and row sums (64 each)
   float* colVs = colVi + kRows;
   float* colZ = colVs + kRows;
@@ -480,12 +546,14 @@ __global__ void __launch_bounds__(kBT, 1)
   const int nv = (int)(L - c0 < Q ? L - c0 : Q);
   const float A_h = a.A[h];
   const size_t slot = (size_t)(bhi * nC + c) * NS * kPd;
+  const uint32_t aBt = ptx::smem_addr(Bt), aCt = ptx::smem_addr(Ct), aXs = ptx::smem_addr(Xs),
+                 aYs = ptx::smem_addr(Ys), aPT = ptx::smem_addr(PT), adS = ptx::smem_addr(dSs),
+                 adST = ptx::smem_addr(dST), aSt = ptx::smem_addr(St);
 
   for (int i = tid; i < 8 * kRows; i += kBT) colVi[i] = 0.f;
-  for (int i = tid; i < Q * K2; i += kBT) dPh[i] = 0.f;
-  chunk_prep<R, NS>(a, b, h, gi, c0, nv, A_h, Bt, Ct, Ph, tk, s_gt, nullptr);
-  load_act_tile<R>(Xs, static_cast<const __nv_bfloat16*>(a.x), b, h, L, H, c0, nv, nullptr);
-  load_act_tile<R>(Ys, static_cast<const __nv_bfloat16*>(a.dy), b, h, L, H, c0, nv, nullptr);
+  chunk_prep<R, NS, SB>(a, b, h, gi, c0, nv, A_h, Bt, Ct, Rt, tk, s_gt, nullptr);
+  load_act_tile8<R, kSX>(Xs, static_cast<const __nv_bfloat16*>(a.x), b, h, L, H, c0, nv);
+  load_act_tile8<R, kSX>(Ys, static_cast<const __nv_bfloat16*>(a.dy), b, h, L, H, c0, nv);
   for (int e = tid * 4; e < NS * kPd; e += kBT * 4) {
     const float4 v = *reinterpret_cast<const float4*>(wsA + slot + e);
     const int n = e / kPd, p = e - n * kPd;
@@ -500,14 +568,27 @@ __global__ void __launch_bounds__(kBT, 1)
     float aS[2][4], aP[2][4];
     zero_acc(aS);
     zero_acc(aP);
-    wgemm<2, false, false>(aS, Ct, SB, m0, Bt, SB, n0, NS, g, tq);
-    wgemm<2, false, false>(aP, Ys, kSX, m0, Xs, kSX, n0, kPd, g, tq);
+    wgemm_l<2, NS, SB, SB, true>(aS, aCt, m0, aBt, nullptr, n0, lane);
+    wgemm_l<2, kPd, kSX, kSX, true>(aP, aYs, m0, aXs, nullptr, n0, lane);
     float rz[2] = {0.f, 0.f};
     float cvi[2][2], cvs[2][2], cz[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int q = 0; q < 2; ++q) cvi[nt][q] = cvs[nt][q] = cz[nt][q] = 0.f;
+    // the token values of the thread's two rows and four columns
+    float lr[2], lcol[2][2], gcol[2][2], bcol[2][2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) lr[q] = tk.lc[(m0 + g + 8 * q) / R];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int s = (n0 + 8 * nt + 2 * tq + q) / R;
+        lcol[nt][q] = tk.lc[s];
+        gcol[nt][q] = tk.gam[s];
+        bcol[nt][q] = tk.bh[s + 1];
+      }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -516,8 +597,8 @@ __global__ void __launch_bounds__(kBT, 1)
         const int t = i / R, s = j / R;
         float pv = 0.f, dsv = 0.f;
         if (t >= s) {
-          const float D = __expf(tk.lc[t] - tk.lc[s]);
-          const float f = tk.gam[s] + (s < t ? tk.bh[s + 1] : 0.f);
+          const float D = __expf(lr[e >> 1] - lcol[nt][e & 1]);
+          const float f = gcol[nt][e & 1] + (s < t ? bcol[nt][e & 1] : 0.f);
           const float M = D * f;
           pv = aS[nt][e] * M;
           dsv = aP[nt][e] * M;
@@ -530,8 +611,9 @@ __global__ void __launch_bounds__(kBT, 1)
             rz[e >> 1] += z;
           }
         }
-        Ps[i * kSX + j] = tf32r(pv);
+        PT[j * kSX + i] = tf32r(pv);
         dSs[i * kSX + j] = tf32r(dsv);
+        dST[j * kSX + i] = tf32r(dsv);
       }
     // column sums over the warp's 16 rows (lanes that differ in g)
 #pragma unroll
@@ -565,6 +647,11 @@ __global__ void __launch_bounds__(kBT, 1)
   //      (64 x N; warp tile 16 x N/4), each followed by the rotation backward
   constexpr int NT3 = NS / 32;
   const int m0 = 16 * (warp >> 2), n0 = (NS / 4) * (warp & 3);
+  float dphr[2][NT3];  // the angle gradient of (row m0 + g + 8q, pair of n-tile nt)
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int nt = 0; nt < NT3; ++nt) dphr[q][nt] = 0.f;
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
     if (pass == 1) {
@@ -583,7 +670,7 @@ __global__ void __launch_bounds__(kBT, 1)
     float acc[NT3][4];
     zero_acc(acc);
     // E = (pass 0) dY H_in^T, (pass 1) X dG^T
-    wgemm<NT3, false, false>(acc, pass ? Xs : Ys, kSX, m0, St, kSX, n0, kPd, g, tq);
+    wgemm_l<NT3, kPd, kSX, kSX, true>(acc, pass ? aXs : aYs, m0, aSt, nullptr, n0, lane);
     // row dots with the own tile: d e^Lam_t (pass 0), dw_s (pass 1)
     {
       float rd[2] = {0.f, 0.f};
@@ -615,29 +702,31 @@ __global__ void __launch_bounds__(kBT, 1)
       }
     }
     // + dS Oth (pass 0) or dS^T Oth (pass 1)
-    if (pass == 0)
-      wgemm<NT3, false, true>(acc, dSs, kSX, m0, Oth, SB, n0, kRows, g, tq);
-    else
-      wgemm<NT3, true, true>(acc, dSs, kSX, m0, Oth, SB, n0, kRows, g, tq);
+    wgemm_l<NT3, kRows, kSX, SB, false>(acc, pass ? adST : adS, m0, 0u, Oth, n0, lane);
     // rotation backward: the raw gradient Rot(Phi_t) d, the angle gradient,
     // and the bias gradient (summed over the warp's rows of equal rank)
     float* graw = pass ? a.dB : a.dC;
     float* gbias = pass ? a.dB_bias : a.dC_bias;
+    float* grow[2];  // the raw gradient's row of each of the thread's two rows
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int i = m0 + g + 8 * q, t = i / R, r = i % R;
+      grow[q] = graw + ((b * L + c0 + t) * G + gi) * NS * R + r;
+    }
 #pragma unroll
     for (int nt = 0; nt < NT3; ++nt) {
       const int col = n0 + 8 * nt + 2 * tq, k = col >> 1;
       float bs0 = 0.f, bs1 = 0.f;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const int i = m0 + g + 8 * q, t = i / R, r = i % R;
+        const int i = m0 + g + 8 * q, t = i / R;
         const float d0 = acc[nt][2 * q], d1 = acc[nt][2 * q + 1];
         const float2 o = *reinterpret_cast<const float2*>(Own + i * SB + col);
-        atomicAdd(&dPh[t * K2 + k], d0 * o.y - d1 * o.x);
-        float sn, cs;
-        __sincosf(wrap_angle(Ph[t * K2 + k]), &sn, &cs);
-        const float r0 = cs * d0 - sn * d1, r1 = sn * d0 + cs * d1;
+        dphr[q][nt] += d0 * o.y - d1 * o.x;
+        const float2 rt = Rt[t * K2 + k];
+        const float r0 = rt.x * d0 - rt.y * d1, r1 = rt.y * d0 + rt.x * d1;
         if (t < nv) {
-          float* dst = graw + ((b * L + c0 + t) * G + gi) * NS * R + col * R + r;
+          float* dst = grow[q] + col * R;
           if (R == 1) {
             atomicAdd(reinterpret_cast<float2*>(dst), make_float2(r0, r1));
           } else {
@@ -669,8 +758,8 @@ __global__ void __launch_bounds__(kBT, 1)
     float a1[2][4], a2[2][4];
     zero_acc(a1);
     zero_acc(a2);
-    wgemm<2, true, true>(a1, Ps, kSX, xm0, Ys, kSX, xn0, kRows, g, tq);
-    wgemm<2, false, true>(a2, Bt, SB, xm0, St, kSX, xn0, NS, g, tq);
+    wgemm_l<2, kRows, kSX, kSX, false>(a1, aPT, xm0, 0u, Ys, xn0, lane);
+    wgemm_l<2, NS, SB, kSX, false>(a2, aBt, xm0, 0u, St, xn0, lane);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int j = xm0 + g + 8 * q, s = j / R, r = j % R;
@@ -685,6 +774,19 @@ __global__ void __launch_bounds__(kBT, 1)
       }
     }
   }
+  __syncthreads();
+  // the angle gradients of the rows into dPh (X is no longer read); rows of
+  // one token (R > 1) are summed over the lanes that hold them
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int nt = 0; nt < NT3; ++nt) {
+      float v = dphr[q][nt];
+      if (R >= 2) v += __shfl_xor_sync(0xffffffffu, v, 4);
+      if (R >= 4) v += __shfl_xor_sync(0xffffffffu, v, 8);
+      const int i = m0 + g + 8 * q, k = (n0 + 8 * nt + 2 * tq) >> 1;
+      if (g % R == 0) dPh[(i / R) * K2 + k] = v;
+    }
   __syncthreads();
 
   // ---- the angle gradients: the chunk-end rotation at the last token, the

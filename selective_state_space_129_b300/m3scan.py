@@ -20,7 +20,7 @@ M3_FLAG_BC_NORM = 1  # m3_dims.flags: BCNorm B and C inside the prefill
 # Exported entry points (kept in step with include/m3scan.h).
 EXPORTS = ("m3_scan_fwd", "m3_scan_fwd_noalloc", "m3_decode_step", "m3_scan_workspace_bytes",
            "m3_status_string", "m3_device_status", "m3_version", "m3_decode_tokens",
-           "m3_scan_fwd_state", "m3_scan_bwd")
+           "m3_scan_fwd_state", "m3_scan_bwd", "m3_scan_bwd_workspace_bytes")
 
 
 class M3Error(RuntimeError):
@@ -74,6 +74,8 @@ def load(path: str = LIB_PATH):
     lib.m3_scan_bwd.restype = i32
     lib.m3_scan_workspace_bytes.argtypes = [dims_p, i32, i32]
     lib.m3_scan_workspace_bytes.restype = ctypes.c_size_t
+    lib.m3_scan_bwd_workspace_bytes.argtypes = [dims_p, i32]
+    lib.m3_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.m3_status_string.argtypes = [i32]
     lib.m3_status_string.restype = ctypes.c_char_p
     lib.m3_device_status.argtypes = [vp]
@@ -173,6 +175,10 @@ def m3_scan_workspace_bytes(dims: m3_dims, R: int, chunk: int) -> int:
     return int(load().m3_scan_workspace_bytes(ctypes.byref(dims), int(R), int(chunk)))
 
 
+def m3_scan_bwd_workspace_bytes(dims: m3_dims, R: int) -> int:
+    return int(load().m3_scan_bwd_workspace_bytes(ctypes.byref(dims), int(R)))
+
+
 def m3_scan_fwd(x, dt, A, lam, B, C, theta, R, chunk, out=None, final_state=None,
                 B_bias=None, C_bias=None, workspace=None, stream=None, want_state=True,
                 bc_norm=False):
@@ -223,10 +229,11 @@ def m3_scan_fwd_state(x, dt, A, lam, B, C, theta, R, chunk, state, B_prev=None, 
 
 
 def m3_scan_bwd(x, dt, A, lam, B, C, theta, dy, R, d_final=None, B_bias=None, C_bias=None,
-                stream=None):
+                stream=None, workspace=None):
     """Gradients of <y, dy> + <h_final, d_final> of a prefill from a zero state.
     Returns a dict of fp32 tensors: x, dt, A, lam, B, C, theta and, when the
-    biases are given, B_bias, C_bias."""
+    biases are given, B_bias, C_bias. ``workspace``: a device tensor of at least
+    m3_scan_bwd_workspace_bytes bytes, or None (the library allocates it)."""
     import torch
     lib = load()
     b, L, H, P, G, N = _check_prefill(x, dt, A, lam, B, C, theta, R, dy, None, B_bias, C_bias)
@@ -240,7 +247,7 @@ def m3_scan_bwd(x, dt, A, lam, B, C, theta, dy, R, d_final=None, B_bias=None, C_
         g["B_bias"] = torch.empty(H, N, R, **f)
     if C_bias is not None:
         g["C_bias"] = torch.empty(H, N, R, **f)
-    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias)
+    dims = make_dims(b, L, H, G, P, N, _act_dtype(x), B_bias, C_bias, workspace)
     st = lib.m3_scan_bwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(lam), _ptr(B), _ptr(C), _ptr(theta),
                          _ptr(dy), _ptr(d_final), ctypes.byref(dims), int(R), _ptr(g["x"]),
                          _ptr(g["dt"]), _ptr(g["A"]), _ptr(g["lam"]), _ptr(g["B"]), _ptr(g["C"]),

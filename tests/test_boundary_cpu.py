@@ -335,3 +335,29 @@ def test_decode_binding_rejects_host_state():
                               torch.zeros(b, G, N, R, dtype=torch.bfloat16),
                               torch.zeros(b, G, N, R, dtype=torch.bfloat16),
                               torch.zeros(b, G, N // 2), R=R)
+
+
+def test_bwd_workspace_query(lib):
+    q = m3scan.m3_scan_bwd_workspace_bytes
+    assert q(_dims(dstate=7), 1) == ctypes.c_size_t(-1).value
+    assert q(_dims(batch=0), 1) == 0
+    # fp32: the CUDA-core kernel's checkpoints, (ceil(L / 64) + 64) N P floats per (b, h)
+    assert q(_dims(), 1) == 4 * (1 + 64) * 8 * 8 * 2 * 4
+    # bf16, P 64, N 128, L 2048: the larger of the CUDA-core kernel's scratch and the
+    # tensor-core path's (two [N][P] states and 2 + N scalars per chunk of 64 / R tokens)
+    d = _dims(batch=2, seqlen=2048, heads=4, groups=1, headdim=64, dstate=128,
+              act_dtype=m3scan.M3_BF16)
+    simt = 4 * (32 + 64) * 128 * 64 * 8
+    for R in (1, 2, 4):
+        tc = 4 * 8 * (2048 * R // 64) * (2 * 128 * 64 + 128 + 2)
+        assert q(d, R) == max(simt, tc)
+
+
+def test_bwd_caller_workspace_checked_on_the_host(lib):
+    d = _dims(batch=2, seqlen=2048, heads=4, groups=1, headdim=64, dstate=128,
+              act_dtype=m3scan.M3_BF16)
+    need = m3scan.m3_scan_bwd_workspace_bytes(d, 1)
+    d.workspace, d.workspace_bytes = FAKE, need - 16
+    assert _bwd(lib, d) == m3scan.M3_ERR_INVALID_ARG    # too small
+    d.workspace, d.workspace_bytes = FAKE + 8, need
+    assert _bwd(lib, d) == m3scan.M3_ERR_INVALID_ARG    # not 16-byte aligned

@@ -696,6 +696,43 @@ def test_decode_tokens_full_batch_mimo(orc):
     assert_bf16(st[bsel], st_ref, "state")
 
 
+@pytest.mark.parametrize("bf16,P,N", [(True, 64, 128), (False, 64, 128), (True, 32, 64)],
+                         ids=["tensor_cores", "cuda_cores_f32", "cuda_cores_bf16"])
+def test_backward_with_a_caller_workspace(bf16, P, N):
+    """m3_scan_bwd with dims.workspace (sized by m3_scan_bwd_workspace_bytes)
+    against the oracle, on both kernels; the workspace is filled with NaN
+    first, so nothing may be read from it before it is written."""
+    from oracle import backward
+    b, L, H, G, R = 1, 100, 2, 1, 1
+    shape = m3synth.ScanShape(b, L, H, G, P, N, R=R, chunk=16, bf16=bf16)
+    inp = m3synth.scan_inputs(shape, seed=175)
+    rng = np.random.default_rng(176)
+    dy = rng.standard_normal((b, L, H, P, R)).astype(np.float32)
+    if bf16:
+        dy = m3synth.to_bf16(dy)
+    dfin = rng.standard_normal((b, H, N, P)).astype(np.float32)
+    d = to_device(inp, bf16)
+    act = torch.bfloat16 if bf16 else torch.float32
+    dims = m3.make_dims(b, L, H, G, P, N, m3.M3_BF16 if bf16 else m3.M3_F32)
+    need = m3.m3_scan_bwd_workspace_bytes(dims, R)
+    ws = torch.full((need // 4 + 1,), float("nan"), device="cuda")
+    g = m3.m3_scan_bwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"],
+                       torch.from_numpy(dy).to(act).cuda(), R=R,
+                       d_final=torch.from_numpy(dfin).cuda(), B_bias=d["B_bias"],
+                       C_bias=d["C_bias"], workspace=ws)
+    torch.cuda.synchronize()
+    assert m3.m3_device_status() == m3.M3_OK
+    ref = backward.scan_grads(inp["x"], inp["dt"], inp["A"], inp["lam"], inp["B"], inp["C"],
+                              inp["theta"], dy, dh=dfin, B_bias=inp["B_bias"],
+                              C_bias=inp["C_bias"])
+    for k in ref:
+        got = g[k].cpu().numpy()
+        if bf16:
+            assert_bf16(got, ref[k], "d" + k)
+        else:
+            assert rel_l2(got, ref[k]) <= 1e-4, k
+
+
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 def test_prefill_then_decode_matches_longer_prefill(orc, bf16):
     shape = m3synth.ScanShape(2, 33, 4, 1, 64, 128, R=1, chunk=16, bf16=bf16)

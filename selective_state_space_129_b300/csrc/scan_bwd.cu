@@ -411,6 +411,7 @@ size_t scan_bwd_workspace_bytes(const BwdArgs& a, bool bf16) {
   BwdArgs shape = a;
   shape.x = shape.dy = nullptr;
   shape.dB = shape.dC = nullptr;
+  shape.B = shape.C = nullptr;
   if (!scan_bwd_tc_ok(shape, bf16)) return simt;
   const size_t tc = scan_bwd_tc_workspace(a);
   return tc > simt ? tc : simt;

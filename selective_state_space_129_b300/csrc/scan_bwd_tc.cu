@@ -175,6 +175,11 @@ __device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
 // The chunk's per-token values, chunk-local angles, and the rotated Bt, Ct
 // tiles ([64][N] rows (t, r), TF32-rounded; zero past the sequence end).
 // Rt (optional): the rotation table [Q][N/2] of (cos, sin). s_gt: [TG][N/2] scratch.
+// bf16 element e of a row of packed pairs, as fp32
+__device__ __forceinline__ float bf_word(uint32_t w, int half) {
+  return __uint_as_float(half ? (w & 0xffff0000u) : (w << 16));
+}
+
 template <int R, int NS, int SB>
 __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t h, int64_t gi,
                                            int c0, int nv, float A_h, float* Bt, float* Ct,
@@ -183,6 +188,44 @@ __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t 
   constexpr int Q = K::Q, K2 = K::K2, TPG = K::TPG;
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t L = a.L, H = a.H, G = a.G;
+  // the fold's thread (pair kk, token group tg) takes tokens tg TPG .. + TPG - 1;
+  // every global load of the prologue is issued here, before the first barrier
+  const int kk = tid % K2, tg = tid / K2;
+  float th[TPG];
+  uint32_t bw[TPG][R], cw[TPG][R];  // B, C rows 2kk, 2kk + 1 of each token (2R bf16)
+  const __nv_bfloat16* Bg = static_cast<const __nv_bfloat16*>(a.B);
+  const __nv_bfloat16* Cg = static_cast<const __nv_bfloat16*>(a.C);
+#pragma unroll
+  for (int j = 0; j < TPG; ++j) {
+    const int t = tg * TPG + j;
+    th[j] = 0.f;
+#pragma unroll
+    for (int w = 0; w < R; ++w) bw[j][w] = cw[j][w] = 0u;
+    if (t < nv) {
+      th[j] = a.theta[((b * L + c0 + t) * G + gi) * K2 + kk];
+      const int64_t bc = ((b * L + c0 + t) * G + gi) * NS * R + 2 * kk * R;
+      if constexpr (R == 1) {
+        bw[j][0] = *reinterpret_cast<const uint32_t*>(Bg + bc);
+        cw[j][0] = *reinterpret_cast<const uint32_t*>(Cg + bc);
+      } else if constexpr (R == 2) {
+        const uint2 u = *reinterpret_cast<const uint2*>(Bg + bc);
+        const uint2 v = *reinterpret_cast<const uint2*>(Cg + bc);
+        bw[j][0] = u.x; bw[j][1] = u.y;
+        cw[j][0] = v.x; cw[j][1] = v.y;
+      } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(Bg + bc);
+        const uint4 v = *reinterpret_cast<const uint4*>(Cg + bc);
+        bw[j][0] = u.x; bw[j][1] = u.y; bw[j][2] = u.z; bw[j][3] = u.w;
+        cw[j][0] = v.x; cw[j][1] = v.y; cw[j][2] = v.z; cw[j][3] = v.w;
+      }
+    }
+  }
+  float bb[2 * R], cb[2 * R];  // the head's biases of rows 2kk, 2kk + 1
+#pragma unroll
+  for (int e = 0; e < 2 * R; ++e) {
+    bb[e] = a.B_bias ? a.B_bias[(h * NS + 2 * kk) * R + e] : 0.f;
+    cb[e] = a.C_bias ? a.C_bias[(h * NS + 2 * kk) * R + e] : 0.f;
+  }
   if (tid <= Q) {
     const int t = tid;
     float d = 0.f, lm = 0.f;
@@ -231,17 +274,14 @@ __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t 
       tk.w[t] = __expf(lend - l1) * (tk.gam[t] + tk.bh[t + 1]);
     }
   }
-  // the fold: thread (pair kk, token group tg), tokens tg TPG .. + TPG - 1
-  const int kk = tid % K2, tg = tid / K2;
+  // the chunk-local angles: this thread's prefix over its tokens, then the
+  // totals of the earlier token groups
   float ang[TPG];
   {
     float run = 0.f;
 #pragma unroll
     for (int j = 0; j < TPG; ++j) {
-      const int t = tg * TPG + j;
-      float phi = 0.f;
-      if (t < nv) phi = tk.dt[t] * a.theta[((b * L + c0 + t) * G + gi) * K2 + kk];
-      run += phi;
+      run += tk.dt[tg * TPG + j] * th[j];
       ang[j] = run;
     }
     s_gt[tg * K2 + kk] = run;
@@ -249,10 +289,6 @@ __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t 
   __syncthreads();
   float off = 0.f;
   for (int q = 0; q < tg; ++q) off += s_gt[q * K2 + kk];
-  const float* bbias = a.B_bias ? a.B_bias + (h * NS + 2 * kk) * R : nullptr;
-  const float* cbias = a.C_bias ? a.C_bias + (h * NS + 2 * kk) * R : nullptr;
-  const __nv_bfloat16* Bg = static_cast<const __nv_bfloat16*>(a.B);
-  const __nv_bfloat16* Cg = static_cast<const __nv_bfloat16*>(a.C);
 #pragma unroll
   for (int j = 0; j < TPG; ++j) {
     const int t = tg * TPG + j;
@@ -261,16 +297,14 @@ __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t 
     float sn, cs;
     __sincosf(wrap_angle(phi), &sn, &cs);
     if (Rt) Rt[t * K2 + kk] = make_float2(cs, sn);
-    const int64_t bc = ((b * L + c0 + t) * G + gi) * NS * R + 2 * kk * R;
+    const bool live = t < nv;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      float b0 = 0.f, b1 = 0.f, q0 = 0.f, q1 = 0.f;
-      if (t < nv) {
-        b0 = __bfloat162float(Bg[bc + r]) + (bbias ? bbias[r] : 0.f);
-        b1 = __bfloat162float(Bg[bc + R + r]) + (bbias ? bbias[R + r] : 0.f);
-        q0 = __bfloat162float(Cg[bc + r]) + (cbias ? cbias[r] : 0.f);
-        q1 = __bfloat162float(Cg[bc + R + r]) + (cbias ? cbias[R + r] : 0.f);
-      }
+      // elements r (row 2kk) and R + r (row 2kk + 1) of the token's 2R
+      const float b0 = live ? bf_word(bw[j][r >> 1], r & 1) + bb[r] : 0.f;
+      const float b1 = live ? bf_word(bw[j][(R + r) >> 1], (R + r) & 1) + bb[R + r] : 0.f;
+      const float q0 = live ? bf_word(cw[j][r >> 1], r & 1) + cb[r] : 0.f;
+      const float q1 = live ? bf_word(cw[j][(R + r) >> 1], (R + r) & 1) + cb[R + r] : 0.f;
       const int row = t * R + r;
       *reinterpret_cast<float2*>(Bt + row * SB + 2 * kk) =
           make_float2(tf32r(cs * b0 + sn * b1), tf32r(cs * b1 - sn * b0));
@@ -282,63 +316,62 @@ __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t 
 }
 
 // A [64][P] activation tile (rows (t, r), word stride ST) from x-like
-// [b,L,H,P,R] bf16, each row scaled by scale[t] (or not), zero past the
-// sequence end. A warp reads 64 consecutive elements of one token (bf16 pairs),
-// so its stores fill rows without bank conflicts for ST = 4 or 8 (mod 32).
-template <int R, int ST>
-__device__ __forceinline__ void load_act_tile(float* T, const __nv_bfloat16* src, int64_t b,
-                                              int64_t h, int64_t L, int64_t H, int c0, int nv,
-                                              const float* scale) {
-  constexpr int Q = kRows / R;
+// [b,L,H,P,R] bf16, in two halves: each thread's loads of 4 bf16 pairs (a
+// warp reads 64 consecutive elements of one token; zero past the sequence
+// end), issued early, and their stores, each row scaled by scale[t]; for ST =
+// 4 or 8 (mod 32) the stores fill rows without bank conflicts.
+template <int R>
+__device__ __forceinline__ void act_ld2(uint32_t (&w)[4], const __nv_bfloat16* src, int64_t b,
+                                        int64_t h, int64_t L, int64_t H, int c0, int nv) {
   constexpr int PR = kPd * R;
-  for (int e = threadIdx.x * 2; e < Q * PR; e += kBT * 2) {
-    const int t = e / PR, rem = e - t * PR;
-    float2 v = make_float2(0.f, 0.f);
-    if (t < nv)
-      v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
-          src + ((b * L + c0 + t) * H + h) * PR + rem));
-    if (scale) {
-      const float sc = scale[t];
-      v = make_float2(tf32r(sc * v.x), tf32r(sc * v.y));
-    }
+  static_assert(kRows * kPd == 8 * kBT, "four bf16 pairs per thread and tile");
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = 2 * (threadIdx.x + k * kBT), t = e / PR, rem = e - t * PR;
+    w[k] = t < nv ? *reinterpret_cast<const uint32_t*>(src + ((b * L + c0 + t) * H + h) * PR + rem)
+                  : 0u;
+  }
+}
+
+template <int R, int ST>
+__device__ __forceinline__ void act_st2(float* T, const uint32_t (&w)[4], const float* scale) {
+  constexpr int PR = kPd * R;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = 2 * (threadIdx.x + k * kBT), t = e / PR, rem = e - t * PR;
+    const float sc = scale[t];
+    const float v0 = tf32r(sc * bf_word(w[k], 0)), v1 = tf32r(sc * bf_word(w[k], 1));
     if (R == 1) {
-      *reinterpret_cast<float2*>(T + t * ST + rem) = v;
+      *reinterpret_cast<float2*>(T + t * ST + rem) = make_float2(v0, v1);
     } else {
       const int p = rem / R, r = rem % R;
-      T[(t * R + r) * ST + p] = v.x;
-      T[(t * R + r + 1) * ST + p] = v.y;
+      T[(t * R + r) * ST + p] = v0;
+      T[(t * R + r + 1) * ST + p] = v1;
     }
   }
 }
 
-// The same tile, each thread reading 8 consecutive elements of a token (one
-// 16-byte load) and storing them one by one.
-template <int R, int ST>
-__device__ __forceinline__ void load_act_tile8(float* T, const __nv_bfloat16* src, int64_t b,
-                                               int64_t h, int64_t L, int64_t H, int c0, int nv) {
-  constexpr int Q = kRows / R;
+// The [64][P] tile of one chunk split in two: each thread's 16-byte load of 8
+// consecutive elements of a token (issued early, zero past the sequence end)
+// and its stores.
+template <int R>
+__device__ __forceinline__ uint4 act_ld8(const __nv_bfloat16* src, int64_t b, int64_t h,
+                                         int64_t L, int64_t H, int c0, int nv) {
   constexpr int PR = kPd * R;
-  for (int e = threadIdx.x * 8; e < Q * PR; e += kBT * 8) {
-    const int t = e / PR, rem = e - t * PR;
-    float v[8];
-    if (t < nv) {
-      const uint4 u = *reinterpret_cast<const uint4*>(src + ((b * L + c0 + t) * H + h) * PR + rem);
-      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+  const int e = threadIdx.x * 8, t = e / PR, rem = e - t * PR;
+  if (t >= nv) return make_uint4(0u, 0u, 0u, 0u);
+  return *reinterpret_cast<const uint4*>(src + ((b * L + c0 + t) * H + h) * PR + rem);
+}
+
+template <int R, int ST>
+__device__ __forceinline__ void act_st8(float* T, uint4 u) {
+  constexpr int PR = kPd * R;
+  const int e = threadIdx.x * 8, t = e / PR, rem = e - t * PR;
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(p2[i]);
-        v[2 * i] = f.x;
-        v[2 * i + 1] = f.y;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int p = (rem + i) / R, r = (rem + i) % R;
-      T[(t * R + r) * ST + p] = v[i];
-    }
+  for (int i = 0; i < 8; ++i) {
+    const int p = (rem + i) / R, r = (rem + i) % R;
+    T[(t * R + r) * ST + p] = bf_word(w[i >> 1], i & 1);
   }
 }
 
@@ -373,10 +406,12 @@ __global__ void __launch_bounds__(kBT, 2)
   const int nv = (int)(a.L - c0 < Q ? a.L - c0 : Q);
   const float A_h = a.A[h];
   float* pe = phi_end + (bhi * nC + c) * K2;
+  uint32_t xw[4], yw[4];  // x and dy, loaded while the prologue runs
+  act_ld2<R>(xw, static_cast<const __nv_bfloat16*>(a.x), b, h, a.L, a.H, c0, nv);
+  act_ld2<R>(yw, static_cast<const __nv_bfloat16*>(a.dy), b, h, a.L, a.H, c0, nv);
   chunk_prep<R, NS, SBP>(a, b, h, gi, c0, nv, A_h, Bt, Ct, nullptr, tk, s_gt, pe);
-  load_act_tile<R, SXP>(Xw, static_cast<const __nv_bfloat16*>(a.x), b, h, a.L, a.H, c0, nv, tk.w);
-  load_act_tile<R, SXP>(Ye, static_cast<const __nv_bfloat16*>(a.dy), b, h, a.L, a.H, c0, nv,
-                        tk.el);
+  act_st2<R, SXP>(Xw, xw, tk.w);
+  act_st2<R, SXP>(Ye, yw, tk.el);
   if (threadIdx.x == 0) lam_end[bhi * nC + c] = tk.lc[Q - 1];
   __syncthreads();
   // [N][P] = Bt^T Xw and Ct^T Ye: warp tile 16 rows x (8 NT) columns
@@ -550,15 +585,25 @@ __global__ void __launch_bounds__(kBT, 1)
                  aYs = ptx::smem_addr(Ys), aPT = ptx::smem_addr(PT), adS = ptx::smem_addr(dSs),
                  adST = ptx::smem_addr(dST), aSt = ptx::smem_addr(St);
 
+  // the chunk's x, dy and entering state, loaded into registers while the
+  // prologue runs (one 64 x 64 tile is exactly one 16-byte load per thread)
+  static_assert(kRows * kPd == 8 * kBT, "one 16-byte load per thread and tile");
+  constexpr int NH = NS * kPd / (4 * kBT);
+  const uint4 xr = act_ld8<R>(static_cast<const __nv_bfloat16*>(a.x), b, h, L, H, c0, nv);
+  const uint4 yr = act_ld8<R>(static_cast<const __nv_bfloat16*>(a.dy), b, h, L, H, c0, nv);
+  float4 hr[NH];
+#pragma unroll
+  for (int j = 0; j < NH; ++j)
+    hr[j] = *reinterpret_cast<const float4*>(wsA + slot + 4 * (tid + j * kBT));
   for (int i = tid; i < 8 * kRows; i += kBT) colVi[i] = 0.f;
   chunk_prep<R, NS, SB>(a, b, h, gi, c0, nv, A_h, Bt, Ct, Rt, tk, s_gt, nullptr);
-  load_act_tile8<R, kSX>(Xs, static_cast<const __nv_bfloat16*>(a.x), b, h, L, H, c0, nv);
-  load_act_tile8<R, kSX>(Ys, static_cast<const __nv_bfloat16*>(a.dy), b, h, L, H, c0, nv);
-  for (int e = tid * 4; e < NS * kPd; e += kBT * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(wsA + slot + e);
-    const int n = e / kPd, p = e - n * kPd;
+  act_st8<R, kSX>(Xs, xr);
+  act_st8<R, kSX>(Ys, yr);
+#pragma unroll
+  for (int j = 0; j < NH; ++j) {
+    const int e = 4 * (tid + j * kBT), n = e / kPd, p = e - n * kPd;
     *reinterpret_cast<float4*>(St + n * kSX + p) =
-        make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
+        make_float4(tf32r(hr[j].x), tf32r(hr[j].y), tf32r(hr[j].z), tf32r(hr[j].w));
   }
   __syncthreads();
 
@@ -652,16 +697,17 @@ __global__ void __launch_bounds__(kBT, 1)
   for (int q = 0; q < 2; ++q)
 #pragma unroll
     for (int nt = 0; nt < NT3; ++nt) dphr[q][nt] = 0.f;
+  float4 gr[NH];  // dG, loaded during the first pass
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
     if (pass == 1) {
       // the state tile: H_in -> dG
       __syncthreads();
-      for (int e = tid * 4; e < NS * kPd; e += kBT * 4) {
-        const float4 v = *reinterpret_cast<const float4*>(wsB + slot + e);
-        const int n = e / kPd, p = e - n * kPd;
+#pragma unroll
+      for (int j = 0; j < NH; ++j) {
+        const int e = 4 * (tid + j * kBT), n = e / kPd, p = e - n * kPd;
         *reinterpret_cast<float4*>(St + n * kSX + p) =
-            make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
+            make_float4(tf32r(gr[j].x), tf32r(gr[j].y), tf32r(gr[j].z), tf32r(gr[j].w));
       }
       __syncthreads();
     }
@@ -703,6 +749,11 @@ __global__ void __launch_bounds__(kBT, 1)
     }
     // + dS Oth (pass 0) or dS^T Oth (pass 1)
     wgemm_l<NT3, kRows, kSX, SB, false>(acc, pass ? adST : adS, m0, 0u, Oth, n0, lane);
+    if (pass == 0) {
+#pragma unroll
+      for (int j = 0; j < NH; ++j)
+        gr[j] = *reinterpret_cast<const float4*>(wsB + slot + 4 * (tid + j * kBT));
+    }
     // rotation backward: the raw gradient Rot(Phi_t) d, the angle gradient,
     // and the bias gradient (summed over the warp's rows of equal rank)
     float* graw = pass ? a.dB : a.dC;
@@ -752,6 +803,18 @@ __global__ void __launch_bounds__(kBT, 1)
     }
   }
 
+  // theta of the angle pass below (thread (pair, token group) as in the fold),
+  // loaded while dX is formed
+  constexpr int TG = K::TG, TPG = K::TPG;
+  float thv[TPG];
+  {
+    const int kk = tid % K2, tg = tid / K2;
+#pragma unroll
+    for (int j = 0; j < TPG; ++j) {
+      const int t = tg * TPG + j;
+      thv[j] = t < nv ? a.theta[((b * L + c0 + t) * G + gi) * K2 + kk] : 0.f;
+    }
+  }
   // ---- dX = P^T dY + diag(w) Bt dG (64 x 64; warp tile 16 x 16)
   {
     const int xm0 = 16 * (warp >> 2), xn0 = 16 * (warp & 3);
@@ -793,14 +856,12 @@ __global__ void __launch_bounds__(kBT, 1)
   //      reverse sum over the chunk's tokens, dtheta, and theta . dphi per
   //      token; thread (pair kk, token group tg) as in the fold
   {
-    constexpr int TG = K::TG, TPG = K::TPG;
     const int kk = tid % K2, tg = tid / K2;
-    float th[TPG], run[TPG];
+    float run[TPG];
     float acc = (tg == TG - 1) ? dphiB[(bhi * nC + c) * K2 + kk] : 0.f;
 #pragma unroll
     for (int j = TPG - 1; j >= 0; --j) {
       const int t = tg * TPG + j;
-      th[j] = t < nv ? a.theta[((b * L + c0 + t) * G + gi) * K2 + kk] : 0.f;
       acc += dPh[t * K2 + kk];
       run[j] = acc;
     }
@@ -814,7 +875,7 @@ __global__ void __launch_bounds__(kBT, 1)
       const float dphi = off + run[j];
       if (t < nv) atomicAdd(a.dtheta + ((b * L + c0 + t) * G + gi) * K2 + kk, tk.dt[t] * dphi);
       // theta . dphi over the pairs: a warp holds 32 pairs of one token
-      float v = th[j] * dphi;
+      float v = thv[j] * dphi;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       if (lane == 0) atomicAdd(&ths[t], v);
@@ -922,8 +983,8 @@ bool scan_bwd_tc_ok(const BwdArgs& a, bool bf16) {
   if (a.batch * a.H > 65535) return false;  // grid y
   const int64_t Q = kRows / a.R, nC = (a.L + Q - 1) / Q;
   if (nC > 0x7fffffffLL) return false;
-  // 16-byte vectors of x / dy rows, 8-byte atomics of dB / dC at R = 1
-  if (!al(a.x) || !al(a.dy) || !al(a.dB) || !al(a.dC)) return false;
+  // 16-byte vectors of x / dy rows and of B / C pairs, 8-byte atomics of dB / dC at R = 1
+  if (!al(a.x) || !al(a.dy) || !al(a.B) || !al(a.C) || !al(a.dB) || !al(a.dC)) return false;
   return true;
 }
 

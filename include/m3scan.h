@@ -192,7 +192,10 @@ m3_status m3_scan_bwd(const void* x, const float* dt, const float* A, const floa
  *           one non-NULL is M3_ERR_INVALID_ARG.
  * dims->seqlen, workspace and workspace_bytes are ignored. The product
  * B_prev x_prev^T is formed on the fly (passing N x P products per head would
- * double the step's memory traffic).
+ * double the step's memory traffic). bf16 at R = 4, P = 64, N a multiple of
+ * 16 up to 128 (all pointers 16-byte aligned, b H a multiple of 4) forms the
+ * rank-8 update on the tensor cores (mma.sync, U in bf16 high and low parts);
+ * every other shape runs on the CUDA cores.
  */
 m3_status m3_decode_step(float* state, const void* x, const float* dt, const float* A,
                          const float* lambda, const void* B_prev, const void* x_prev,
@@ -223,7 +226,10 @@ m3_status m3_decode_step(float* state, const void* x, const float* dt, const flo
  * head), every per-token block of x, B, C, theta and the biases a multiple of
  * 16 bytes and 16-byte aligned, and the block's activations within 200 KB of
  * shared memory; other valid shapes return M3_ERR_UNSUPPORTED (use
- * m3_decode_step per token).
+ * m3_decode_step per token). bf16 at R = 4, P = 64, N a multiple of 16 up to
+ * 128 runs the tokens' updates on the tensor cores (mma.sync) when the
+ * block's activations fit its shared-memory layout (about 20 tokens at
+ * N = 128); other shapes run on the CUDA cores.
  */
 m3_status m3_decode_tokens(float* state, const void* x, const float* dt, const float* A,
                            const float* lambda, const void* B_prev, const void* x_prev,

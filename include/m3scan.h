@@ -8,12 +8,18 @@
  *   y_t = C_t^T h_t
  *
  *   alpha_t = exp(Delta_t A),  beta_t = (1 - lambda_t) Delta_t alpha_t,  gamma_t = lambda_t Delta_t
- *       -- exponential-trapezoidal discretisation, aipaper.cc summary, sec. 4.1, Prop. 1
+ *       -- exponential-trapezoidal discretisation, [A] sec. 4.1, Prop. 1
  *   R_t = block-diagonal 2x2 rotations [[cos,-sin],[sin,cos]] by Delta_t theta[t,k] on state
- *         rows (2k, 2k+1)  -- complex-valued state, aipaper.cc sec. 4.2 (Prop. 2/3);
- *         rotation matrix from the metaphor-xennon blog, sec. 2.2
+ *         rows (2k, 2k+1)  -- complex-valued state, [A] sec. 4.2 (Prop. 2/3);
+ *         rotation matrix from [X] sec. 2.2
  *   B_t = B[b,t,g] + B_bias[h] (N x R), C_t = C[b,t,g] + C_bias[h], x_t (P x R)
- *       -- MIMO rank R, papernotes.org sec. 3; head-specific B/C bias, papernotes.org sec. 4
+ *       -- MIMO rank R, [N] sec. 3; head-specific B/C bias, [N] sec. 4
+ *
+ * Sources (web pages on the method), cited by letter with the page's section:
+ *   [A] "MAMBA-3: IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc)
+ *   [N] "Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org)
+ *   [X] "State Space Models 家族对比分析：S4 → Mamba → Mamba-2 → Mamba-3" (metaphor-xennon blog)
+ *   [U] "Mamba-3: Improved Sequence Modeling using State Space Principles" (bud-325 notes)
  *   g = h / (H / G): heads are split into G equal groups that share B, C and theta.
  *   h_{-1} = 0 and B_{-1} x_{-1} = 0 for prefill.
  *
@@ -71,9 +77,7 @@ typedef enum {
  * of B (and of C) over the N state rows is divided by its root mean square,
  *   B[b,t,g,:,r] / sqrt(mean_n B[b,t,g,n,r]^2 + 1e-6),
  * with no learned weight, before the per-head bias and the rotation
- * (papernotes.org "Mamba-3: Improved Sequence Modeling using State Space
- * Principles", sec. 4, BC normalisation and B/C bias; bud-325 notes, key
- * claims). Supported by m3_scan_fwd and m3_scan_fwd_noalloc on the tensor-core
+ * ([N] sec. 4, BC normalisation and B/C bias; [U] Key claims). Supported by m3_scan_fwd and m3_scan_fwd_noalloc on the tensor-core
  * path (bf16, P = 64, N in {64, 128}, chunk * R = 64, the alignments given
  * there); every other call with it returns M3_ERR_UNSUPPORTED, as do
  * m3_scan_fwd_state, the decode calls and m3_scan_bwd (normalise B and C

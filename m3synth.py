@@ -21,7 +21,7 @@ workload is bf16; every array is returned as float32 holding exactly the value
 the kernels see. dt, lambda, theta, A and the biases stay fp32.
 
 Parity stress case (state tracking, the R(pi x_t) construction on the
-papernotes.org page, sec. 2): A = 0, bits ~ Bernoulli(0.5) per (b, t),
+"Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org), sec. 2): A = 0, bits ~ Bernoulli(0.5) per (b, t),
 dt drawn per (b, t) and shared by all heads, theta = pi * bit / dt for every
 state pair, and an impulse input: x is N(0,1) at t = 0 and zero after.
 """

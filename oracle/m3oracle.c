@@ -10,18 +10,23 @@
  * GPU receives in bf16 are rounded to bf16 by the input generator first and
  * then widened, so the oracle sees exactly the numbers the kernels see).
  *
- * What is computed, per batch row b and head h (sources are the web pages on
- * "Mamba-3: Improved Sequence Modeling using State Space Principles"):
+ * Sources, cited below by letter with the page's section:
+ *   [A] "MAMBA-3: IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc)
+ *   [N] "Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org)
+ *   [X] "State Space Models 家族对比分析：S4 → Mamba → Mamba-2 → Mamba-3" (metaphor-xennon blog)
+ *   [U] "Mamba-3: Improved Sequence Modeling using State Space Principles" (bud-325 notes)
+ *
+ * What is computed, per batch row b and head h:
  *
  *   Delta_t = dt[b,t,h],  A = A[h] (scalar per head),  lambda_t = lam[b,t,h]
- *   alpha_t = exp(Delta_t A)                                   (aipaper.cc, sec. 4.1, Prop. 1)
+ *   alpha_t = exp(Delta_t A)                                   ([A] sec. 4.1, Prop. 1)
  *   beta_t  = (1 - lambda_t) Delta_t exp(Delta_t A)            (same)
  *   gamma_t = lambda_t Delta_t                                 (same)
  *   R_t     = block-diag of 2x2 rotations [[cos,-sin],[sin,cos]] by
  *             Delta_t * theta[b,t,g,k] acting on state rows (2k,2k+1)
- *                                                              (metaphor-xennon blog, sec. 2.2 / 6.4)
+ *                                                              ([X] sec. 2.2 / 6.4)
  *   B_t = B[b,t,g] + B_bias[h]  (N x R),  C_t likewise,  x_t (P x R)
- *                                                              (papernotes.org, sec. 3 MIMO; sec. 4 B/C bias)
+ *                                                              ([N] sec. 3 MIMO; sec. 4 B/C bias)
  *   h_t = alpha_t R_t h_{t-1} + beta_t R_t B_{t-1} x_{t-1}^T + gamma_t B_t x_t^T
  *   y_t = C_t^T h_t   (R x P, stored as [P][R])
  *
@@ -35,11 +40,10 @@
  * against one another and against closed forms:
  *   m3o_scan_seq     explicit-rotation sequential recurrence (the definition)
  *   m3o_scan_rope    Prop. 3 form: cumulative rotation applied to B and C,
- *                    real scalar-decay state (aipaper.cc, sec. 4.2, Prop. 3)
+ *                    real scalar-decay state ([A] sec. 4.2, Prop. 3)
  *   m3o_scan_chunked chunked SSD form: per-chunk masked C B^T block plus
  *                    inter-chunk state passing (SSD duality Y = (L o C B^T) X,
- *                    metaphor-xennon blog, sec. 1.3 / 6.3; mask = decay x
- *                    2-band, papernotes.org sec. 1)
+ *                    [X] sec. 1.3 / 6.3; mask = decay x 2-band, [N] sec. 1)
  * and a single decode step m3o_decode_step (the recurrence body for one t).
  * m3o_bc_norm is BCNorm, the weightless RMS normalisation of B and C over N
  * that the scan can apply to its raw B / C inputs before the bias.
@@ -433,9 +437,9 @@ int m3o_decode_step(int64_t batch, int64_t H, int64_t G, int64_t P, int64_t N, i
 /* BCNorm: RMS normalisation of B (or C) over the state dimension N, per     */
 /* (batch, token, group, rank), with no learned weight:                      */
 /*   out[b,t,g,n,r] = in[b,t,g,n,r] / sqrt(mean_n in[b,t,g,n,r]^2 + eps)      */
-/* (papernotes.org, sec. 4: BC normalisation applied to the projected B and  */
-/* C, before the per-head B/C bias; bud-325 notes, key claims: BCNorm is an  */
-/* RMSNorm on the B/C activations). The scan then takes out as its B / C.    */
+/* ([N] sec. 4: BC normalisation applied to the projected B and C, before   */
+/* the per-head B/C bias; [U] Key claims: BCNorm is an RMSNorm on the B/C    */
+/* activations). The scan then takes out as its B / C.                       */
 /* ------------------------------------------------------------------------ */
 int m3o_bc_norm(int64_t batch, int64_t L, int64_t G, int64_t N, int64_t R, const double* in,
                 double* out, double eps) {

@@ -16,8 +16,8 @@
 //   w_s   = e^{Lam_end - Lam_s} (gamma_s + bhat_{s+1})
 // (bhat of the token after the chunk; 0 past the end). Flattening (token, rank)
 // into QR = 64 rows, S = Ct Bt^T, P = S o W and Y = P X + diag(e^Lam) Ct H_in
-// is the chunked form of the scan (papernotes.org sec. 1; SSD form
-// Y = (L o C B^T) X).
+// is the chunked form of the scan (the papernotes.org page named above,
+// sec. 1; SSD form Y = (L o C B^T) X).
 //
 // Backward, per chunk, with dG = Rot(-Phi_end) dH_out (dH_out = d_final for
 // the last chunk) and H_in from a forward pass over the chunk boundaries:

@@ -6,11 +6,13 @@
 //   Lam_t = sum_{u=t0..t} dt_u A                       (decay exponent)
 //   Phi_t = sum_{u=t0..t} dt_u theta_u (per pair)      (rotation angle)
 //   Bt_s = Rot(-Phi_s)(B_s + bias), Ct_t = Rot(-Phi_t)(C_t + bias)
-//        -- the rotation folded into B and C (Prop. 3, aipaper.cc sec. 4.2)
+//        -- the rotation folded into B and C (Prop. 3, sec. 4.2 of "MAMBA-3:
+//           IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc))
 //   S[(t,r'),(s,r)] = Ct_t[:,r'] . Bt_s[:,r]  masked by
 //   M[t,s] = exp(Lam_t - Lam_s) (gamma_s + [s<t] beta_hat_{s+1}), s <= t
 //        -- decay (1-semiseparable) times the 2-band trapezoid mask
-//           (papernotes.org sec. 1; SSD form Y = (L o C B^T) X)
+//           (sec. 1 of "Mamba-3: Improved Sequence Modeling using State Space
+//           Principles" (papernotes.org); SSD form Y = (L o C B^T) X)
 //   y_t = sum_s S M x_s + exp(Lam_t) Ct_t^T H_in
 //   H_out = Rot(Phi_end)(exp(Lam_end) H_in + sum_s exp(Lam_end-Lam_s) w_s Bt_s x_s^T)
 //   w_s = gamma_s + beta_hat_{s+1}   (beta_hat of the token after s; 0 at the end)

@@ -1,7 +1,7 @@
 """GPU parity of the prefill with BCNorm fused into its prologue
 (M3_FLAG_BC_NORM): the kernel takes un-normalised B and C; the oracle is the
-sequential scan of the oracle's own BCNorm of them (papernotes.org
-"Mamba-3: Improved Sequence Modeling using State Space Principles", sec. 4).
+sequential scan of the oracle's own BCNorm of them ("Mamba-3: Improved Sequence
+Modeling using State Space Principles" (papernotes.org), sec. 4).
 
 The raw B and C are the workload recipe's vectors times a random positive
 scale per (b, t, g, r) vector (0.05 .. 20), rounded to bf16, so that the

@@ -191,7 +191,7 @@ def test_long_context_bf16_sampled(orc, name):
 @pytest.mark.parametrize("name", ["long_siso_n128", "long_mimo_n128"])
 def test_long_context_parity_signs(orc, name):
     """A = 0 and theta = pi*bit/dt: the output's sign carries the running
-    parity (papernotes.org sec. 2). Over the whole 65536-token sequence of
+    parity ("Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org), sec. 2). Over the whole 65536-token sequence of
     four sampled heads every sign must equal the oracle's wherever |y| is
     above 1% of RMS(y) (below it the bf16 output cannot fix a sign); the
     counts compared and left out are printed."""

@@ -39,7 +39,7 @@ def _rel(a, b):
 
 # ---------------------------------------------------------------------------
 # 1. lambda = 1, theta = 0, R = 1 reduces to the Mamba-2 Euler recurrence
-#    (aipaper.cc sec. 4.1: "When lambda_t = 1, this rule reduces to Mamba-2's
+#    ("MAMBA-3: IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc), sec. 4.1: "When lambda_t = 1, this rule reduces to Mamba-2's
 #    Euler method"; the Euler rule h_t = e^{Delta A} h_{t-1} + Delta B_t x_t).
 # ---------------------------------------------------------------------------
 def test_euler_reduction(orc):
@@ -70,7 +70,7 @@ def test_euler_reduction(orc):
 # 2. Convergence order on a smooth complex ODE with a closed-form solution.
 #    h'(tau) = (A + i w) h + b u(tau), u = sin(W tau), h(0) = 0.
 #    The exponential-trapezoidal rule (lambda = 1/2) is second order, the
-#    exponential-Euler rule (lambda = 1) first order (papernotes.org sec. 1:
+#    exponential-Euler rule (lambda = 1) first order ("Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org), sec. 1:
 #    local error O(Delta^2) vs O(Delta^3)). A non-uniform grid pins that beta
 #    uses the current step's Delta, and the complex rate pins that the
 #    previous-input term is rotated as well.
@@ -106,7 +106,7 @@ def test_convergence_order(orc, lam_val, order):
 # 3. Constant inputs: geometric series closed form. With z = alpha e^{i phi}
 #    per state pair, h_t = z^t gamma U + (z beta_hat + gamma) U (1 - z^t)/(1 - z).
 #    Pins the rotation direction ([[c,-s],[s,c]] = multiplication by e^{i phi},
-#    metaphor-xennon blog sec. 2.2) and the weights of both input terms.
+#    "State Space Models 家族对比分析：S4 → Mamba → Mamba-2 → Mamba-3" (metaphor-xennon blog), sec. 2.2) and the weights of both input terms.
 # ---------------------------------------------------------------------------
 def test_geometric_series(orc):
     rng = np.random.default_rng(3)
@@ -136,7 +136,7 @@ def test_geometric_series(orc):
 
 
 # ---------------------------------------------------------------------------
-# 4. Prop. 3 (aipaper.cc sec. 4.2): the real SSM with the cumulative rotation
+# 4. Prop. 3 ("MAMBA-3: IMPROVED SEQUENCE MODELING USING STATE SPACE PRINCIPLES" (aipaper.cc), sec. 4.2): the real SSM with the cumulative rotation
 #    applied to B and C equals the complex (explicitly rotated) SSM.
 # ---------------------------------------------------------------------------
 def test_rope_form_equals_explicit_rotation(orc):
@@ -148,7 +148,7 @@ def test_rope_form_equals_explicit_rotation(orc):
 
 
 # ---------------------------------------------------------------------------
-# 5. Parity (papernotes.org sec. 2, rotation R(pi x_t)); hand fixture.
+# 5. Parity ("Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org), sec. 2, rotation R(pi x_t)); hand fixture.
 # ---------------------------------------------------------------------------
 def _read_kv(path):
     out = {}
@@ -218,11 +218,13 @@ def test_chunked_equals_sequential(orc, chunk, R):
 
 
 # ---------------------------------------------------------------------------
-# 8. Structured-mask form (papernotes.org sec. 1; bud-325 notes, key claims):
+# 8. Structured-mask form:
+#    "Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org), sec. 1;
+#    "Mamba-3: Improved Sequence Modeling using State Space Principles" (bud-325 notes), Key claims:
 #    the whole-sequence mask is (1-semiseparable decay) @ (2-band matrix) with
 #    gamma_s on the diagonal and beta_{s'} on the sub-diagonal; Y = (M o C B^T) X
-#    in the frame rotated by the cumulative angle (SSD form, metaphor-xennon
-#    blog sec. 1.3). Built densely here with numpy.
+#    in the frame rotated by the cumulative angle (SSD form,
+#    "State Space Models 家族对比分析：S4 → Mamba → Mamba-2 → Mamba-3" (metaphor-xennon blog), sec. 1.3). Built densely here with numpy.
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("rotate", [False, True])
 def test_dense_mask_product_form(orc, rotate):
@@ -258,7 +260,7 @@ def test_dense_mask_product_form(orc, rotate):
 
 
 # ---------------------------------------------------------------------------
-# 9. MIMO = sum of R^2 SISO calls (papernotes.org sec. 3): output column r'
+# 9. MIMO = sum of R^2 SISO calls ("Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org), sec. 3): output column r'
 #    equals sum over r of the SISO scan with (B_r, x_r, C_r').
 # ---------------------------------------------------------------------------
 def test_mimo_is_sum_of_siso(orc):
@@ -401,7 +403,7 @@ def test_generator_is_bf16_exact_and_seeded():
 
 
 # ---------------------------------------------------------------------------
-# BCNorm (papernotes.org sec. 4; bud-325 notes, key claims): RMS normalisation
+# BCNorm ("Mamba-3: Improved Sequence Modeling using State Space Principles" (papernotes.org), sec. 4; "Mamba-3: Improved Sequence Modeling using State Space Principles" (bud-325 notes), Key claims): RMS normalisation
 # over N per (b, t, g, r) with no weight, eps = 1e-6 under the root.
 # ---------------------------------------------------------------------------
 def _read_bc_fixture():

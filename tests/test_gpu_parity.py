@@ -696,6 +696,42 @@ def test_decode_tokens_full_batch_mimo(orc):
     assert_bf16(st[bsel], st_ref, "state")
 
 
+def test_backward_headline_workload_sampled():
+    """The backward pass at the headline workload's full size (b8 L2048 H32 P64
+    N128 R1, bf16: 32 chunks per sequence on the tensor cores) with a final-
+    state gradient. The per-sequence gradients (dx, ddt, dlambda) of three
+    sampled (batch, head) sequences are checked against the oracle run on that
+    sequence alone; the gradients summed over heads or batch rows (dB, dC,
+    dtheta, dA, the biases) are covered by the smaller whole-problem cases."""
+    from oracle import backward
+    shape = m3synth.ScanShape(8, 2048, 32, 1, 64, 128, R=1, chunk=64, bf16=True)
+    inp = m3synth.scan_inputs(shape, seed=177)
+    rng = np.random.default_rng(178)
+    dy = m3synth.to_bf16(rng.standard_normal((8, 2048, 32, 64, 1)).astype(np.float32))
+    dfin = rng.standard_normal((8, 32, 128, 64)).astype(np.float32)
+    d = to_device(inp, True)
+    g = m3.m3_scan_bwd(d["x"], d["dt"], d["A"], d["lam"], d["B"], d["C"], d["theta"],
+                       torch.from_numpy(dy).to(torch.bfloat16).cuda(), R=1,
+                       d_final=torch.from_numpy(dfin).cuda(), B_bias=d["B_bias"],
+                       C_bias=d["C_bias"])
+    torch.cuda.synchronize()
+    assert m3.m3_device_status() == m3.M3_OK
+    got = {k: g[k].cpu().numpy() for k in ("x", "dt", "lam")}
+    worst = {}
+    for (b, h) in _pairs(shape, 3, 179):
+        sub = head_slice(inp, b, h)
+        ref = backward.scan_grads(sub["x"], sub["dt"], sub["A"], sub["lam"], sub["B"], sub["C"],
+                                  sub["theta"], dy[b:b + 1, :, h:h + 1],
+                                  dh=dfin[b:b + 1, h:h + 1], B_bias=sub["B_bias"],
+                                  C_bias=sub["C_bias"])
+        for k in ("x", "dt", "lam"):
+            gk = got[k][b:b + 1, :, h:h + 1]
+            assert_bf16(gk, ref[k], "d%s of (b %d, h %d)" % (k, b, h))
+            worst[k] = max(worst.get(k, 0.0), max_over_rms(gk, ref[k]))
+    print("backward at full size, sampled sequences, max|err|/RMS: %s"
+          % ", ".join("d%s %.1e" % (k, worst[k]) for k in sorted(worst)))
+
+
 @pytest.mark.parametrize("bf16,P,N", [(True, 64, 128), (False, 64, 128), (True, 32, 64)],
                          ids=["tensor_cores", "cuda_cores_f32", "cuda_cores_bf16"])
 def test_backward_with_a_caller_workspace(bf16, P, N):

@@ -77,6 +77,24 @@ def prefill_flops(s: m3synth.ScanShape) -> int:
     return s.batch * s.seqlen * s.heads * (2 * Q * R * R * (N + P) + 4 * R * N * P)
 
 
+def prefill_flops_causal(s: m3synth.ScanShape) -> int:
+    """The same count with only the causal half of the intra-chunk block: per
+    token and head Q R^2 (N + P) + 4 R N P."""
+    Q, R, N, P = s.chunk, s.R, s.dstate, s.headdim
+    return s.batch * s.seqlen * s.heads * (Q * R * R * (N + P) + 4 * R * N * P)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (for the CPU baseline's record)."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def decode_bytes(s: m3synth.ScanShape, act: int = 2) -> int:
     """Per decode step: state read + write, plus the token's activations
     (``act`` bytes per activation element)."""
@@ -274,7 +292,7 @@ def run_reference(args, rank, world):
         "config": headline_config(shape, world),
         "note": "fp64 CPU oracle (sequential explicit-rotation recurrence) on the host cores",
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -404,6 +422,9 @@ def run_ours(args, rank, world, local_rank):
         "roofline_tensor": {"bound": "tensor", "achieved": tfs, "peak": peaks["bf16"],
                             "unit": "TFLOP/s", "frac": tfs / peaks["bf16"],
                             "algorithmic_flops": nflops,
+                            "frac_causal_half": prefill_flops_causal(shape) / (ms * 1e-3) / 1e12
+                                                / peaks["bf16"],
+                            "algorithmic_flops_causal_half": prefill_flops_causal(shape),
                             "peak_source": peaks["src"] + " bf16 dense (burst)"},
         "clocks": clk.summary(),
         "gpu_launches": args.steps,
@@ -439,7 +460,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         rate, cores, sample = oracle_rate(shape, inp)
         line["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": cores,
-                                "kind": "oracle", "sample": sample}
+                                "kind": "oracle", "sample": sample, "cpu_model": cpu_model()}
     print(json.dumps(line), flush=True)
 
 

@@ -33,8 +33,9 @@
 // each scaled by a power of two chosen per chunk from a bound of its
 // magnitude, so fp16's range never limits the inputs. The scales are undone
 // exactly where a per-element factor is applied anyway (mask, state rescale,
-// output). P is split into bf16 high and low parts so that P X (X is an exact
-// bf16 input) keeps ~16 significant bits. The cumulative angle is carried
+// output). P and the X operand of P X are fp16 too (X scaled by a power of
+// two: exact for bf16 inputs), so that P keeps the same 11 bits as the
+// operands it is made from. The cumulative angle is carried
 // from chunk to chunk as a float-float pair, so it does not drift over long
 // sequences.
 //
@@ -46,11 +47,11 @@
 //   fold   raw B, C, x tiles (TMA, refilled with the next chunk as soon as they
 //          are read) -> magnitude bounds and per-token-group angle sums ->
 //          barrier -> fp16 scales, angle offsets, sincos, RoPE fold of B and C
-//          into 128-byte-swizzled fp16 UMMA tiles, w X, the bf16 X operand, and
+//          into 128-byte-swizzled fp16 UMMA tiles, w X, the fp16 X operand, and
 //          the rescale of the state held in TMEM by exp(Lam_end) and the change
 //          of scale -> barrier -> one thread issues D (accumulated onto the
 //          state), S and Yoff = Ct H_in
-//   mask   S -> P (bf16 high + low, over the Bt tile, which D and S no longer
+//   mask   S -> P (fp16, scaled; over the Bt tile, which D and S no longer
 //          read) -> barrier -> one thread issues Y = P X
 //   state  the state after D (TMEM) -> its bound -> barrier -> its scaled fp16
 //          copy for the next chunk's Yoff
@@ -119,8 +120,8 @@ struct Cfg {
   static constexpr uint32_t kRawC = kRawB + Q * NS * R * AB;
   static constexpr uint32_t kRawX = align1k(kRawC + Q * NS * R * AB);
   static constexpr uint32_t kRawEnd = kRawX + (uint32_t)(Q * kP * R * AB);
-  // operand tiles: Bt, Ct [64][NS] fp16, w X [64][64] fp16, X [64][64] (bf16;
-  // F32: fp16), the fp16 state copy [NS][64]; F32: each followed by its residual
+  // operand tiles: Bt, Ct [64][NS] fp16, w X [64][64] fp16, X [64][64] fp16,
+  // the fp16 state copy [NS][64]; F32: each followed by its residual
   static constexpr uint32_t kBtLo = 64 * NS * 2;   // hi -> lo offset of Bt, Ct
   static constexpr uint32_t kXLo = kTileBytes;     // ... of w X, X, P
   static constexpr uint32_t kHLo = NS * 128;       // ... of the state copy
@@ -132,12 +133,13 @@ struct Cfg {
   static constexpr uint32_t kXo = kXw + OPS * kTileBytes;
   static constexpr uint32_t kH = kXo + OPS * kTileBytes;
   static constexpr uint32_t kHEnd = kH + OPS * NS * 128;
-  // masked scores P (high, low parts): over Bt (hi, lo) when it is large enough
+  // masked scores P (F32: high and low parts): over Bt when it is large enough
   static constexpr uint32_t kPh = (NS == 128 || F32) ? kBt : kHEnd;
   static constexpr uint32_t kPl = kPh + kTileBytes;
+  static constexpr uint32_t kPEnd = F32 ? kPl + kTileBytes : kPl;
   // output staging (R > 1): over w X (hi, lo), which only D reads
   static constexpr uint32_t kYs = kXw;
-  static constexpr uint32_t kBytes = (kPl + kTileBytes > kHEnd) ? kPl + kTileBytes : kHEnd;
+  static constexpr uint32_t kBytes = (kPEnd > kHEnd) ? kPEnd : kHEnd;
   static constexpr uint32_t kSmem = kBytes + 1024;  // + alignment slack
   // bytes landing on the raw barrier per chunk (full pass; state-only pass)
   static constexpr uint32_t kTxBytes = 2u * Q * NS * R * AB + (uint32_t)(Q * kP * R * AB);
@@ -155,7 +157,8 @@ struct __align__(16) Scal {
   float dt[64];    // Delta_t
   float eLend, lamend2, wmax;  // exp(Lam_end), Lam_end (log2), max |wend|
   float invB, invC, invX;      // inverse fp16 scales of Bt, Ct, w X
-  float pmul;                  // S -> P units: invB invC (F32: times P's scale)
+  float pmul;                  // S -> P units: invB invC times P's scale
+  float ykY;                   // Y units -> y: the inverse scales of P and X
   float wpmax;                 // max over the chunk of |gamma_t|, |gamma_t + bhat_{t+1}|
 };
 
@@ -481,9 +484,8 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
   constexpr uint32_t kIdS = ptx::idesc_f16_f32(64, 64, false, false);
   constexpr uint32_t kIdD = ptx::idesc_f16_f32(NS, 64, true, true);
   constexpr uint32_t kIdYo = ptx::idesc_f16_f32(64, 64, false, true);
-  // Y = P X: bf16 parts of P times the exact bf16 X, or (F32) fp16 parts
-  constexpr uint32_t kIdY =
-      F32 ? ptx::idesc_f16_f32(64, 64, false, true) : ptx::idesc_bf16_f32(64, 64, false, true);
+  // Y = P X: fp16 P times the fp16 X operand (F32: their high and low parts)
+  constexpr uint32_t kIdY = ptx::idesc_f16_f32(64, 64, false, true);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -875,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
 
     // ================================================= fold, part 2
     float sigB, invB, sigC, invC, sigX, invX;
-    float sigXo = 1.f, ykY = 1.f;  // F32: scale of the X tile; Y units -> y
+    float sigXo = 1.f;  // scale of the X operand tile
     {
       const float mb = __uint_as_float(s_max[g & 1][0]);
       const float mc = __uint_as_float(s_max[g & 1][1]);
@@ -896,15 +898,17 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       pow2_scale<-26>(2.f * ((NORM ? kNormBound : mc) + cmax_bias), &sigC, &invC);
       pow2_scale<-26>(mx * sc.wmax, &sigX, &invX);
       float pmul = invB * invC;
-      if constexpr (F32) {
-        // X (fp16 hi + lo) by its own scale; P by one from a bound of |P|:
-        // |S| <= N max|Bt| max|Ct|, the mask <= max(|gamma|, |gamma + bhat|)
+      {
+        // the X operand (fp16; F32: hi + lo) by its own scale; P by one from
+        // a bound of |P|: |S| <= N max|Bt| max|Ct|, the mask <= max(|gamma|,
+        // |gamma + bhat|)
         float invXo, sigP, invP;
         pow2_scale(mx, &sigXo, &invXo);
-        pow2_scale((float)NS * (2.f * (mb + bmax_bias)) * (2.f * (mc + cmax_bias)) * sc.wpmax,
+        pow2_scale((float)NS * (2.f * ((NORM ? kNormBound : mb) + bmax_bias)) *
+                       (2.f * ((NORM ? kNormBound : mc) + cmax_bias)) * sc.wpmax,
                    &sigP, &invP);
         pmul *= sigP;
-        ykY = invP * invXo;
+        if (tid == 0) sc.ykY = invP * invXo;
       }
       if (tid == 0) {
         sc.invB = invB;
@@ -967,8 +971,8 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         for (int i = 0; i < TPG; ++i) ph[i] = make_float2(wrap_rad(ph[i].x), wrap_rad(ph[i].y));
       }
     }
-    // w X (fp16, scaled) and X as the [(token, rank)][p] operand: the exact
-    // bf16 input, or (F32) fp16 hi + lo of sigXo x
+    // w X (fp16, scaled) and X as the [(token, rank)][p] operand: fp16 of
+    // sigXo x (exact for bf16 inputs), or (F32) its fp16 hi + lo
 #pragma unroll
     for (int j = 0; j < kXItems; ++j) {
       const int it = tid + kThreads * j;
@@ -977,12 +981,18 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         const uint32_t row = (uint32_t)it >> 3;
         const float w = sc.wend[row] * sigX;
         const float2 w2 = make_float2(w, w);
-        const uint4 v = make_uint4(xw[j][0], xw[j][1], xw[j][2], xw[j][3]);
-        if constexpr (!SO) sts128(sbase + K::kXo + (uint32_t)it * 16u, v);
-        const float2 p0 = mul2(w2, make_float2(bf_lo(v.x), bf_hi(v.x)));
-        const float2 p1 = mul2(w2, make_float2(bf_lo(v.y), bf_hi(v.y)));
-        const float2 p2 = mul2(w2, make_float2(bf_lo(v.z), bf_hi(v.z)));
-        const float2 p3 = mul2(w2, make_float2(bf_lo(v.w), bf_hi(v.w)));
+        const float2 x0 = make_float2(bf_lo(xw[j][0]), bf_hi(xw[j][0]));
+        const float2 x1 = make_float2(bf_lo(xw[j][1]), bf_hi(xw[j][1]));
+        const float2 x2 = make_float2(bf_lo(xw[j][2]), bf_hi(xw[j][2]));
+        const float2 x3 = make_float2(bf_lo(xw[j][3]), bf_hi(xw[j][3]));
+        if constexpr (!SO) {
+          const float2 s2 = make_float2(sigXo, sigXo);
+          const float2 q0 = mul2(s2, x0), q1 = mul2(s2, x1), q2 = mul2(s2, x2), q3 = mul2(s2, x3);
+          sts128(sbase + K::kXo + (uint32_t)it * 16u,
+                 make_uint4(pack_f16(q0.x, q0.y), pack_f16(q1.x, q1.y), pack_f16(q2.x, q2.y),
+                            pack_f16(q3.x, q3.y)));
+        }
+        const float2 p0 = mul2(w2, x0), p1 = mul2(w2, x1), p2 = mul2(w2, x2), p3 = mul2(w2, x3);
         sts128(sbase + K::kXw + (uint32_t)it * 16u,
                make_uint4(pack_f16(p0.x, p0.y), pack_f16(p1.x, p1.y), pack_f16(p2.x, p2.y),
                           pack_f16(p3.x, p3.y)));
@@ -1035,7 +1045,8 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
               sts64(sbase + K::kXo + K::kXLo + o, f16_residual(x0, a0, a1), f16_residual(x1, a2, a3));
             }
           } else if constexpr (!SO) {
-            sts64(sbase + K::kXo + o, pack_bf16(v4[0], v4[1]), pack_bf16(v4[2], v4[3]));
+            sts64(sbase + K::kXo + o, pack_f16(sigXo * v4[0], sigXo * v4[1]),
+                  pack_f16(sigXo * v4[2], sigXo * v4[3]));
           }
         }
       }
@@ -1188,18 +1199,16 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
     if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
     if (tid == 0) {
       // D = Bt^T (w X) onto the state; S = Ct Bt^T; Yoff = Ct H_in
-      ptx::tc_fence_after_sync();
       // (F32: every product is hi hi + hi lo + lo hi of the split operands)
+      ptx::tc_fence_after_sync();
       const Desc dBm = make_desc(opBt, 64u * 128u), dXw = make_desc(sbase + K::kXw, 64u * 128u);
 #pragma unroll
-      for (int kk = 0; kk < kQR / 16; ++kk)
+      for (int kk = 0; kk < kQR / 16; ++kk) {
         ptx::mma_bf16_ss(tmem + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD,
                          (has_state || kk > 0) ? 1u : 0u);
-      if constexpr (F32) {
-        const Desc dBml = make_desc(opBt + K::kBtLo, 64u * 128u);
-        const Desc dXwl = make_desc(sbase + K::kXw + K::kXLo, 64u * 128u);
-#pragma unroll
-        for (int kk = 0; kk < kQR / 16; ++kk) {
+        if constexpr (F32) {
+          const Desc dBml = make_desc(opBt + K::kBtLo, 64u * 128u);
+          const Desc dXwl = make_desc(sbase + K::kXw + K::kXLo, 64u * 128u);
           ptx::mma_bf16_ss(tmem + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXwl, koff_mn(kk)), kIdD, 1u);
           ptx::mma_bf16_ss(tmem + kColD, desc_at(dBml, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD, 1u);
         }
@@ -1207,13 +1216,11 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       if constexpr (!SO) {
         const Desc dBk = make_desc(opBt, 16u), dCk = make_desc(opCt, 16u);
 #pragma unroll
-        for (int kk = 0; kk < NS / 16; ++kk)
+        for (int kk = 0; kk < NS / 16; ++kk) {
           ptx::mma_bf16_ss(tmem + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
                            kIdS, kk > 0);
-        if constexpr (F32) {
-          const Desc dBkl = make_desc(opBt + K::kBtLo, 16u), dCkl = make_desc(opCt + K::kBtLo, 16u);
-#pragma unroll
-          for (int kk = 0; kk < NS / 16; ++kk) {
+          if constexpr (F32) {
+            const Desc dBkl = make_desc(opBt + K::kBtLo, 16u), dCkl = make_desc(opCt + K::kBtLo, 16u);
             ptx::mma_bf16_ss(tmem + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBkl, koff_k(kk, 64)),
                              kIdS, 1u);
             ptx::mma_bf16_ss(tmem + kColS, desc_at(dCkl, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
@@ -1228,14 +1235,12 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         if (yoff_ready) {
           const Desc dCk = make_desc(opCt, 16u), dH = make_desc(sbase + K::kH, (uint32_t)NS * 128u);
 #pragma unroll
-          for (int kk = 0; kk < NS / 16; ++kk)
+          for (int kk = 0; kk < NS / 16; ++kk) {
             ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)),
                              kIdYo, kk > 0);
-          if constexpr (F32) {
-            const Desc dCkl = make_desc(opCt + K::kBtLo, 16u);
-            const Desc dHl = make_desc(sbase + K::kH + K::kHLo, (uint32_t)NS * 128u);
-#pragma unroll
-            for (int kk = 0; kk < NS / 16; ++kk) {
+            if constexpr (F32) {
+              const Desc dCkl = make_desc(opCt + K::kBtLo, 16u);
+              const Desc dHl = make_desc(sbase + K::kH + K::kHLo, (uint32_t)NS * 128u);
               ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dHl, koff_mn(kk)),
                                kIdYo, 1u);
               ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCkl, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)),
@@ -1267,12 +1272,15 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         const int a = 16 * quad + (lane & 15);
         const int t = a / R;
         const int c0 = 32 * half + 16 * (lane >> 4);
-        uint32_t ph_[8], pl_[8];
+        uint32_t ph_[8], pl_[F32 ? 8 : 1];
         // a warp whose 16 rows x 32 columns lie wholly above the diagonal
         // only writes zeros; elsewhere the mask itself zeroes s > t
         if ((32 * half) / R > (16 * quad + 15) / R) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ph_[j] = pl_[j] = 0u;
+          for (int j = 0; j < 8; ++j) {
+            ph_[j] = 0u;
+            if constexpr (F32) pl_[j] = 0u;
+          }
         } else {
           uint32_t sv[16];
           ptx::tmem_ld16_16x32bx2<16>(tmem + kColS + tq + 32u * half, sv);
@@ -1303,17 +1311,10 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
               const float m1 = (s0 + u1 < t) ? mo.y : ((s0 + u1 == t) ? gdiag : 0.f);
               const float2 v2 = mul2(make_float2(m0, m1),
                                      make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])));
-              if constexpr (F32) {
-                // fp16 high part and residual (P is in units of its own scale)
-                const uint32_t hw = pack_f16(v2.x, v2.y);
-                ph_[j >> 1] = hw;
-                pl_[j >> 1] = f16_residual(hw, v2.x, v2.y);
-              } else {
-                const uint32_t hw = pack_bf16(v2.x, v2.y);
-                ph_[j >> 1] = hw;
-                const float2 lo = ptx::sub2(v2, make_float2(bf_lo(hw), bf_hi(hw)));
-                pl_[j >> 1] = pack_bf16(lo.x, lo.y);
-              }
+              // fp16 (P is in units of its own scale); F32: and the residual
+              const uint32_t hw = pack_f16(v2.x, v2.y);
+              ph_[j >> 1] = hw;
+              if constexpr (F32) pl_[j >> 1] = f16_residual(hw, v2.x, v2.y);
             }
           }
         }
@@ -1321,29 +1322,32 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         const uint32_t o1 = sw128((uint32_t)a, (uint32_t)c0 + 8u);
         sts128(sbase + K::kPh + o0, make_uint4(ph_[0], ph_[1], ph_[2], ph_[3]));
         sts128(sbase + K::kPh + o1, make_uint4(ph_[4], ph_[5], ph_[6], ph_[7]));
-        sts128(sbase + K::kPl + o0, make_uint4(pl_[0], pl_[1], pl_[2], pl_[3]));
-        sts128(sbase + K::kPl + o1, make_uint4(pl_[4], pl_[5], pl_[6], pl_[7]));
+        if constexpr (F32) {
+          sts128(sbase + K::kPl + o0, make_uint4(pl_[0], pl_[1], pl_[2], pl_[3]));
+          sts128(sbase + K::kPl + o1, make_uint4(pl_[4], pl_[5], pl_[6], pl_[7]));
+        }
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before_sync();
       __syncthreads();  // ------------------------------------------ mask
       if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
       if (tid == 0) {
-        // Y = P X (P = high + low parts)
+        // Y = P X
         ptx::tc_fence_after_sync();
-        const Desc dPh = make_desc(sbase + K::kPh, 16u), dPl = make_desc(sbase + K::kPl, 16u);
+        const Desc dPh = make_desc(sbase + K::kPh, 16u);
         const Desc dX = make_desc(sbase + K::kXo, 64u * 128u);
 #pragma unroll
         for (int kk = 0; kk < kQR / 16; ++kk)
           ptx::mma_bf16_ss(tmem + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
                            kIdY, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < kQR / 16; ++kk)
-          ptx::mma_bf16_ss(tmem + kColY, desc_at(dPl, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
-                           kIdY, 1u);
         if constexpr (F32) {
-          // ... + P_hi X_lo (the X tile is split too)
+          // ... + P_lo X_hi + P_hi X_lo (both tiles are split)
+          const Desc dPl = make_desc(sbase + K::kPl, 16u);
           const Desc dXl = make_desc(sbase + K::kXo + K::kXLo, 64u * 128u);
+#pragma unroll
+          for (int kk = 0; kk < kQR / 16; ++kk)
+            ptx::mma_bf16_ss(tmem + kColY, desc_at(dPl, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
+                             kIdY, 1u);
 #pragma unroll
           for (int kk = 0; kk < kQR / 16; ++kk)
             ptx::mma_bf16_ss(tmem + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dXl, koff_mn(kk)),
@@ -1382,8 +1386,9 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         ptx::tmem_ld16_16x32bx2<16>(tmem + kColY + tq + 32u * half, yv);
         ptx::tmem_ld_wait(yv);
         float y[16];
+        const float ykY = sc.ykY;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) y[j] = F32 ? ykY * __uint_as_float(yv[j]) : __uint_as_float(yv[j]);
+        for (int j = 0; j < 16; ++j) y[j] = ykY * __uint_as_float(yv[j]);
         if (yoff_ready) {
           uint32_t yo[16];
           ptx::tmem_ld16_16x32bx2<16>(tmem + kColYo + tq + 32u * half, yo);

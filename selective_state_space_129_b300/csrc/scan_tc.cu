@@ -1188,8 +1188,10 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       state_st(hv);
     }
     u_prev = invB * invX;
-    // the next chunk's theta and decay inputs (loads only; used next chunk)
-    if (has_next) {
+    // the next chunk's theta and decay inputs (loads only; used next chunk).
+    // The full pass issues them after the fold barrier, while the MMAs run,
+    // so that no warp reaches that barrier late behind its loads.
+    if (SO && has_next) {
       load_theta<KP, TPG>(p, nxt, Q, tg, k0, th);
       if (warp == kDecayWarp) load_decay_raw(p, nxt, Q, lane, dr);
     }
@@ -1255,6 +1257,10 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
     has_state = true;
 
     if constexpr (!SO) {
+      if (has_next) {
+        load_theta<KP, TPG>(p, nxt, Q, tg, k0, th);
+        if (warp == kDecayWarp) load_decay_raw(p, nxt, Q, lane, dr);
+      }
       // ================================================= mask: P = S o Mask
       wait_or_abort(&bar_ds, (uint32_t)(g & 1), &abort_flag, p.status);
       ptx::tc_fence_after_sync();

@@ -49,8 +49,10 @@
 //          barrier -> fp16 scales, angle offsets, sincos, RoPE fold of B and C
 //          into 128-byte-swizzled fp16 UMMA tiles, w X, the fp16 X operand, and
 //          the rescale of the state held in TMEM by exp(Lam_end) and the change
-//          of scale -> barrier -> one thread issues D (accumulated onto the
-//          state), S and Yoff = Ct H_in
+//          of scale -> barrier -> one thread (lane 0 of warp 5) issues D
+//          (accumulated onto the state), S and Yoff = Ct H_in; every thread
+//          then issues its loads of the next chunk's theta (and warp 4 those
+//          of the decay inputs)
 //   mask   S -> P (fp16, scaled; over the Bt tile, which D and S no longer
 //          read) -> barrier -> one thread issues Y = P X
 //   state  the state after D (TMEM) -> its bound -> barrier -> its scaled fp16
@@ -514,6 +516,10 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
   // every R, so it only writes zeros there); in the state-only pass by warp 0
   // at the end of the chunk.
   constexpr int kDecayWarp = SO ? 0 : 4;
+  // The MMAs are issued by lane 0 of warp 5, which (like warp 4) has no share
+  // of the mask phase, rather than by thread 0: the issue takes about a
+  // microsecond per chunk, which warp 5 spends where it would otherwise wait.
+  constexpr int kMmaTid = 160;
   // accumulator mapping: TMEM lane quadrant, 32-column half
   const int quad = warp & 3, half = warp >> 2;
 
@@ -650,8 +656,9 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
   float h_inv_prev = 1.f;   // inverse scale of the state tile read by this chunk's Yoff
   float dsum = 0.f;         // log2 decay over the unit (state-only pass)
   float bmax_bias = 0.f, cmax_bias = 0.f;  // bounds of the head's bias magnitudes
-  // (thread 0) parity of a raw load issued and not yet waited for, and the
-  // barrier and parity of its last MMA commit: what an early exit waits for
+  // (thread 0) parity of a raw load issued and not yet waited for; (the MMA
+  // thread) the barrier and parity of its last commit: what an early exit
+  // waits for
   int raw_pending = 0;
   uint64_t* last_commit = nullptr;
   uint32_t last_parity = 0;
@@ -1199,7 +1206,7 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
     ptx::tc_fence_before_sync();
     __syncthreads();  // ------------------------------------------ fold B
     if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
-    if (tid == 0) {
+    if (tid == kMmaTid) {
       // D = Bt^T (w X) onto the state; S = Ct Bt^T; Yoff = Ct H_in
       // (F32: every product is hi hi + hi lo + lo hi of the split operands)
       ptx::tc_fence_after_sync();
@@ -1337,7 +1344,7 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       ptx::tc_fence_before_sync();
       __syncthreads();  // ------------------------------------------ mask
       if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
-      if (tid == 0) {
+      if (tid == kMmaTid) {
         // Y = P X
         ptx::tc_fence_after_sync();
         const Desc dPh = make_desc(sbase + K::kPh, 16u);
@@ -1527,9 +1534,9 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
     // memory the CTA no longer owns. After a normal exit these phases are
     // complete already.
     if (raw_pending >= 0) ptx::mbar_wait(&bar_raw, (uint32_t)raw_pending, kWaitNs);
-    if (last_commit) ptx::mbar_wait(last_commit, last_parity, kWaitNs);
     if (!SO && R > 1) ptx::tma_store_wait_all<0>();
   }
+  if (tid == kMmaTid && last_commit) ptx::mbar_wait(last_commit, last_parity, kWaitNs);
   ptx::tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) {

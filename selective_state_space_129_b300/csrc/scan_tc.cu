@@ -744,6 +744,11 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
     }
 
     // ================================================= fold, part 1
+    Sched nxt = sch;
+    if (has_next) nxt.next(p);
+    // state-only pass: warp 0's loads of the next chunk's decay inputs (used
+    // at the end of this chunk), a whole fold ahead of their use
+    if (SO && warp == kDecayWarp && has_next) load_decay_raw(p, nxt, Q, lane, dr);
     // every thread waits for this chunk's raw tiles itself
     if (wait_or_abort(&bar_raw, (uint32_t)(g & 1), &abort_flag, p.status) && tid == 0)
       raw_pending = -1;
@@ -869,8 +874,6 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         atomicMax(&s_max[g & 1][2], __float_as_uint(xm));
       }
     }
-    Sched nxt = sch;
-    if (has_next) nxt.next(p);
     // the staging tile of the previous chunk's output (over w X) is free
     if (!SO && R > 1 && tid == 0) ptx::tma_store_wait_read<0>();
     __syncthreads();  // ------------------------------------------ fold A
@@ -1198,10 +1201,6 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
     // the next chunk's theta and decay inputs (loads only; used next chunk).
     // The full pass issues them after the fold barrier, while the MMAs run,
     // so that no warp reaches that barrier late behind its loads.
-    if (SO && has_next) {
-      load_theta<KP, TPG>(p, nxt, Q, tg, k0, th);
-      if (warp == kDecayWarp) load_decay_raw(p, nxt, Q, lane, dr);
-    }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before_sync();
     __syncthreads();  // ------------------------------------------ fold B
@@ -1262,12 +1261,12 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       }
     }
     has_state = true;
+    if (has_next) {
+      load_theta<KP, TPG>(p, nxt, Q, tg, k0, th);
+      if (!SO && warp == kDecayWarp) load_decay_raw(p, nxt, Q, lane, dr);
+    }
 
     if constexpr (!SO) {
-      if (has_next) {
-        load_theta<KP, TPG>(p, nxt, Q, tg, k0, th);
-        if (warp == kDecayWarp) load_decay_raw(p, nxt, Q, lane, dr);
-      }
       // ================================================= mask: P = S o Mask
       wait_or_abort(&bar_ds, (uint32_t)(g & 1), &abort_flag, p.status);
       ptx::tc_fence_after_sync();

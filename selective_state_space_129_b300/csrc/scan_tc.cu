@@ -1432,17 +1432,25 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
             }
           }
         } else {
-          // staging in the global layout of one chunk: [token][p][r]
+          // staging in the global layout of one chunk: [token][p][r]; bf16 as
+          // 128-byte rows of 64 (p, r) elements, 128-byte swizzled like the
+          // store's tensor map (without the swizzle a warp's stores hit one
+          // bank pair eight times over)
           const int t = a / R, r = a % R;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const uint32_t e = (uint32_t)((t * kP + c0 + j) * R + r);
             if constexpr (F32) {
+              const uint32_t e = (uint32_t)((t * kP + c0 + j) * R + r);
               asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + K::kYs + e * 4u), "f"(y[j])
                            : "memory");
             } else {
+              constexpr int kPpr = 64 / R;  // p per 128-byte row
+              const int pp = c0 + j;
+              const uint32_t row = (uint32_t)(t * R + pp / kPpr);
+              const uint32_t inner = (uint32_t)((pp % kPpr) * R + r);
+              const uint32_t off = row * 128u + ((((inner >> 3) ^ row) & 7u) << 4) + (inner & 7u) * 2u;
               __nv_bfloat16 v = __float2bfloat16_rn(y[j]);
-              sts16(sbase + K::kYs + e * 2u, *reinterpret_cast<uint16_t*>(&v));
+              sts16(sbase + K::kYs + off, *reinterpret_cast<uint16_t*>(&v));
             }
           }
           ptx::fence_proxy_async_smem();
@@ -1517,7 +1525,10 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       }
       __syncthreads();  // ------------------------------------------ end of chunk
       if (!SO && R > 1 && tid == 0) {
-        ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, h, c * Q, b);
+        if constexpr (F32)
+          ptx::tma_store_4d(&tm_y, smem + K::kYs, 0, h, c * Q, b);
+        else
+          ptx::tma_store_5d(&tm_y, smem + K::kYs, 0, 0, h, c * Q, b);
         ptx::tma_store_commit();
       }
       if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
@@ -1584,6 +1595,19 @@ bool make_act_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
   return encode(m, a.f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                 ptr, dims, strides, box,
                 (a.R == 1 && !a.f32) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// y [b, L, H, P, R] for the TMA store of R > 1 (bf16): a 5-D tensor {64,
+// P*R/64, H, L, b} whose box is one head's chunk as 128-byte rows of 64
+// (p, r) elements, 128-byte swizzled; fp32 keeps the 4-D map above.
+bool make_out_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
+  if (a.f32) return make_act_map(m, ptr, a);
+  const uint64_t PR = (uint64_t)a.P * a.R;
+  cuuint64_t dims[5] = {64, PR / 64, (cuuint64_t)a.H, (cuuint64_t)a.L, (cuuint64_t)a.batch};
+  cuuint64_t strides[4] = {128, PR * 2, PR * 2 * a.H, PR * 2 * a.H * a.L};
+  cuuint32_t box[5] = {64, (cuuint32_t)(PR / 64), 1, (cuuint32_t)a.Q, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, ptr, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // B / C [b, L, G, N, R] as a 5-D tensor {d0, N*R/d0, G, L, b} with d0 <= 256.
@@ -1733,7 +1757,8 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   // B, C, x and (R > 1: the output is stored by TMA) y
   CUtensorMap maps[4];
   if (!make_bc_map(&maps[0], a.B, a) || !make_bc_map(&maps[1], a.C, a) ||
-      !make_act_map(&maps[2], a.x, a) || !make_act_map(&maps[3], R > 1 ? a.out : a.x, a))
+      !make_act_map(&maps[2], a.x, a) ||
+      !(R > 1 ? make_out_map(&maps[3], a.out, a) : make_act_map(&maps[3], a.x, a)))
     return cudaErrorInvalidValue;
   TcParams p;
   p.dt = a.dt; p.A = a.A; p.lam = a.lam; p.theta = a.theta;

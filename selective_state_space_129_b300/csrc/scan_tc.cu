@@ -516,6 +516,10 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
   // every R, so it only writes zeros there); in the state-only pass by warp 0
   // at the end of the chunk.
   constexpr int kDecayWarp = SO ? 0 : 4;
+  // R = 4 (bf16): the raw B, C and x tiles arrive 128-byte swizzled (a thread
+  // reads 32 bytes per token row, and unswizzled rows put two lanes of every
+  // quarter-warp on the same banks)
+  constexpr bool kSwRaw = R == 4 && !F32;
   // The MMAs are issued by lane 0 of warp 5, which (like warp 4) has no share
   // of the mask phase, rather than by thread 0: the issue takes about a
   // microsecond per chunk, which warp 5 spends where it would otherwise wait.
@@ -554,7 +558,10 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
     ptx::mbar_arrive_expect_tx(&bar_raw, SO ? K::kTxBytesSO : K::kTxBytes);
     ptx::tma_load_5d(smem + K::kRawB, &tm_B, &bar_raw, 0, 0, gi, t0, u.b);
     if (!SO) ptx::tma_load_5d(smem + K::kRawC, &tm_C, &bar_raw, 0, 0, gi, t0, u.b);
-    ptx::tma_load_4d(smem + K::kRawX, &tm_x, &bar_raw, 0, u.h, t0, u.b);
+    if constexpr (kSwRaw)
+      ptx::tma_load_5d(smem + K::kRawX, &tm_x, &bar_raw, 0, 0, u.h, t0, u.b);
+    else
+      ptx::tma_load_4d(smem + K::kRawX, &tm_x, &bar_raw, 0, u.h, t0, u.b);
   };
 
   // state element (n, cb + j) of this thread's 16-column block `blk` is hv[16 blk + j]
@@ -782,10 +789,17 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       } else {
 #pragma unroll
         for (int q = 0; q < K::BW / 4; ++q) {
-          const uint4 vb = lds128(sbase + K::kRawB + ob + 16u * q);
+          uint32_t o = ob + 16u * q;
+          if constexpr (kSwRaw) {
+            // token t's NS / 16 rows of 128 bytes; this thread's 32 bytes are
+            // chunks 2 (kk2 & 3) + q of row t NS / 16 + kk2 / 4
+            const uint32_t row = (uint32_t)(t * (NS / 16) + kk2 / 4);
+            o = row * 128u + ((((uint32_t)(2 * (kk2 & 3) + q)) ^ (row & 7u)) << 4);
+          }
+          const uint4 vb = lds128(sbase + K::kRawB + o);
           bw[i][4 * q] = vb.x; bw[i][4 * q + 1] = vb.y; bw[i][4 * q + 2] = vb.z; bw[i][4 * q + 3] = vb.w;
           if constexpr (!SO) {
-            const uint4 vc = lds128(sbase + K::kRawC + ob + 16u * q);
+            const uint4 vc = lds128(sbase + K::kRawC + o);
             cw[i][4 * q] = vc.x; cw[i][4 * q + 1] = vc.y; cw[i][4 * q + 2] = vc.z; cw[i][4 * q + 3] = vc.w;
           }
         }
@@ -830,7 +844,14 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       }
 #pragma unroll
       for (int q = 0; q < K::XW / 4; ++q) {
-        const uint4 v = lds128(src + 16u * q);
+        uint32_t a_ = src + 16u * q;
+        if constexpr (kSwRaw) {
+          // token sx's four rows of 128 bytes (64 (p, r) elements each)
+          const int sx = it / (kP / 4), pb = it % (kP / 4);
+          const uint32_t row = (uint32_t)(sx * 4 + pb / 4);
+          a_ = sbase + K::kRawX + row * 128u + ((((uint32_t)(2 * (pb & 3) + q)) ^ (row & 7u)) << 4);
+        }
+        const uint4 v = lds128(a_);
         xw[j][4 * q] = v.x; xw[j][4 * q + 1] = v.y; xw[j][4 * q + 2] = v.z; xw[j][4 * q + 3] = v.w;
       }
 #pragma unroll
@@ -1597,9 +1618,10 @@ bool make_act_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
                 (a.R == 1 && !a.f32) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// y [b, L, H, P, R] for the TMA store of R > 1 (bf16): a 5-D tensor {64,
-// P*R/64, H, L, b} whose box is one head's chunk as 128-byte rows of 64
-// (p, r) elements, 128-byte swizzled; fp32 keeps the 4-D map above.
+// y (the TMA store of R > 1) or x (the load of R = 4) [b, L, H, P, R], bf16:
+// a 5-D tensor {64, P*R/64, H, L, b} whose box is one head's chunk as
+// 128-byte rows of 64 (p, r) elements, 128-byte swizzled; fp32 keeps the 4-D
+// map above.
 bool make_out_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
   if (a.f32) return make_act_map(m, ptr, a);
   const uint64_t PR = (uint64_t)a.P * a.R;
@@ -1613,6 +1635,14 @@ bool make_out_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
 // B / C [b, L, G, N, R] as a 5-D tensor {d0, N*R/d0, G, L, b} with d0 <= 256.
 bool make_bc_map(CUtensorMap* m, const void* ptr, const ScanArgs& a) {
   const uint64_t NR = (uint64_t)a.N * a.R, es = a.f32 ? 4 : 2;
+  if (a.R == 4 && !a.f32) {
+    // R = 4, bf16: 128-byte rows {64, N R / 64, G, L, b}, 128-byte swizzled
+    cuuint64_t dims[5] = {64, NR / 64, (cuuint64_t)a.G, (cuuint64_t)a.L, (cuuint64_t)a.batch};
+    cuuint64_t strides[4] = {128, NR * 2, NR * 2 * a.G, NR * 2 * a.G * a.L};
+    cuuint32_t box[5] = {64, (cuuint32_t)(NR / 64), 1, (cuuint32_t)a.Q, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, ptr, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   const uint64_t d0 = NR < 256 ? NR : 256, d1 = NR / d0;
   cuuint64_t dims[5] = {d0, d1, (cuuint64_t)a.G, (cuuint64_t)a.L, (cuuint64_t)a.batch};
   cuuint64_t strides[4] = {d0 * es, NR * es, NR * es * a.G, NR * es * a.G * a.L};
@@ -1757,7 +1787,7 @@ cudaError_t launch_rn(const ScanArgs& a, unsigned int* status, cudaStream_t s) {
   // B, C, x and (R > 1: the output is stored by TMA) y
   CUtensorMap maps[4];
   if (!make_bc_map(&maps[0], a.B, a) || !make_bc_map(&maps[1], a.C, a) ||
-      !make_act_map(&maps[2], a.x, a) ||
+      !(R == 4 && !F32 ? make_out_map(&maps[2], a.x, a) : make_act_map(&maps[2], a.x, a)) ||
       !(R > 1 ? make_out_map(&maps[3], a.out, a) : make_act_map(&maps[3], a.x, a)))
     return cudaErrorInvalidValue;
   TcParams p;

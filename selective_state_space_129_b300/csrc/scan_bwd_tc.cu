@@ -128,20 +128,30 @@ __device__ __forceinline__ void ldm4(uint32_t addr, uint32_t& r0, uint32_t& r1, 
                : "r"(addr));
 }
 
+// Row order of the per-chunk kernel's tiles that serve as B operands: within
+// each block of 8 rows, row k is stored at 2 (k % 4) + k / 4 (so rows 0..7 at
+// 0, 2, 4, 6, 1, 3, 5, 7). A B fragment's two k rows, tq and tq + 4, then sit
+// side by side at 2 tq, 2 tq + 1, and its word loads from a [k][n] tile (word
+// stride 4 mod 32) fall on 32 different banks; ldmatrix takes any row order.
+__device__ __forceinline__ int prow(int k) { return (k & ~7) | ((k & 3) << 1) | ((k >> 2) & 1); }
+
 // acc[nt] += A (rows m0 .. m0+15 of a row-major [m][k] fp32 tile, word stride
 // SA, at shared address a_tile) x B (K x 8 NT, columns n0 + 8 nt ..). The A
 // fragments come by ldmatrix: an 8 x 4 block of 32-bit words is the b16 8 x 8
 // matrix whose distribution (thread t: row t / 4, word t % 4) is the TF32
 // fragment's. BL: B is stored [n][k] (word stride SBS, at b_tile) and comes by
 // ldmatrix, two n-tiles at a time; else B is stored [k][n] (Bp) and each
-// fragment word is loaded alone.
-template <int NT, int K, int SA, int SBS, bool BL>
+// fragment word is loaded alone. B's rows are in prow order; A's rows too
+// when PA.
+template <int NT, int K, int SA, int SBS, bool BL, bool PA>
 __device__ __forceinline__ void wgemm_l(float (&acc)[NT][4], uint32_t a_tile, int m0,
                                         uint32_t b_tile, const float* Bp, int n0, int lane) {
   const int g = lane >> 2, tq = lane & 3, mi = lane >> 3, rr = lane & 7;
-  const uint32_t a_lane = a_tile + 4u * (uint32_t)((m0 + rr + 8 * (mi & 1)) * SA + 4 * (mi >> 1));
-  const uint32_t b_lane = b_tile + 4u * (uint32_t)((n0 + rr + 8 * (mi >> 1)) * SBS + 4 * (mi & 1));
-  const float* bp = Bp + tq * SBS + n0 + g;
+  const int ra = m0 + rr + 8 * (mi & 1);
+  const uint32_t a_lane = a_tile + 4u * (uint32_t)((PA ? prow(ra) : ra) * SA + 4 * (mi >> 1));
+  const uint32_t b_lane = b_tile + 4u * (uint32_t)(prow(n0 + rr + 8 * (mi >> 1)) * SBS + 4 * (mi & 1));
+  // k rows k0 + tq and k0 + tq + 4 are stored at k0 + 2 tq and k0 + 2 tq + 1
+  const float* bp = Bp + 2 * tq * SBS + n0 + g;
 #pragma unroll
   for (int k0 = 0; k0 < K; k0 += 8) {
     uint32_t a0, a1, a2, a3;
@@ -159,7 +169,7 @@ __device__ __forceinline__ void wgemm_l(float (&acc)[NT][4], uint32_t a_tile, in
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const uint32_t b0 = __float_as_uint(bp[k0 * SBS + 8 * nt]);
-        const uint32_t b1 = __float_as_uint(bp[(k0 + 4) * SBS + 8 * nt]);
+        const uint32_t b1 = __float_as_uint(bp[(k0 + 1) * SBS + 8 * nt]);
         mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
       }
     }
@@ -180,7 +190,7 @@ __device__ __forceinline__ float bf_word(uint32_t w, int half) {
   return __uint_as_float(half ? (w & 0xffff0000u) : (w << 16));
 }
 
-template <int R, int NS, int SB>
+template <int R, int NS, int SB, bool PERM = false>
 __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t h, int64_t gi,
                                            int c0, int nv, float A_h, float* Bt, float* Ct,
                                            float2* Rt, TokTab& tk, float* s_gt, float* phi_end) {
@@ -305,7 +315,7 @@ __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t 
       const float b1 = live ? bf_word(bw[j][(R + r) >> 1], (R + r) & 1) + bb[R + r] : 0.f;
       const float q0 = live ? bf_word(cw[j][r >> 1], r & 1) + cb[r] : 0.f;
       const float q1 = live ? bf_word(cw[j][(R + r) >> 1], (R + r) & 1) + cb[R + r] : 0.f;
-      const int row = t * R + r;
+      const int row = PERM ? prow(t * R + r) : t * R + r;
       *reinterpret_cast<float2*>(Bt + row * SB + 2 * kk) =
           make_float2(tf32r(cs * b0 + sn * b1), tf32r(cs * b1 - sn * b0));
       *reinterpret_cast<float2*>(Ct + row * SB + 2 * kk) =
@@ -371,7 +381,7 @@ __device__ __forceinline__ void act_st8(float* T, uint4 u) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int p = (rem + i) / R, r = (rem + i) % R;
-    T[(t * R + r) * ST + p] = bf_word(w[i >> 1], i & 1);
+    T[prow(t * R + r) * ST + p] = bf_word(w[i >> 1], i & 1);
   }
 }
 
@@ -596,13 +606,13 @@ __global__ void __launch_bounds__(kBT, 1)
   for (int j = 0; j < NH; ++j)
     hr[j] = *reinterpret_cast<const float4*>(wsA + slot + 4 * (tid + j * kBT));
   for (int i = tid; i < 8 * kRows; i += kBT) colVi[i] = 0.f;
-  chunk_prep<R, NS, SB>(a, b, h, gi, c0, nv, A_h, Bt, Ct, Rt, tk, s_gt, nullptr);
+  chunk_prep<R, NS, SB, true>(a, b, h, gi, c0, nv, A_h, Bt, Ct, Rt, tk, s_gt, nullptr);
   act_st8<R, kSX>(Xs, xr);
   act_st8<R, kSX>(Ys, yr);
 #pragma unroll
   for (int j = 0; j < NH; ++j) {
     const int e = 4 * (tid + j * kBT), n = e / kPd, p = e - n * kPd;
-    *reinterpret_cast<float4*>(St + n * kSX + p) =
+    *reinterpret_cast<float4*>(St + prow(n) * kSX + p) =
         make_float4(tf32r(hr[j].x), tf32r(hr[j].y), tf32r(hr[j].z), tf32r(hr[j].w));
   }
   __syncthreads();
@@ -613,8 +623,8 @@ __global__ void __launch_bounds__(kBT, 1)
     float aS[2][4], aP[2][4];
     zero_acc(aS);
     zero_acc(aP);
-    wgemm_l<2, NS, SB, SB, true>(aS, aCt, m0, aBt, nullptr, n0, lane);
-    wgemm_l<2, kPd, kSX, kSX, true>(aP, aYs, m0, aXs, nullptr, n0, lane);
+    wgemm_l<2, NS, SB, SB, true, true>(aS, aCt, m0, aBt, nullptr, n0, lane);
+    wgemm_l<2, kPd, kSX, kSX, true, true>(aP, aYs, m0, aXs, nullptr, n0, lane);
     float rz[2] = {0.f, 0.f};
     float cvi[2][2], cvs[2][2], cz[2][2];
 #pragma unroll
@@ -706,7 +716,7 @@ __global__ void __launch_bounds__(kBT, 1)
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
         const int e = 4 * (tid + j * kBT), n = e / kPd, p = e - n * kPd;
-        *reinterpret_cast<float4*>(St + n * kSX + p) =
+        *reinterpret_cast<float4*>(St + prow(n) * kSX + p) =
             make_float4(tf32r(gr[j].x), tf32r(gr[j].y), tf32r(gr[j].z), tf32r(gr[j].w));
       }
       __syncthreads();
@@ -716,7 +726,7 @@ __global__ void __launch_bounds__(kBT, 1)
     float acc[NT3][4];
     zero_acc(acc);
     // E = (pass 0) dY H_in^T, (pass 1) X dG^T
-    wgemm_l<NT3, kPd, kSX, kSX, true>(acc, pass ? aXs : aYs, m0, aSt, nullptr, n0, lane);
+    wgemm_l<NT3, kPd, kSX, kSX, true, true>(acc, pass ? aXs : aYs, m0, aSt, nullptr, n0, lane);
     // row dots with the own tile: d e^Lam_t (pass 0), dw_s (pass 1)
     {
       float rd[2] = {0.f, 0.f};
@@ -725,7 +735,7 @@ __global__ void __launch_bounds__(kBT, 1)
         const int col = n0 + 8 * nt + 2 * tq;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const float2 o = *reinterpret_cast<const float2*>(Own + (m0 + g + 8 * q) * SB + col);
+          const float2 o = *reinterpret_cast<const float2*>(Own + prow(m0 + g + 8 * q) * SB + col);
           rd[q] = fmaf(o.x, acc[nt][2 * q], fmaf(o.y, acc[nt][2 * q + 1], rd[q]));
         }
       }
@@ -748,7 +758,7 @@ __global__ void __launch_bounds__(kBT, 1)
       }
     }
     // + dS Oth (pass 0) or dS^T Oth (pass 1)
-    wgemm_l<NT3, kRows, kSX, SB, false>(acc, pass ? adST : adS, m0, 0u, Oth, n0, lane);
+    wgemm_l<NT3, kRows, kSX, SB, false, false>(acc, pass ? adST : adS, m0, 0u, Oth, n0, lane);
     if (pass == 0) {
 #pragma unroll
       for (int j = 0; j < NH; ++j)
@@ -772,7 +782,7 @@ __global__ void __launch_bounds__(kBT, 1)
       for (int q = 0; q < 2; ++q) {
         const int i = m0 + g + 8 * q, t = i / R;
         const float d0 = acc[nt][2 * q], d1 = acc[nt][2 * q + 1];
-        const float2 o = *reinterpret_cast<const float2*>(Own + i * SB + col);
+        const float2 o = *reinterpret_cast<const float2*>(Own + prow(i) * SB + col);
         dphr[q][nt] += d0 * o.y - d1 * o.x;
         const float2 rt = Rt[t * K2 + k];
         const float r0 = rt.x * d0 - rt.y * d1, r1 = rt.y * d0 + rt.x * d1;
@@ -821,8 +831,8 @@ __global__ void __launch_bounds__(kBT, 1)
     float a1[2][4], a2[2][4];
     zero_acc(a1);
     zero_acc(a2);
-    wgemm_l<2, kRows, kSX, kSX, false>(a1, aPT, xm0, 0u, Ys, xn0, lane);
-    wgemm_l<2, NS, SB, kSX, false>(a2, aBt, xm0, 0u, St, xn0, lane);
+    wgemm_l<2, kRows, kSX, kSX, false, false>(a1, aPT, xm0, 0u, Ys, xn0, lane);
+    wgemm_l<2, NS, SB, kSX, false, true>(a2, aBt, xm0, 0u, St, xn0, lane);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int j = xm0 + g + 8 * q, s = j / R, r = j % R;

@@ -67,6 +67,10 @@ struct BCfg {
   static constexpr int Q = kRows / R;
   static constexpr int K2 = NS / 2;
   static constexpr int SB = NS + 4;   // word stride of the [64][N] tiles
+  // row pitch (in (cos, sin) pairs) of the rotation table: 8 words mod 32, so
+  // that the rotation backward's reads of 4 tokens x 4 pairs per half-warp
+  // fall on 32 different banks
+  static constexpr int RP = K2 + 4;
   static constexpr int TG = kBT / K2;  // token groups of the fold
   static constexpr int TPG = Q / TG;   // tokens per fold thread
   static_assert(TPG >= 1 && Q % TG == 0, "token groups must divide the chunk");
@@ -306,7 +310,7 @@ __device__ __forceinline__ void chunk_prep(const BwdArgs& a, int64_t b, int64_t 
     if (phi_end && t == Q - 1) phi_end[kk] = phi;
     float sn, cs;
     __sincosf(wrap_angle(phi), &sn, &cs);
-    if (Rt) Rt[t * K2 + kk] = make_float2(cs, sn);
+    if (Rt) Rt[t * K::RP + kk] = make_float2(cs, sn);
     const bool live = t < nv;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -378,10 +382,19 @@ __device__ __forceinline__ void act_st8(float* T, uint4 u) {
   constexpr int PR = kPd * R;
   const int e = threadIdx.x * 8, t = e / PR, rem = e - t * PR;
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  if constexpr (R == 1) {
+    // 8 consecutive elements of one row: two 16-byte stores (a quarter-warp
+    // fills 128 contiguous bytes)
+    static_assert(ST % 4 == 0, "16-byte aligned rows");
+    float4* d = reinterpret_cast<float4*>(T + prow(t) * ST + rem);
+    d[0] = make_float4(bf_word(w[0], 0), bf_word(w[0], 1), bf_word(w[1], 0), bf_word(w[1], 1));
+    d[1] = make_float4(bf_word(w[2], 0), bf_word(w[2], 1), bf_word(w[3], 0), bf_word(w[3], 1));
+  } else {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int p = (rem + i) / R, r = (rem + i) % R;
-    T[prow(t * R + r) * ST + p] = bf_word(w[i >> 1], i & 1);
+    for (int i = 0; i < 8; ++i) {
+      const int p = (rem + i) / R, r = (rem + i) % R;
+      T[prow(t * R + r) * ST + p] = bf_word(w[i >> 1], i & 1);
+    }
   }
 }
 
@@ -549,7 +562,7 @@ __global__ void __launch_bounds__(256)
 template <int R, int NS>
 constexpr size_t chunk_smem() {
   using K = BCfg<R, NS>;
-  return sizeof(float) * (2 * kRows * K::SB + 5 * kRows * kSX + NS * kSX + 2 * K::Q * K::K2 +
+  return sizeof(float) * (2 * kRows * K::SB + 5 * kRows * kSX + NS * kSX + 2 * K::Q * K::RP +
                           K::TG * K::K2 + 8 * kRows) +
          sizeof(TokTab);
 }
@@ -570,9 +583,9 @@ __global__ void __launch_bounds__(kBT, 1)
   float* dSs = PT + kRows * kSX;  // dS
   float* dST = dSs + kRows * kSX; // dS transposed
   float* St = dST + kRows * kSX;  // [N][P]: H_in, then dG
-  float2* Rt = reinterpret_cast<float2*>(St + NS * kSX);  // [Q][K2] (cos, sin) of the angles
+  float2* Rt = reinterpret_cast<float2*>(St + NS * kSX);  // [Q][RP] (cos, sin) of the angles
   float* dPh = Xs;  // [Q][K2] angle gradients, once X is no longer read
-  float* s_gt = reinterpret_cast<float*>(Rt + Q * K2);
+  float* s_gt = reinterpret_cast<float*>(Rt + Q * K::RP);
   float* colVi = s_gt + K::TG * K2;  // per token: column sums and row sums (64 each)
   float* colVs = colVi + kRows;
   float* colZ = colVs + kRows;
@@ -784,7 +797,7 @@ __global__ void __launch_bounds__(kBT, 1)
         const float d0 = acc[nt][2 * q], d1 = acc[nt][2 * q + 1];
         const float2 o = *reinterpret_cast<const float2*>(Own + prow(i) * SB + col);
         dphr[q][nt] += d0 * o.y - d1 * o.x;
-        const float2 rt = Rt[t * K2 + k];
+        const float2 rt = Rt[t * K::RP + k];
         const float r0 = rt.x * d0 - rt.y * d1, r1 = rt.y * d0 + rt.x * d1;
         if (t < nv) {
           float* dst = grow[q] + col * R;
@@ -967,6 +980,8 @@ cudaError_t launch_rn(const BwdArgs& a, float* ws, int nC, cudaStream_t s) {
   float* dotgh = dphiB + (size_t)nbh * nC * K2;
   cudaError_t e = cudaMemsetAsync(dphiB, 0, sizeof(float) * (size_t)nbh * nC * (K2 + 1), s);
   if (e != cudaSuccess) return e;
+  static_assert(chunk_smem<R, NS>() <= 227 * 1024 && parts_smem<R, NS>() <= 227 * 1024,
+                "the per-chunk tiles fit one CTA's shared memory");
   const size_t sp = parts_smem<R, NS>(), sc = chunk_smem<R, NS>();
   e = cudaFuncSetAttribute(bwd_parts_kernel<R, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sp);

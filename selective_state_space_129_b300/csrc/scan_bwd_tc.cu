@@ -584,7 +584,11 @@ __global__ void __launch_bounds__(kBT, 1)
   float* dST = dSs + kRows * kSX; // dS transposed
   float* St = dST + kRows * kSX;  // [N][P]: H_in, then dG
   float2* Rt = reinterpret_cast<float2*>(St + NS * kSX);  // [Q][RP] (cos, sin) of the angles
-  float* dPh = Xs;  // [Q][K2] angle gradients, once X is no longer read
+  // [Q][K2] angle gradients (row pitch K2 + 4: the stores of a warp's 8 rows
+  // x 4 pairs fall on different banks), once X is no longer read
+  constexpr int kDP = K2 + 4;
+  static_assert(Q * kDP <= kRows * kSX, "the angle gradients fit the X tile");
+  float* dPh = Xs;
   float* s_gt = reinterpret_cast<float*>(Rt + Q * K::RP);
   float* colVi = s_gt + K::TG * K2;  // per token: column sums and row sums (64 each)
   float* colVs = colVi + kRows;
@@ -871,7 +875,7 @@ __global__ void __launch_bounds__(kBT, 1)
       if (R >= 2) v += __shfl_xor_sync(0xffffffffu, v, 4);
       if (R >= 4) v += __shfl_xor_sync(0xffffffffu, v, 8);
       const int i = m0 + g + 8 * q, k = (n0 + 8 * nt + 2 * tq) >> 1;
-      if (g % R == 0) dPh[(i / R) * K2 + k] = v;
+      if (g % R == 0) dPh[(i / R) * kDP + k] = v;
     }
   __syncthreads();
 
@@ -885,7 +889,7 @@ __global__ void __launch_bounds__(kBT, 1)
 #pragma unroll
     for (int j = TPG - 1; j >= 0; --j) {
       const int t = tg * TPG + j;
-      acc += dPh[t * K2 + kk];
+      acc += dPh[t * kDP + kk];
       run[j] = acc;
     }
     s_gt[tg * K2 + kk] = acc;

@@ -470,6 +470,33 @@ __device__ __forceinline__ float bc_inv_rms(const uint32_t (&w)[BW], int r) {
   return rsqrtf(fmaf(ss, 1.f / NS, 1e-6f));
 }
 
+// R = 1, N = 128 (a whole warp holds one token row of B and of C): the
+// inverse RMS of V = TPG (B only) or 2 TPG (B, then C) rows at once. A
+// reduce-scatter over the lane masks 16, 8, ... leaves each lane the full sum
+// of one row (16 shuffles for 16 rows instead of 80), whose inverse RMS is
+// then gathered back from the lane holding it.
+template <int V>
+__device__ __forceinline__ void inv_rms_rows(float (&v)[V], int lane) {
+  static_assert(V >= 2 && V <= 16 && (V & (V - 1)) == 0, "a power of two up to 16 rows");
+  int m = 16;
+#pragma unroll
+  for (int n = V; n > 1; n >>= 1, m >>= 1) {
+    const bool up = (lane & m) != 0;  // keep the upper half of the rows
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = up ? v[i] : v[i + n / 2];
+      const float keep = up ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+#pragma unroll
+  for (; m >= 1; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+  // lane 32 i / V now holds row i's sum over the warp
+  const float r = rsqrtf(fmaf(v[0], 1.f / 128.f, 1e-6f));
+#pragma unroll
+  for (int i = 0; i < V; ++i) v[i] = __shfl_sync(0xffffffffu, r, i * (32 / V));
+}
+
 // SO: the state-only pass of a segmented scan (no C, no outputs).
 // NORM: B and C arrive un-normalised; BCNorm them here (each token's and
 // rank's vector over N divided by its root mean square), before the bias.
@@ -1098,6 +1125,28 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       const float2 bs1 = mul2(sB2, make_float2(bq[0].y, bq[0].w));
       const float2 cs0 = mul2(sC2, make_float2(cq[0].x, cq[0].z));
       const float2 cs1 = mul2(sC2, make_float2(cq[0].y, cq[0].w));
+      // (NORM, N = 128) the tokens' inverse RMS of B, then of C, all at once
+      constexpr bool kRowsAtOnce = NORM && NS == 128;
+      constexpr int kNR = kRowsAtOnce ? (SO ? TPG : 2 * TPG) : 2;
+      float irs[kNR];
+      if constexpr (kRowsAtOnce) {
+#pragma unroll
+        for (int i = 0; i < TPG; ++i) {
+          float sb = 0.f, sc2 = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float vb = bf_at(bw[i], e);
+            sb = fmaf(vb, vb, sb);
+            if constexpr (!SO) {
+              const float vc = bf_at(cw[i], e);
+              sc2 = fmaf(vc, vc, sc2);
+            }
+          }
+          irs[i] = sb;
+          if constexpr (!SO) irs[TPG + i] = sc2;
+        }
+        inv_rms_rows<kNR>(irs, lane);
+      }
 #pragma unroll
       for (int i = 0; i < TPG; ++i) {
         float2 sn, cs;
@@ -1107,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         // .x holds pair k0 (rows 4kk2, 4kk2 + 1), .y pair k0 + 1
         float2 sBi = sB2;
         if constexpr (NORM) {
-          const float v = sigB * bc_inv_rms<R, NS, K::BW>(bw[i], 0);
+          const float v = sigB * (kRowsAtOnce ? irs[i] : bc_inv_rms<R, NS, K::BW>(bw[i], 0));
           sBi = make_float2(v, v);
         }
         const float2 b0 = fma2(sBi, make_float2(act_at<F32>(bw[i], 0), act_at<F32>(bw[i], 2)), bs0);
@@ -1124,7 +1173,8 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         if constexpr (!SO) {
           float2 sCi = sC2;
           if constexpr (NORM) {
-            const float v = sigC * bc_inv_rms<R, NS, K::BW>(cw[i], 0);
+            const float v =
+                sigC * (kRowsAtOnce ? irs[(TPG + i) % kNR] : bc_inv_rms<R, NS, K::BW>(cw[i], 0));
             sCi = make_float2(v, v);
           }
           const float2 c0 = fma2(sCi, make_float2(act_at<F32>(cw[i], 0), act_at<F32>(cw[i], 2)), cs0);

@@ -1198,6 +1198,28 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         __sincosf(ph[i].y, &snv[i].y, &csv[i].y);
       }
       const int64_t ob = ((int64_t)h * NS + 4 * kk2) * R;
+      // (NORM, N = 128) the inverse RMS of every (token, rank) row of B, then
+      // of C, all at once: row (i, r) of pass q is entry (q TPG + i) R + r
+      constexpr bool kRowsAtOnce = NORM && NS == 128;
+      constexpr int kNR = kRowsAtOnce ? (SO ? 1 : 2) * TPG * R : 2;
+      float irs[kNR];
+      if constexpr (kRowsAtOnce) {
+#pragma unroll
+        for (int q = 0; q < (SO ? 1 : 2); ++q)
+#pragma unroll
+          for (int i = 0; i < TPG; ++i)
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              float ss = 0.f;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float v = bf_at(q == 0 ? bw[i] : cw[i], e * R + r);
+                ss = fmaf(v, v, ss);
+              }
+              irs[(q * TPG + i) * R + r] = ss;
+            }
+        inv_rms_rows<kNR>(irs, lane);
+      }
 #pragma unroll
       for (int pass = 0; pass < (SO ? 1 : 2); ++pass) {
         const float* bias = pass == 0 ? p.B_bias : p.C_bias;
@@ -1229,7 +1251,8 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
             const float2 v1 = make_float2(act_at<F32>(raw[i], 1 * R + r), act_at<F32>(raw[i], 3 * R + r));
             float2 b0, b1;
             if constexpr (NORM) {
-              const float rs = bc_inv_rms<R, NS, K::BW>(raw[i], r);
+              const float rs = kRowsAtOnce ? irs[((pass * TPG + i) * R + r) % kNR]
+                                           : bc_inv_rms<R, NS, K::BW>(raw[i], r);
               b0 = fma2(make_float2(rs, rs), v0, bb0);
               b1 = fma2(make_float2(rs, rs), v1, bb1);
             } else {

@@ -90,12 +90,14 @@ def test_bc_norm_prefill_1p5b_sampled(orc, name):
         assert_bf16(fs[b:b + 1, h:h + 1], fs_ref, "state[b=%d,h=%d]" % (b, h))
 
 
-def test_bc_norm_segmented_prefill(orc):
+@pytest.mark.parametrize("L,R", [(3000, 1), (1000, 4)], ids=["R1", "R4"])
+def test_bc_norm_segmented_prefill(orc, L, R):
     """Few sequences, so the call runs segmented (state-only pass, combine,
-    full pass), each pass normalising B (and C) itself."""
-    shape = m3synth.ScanShape(1, 3000, 2, 1, 64, 128, R=1, chunk=64, bf16=True, rms_bc=True)
-    dims = m3.make_dims(1, 3000, 2, 1, 64, 128, m3.M3_BF16)
-    assert m3.m3_scan_workspace_bytes(dims, 1, 64) > 0, "expected a segmented launch"
+    full pass), each pass normalising B (and C) itself; SISO and MIMO R = 4."""
+    Q = 64 // R
+    shape = m3synth.ScanShape(1, L, 2, 1, 64, 128, R=R, chunk=Q, bf16=True, rms_bc=True)
+    dims = m3.make_dims(1, L, 2, 1, 64, 128, m3.M3_BF16)
+    assert m3.m3_scan_workspace_bytes(dims, R, Q) > 0, "expected a segmented launch"
     inp = _raw_bc(m3synth.scan_inputs(shape, seed=77), seed=78)
     y, fs = _gpu_bc(inp, shape)
     y_ref, fs_ref = _oracle_bc(orc, inp)

@@ -212,8 +212,9 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation (kind::f16).
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit inputs (fp16 or bf16, as the
+// instruction descriptor says), fp32 accumulation (kind::f16).
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -230,25 +231,14 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
-// a_mn / b_mn select MN-major (transposed) operand layouts.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4)                        // D format: f32
-         | (1u << 7)                      // A format: bf16
-         | (1u << 10)                     // B format: bf16
+// Instruction descriptor for kind::f16 with fp16 A/B and fp32 D; a_mn / b_mn
+// select MN-major (transposed) operand layouts.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                        // D format: f32 (A, B format 0: fp16)
          | ((a_mn ? 1u : 0u) << 15)       // A major-ness
          | ((b_mn ? 1u : 0u) << 16)       // B major-ness
          | ((uint32_t)(N >> 3) << 17)     // N / 8
          | ((uint32_t)(M >> 4) << 24);    // M / 16
-}
-
-// Instruction descriptor for kind::f16 with fp16 A/B and fp32 D.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4)                        // D format: f32
-         | ((a_mn ? 1u : 0u) << 15)
-         | ((b_mn ? 1u : 0u) << 16)
-         | ((uint32_t)(N >> 3) << 17)
-         | ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle. Addresses and offsets in

@@ -1306,26 +1306,26 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
       const Desc dBm = make_desc(opBt, 64u * 128u), dXw = make_desc(sbase + K::kXw, 64u * 128u);
 #pragma unroll
       for (int kk = 0; kk < kQR / 16; ++kk) {
-        ptx::mma_bf16_ss(tmem + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD,
+        ptx::mma_f16_ss(tmem + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD,
                          (has_state || kk > 0) ? 1u : 0u);
         if constexpr (F32) {
           const Desc dBml = make_desc(opBt + K::kBtLo, 64u * 128u);
           const Desc dXwl = make_desc(sbase + K::kXw + K::kXLo, 64u * 128u);
-          ptx::mma_bf16_ss(tmem + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXwl, koff_mn(kk)), kIdD, 1u);
-          ptx::mma_bf16_ss(tmem + kColD, desc_at(dBml, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD, 1u);
+          ptx::mma_f16_ss(tmem + kColD, desc_at(dBm, koff_mn(kk)), desc_at(dXwl, koff_mn(kk)), kIdD, 1u);
+          ptx::mma_f16_ss(tmem + kColD, desc_at(dBml, koff_mn(kk)), desc_at(dXw, koff_mn(kk)), kIdD, 1u);
         }
       }
       if constexpr (!SO) {
         const Desc dBk = make_desc(opBt, 16u), dCk = make_desc(opCt, 16u);
 #pragma unroll
         for (int kk = 0; kk < NS / 16; ++kk) {
-          ptx::mma_bf16_ss(tmem + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
+          ptx::mma_f16_ss(tmem + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
                            kIdS, kk > 0);
           if constexpr (F32) {
             const Desc dBkl = make_desc(opBt + K::kBtLo, 16u), dCkl = make_desc(opCt + K::kBtLo, 16u);
-            ptx::mma_bf16_ss(tmem + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBkl, koff_k(kk, 64)),
+            ptx::mma_f16_ss(tmem + kColS, desc_at(dCk, koff_k(kk, 64)), desc_at(dBkl, koff_k(kk, 64)),
                              kIdS, 1u);
-            ptx::mma_bf16_ss(tmem + kColS, desc_at(dCkl, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
+            ptx::mma_f16_ss(tmem + kColS, desc_at(dCkl, koff_k(kk, 64)), desc_at(dBk, koff_k(kk, 64)),
                              kIdS, 1u);
           }
         }
@@ -1338,14 +1338,14 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
           const Desc dCk = make_desc(opCt, 16u), dH = make_desc(sbase + K::kH, (uint32_t)NS * 128u);
 #pragma unroll
           for (int kk = 0; kk < NS / 16; ++kk) {
-            ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)),
+            ptx::mma_f16_ss(tmem + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)),
                              kIdYo, kk > 0);
             if constexpr (F32) {
               const Desc dCkl = make_desc(opCt + K::kBtLo, 16u);
               const Desc dHl = make_desc(sbase + K::kH + K::kHLo, (uint32_t)NS * 128u);
-              ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dHl, koff_mn(kk)),
+              ptx::mma_f16_ss(tmem + kColYo, desc_at(dCk, koff_k(kk, 64)), desc_at(dHl, koff_mn(kk)),
                                kIdYo, 1u);
-              ptx::mma_bf16_ss(tmem + kColYo, desc_at(dCkl, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)),
+              ptx::mma_f16_ss(tmem + kColYo, desc_at(dCkl, koff_k(kk, 64)), desc_at(dH, koff_mn(kk)),
                                kIdYo, 1u);
             }
           }
@@ -1444,7 +1444,7 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
         const Desc dX = make_desc(sbase + K::kXo, 64u * 128u);
 #pragma unroll
         for (int kk = 0; kk < kQR / 16; ++kk)
-          ptx::mma_bf16_ss(tmem + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
+          ptx::mma_f16_ss(tmem + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
                            kIdY, kk > 0);
         if constexpr (F32) {
           // ... + P_lo X_hi + P_hi X_lo (both tiles are split)
@@ -1452,11 +1452,11 @@ __global__ void __launch_bounds__(kThreads, F32 ? 1 : 2)
           const Desc dXl = make_desc(sbase + K::kXo + K::kXLo, 64u * 128u);
 #pragma unroll
           for (int kk = 0; kk < kQR / 16; ++kk)
-            ptx::mma_bf16_ss(tmem + kColY, desc_at(dPl, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
+            ptx::mma_f16_ss(tmem + kColY, desc_at(dPl, koff_k(kk, 64)), desc_at(dX, koff_mn(kk)),
                              kIdY, 1u);
 #pragma unroll
           for (int kk = 0; kk < kQR / 16; ++kk)
-            ptx::mma_bf16_ss(tmem + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dXl, koff_mn(kk)),
+            ptx::mma_f16_ss(tmem + kColY, desc_at(dPh, koff_k(kk, 64)), desc_at(dXl, koff_mn(kk)),
                              kIdY, 1u);
         }
         ptx::mma_commit(&bar_y);
